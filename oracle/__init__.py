@@ -1,0 +1,197 @@
+"""CPU oracle for the CSA/HCA attention path -- TEST INFRASTRUCTURE ONLY.
+
+A plain double-precision C implementation (``oracle.c``) of what the hybrid
+compressed attention of DeepSeek-V4 computes, wrapped for numpy.  Only ``tests/``,
+``__graft_entry__.smoke()`` and ``bench.py`` (its cpu_baseline leg and its
+reference arm) may import this package.  It shares no code with the CUDA library
+and the CUDA library never calls it.
+
+bf16 data is passed as numpy ``uint16`` arrays holding the raw bf16 bit patterns;
+results come back as float64.
+
+Every function below only marshals arguments; the arithmetic and the citations to
+the pages live in ``oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` with gcc (no fast-math: plain IEEE double)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        P = ctypes.c_void_p
+        L = ctypes.c_long
+        I = ctypes.c_int
+        D = ctypes.c_double
+        lib.orc_compress.argtypes = [I, I, I, P, P, L, L, P, P, D, I, D, L, L, P]
+        lib.orc_compress.restype = I
+        lib.orc_window_row.argtypes = [I, P, P, D, I, D, L, P]
+        lib.orc_window_row.restype = None
+        lib.orc_indexer_scores.argtypes = [I, I, P, P, P, L, P]
+        lib.orc_indexer_scores.restype = None
+        lib.orc_visible_entries.argtypes = [L, I]
+        lib.orc_visible_entries.restype = L
+        lib.orc_topk.argtypes = [P, L, I, P]
+        lib.orc_topk.restype = I
+        lib.orc_attend.argtypes = [I, I, I, D, D, D, P, P, L, P, L, P, L, L, P, L, L, P, P, P]
+        lib.orc_attend.restype = I
+        lib.orc_gemm_bf16.argtypes = [L, L, L, P, P, P]
+        lib.orc_gemm_bf16.restype = None
+        lib.orc_grouped_oproj.argtypes = [I, I, I, I, I, P, P, P, P]
+        lib.orc_grouped_oproj.restype = I
+        _lib = lib
+    return _lib
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError("bf16 data must be passed as uint16 bit patterns, got %s" % a.dtype)
+    return a
+
+
+def _f32(a) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def compress(tok_v, tok_z, tok_pos0, bias, gamma, eps, rope_dims, rope_base,
+             span, stride, first_entry, n_new):
+    """Entries first_entry .. first_entry+n_new-1 of a compressed cache (float64 [n_new, width]).
+
+    tok_v: uint16 [n_tok, width], tok_z: float32 [n_tok] for tokens tok_pos0 .. tok_pos0+n_tok-1.
+    CSA: span=2m, stride=m.  HCA: span=stride=m'.  gamma=None skips the RMSNorm.
+    """
+    lib = _load()
+    tok_v = _u16(tok_v)
+    tok_z = _f32(tok_z)
+    bias = _f32(bias)
+    g = None if gamma is None else _f32(gamma)
+    n_tok, width = tok_v.shape
+    assert tok_z.shape == (n_tok,) and bias.shape == (span,)
+    out = np.empty((n_new, width), dtype=np.float64)
+    rc = lib.orc_compress(span, stride, width, _ptr(tok_v), _ptr(tok_z), tok_pos0, n_tok,
+                          _ptr(bias), _ptr(g), eps, rope_dims, rope_base, first_entry, n_new, _ptr(out))
+    if rc != 0:
+        raise ValueError("orc_compress: tokens needed by the requested entries are missing (rc=%d)" % rc)
+    return out
+
+
+def window_row(v, gamma, eps, rope_dims, rope_base, pos):
+    """Sliding-window row of one token: RMSNorm(v)*gamma, then RoPE at pos (float64 [c])."""
+    lib = _load()
+    v = _u16(v)
+    g = _f32(gamma)
+    out = np.empty(v.shape[0], dtype=np.float64)
+    lib.orc_window_row(v.shape[0], _ptr(v), _ptr(g), eps, rope_dims, rope_base, pos, _ptr(out))
+    return out
+
+
+def visible_entries(pos: int, ratio: int) -> int:
+    return int(_load().orc_visible_entries(pos, ratio))
+
+
+def indexer_scores(q, w, keys, n_vis):
+    """s_j = sum_h w_h ReLU(q_h . k_j) for j < n_vis (float64 [n_vis]).  q: uint16 [H_I, d_I]."""
+    lib = _load()
+    q = _u16(q)
+    w = _f32(w)
+    keys = _u16(keys)
+    n_heads, dim = q.shape
+    assert keys.shape[1] == dim and keys.shape[0] >= n_vis and w.shape == (n_heads,)
+    out = np.empty(n_vis, dtype=np.float64)
+    lib.orc_indexer_scores(n_heads, dim, _ptr(q), _ptr(w), _ptr(keys), n_vis, _ptr(out))
+    return out
+
+
+def topk(scores, k):
+    """Top-k under (score desc, index asc), ascending indices, -1 padded (int32 [k])."""
+    lib = _load()
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    out = np.empty(k, dtype=np.int32)
+    rc = lib.orc_topk(_ptr(s), s.shape[0], k, _ptr(out))
+    if rc != 0:
+        raise MemoryError("orc_topk")
+    return out
+
+
+def attend(q, gamma_q, pos, comp, sink, win, win_cap, W, rope_dims, rope_base, eps, scale,
+           idx=None, n_dense=0):
+    """One query's core attention (CSA when idx is given, HCA over comp[:n_dense] otherwise).
+
+    q: uint16 [H, c]; comp: uint16 [rows, c]; win: uint16 [win_cap, c] ring; sink: float32 [H].
+    Returns (out float64 [H, c], lse float64 [H]).
+    """
+    lib = _load()
+    q = _u16(q)
+    comp = _u16(comp)
+    win = _u16(win)
+    g = _f32(gamma_q)
+    sk = _f32(sink)
+    H, c = q.shape
+    ix = None if idx is None else np.ascontiguousarray(idx, dtype=np.int32)
+    out = np.empty((H, c), dtype=np.float64)
+    lse = np.empty(H, dtype=np.float64)
+    rc = lib.orc_attend(H, c, rope_dims, rope_base, eps, scale, _ptr(q), _ptr(g), pos,
+                        _ptr(comp), comp.shape[0], _ptr(ix), 0 if ix is None else ix.shape[0], n_dense,
+                        _ptr(win), win_cap, W, _ptr(sk), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("orc_attend: index outside the compressed cache (rc=%d)" % rc)
+    return out, lse
+
+
+def gemm_bf16(A, B):
+    """out = A @ B.T in float64 (A: uint16 [M, K], B: uint16 [N, K])."""
+    lib = _load()
+    A = _u16(A)
+    B = _u16(B)
+    M, K = A.shape
+    N = B.shape[0]
+    assert B.shape[1] == K
+    out = np.empty((M, N), dtype=np.float64)
+    lib.orc_gemm_bf16(M, N, K, _ptr(A), _ptr(B), _ptr(out))
+    return out
+
+
+def grouped_oproj(o, Wg, Wm, groups):
+    """Grouped output projection of one token: o uint16 [H, c] -> float64 [d_model]."""
+    lib = _load()
+    o = _u16(o)
+    Wg = _u16(Wg)
+    Wm = _u16(Wm)
+    H, c = o.shape
+    G = groups
+    d_g = Wg.shape[0] // G
+    d_model = Wm.shape[0]
+    assert Wg.shape == (G * d_g, (H // G) * c) and Wm.shape == (d_model, G * d_g)
+    y = np.empty(d_model, dtype=np.float64)
+    rc = lib.orc_grouped_oproj(H, c, G, d_g, d_model, _ptr(o), _ptr(Wg), _ptr(Wm), _ptr(y))
+    if rc != 0:
+        raise ValueError("orc_grouped_oproj: heads not divisible by groups")
+    return y

@@ -1,0 +1,371 @@
+/*
+ * oracle.c -- TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.
+ *
+ * A plain, slow, single-threaded CPU statement, in double precision, of what the
+ * hybrid compressed attention (CSA + HCA) of DeepSeek-V4 computes.  It exists only
+ * so that tests/, __graft_entry__.smoke() and bench.py's cpu_baseline / reference
+ * arm can check and time the CUDA library against it.  It shares no code, header,
+ * table or helper with the CUDA library, and the CUDA library never calls it.
+ *
+ * Sources (web pages on DeepSeek-V4, cited by address and section):
+ *   [P1] gxgjx.lffhtl.com/lxrt/355279.html, section "混肃穆力机制" (hybrid attention):
+ *        CSA steps one to four, the HCA paragraph, and the tricks list
+ *        (Q/KV normalization, Partial RoPE with the output RoPE at -i,
+ *        sliding-window branch, attention sink).
+ *   [P4] zhinnengdao.top, "DeepSeek-V4开源解读", section 3.1 "Hybrid Attention: CSA + HCA"
+ *        (Flash hyper-parameters: m=4, 64 indexer heads of dim 128, top-k 512,
+ *        m'=128, RoPE on the last 64 dims, one sink logit per head, SWA branch).
+ * Where the pages leave a step open the plainest reading is taken; each such
+ * reading is named at the function that encodes it.
+ *
+ * Conventions: bf16 values arrive as their raw 16-bit patterns (uint16_t) and are
+ * widened exactly to double.  Every sum is a left-to-right loop in double.
+ * Functions return 0 on success and a negative code when the inputs do not hold
+ * what the definition needs (a missing token, an index out of range).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Exact widening of a bf16 bit pattern: bf16 is the top half of an IEEE fp32. */
+static double bf16_bits_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Partial RoPE ([P1] "Partial RoPE"; [P4] 3.1 "最后64维加RoPE").
+ * Rotates only the trailing R dims of x[0..c).  Reading taken (pages silent):
+ * half-split pairing -- pair d (0 <= d < R/2) is (x[c-R+d], x[c-R+d+R/2]) --
+ * frequency theta_d = base^(-2d/R), rotation angle pos * theta_d, and the
+ * rotation (a, b) -> (a cos - b sin, a sin + b cos).
+ */
+static void rope_rotate(double *x, int c, int R, double base, double pos)
+{
+    int half = R / 2;
+    for (int d = 0; d < half; ++d) {
+        double theta = pow(base, -2.0 * (double)d / (double)R);
+        double angle = pos * theta;
+        double cs = cos(angle), sn = sin(angle);
+        double a = x[c - R + d];
+        double b = x[c - R + d + half];
+        x[c - R + d] = a * cs - b * sn;
+        x[c - R + d + half] = a * sn + b * cs;
+    }
+}
+
+/*
+ * RMSNorm ([P1] "Q/KV normalization": queries and KV entries are RMS-normalised
+ * before core attention).  y_i = x_i / sqrt(mean(x^2) + eps) * gamma_i.
+ */
+static void rms_normalize(double *x, int c, const float *gamma, double eps)
+{
+    double ss = 0.0;
+    for (int i = 0; i < c; ++i)
+        ss += x[i] * x[i];
+    double inv = 1.0 / sqrt(ss / (double)c + eps);
+    for (int i = 0; i < c; ++i)
+        x[i] = x[i] * inv * (double)gamma[i];
+}
+
+/*
+ * KV compression, CSA step one and the HCA compressor ([P1] "步，KV 压缩" and the
+ * HCA paragraph; [P4] 3.1: m=4 for CSA, m'=128 for HCA).
+ *
+ * Entry j pools the tokens t in [stride*(j+1) - span, stride*(j+1)), clipped at 0:
+ *   CSA: span = 2m, stride = m  (overlapping windows of 2m, one entry per m tokens)
+ *   HCA: span = stride = m'     (no overlap)
+ * Learned softmax pooling, reading taken: a scalar logit z_t per token plus a
+ * learned bias b[r] per offset r = t - (stride*(j+1) - span) inside the nominal
+ * window (so a window clipped at position 0 keeps the offsets of its surviving
+ * tokens); weights a_t = softmax over the surviving tokens of (z_t + b[r]);
+ * u_j = sum_t a_t v_t.  Then, when gamma is given, RMSNorm with gamma, and when
+ * rope_dims > 0, RoPE at the entry's position p_j = stride*(j+1) - 1 (its last token).
+ *
+ * tok_v[t_local*width + i], tok_z[t_local] hold token tok_pos0 + t_local.
+ * out[(e*width) + i] receives entry first_entry + e, e < n_new.
+ */
+int orc_compress(int span, int stride, int width,
+                 const uint16_t *tok_v, const float *tok_z, long tok_pos0, long n_tok,
+                 const float *bias, const float *gamma, double eps,
+                 int rope_dims, double rope_base,
+                 long first_entry, long n_new, double *out)
+{
+    double *u = (double *)malloc(sizeof(double) * (size_t)width);
+    if (!u)
+        return -3;
+    for (long e = 0; e < n_new; ++e) {
+        long j = first_entry + e;
+        long end = (long)stride * (j + 1);      /* one past the entry's last token */
+        long nominal_begin = end - span;
+        long begin = nominal_begin < 0 ? 0 : nominal_begin;
+        if (begin < tok_pos0 || end > tok_pos0 + n_tok) {
+            free(u);
+            return -1;
+        }
+        double zmax = -INFINITY;
+        for (long t = begin; t < end; ++t) {
+            double s = (double)tok_z[t - tok_pos0] + (double)bias[t - nominal_begin];
+            if (s > zmax)
+                zmax = s;
+        }
+        double den = 0.0;
+        for (long t = begin; t < end; ++t) {
+            double s = (double)tok_z[t - tok_pos0] + (double)bias[t - nominal_begin];
+            den += exp(s - zmax);
+        }
+        for (int i = 0; i < width; ++i)
+            u[i] = 0.0;
+        for (long t = begin; t < end; ++t) {
+            double s = (double)tok_z[t - tok_pos0] + (double)bias[t - nominal_begin];
+            double a = exp(s - zmax) / den;
+            const uint16_t *v = tok_v + (size_t)(t - tok_pos0) * (size_t)width;
+            for (int i = 0; i < width; ++i)
+                u[i] += a * bf16_bits_to_double(v[i]);
+        }
+        if (gamma)
+            rms_normalize(u, width, gamma, eps);
+        if (rope_dims > 0)
+            rope_rotate(u, width, rope_dims, rope_base, (double)(end - 1));
+        memcpy(out + (size_t)e * (size_t)width, u, sizeof(double) * (size_t)width);
+    }
+    free(u);
+    return 0;
+}
+
+/*
+ * One row of the sliding-window branch ([P1] "Sliding window attention": each query
+ * also sees the uncompressed KV of the most recent tokens).  Reading taken: the
+ * uncompressed row of token t is that token's own KV vector, RMS-normalised with
+ * the KV gamma and rotated by RoPE at position t, like every other key.
+ */
+void orc_window_row(int c, const uint16_t *v, const float *gamma, double eps,
+                    int rope_dims, double rope_base, long pos, double *out)
+{
+    for (int i = 0; i < c; ++i)
+        out[i] = bf16_bits_to_double(v[i]);
+    rms_normalize(out, c, gamma, eps);
+    if (rope_dims > 0)
+        rope_rotate(out, c, rope_dims, rope_base, (double)pos);
+}
+
+/*
+ * Lightning indexer, CSA step two ([P1] "二步，lightning indexer + top-k";
+ * [P4] 3.1: 64 indexer query heads of dim 128).  The pages give no formula; the
+ * one taken is the DeepSeek-V3.2 indexer score
+ *     s_j = sum_h w_h * ReLU(q_h . k_j),   j < n_vis,
+ * with no RoPE and no normalisation inside the indexer.
+ * q[h*dim + d], w[h], keys[j*dim + d]; out[j] for j < n_vis.
+ */
+void orc_indexer_scores(int n_heads, int dim, const uint16_t *q, const float *w,
+                        const uint16_t *keys, long n_vis, double *out)
+{
+    for (long j = 0; j < n_vis; ++j) {
+        const uint16_t *k = keys + (size_t)j * (size_t)dim;
+        double s = 0.0;
+        for (int h = 0; h < n_heads; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < dim; ++d)
+                dot += bf16_bits_to_double(q[h * dim + d]) * bf16_bits_to_double(k[d]);
+            double relu = dot > 0.0 ? dot : 0.0;
+            s += (double)w[h] * relu;
+        }
+        out[j] = s;
+    }
+}
+
+/* Visible entries for a query at position pos ([P1]: compressed attention is strictly
+ * causal, a query does not see the block it is in): entry j is visible iff its last
+ * token m*(j+1)-1 is at or before pos, i.e. n_vis = floor((pos+1)/m). */
+long orc_visible_entries(long pos, int ratio)
+{
+    return (pos + 1) / ratio;
+}
+
+typedef struct {
+    double score;
+    int32_t index;
+} scored_entry;
+
+/* (score descending, index ascending): the lower index wins a tie. */
+static int by_score_then_index(const void *pa, const void *pb)
+{
+    const scored_entry *a = (const scored_entry *)pa, *b = (const scored_entry *)pb;
+    if (a->score > b->score)
+        return -1;
+    if (a->score < b->score)
+        return 1;
+    return (a->index > b->index) - (a->index < b->index);
+}
+
+static int by_index(const void *pa, const void *pb)
+{
+    int32_t a = *(const int32_t *)pa, b = *(const int32_t *)pb;
+    return (a > b) - (a < b);
+}
+
+/*
+ * Top-k selection ([P1] CSA step two and "n/m 造成 top-k"; [P4] 3.1 top-k=512).
+ * The first min(k, n) entries of the total order (score descending, index
+ * ascending), written in ascending index order, the rest of out[0..k) set to -1.
+ */
+int orc_topk(const double *scores, long n, int k, int32_t *out)
+{
+    scored_entry *all = (scored_entry *)malloc(sizeof(scored_entry) * (size_t)(n > 0 ? n : 1));
+    if (!all)
+        return -3;
+    for (long j = 0; j < n; ++j) {
+        all[j].score = scores[j];
+        all[j].index = (int32_t)j;
+    }
+    qsort(all, (size_t)n, sizeof(scored_entry), by_score_then_index);
+    long take = n < k ? n : k;
+    for (long i = 0; i < take; ++i)
+        out[i] = all[i].index;
+    qsort(out, (size_t)take, sizeof(int32_t), by_index);
+    for (long i = take; i < k; ++i)
+        out[i] = -1;
+    free(all);
+    return 0;
+}
+
+/*
+ * Core attention for one query, CSA step three and HCA's dense attention, with the
+ * tricks of [P1] (Q/KV normalisation, partial RoPE, output RoPE at -i,
+ * sliding-window branch, attention sink) and [P4] 3.1.
+ *
+ * Key set (each row is both key and value, Multi-Query: one set shared by all heads):
+ *   - compressed rows: comp[idx[i]] for every idx[i] >= 0 (CSA, idx != NULL), or
+ *     comp[0 .. n_dense) (HCA, idx == NULL);
+ *   - window rows: tokens t in [max(0, pos-W+1), pos] read from the ring at row
+ *     t mod win_cap.  A token present both in the window and inside a chosen
+ *     entry is counted in both (reading taken: no de-duplication).
+ * Per head h:
+ *   q_h = RoPE(RMSNorm(q_h) * gamma_q, pos);  l_r = scale * (q_h . row_r);
+ *   p_r = exp(l_r) / (exp(sink_h) + sum_r exp(l_r));   (sink: denominator only)
+ *   o_h = RoPE(sum_r p_r row_r, -pos);   lse_h = log(exp(sink_h) + sum_r exp(l_r)).
+ * Rows already carry RMSNorm and RoPE at their own positions.
+ */
+int orc_attend(int H, int c, int rope_dims, double rope_base, double eps, double scale,
+               const uint16_t *q, const float *gamma_q, long pos,
+               const uint16_t *comp, long comp_rows,
+               const int32_t *idx, long n_idx, long n_dense,
+               const uint16_t *win, long win_cap, long W,
+               const float *sink, double *out, double *lse)
+{
+    long win_begin = pos - W + 1;
+    if (win_begin < 0)
+        win_begin = 0;
+    long n_win = pos - win_begin + 1;
+    long n_comp = idx ? n_idx : n_dense;
+    long max_rows = n_comp + n_win;
+    const uint16_t **rows = (const uint16_t **)malloc(sizeof(*rows) * (size_t)(max_rows > 0 ? max_rows : 1));
+    double *qh = (double *)malloc(sizeof(double) * (size_t)c);
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(max_rows > 0 ? max_rows : 1));
+    double *acc = (double *)malloc(sizeof(double) * (size_t)c);
+    if (!rows || !qh || !logit || !acc) {
+        free(rows); free(qh); free(logit); free(acc);
+        return -3;
+    }
+    long n_rows = 0;
+    for (long i = 0; i < n_comp; ++i) {
+        long j = idx ? (long)idx[i] : i;
+        if (j < 0)
+            continue;
+        if (j >= comp_rows) {
+            free(rows); free(qh); free(logit); free(acc);
+            return -2;
+        }
+        rows[n_rows++] = comp + (size_t)j * (size_t)c;
+    }
+    for (long t = win_begin; t <= pos; ++t)
+        rows[n_rows++] = win + (size_t)(t % win_cap) * (size_t)c;
+
+    for (int h = 0; h < H; ++h) {
+        for (int i = 0; i < c; ++i)
+            qh[i] = bf16_bits_to_double(q[(size_t)h * (size_t)c + i]);
+        rms_normalize(qh, c, gamma_q, eps);
+        if (rope_dims > 0)
+            rope_rotate(qh, c, rope_dims, rope_base, (double)pos);
+
+        double mx = (double)sink[h];
+        for (long r = 0; r < n_rows; ++r) {
+            double dot = 0.0;
+            for (int i = 0; i < c; ++i)
+                dot += qh[i] * bf16_bits_to_double(rows[r][i]);
+            logit[r] = scale * dot;
+            if (logit[r] > mx)
+                mx = logit[r];
+        }
+        double den = exp((double)sink[h] - mx);
+        for (long r = 0; r < n_rows; ++r)
+            den += exp(logit[r] - mx);
+        for (int i = 0; i < c; ++i)
+            acc[i] = 0.0;
+        for (long r = 0; r < n_rows; ++r) {
+            double p = exp(logit[r] - mx) / den;
+            for (int i = 0; i < c; ++i)
+                acc[i] += p * bf16_bits_to_double(rows[r][i]);
+        }
+        if (rope_dims > 0)
+            rope_rotate(acc, c, rope_dims, rope_base, -(double)pos);
+        memcpy(out + (size_t)h * (size_t)c, acc, sizeof(double) * (size_t)c);
+        if (lse)
+            lse[h] = mx + log(den);
+    }
+    free(rows); free(qh); free(logit); free(acc);
+    return 0;
+}
+
+/* Plain matrix product out[m*N + n] = sum_k A[m*K + k] * B[n*K + k] (bf16 inputs). */
+void orc_gemm_bf16(long M, long N, long K, const uint16_t *A, const uint16_t *B, double *out)
+{
+    for (long m = 0; m < M; ++m)
+        for (long n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (long k = 0; k < K; ++k)
+                s += bf16_bits_to_double(A[m * K + k]) * bf16_bits_to_double(B[n * K + k]);
+            out[m * N + n] = s;
+        }
+}
+
+/*
+ * Grouped output projection, CSA step four ([P1] "四步，grouped output projection"):
+ * the H heads' outputs (each of dim c) are split into G groups of H/G heads; group g
+ * is projected by its own matrix Wg[g] (d_g x (H/G)*c) to d_g; the G results are
+ * concatenated and projected by Wm (d_model x G*d_g).  Reading taken: two linear maps,
+ * no bias, no activation in between.
+ * o[h*c + i] (bf16), Wg[(g*d_g + r)*(H/G*c) + k], Wm[(n)*(G*d_g) + k]; y[n].
+ */
+int orc_grouped_oproj(int H, int c, int G, int d_g, int d_model,
+                      const uint16_t *o, const uint16_t *Wg, const uint16_t *Wm, double *y)
+{
+    if (G <= 0 || H % G != 0)
+        return -2;
+    long in_g = (long)(H / G) * c;
+    double *mid = (double *)malloc(sizeof(double) * (size_t)G * (size_t)d_g);
+    if (!mid)
+        return -3;
+    for (int g = 0; g < G; ++g)
+        for (int r = 0; r < d_g; ++r) {
+            const uint16_t *wrow = Wg + ((size_t)g * d_g + r) * (size_t)in_g;
+            const uint16_t *og = o + (size_t)g * (size_t)in_g;
+            double s = 0.0;
+            for (long k = 0; k < in_g; ++k)
+                s += bf16_bits_to_double(wrow[k]) * bf16_bits_to_double(og[k]);
+            mid[(size_t)g * d_g + r] = s;
+        }
+    for (int n = 0; n < d_model; ++n) {
+        const uint16_t *wrow = Wm + (size_t)n * (size_t)G * (size_t)d_g;
+        double s = 0.0;
+        for (long k = 0; k < (long)G * d_g; ++k)
+            s += bf16_bits_to_double(wrow[k]) * mid[k];
+        y[n] = s;
+    }
+    free(mid);
+    return 0;
+}
