@@ -1,0 +1,657 @@
+"""Benchmark of the CSA/HCA attention path on B300 (one JSON line on stdout).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one pass of a layer's whole path over one batch: compression of the block the new
+tokens complete, the window rows of the new tokens, (CSA) indexer scores and top-k, core
+attention with split-K combine.  Workloads (sizes of the pages' V4-Flash configuration):
+  csa_decode_128k (default)  batch 32, 128K context, one query per sequence
+  hca_decode_1m              batch 16, 1M context, one query per sequence
+  csa_prefill_1m             one 8192-query chunk at 1M context
+Inputs are seeded synthetic tensors (workloads.py); the caches are larger than L2 and L2 is
+also flushed between timed steps.  Under torchrun each rank runs the workload on its own
+GPU (sequences shard with no exchange: weak scaling); the value is all ranks' tokens over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+METRIC = "CSA/HCA attention tokens/s per layer at 128K–1M ctx; % of HBM/tensor roofline"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained", d["bf16_tflops"]), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+# ------------------------------------------------------------------------- clocks -----
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------- workloads -----
+
+class Workload:
+    """Common shape of a benchmark workload (device state + per-step inputs)."""
+    name = ""
+    tokens = 0                 # tokens processed per step (per rank)
+    launches = 0               # our kernel launches per step
+    dominant = ""              # name of the dominant kernel
+    bound = "hbm"
+
+    def step(self, ev=None):   # ev: optional (start, end) events around the dominant kernel
+        raise NotImplementedError
+
+    def e2e_step(self):
+        raise NotImplementedError
+
+
+class CsaDecode(Workload):
+    def __init__(self, cfg: dict, seed: int = 0):
+        from long_context_attention_04_b300 import api
+        from long_context_attention_04_b300.layers import CsaLayer, LayerWeights
+        self.api = api
+        s = cfg["shape"]
+        self.cfg = cfg
+        B, pos, entries = cfg["B"], cfg["pos"], cfg["entries"]
+        self.B, self.pos, self.entries = B, pos, entries
+        self.p = api.params_from(s)
+        self.s = s
+        rng = wl.Rng(seed, device="cuda")
+        d = wl.decode_inputs(rng, s, B, pos, entries, csa=True)
+        self.d = d
+        w = LayerWeights(d["gamma_kv"], d["gamma_q"], d["bias_kv"], d["sink"], d["bias_idx"])
+        self.layer = CsaLayer(self.p, w, d["kv_cache"], d["idx_cache"], d["win_kv"], n_q=1)
+        i32 = dict(dtype=torch.int32, device="cuda")
+        self.tok_pos0 = torch.full((B,), d["tok_pos0"], **i32)
+        self.first = torch.full((B,), entries - 1, **i32)
+        self.new_pos = torch.full((B,), pos, **i32)
+        self.q_pos = torch.full((B, 1), pos, **i32)
+        self.out = torch.empty((B, 1, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+        self.scores = self.layer.ws_idx.view(torch.float32).view(B, 1, -1)
+        self.tokens = B
+        self.launches = 7
+        self.dominant = "indexer"
+        # per-step inputs, pinned on the host for the end-to-end leg
+        self.host_in = {k: d[k].cpu().pin_memory() for k in ("tok_v", "tok_z", "tok_vi", "tok_zi", "q", "q_idx",
+                                                               "w_idx")}
+        self.host_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+        # algorithmic bytes of one indexer launch: keys of the visible entries, queries, weights, scores
+        n_vis = (pos + 1) // s.ratio
+        self.dom_bytes = B * (n_vis * s.idx_dim * 2 + s.idx_heads * s.idx_dim * 2 + s.idx_heads * 4 + n_vis * 4)
+        self.dom_flops = 2.0 * B * n_vis * s.idx_heads * s.idx_dim
+
+    def step(self, ev=None):
+        api, L, d = self.api, self.layer, self.d
+        L.compress(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, 1)
+        L.window(d["tok_v"][:, -1:], self.new_pos)
+        if ev:
+            ev[0].record()
+        api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
+        if ev:
+            ev[1].record()
+        api.lca_topk(self.p, self.scores, self.q_pos, self.entries, L.idx)
+        L.attend(d["q"], self.q_pos, self.out)
+
+    def e2e_step(self):
+        d = self.d
+        for k, t in self.host_in.items():
+            d[k].copy_(t, non_blocking=True)
+        self.step()
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def cpu_sample(self, budget_s: float) -> dict:
+        """The oracle on whole sequences of this step until the budget is spent."""
+        import oracle
+        from workloads import bf16_bits
+        s = self.s
+        t_total, n_done = 0.0, 0
+        for b in range(self.B):
+            kvb = bf16_bits(self.kv_host[b])
+            ixb = bf16_bits(self.idx_host[b])
+            winb = bf16_bits(self.win_host[b])
+            tv, tz = bf16_bits(self.host_in["tok_v"][b]), self.host_in["tok_z"][b].numpy()
+            tvi, tzi = bf16_bits(self.host_in["tok_vi"][b]), self.host_in["tok_zi"][b].numpy()
+            q = bf16_bits(self.host_in["q"][b, 0])
+            qi = bf16_bits(self.host_in["q_idx"][b, 0])
+            wi = self.host_in["w_idx"][b, 0].numpy()
+            g = self.w_host["gamma_kv"]
+            t0 = time.perf_counter()
+            kv_new = oracle.compress(tv, tz, self.d["tok_pos0"], self.w_host["bias_kv"], g, s.rms_eps, s.rope_dims,
+                                     s.rope_base, 2 * s.ratio, s.ratio, self.entries - 1, 1)
+            k_new = oracle.compress(tvi, tzi, self.d["tok_pos0"], self.w_host["bias_idx"], None, s.rms_eps, 0,
+                                    s.rope_base, 2 * s.ratio, s.ratio, self.entries - 1, 1)
+            w_new = oracle.window_row(tv[-1], g, s.rms_eps, s.rope_dims, s.rope_base, self.pos)
+            t1 = time.perf_counter()
+            kvb[-1] = _round_bits(kv_new[0])
+            ixb[-1] = _round_bits(k_new[0])
+            winb[self.pos % winb.shape[0]] = _round_bits(w_new)
+            t2 = time.perf_counter()
+            n_vis = oracle.visible_entries(self.pos, s.ratio)
+            sc = oracle.indexer_scores(qi, wi, ixb, n_vis)
+            idx = oracle.topk(sc, s.topk)
+            oracle.attend(q, self.w_host["gamma_q"], self.pos, kvb, self.w_host["sink"], winb, winb.shape[0],
+                          s.window, s.rope_dims, s.rope_base, s.rms_eps, self.p.scale, idx=idx)
+            t3 = time.perf_counter()
+            t_total += (t1 - t0) + (t3 - t2)
+            n_done += 1
+            if t_total >= budget_s:
+                break
+        return dict(value=n_done / t_total, unit="tokens/s", cores=1, kind="oracle",
+                    sample="%d of %d sequences of the step (compression, window row, indexer over %d entries, "
+                           "top-%d, attention), single-threaded fp64" % (n_done, self.B, self.entries, s.topk))
+
+    def snapshot_host(self):
+        """Host copies of the state the oracle needs, taken before any GPU step touches it."""
+        n = min(self.B, 64)
+        self.kv_host = self.d["kv_cache"][:n].cpu()
+        self.idx_host = self.d["idx_cache"][:n].cpu()
+        self.win_host = self.d["win_kv"][:n].cpu()
+        self.w_host = {k: self.d[k].cpu().numpy() for k in ("gamma_kv", "gamma_q", "bias_kv", "bias_idx", "sink")}
+
+
+class HcaDecode(Workload):
+    def __init__(self, cfg: dict, seed: int = 0):
+        from long_context_attention_04_b300 import api
+        from long_context_attention_04_b300.layers import HcaLayer, LayerWeights
+        self.api = api
+        s = cfg["shape"]
+        self.cfg, self.s = cfg, s
+        B, pos, entries = cfg["B"], cfg["pos"], cfg["entries"]
+        self.B, self.pos, self.entries = B, pos, entries
+        self.p = api.params_from(s)
+        rng = wl.Rng(seed, device="cuda")
+        d = wl.decode_inputs(rng, s, B, pos, entries, csa=False)
+        self.d = d
+        w = LayerWeights(d["gamma_kv"], d["gamma_q"], d["bias_kv"], d["sink"])
+        self.layer = HcaLayer(self.p, w, d["kv_cache"], d["win_kv"], n_q=1)
+        i32 = dict(dtype=torch.int32, device="cuda")
+        self.tok_pos0 = torch.full((B,), d["tok_pos0"], **i32)
+        self.first = torch.full((B,), entries - 1, **i32)
+        self.new_pos = torch.full((B,), pos, **i32)
+        self.q_pos = torch.full((B, 1), pos, **i32)
+        self.out = torch.empty((B, 1, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+        self.tokens = B
+        self.launches = 4
+        self.dominant = "attend"
+        self.host_in = {k: d[k].cpu().pin_memory() for k in ("tok_v", "tok_z", "q")}
+        self.host_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+        n_vis = (pos + 1) // s.ratio
+        rows = n_vis + s.window
+        self.dom_bytes = B * (rows * s.head_dim * 2 + 2 * s.heads * s.head_dim * 2)
+        self.dom_flops = 4.0 * B * rows * s.heads * s.head_dim
+
+    def step(self, ev=None):
+        L, d = self.layer, self.d
+        L.compress(d["tok_v"], d["tok_z"], self.tok_pos0, self.first, 1)
+        L.window(d["tok_v"][:, -1:], self.new_pos)
+        if ev:
+            ev[0].record()
+        L.attend(d["q"], self.q_pos, self.out)
+        if ev:
+            ev[1].record()
+
+    def e2e_step(self):
+        d = self.d
+        for k, t in self.host_in.items():
+            d[k].copy_(t, non_blocking=True)
+        self.step()
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def snapshot_host(self):
+        n = min(self.B, 64)
+        self.kv_host = self.d["kv_cache"][:n].cpu()
+        self.win_host = self.d["win_kv"][:n].cpu()
+        self.w_host = {k: self.d[k].cpu().numpy() for k in ("gamma_kv", "gamma_q", "bias_kv", "sink")}
+
+    def cpu_sample(self, budget_s: float) -> dict:
+        import oracle
+        from workloads import bf16_bits
+        s = self.s
+        t_total, n_done = 0.0, 0
+        for b in range(self.B):
+            kvb = bf16_bits(self.kv_host[b])
+            winb = bf16_bits(self.win_host[b])
+            tv, tz = bf16_bits(self.host_in["tok_v"][b]), self.host_in["tok_z"][b].numpy()
+            q = bf16_bits(self.host_in["q"][b, 0])
+            g = self.w_host["gamma_kv"]
+            t0 = time.perf_counter()
+            kv_new = oracle.compress(tv, tz, self.d["tok_pos0"], self.w_host["bias_kv"], g, s.rms_eps, s.rope_dims,
+                                     s.rope_base, s.ratio, s.ratio, self.entries - 1, 1)
+            w_new = oracle.window_row(tv[-1], g, s.rms_eps, s.rope_dims, s.rope_base, self.pos)
+            t1 = time.perf_counter()
+            kvb[-1] = _round_bits(kv_new[0])
+            winb[self.pos % winb.shape[0]] = _round_bits(w_new)
+            t2 = time.perf_counter()
+            oracle.attend(q, self.w_host["gamma_q"], self.pos, kvb, self.w_host["sink"], winb, winb.shape[0],
+                          s.window, s.rope_dims, s.rope_base, s.rms_eps, self.p.scale,
+                          n_dense=oracle.visible_entries(self.pos, s.ratio))
+            t3 = time.perf_counter()
+            t_total += (t1 - t0) + (t3 - t2)
+            n_done += 1
+            if t_total >= budget_s:
+                break
+        return dict(value=n_done / t_total, unit="tokens/s", cores=1, kind="oracle",
+                    sample="%d of %d sequences of the step (compression of the 128-token block, window row, "
+                           "attention over %d entries + %d window rows), single-threaded fp64"
+                           % (n_done, self.B, self.entries, s.window))
+
+
+class CsaPrefill(Workload):
+    def __init__(self, cfg: dict, seed: int = 0):
+        from long_context_attention_04_b300 import api
+        from long_context_attention_04_b300.layers import CsaLayer, LayerWeights
+        self.api = api
+        s = cfg["shape"]
+        self.cfg, self.s = cfg, s
+        Tq, entries, q_begin = cfg["Tq"], cfg["entries"], cfg["q_begin"]
+        self.Tq, self.entries, self.q_begin = Tq, entries, q_begin
+        self.p = api.params_from(s)
+        win_cap = Tq + s.window
+        rng = wl.Rng(seed, device="cuda")
+        d = wl.prefill_chunk_inputs(rng, s, q_begin, Tq, entries, win_cap)
+        self.d = d
+        w = LayerWeights(d["gamma_kv"], d["gamma_q"], d["bias_kv"], d["sink"], d["bias_idx"])
+        self.layer = CsaLayer(self.p, w, d["kv_cache"], d["idx_cache"], d["win_kv"], n_q=Tq)
+        i32 = dict(dtype=torch.int32, device="cuda")
+        self.tok_pos0 = torch.tensor([d["tok_pos0"]], **i32)
+        self.first = torch.tensor([d["first_entry"]], **i32)
+        self.new_pos = torch.tensor([q_begin], **i32)
+        self.q_pos = torch.arange(q_begin, q_begin + Tq, **i32).view(1, Tq)
+        self.out = torch.empty((1, Tq, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
+        self.scores = self.layer.ws_idx.view(torch.float32).view(1, Tq, -1)
+        self.tokens = Tq
+        self.launches = 7
+        self.dominant = "indexer"
+        self.bound = "tensor"
+        self.host_in = {k: d[k].cpu().pin_memory() for k in ("tok_v", "tok_z", "tok_vi", "tok_zi", "q", "q_idx",
+                                                               "w_idx")}
+        self.host_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+        n_vis = np.array([(q_begin + i + 1) // s.ratio for i in range(Tq)], dtype=np.float64)
+        self.dom_flops = float(2.0 * n_vis.sum() * s.idx_heads * s.idx_dim)
+        self.dom_bytes = entries * s.idx_dim * 2 + Tq * s.idx_heads * (s.idx_dim * 2 + 4) + float(n_vis.sum()) * 4
+
+    def step(self, ev=None):
+        api, L, d = self.api, self.layer, self.d
+        L.compress(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, self.Tq // self.s.ratio)
+        L.window(d["tok_v"][:, self.s.ratio:], self.new_pos)
+        if ev:
+            ev[0].record()
+        api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
+        if ev:
+            ev[1].record()
+        api.lca_topk(self.p, self.scores, self.q_pos, self.entries, L.idx)
+        L.attend(d["q"], self.q_pos, self.out)
+
+    def e2e_step(self):
+        d = self.d
+        for k, t in self.host_in.items():
+            d[k].copy_(t, non_blocking=True)
+        self.step()
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def snapshot_host(self):
+        self.kv_host = self.d["kv_cache"][0].cpu()
+        self.idx_host = self.d["idx_cache"][0].cpu()
+        self.win_host = self.d["win_kv"][0].cpu()
+        self.w_host = {k: self.d[k].cpu().numpy() for k in ("gamma_kv", "gamma_q", "bias_kv", "bias_idx", "sink")}
+
+    def cpu_sample(self, budget_s: float) -> dict:
+        """Oracle on evenly spaced queries of the chunk (their indexer over ~262K entries dominates),
+        with the compression and window rows those queries need."""
+        import oracle
+        from workloads import bf16_bits
+        s = self.s
+        kvb = bf16_bits(self.kv_host)
+        ixb = bf16_bits(self.idx_host)
+        winb = bf16_bits(self.win_host)
+        tv, tz = bf16_bits(self.host_in["tok_v"][0]), self.host_in["tok_z"][0].numpy()
+        tvi, tzi = bf16_bits(self.host_in["tok_vi"][0]), self.host_in["tok_zi"][0].numpy()
+        g = self.w_host["gamma_kv"]
+        t_total = 0.0
+        # compression of the chunk's entries and its window rows, timed once and charged per query
+        t0 = time.perf_counter()
+        n_new = self.Tq // s.ratio
+        kv_new = oracle.compress(tv, tz, self.d["tok_pos0"], self.w_host["bias_kv"], g, s.rms_eps, s.rope_dims,
+                                 s.rope_base, 2 * s.ratio, s.ratio, self.d["first_entry"], n_new)
+        k_new = oracle.compress(tvi, tzi, self.d["tok_pos0"], self.w_host["bias_idx"], None, s.rms_eps, 0,
+                                s.rope_base, 2 * s.ratio, s.ratio, self.d["first_entry"], n_new)
+        rows = [oracle.window_row(tv[s.ratio + t], g, s.rms_eps, s.rope_dims, s.rope_base, self.q_begin + t)
+                for t in range(self.Tq)]
+        t_shared = time.perf_counter() - t0
+        fe = self.d["first_entry"]
+        kvb[fe:fe + n_new] = _round_bits(kv_new)
+        ixb[fe:fe + n_new] = _round_bits(k_new)
+        for t in range(self.Tq):
+            winb[(self.q_begin + t) % winb.shape[0]] = _round_bits(rows[t])
+        n_done = 0
+        for i in np.linspace(0, self.Tq - 1, 32).astype(int):
+            pos = self.q_begin + int(i)
+            qi = bf16_bits(self.host_in["q_idx"][0, i])
+            wi = self.host_in["w_idx"][0, i].numpy()
+            q = bf16_bits(self.host_in["q"][0, i])
+            t0 = time.perf_counter()
+            n_vis = oracle.visible_entries(pos, s.ratio)
+            sc = oracle.indexer_scores(qi, wi, ixb, n_vis)
+            idx = oracle.topk(sc, s.topk)
+            oracle.attend(q, self.w_host["gamma_q"], pos, kvb, self.w_host["sink"], winb, winb.shape[0], s.window,
+                          s.rope_dims, s.rope_base, s.rms_eps, self.p.scale, idx=idx)
+            t_total += time.perf_counter() - t0
+            n_done += 1
+            if t_total >= budget_s:
+                break
+        per_query = t_total / n_done + t_shared / self.Tq
+        return dict(value=1.0 / per_query, unit="tokens/s", cores=1, kind="oracle",
+                    sample="%d evenly spaced queries of the 8192-query chunk (indexer over ~262K entries, top-%d, "
+                           "attention) plus the chunk's compression and window rows charged per query; "
+                           "single-threaded fp64, extrapolated per query" % (n_done, s.topk))
+
+
+def _round_bits(x: np.ndarray) -> np.ndarray:
+    from workloads import bf16_bits
+    return bf16_bits(torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16))
+
+
+WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill}
+
+
+# ------------------------------------------------------------------- distributed -----
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Largest value over all ranks (the slowest rank's time); identity on one process."""
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- main -----
+
+def time_steps(wk: Workload, steps: int, warmup: int, flush: torch.Tensor, e2e: bool, world: int):
+    """Per-step device times (ms) of `steps` steps after `warmup`, L2 flushed before each step."""
+    stream = torch.cuda.current_stream()
+    fn = wk.e2e_step if e2e else wk.step
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    dom_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush.zero_()
+        step_ev[i][0].record(stream)
+        if e2e:
+            fn()
+        else:
+            wk.step(dom_ev[i])
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    dom_ms = [a.elapsed_time(b) for a, b in dom_ev] if not e2e else []
+    return step_ms, dom_ms
+
+
+def run_ours(args):
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    from long_context_attention_04_b300 import build as lca_build
+    if rank == 0:
+        lca_build.build()
+    barrier(world)
+    cfg = wl.WORKLOADS[args.workload]
+    wk = WORKLOADS[args.workload](cfg, seed=args.seed + rank)
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    if do_cpu:
+        wk.snapshot_host()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        step_ms, dom_ms = time_steps(wk, args.steps, args.warmup, flush, False, world)
+    e2e_ms, _ = time_steps(wk, args.steps, max(1, args.warmup // 2), flush, True, world)
+    ms = float(np.mean(step_ms))
+    ms_all = max_over_ranks(ms, world, device)
+    e2e_all = max_over_ranks(float(np.mean(e2e_ms)), world, device)
+    dom = float(np.mean(dom_ms))
+    from long_context_attention_04_b300 import api
+    dev_err = api.lca_device_error()
+    peaks = measured_peaks()
+    if wk.bound == "hbm":
+        achieved = wk.dom_bytes / (dom * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None, "kernel": wk.dominant,
+                "kernel_ms": round(dom, 4), "peak_source": peaks["source"]}
+    else:
+        achieved = wk.dom_flops / (dom * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None, "kernel": wk.dominant,
+                "kernel_ms": round(dom, 4), "peak_source": peaks["source"]}
+    value = world * wk.tokens / (ms_all * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_all, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded N(0,1) caches, tokens, queries; N(0,0.02) biases (workloads.py)",
+        "config": {"workload": cfg["name"], "name": args.workload, "batch": cfg.get("B", 1),
+                   "l2": "caches larger than L2, and L2 flushed (512 MiB write) before every timed step"},
+        "roofline": roof,
+        "e2e": {"value": round(world * wk.tokens / (e2e_all * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": wk.h2d_bytes, "d2h_bytes_per_step": wk.d2h_bytes},
+        "gpu_launches": wk.launches * args.steps,
+        "clocks": clk.summary(),
+        "device_error_word": dev_err,
+    }
+    if do_cpu:
+        line["cpu_baseline"] = wk.cpu_sample(args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle (CPU, fp64, single thread) as the reference arm: each step is a bounded sample."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    cfg = wl.WORKLOADS[args.workload]
+    wk = _HostOnly(args.workload, cfg, args.seed)
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        wk.one_unit()
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    per_unit = float(np.mean(times))
+    value = 1.0 / per_unit
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_unit * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded (workloads.py)",
+        "config": {"workload": cfg["name"], "name": args.workload, "batch": cfg.get("B", 1)},
+        "cpu_baseline": {"kind": "oracle", "cores": 1, "value": round(value, 3), "unit": "tokens/s",
+                         "sample": "one token of the workload per step: " + wk.sample},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+class _HostOnly:
+    """Host-side inputs of one token of a workload for the oracle arm (no GPU touched)."""
+
+    def __init__(self, name, cfg, seed):
+        import oracle
+        from workloads import bf16_bits
+        self.oracle = oracle
+        s = cfg["shape"]
+        self.s = s
+        rng = wl.Rng(seed)
+        self.kind = name
+        if name == "csa_decode_128k" or name == "csa_prefill_1m":
+            entries = cfg["entries"]
+            pos = cfg.get("pos", cfg.get("q_begin", 0) + cfg.get("Tq", 1) - 1)
+            self.pos = pos
+            self.kv = bf16_bits(rng.normal_bf16((entries, s.head_dim)))
+            self.keys = bf16_bits(rng.normal_bf16((entries, s.idx_dim)))
+            self.win = bf16_bits(rng.normal_bf16((s.window, s.head_dim)))
+            self.tok_v = bf16_bits(rng.normal_bf16((2 * s.ratio, s.head_dim)))
+            self.tok_vi = bf16_bits(rng.normal_bf16((2 * s.ratio, s.idx_dim)))
+            self.tok_z = rng.normal_f32((2 * s.ratio,)).numpy()
+            self.q = bf16_bits(rng.normal_bf16((s.heads, s.head_dim)))
+            self.qi = bf16_bits(rng.normal_bf16((s.idx_heads, s.idx_dim)))
+            self.wi = (rng.normal_f32((s.idx_heads,)) / math.sqrt(s.idx_heads)).numpy()
+            self.sample = "compression, window row, indexer over %d entries, top-%d, attention" % (entries, s.topk)
+        else:
+            entries = cfg["entries"]
+            self.pos = cfg["pos"]
+            self.kv = bf16_bits(rng.normal_bf16((entries, s.head_dim)))
+            self.win = bf16_bits(rng.normal_bf16((s.window, s.head_dim)))
+            self.tok_v = bf16_bits(rng.normal_bf16((s.ratio, s.head_dim)))
+            self.tok_z = rng.normal_f32((s.ratio,)).numpy()
+            self.q = bf16_bits(rng.normal_bf16((s.heads, s.head_dim)))
+            self.sample = "compression of a %d-token block, window row, attention over %d entries" % (s.ratio, entries)
+        self.ones = np.ones(s.head_dim, np.float32)
+        self.sink = rng.normal_f32((s.heads,)).numpy()
+
+    def one_unit(self):
+        o, s = self.oracle, self.s
+        span = 2 * s.ratio if self.kind != "hca_decode_1m" else s.ratio
+        bias = np.zeros(span, np.float32)
+        p0 = self.pos + 1 - span
+        j = (self.pos + 1) // s.ratio - 1
+        o.compress(self.tok_v, self.tok_z, p0, bias, self.ones, s.rms_eps, s.rope_dims, s.rope_base, span, s.ratio,
+                   j, 1)
+        o.window_row(self.tok_v[-1], self.ones, s.rms_eps, s.rope_dims, s.rope_base, self.pos)
+        scale = 1.0 / math.sqrt(s.head_dim)
+        if self.kind != "hca_decode_1m":
+            o.compress(self.tok_vi, self.tok_z, p0, bias, None, s.rms_eps, 0, s.rope_base, span, s.ratio, j, 1)
+            sc = o.indexer_scores(self.qi, self.wi, self.keys, o.visible_entries(self.pos, s.ratio))
+            idx = o.topk(sc, s.topk)
+            o.attend(self.q, self.ones, self.pos, self.kv, self.sink, self.win, self.win.shape[0], s.window,
+                     s.rope_dims, s.rope_base, s.rms_eps, scale, idx=idx)
+        else:
+            o.attend(self.q, self.ones, self.pos, self.kv, self.sink, self.win, self.win.shape[0], s.window,
+                     s.rope_dims, s.rope_base, s.rms_eps, scale, n_dense=o.visible_entries(self.pos, s.ratio))
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="csa_decode_128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,236 @@
+/*
+ * lca.h -- C ABI of the B300 (sm_103a) hybrid compressed attention library (liblca.so).
+ *
+ * The library implements the attention path of DeepSeek-V4 as described in the
+ * web write-ups on the model:
+ *   [P1] gxgjx.lffhtl.com/lxrt/355279.html, section "混肃穆力机制" (hybrid attention):
+ *        CSA steps one to four (KV compression; lightning indexer + top-k; core
+ *        Multi-Query Attention; grouped output projection), the HCA paragraph, and the
+ *        tricks: Q/KV RMSNorm, partial RoPE with an output RoPE at -i, a sliding-window
+ *        branch, and an attention sink.
+ *   [P4] zhinnengdao.top, "DeepSeek-V4开源解读", section 3.1 "Hybrid Attention: CSA + HCA":
+ *        m=4, 64 indexer heads of dim 128, top-k 512, m'=128, RoPE on the last 64 dims,
+ *        one learnable sink logit per head, an SWA branch next to each attention.
+ *
+ * Conventions for every entry point:
+ *   - All data pointers are DEVICE pointers to buffers the caller owns; the library
+ *     allocates nothing and keeps no pointer after the call returns.
+ *   - Work is enqueued on `stream` and runs asynchronously; results are ready when the
+ *     stream reaches that point.
+ *   - Arguments are validated on the host before anything is launched: a bad size,
+ *     a NULL pointer, a pointer not aligned to 16 bytes, an unsupported shape or a
+ *     workspace that is too small returns an error status and launches nothing.
+ *     lca_last_error() then describes the problem (thread-local string).
+ *   - Values that live on the device (positions, first entries, indices) are checked by
+ *     the kernels: a violation skips the offending row and sets a bit in the device
+ *     error word, which lca_device_error() reads and clears.
+ *   - bf16 tensors are passed as raw 16-bit patterns (lca_bf16).  Row-major layouts;
+ *     strides are in ELEMENTS.
+ */
+#ifndef LCA_H
+#define LCA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Every declaration below is an exported symbol of liblca.so (built with hidden default
+ * visibility; only this ABI is visible). */
+#if defined(__GNUC__)
+#pragma GCC visibility push(default)
+#endif
+
+typedef struct CUstream_st *cudaStream_t; /* the CUDA runtime's stream handle */
+typedef uint16_t lca_bf16;                /* raw bfloat16 bit pattern */
+
+typedef enum lca_status {
+    LCA_OK = 0,
+    LCA_ERR_INVALID_ARG = 1,  /* bad size, NULL or misaligned pointer */
+    LCA_ERR_UNSUPPORTED = 2,  /* shape outside what the kernels are built for */
+    LCA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than the *_workspace() size */
+    LCA_ERR_CUDA = 4,         /* a CUDA runtime call or a launch failed */
+    LCA_ERR_TIMEOUT = 5,      /* a kernel gave up on a bounded wait (device error word) */
+    LCA_ERR_DEVICE = 6        /* a device-side check fired (device error word) */
+} lca_status;
+
+/* Bits of the device error word (see lca_device_error). */
+#define LCA_DEVERR_MISSING_TOKEN  0x1u  /* compress: a window token outside the staging rows */
+#define LCA_DEVERR_INDEX_RANGE    0x2u  /* attend: an index outside [0, cache_rows) (not -1) */
+#define LCA_DEVERR_VISIBLE_RANGE  0x4u  /* visible entries exceed cache_rows; clamped */
+#define LCA_DEVERR_NEGATIVE_POS   0x8u  /* a negative position */
+#define LCA_DEVERR_TIMEOUT        0x100u /* a bounded wait inside a kernel ran out */
+
+/* Layer parameters (names follow the pages' notation). */
+typedef struct lca_attn_params {
+    int heads;           /* H: query heads sharing one KV (MQA); 1..64 */
+    int head_dim;        /* c: width of a KV entry and of a head; 128, 256 or 512 */
+    int rope_dims;       /* R: trailing dims rotated by RoPE; even, 0..c, R/2 <= 64 */
+    float rope_base;     /* RoPE base; frequency of pair d is base^(-2d/R) */
+    float rms_eps;       /* RMSNorm epsilon */
+    float softmax_scale; /* logit scale; 0 selects 1/sqrt(c) */
+    int window;          /* W: sliding-window tokens, the query's own token included */
+    int ratio;           /* m (CSA) or m' (HCA): tokens per compressed entry */
+    int topk;            /* k: entries selected per query (CSA) */
+    int idx_heads;       /* H_I: indexer query heads */
+    int idx_dim;         /* d_I: indexer head dim */
+} lca_attn_params;
+
+/* ---------------------------------------------------------------------------------
+ * KV compression ([P1] CSA step one "KV 压缩" and the HCA paragraph; [P4] 3.1).
+ *
+ * For each sequence b and e < n_new, entry j = first_entry[b] + e pools the tokens
+ *   CSA: t in [m(j-1), m(j+1)) clipped at 0   (windows of 2m, stride m, overlapping)
+ *   HCA: t in [m'j, m'(j+1))                   (no overlap)
+ * with softmax weights over (tok_z[t] + pos_bias[t - nominal window start]), then applies
+ * RMSNorm with gamma (skipped when gamma == NULL) and, when apply_rope != 0, RoPE at the
+ * entry's last token m(j+1)-1 to the trailing rope_dims dims, and stores the row in bf16
+ * at cache[b*cache_batch_stride + j*width].
+ *   width       row width: head_dim for the KV cache, idx_dim for the indexer keys;
+ *               multiple of 8, at most 1024.
+ *   tok_v       [batch][n_tok][width] bf16, token t of sequence b at local row
+ *               t - tok_pos0[b]; tok_v_batch_stride elements between sequences.
+ *   tok_z       [batch][n_tok] fp32 compressor logits, tok_z_batch_stride between sequences.
+ *   tok_pos0    [batch] int32 (device): position of local row 0.
+ *   pos_bias    [2m] (CSA) or [m'] (HCA) fp32 learned offset biases.
+ *   gamma       [width] fp32 or NULL.
+ *   first_entry [batch] int32 (device).
+ *   cache_rows  rows available per sequence; j >= cache_rows is an error.
+ * A window token outside the staging rows sets LCA_DEVERR_MISSING_TOKEN and skips the entry.
+ * ------------------------------------------------------------------------------- */
+lca_status csa_compress_kv(const lca_attn_params *p, int batch, int width,
+                           const lca_bf16 *tok_v, int64_t tok_v_batch_stride, int n_tok,
+                           const float *tok_z, int64_t tok_z_batch_stride,
+                           const int32_t *tok_pos0, const float *pos_bias, const float *gamma,
+                           int apply_rope, const int32_t *first_entry, int n_new,
+                           lca_bf16 *cache, int64_t cache_batch_stride, int64_t cache_rows,
+                           cudaStream_t stream);
+lca_status hca_compress_kv(const lca_attn_params *p, int batch, int width,
+                           const lca_bf16 *tok_v, int64_t tok_v_batch_stride, int n_tok,
+                           const float *tok_z, int64_t tok_z_batch_stride,
+                           const int32_t *tok_pos0, const float *pos_bias, const float *gamma,
+                           int apply_rope, const int32_t *first_entry, int n_new,
+                           lca_bf16 *cache, int64_t cache_batch_stride, int64_t cache_rows,
+                           cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Sliding-window rows ([P1] "Sliding window attention" branch: the last W uncompressed
+ * tokens).  For each of the n_tok tokens of each sequence (position tok_pos0[b] + t),
+ * writes RoPE(RMSNorm(v) * gamma, position) in bf16 to the ring row
+ * (position mod win_cap) of win_kv[b*win_batch_stride ...].  Width is head_dim.
+ * A ring of win_cap >= W rows serves decode; a prefill chunk of T tokens needs
+ * win_cap >= T + W - 1 so that no row a query reads is overwritten.
+ * ------------------------------------------------------------------------------- */
+lca_status lca_window_update(const lca_attn_params *p, int batch,
+                             const lca_bf16 *tok_v, int64_t tok_v_batch_stride, int n_tok,
+                             const int32_t *tok_pos0, const float *gamma,
+                             lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                             cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Lightning indexer scores ([P1] CSA step two; [P4] 3.1: 64 heads x 128):
+ *   s[b][i][j] = sum_h w[b][i][h] * ReLU(q[b][i][h] . k[b][j])   for j < n_vis(i),
+ *   n_vis(i) = floor((q_pos[b][i] + 1) / m), entries j >= n_vis(i) set to -inf.
+ *   q_idx   [batch][n_q][H_I][d_I] bf16;  w_idx [batch][n_q][H_I] fp32.
+ *   k_cache [batch][cache_rows][d_I] bf16 (k_batch_stride between sequences).
+ *   q_pos   [batch][n_q] int32 (device).
+ *   scores  [batch][n_q][scores_stride] fp32, scores_stride >= cache_rows, multiple of 4.
+ * Supported: d_I in {64, 128}, H_I in {16, 32, 64}; (d_I, H_I) = (32, 4) also accepted.
+ * ------------------------------------------------------------------------------- */
+lca_status csa_indexer_scores(const lca_attn_params *p, int batch, int n_q,
+                              const lca_bf16 *q_idx, const float *w_idx,
+                              const lca_bf16 *k_cache, int64_t k_batch_stride, int64_t cache_rows,
+                              const int32_t *q_pos, float *scores, int64_t scores_stride,
+                              cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Top-k selection ([P1] CSA step two; [P4] 3.1 top-k): for each query, the first
+ * min(k, n_vis) entries under (score descending, index ascending), written in ascending
+ * index order to out_idx[b][i][0..k), the remainder set to -1.  Scores as produced by
+ * csa_indexer_scores (only the first n_vis(i) entries of each row are read).
+ * ------------------------------------------------------------------------------- */
+lca_status lca_topk(const lca_attn_params *p, int batch, int n_q,
+                    const float *scores, int64_t scores_stride, const int32_t *q_pos,
+                    int64_t max_entries, int32_t *out_idx, cudaStream_t stream);
+
+/* Indexer scores followed by top-k; the scores go to the workspace. */
+size_t csa_indexer_workspace(const lca_attn_params *p, int batch, int n_q, int64_t cache_rows);
+lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q,
+                            const lca_bf16 *q_idx, const float *w_idx,
+                            const lca_bf16 *k_cache, int64_t k_batch_stride, int64_t cache_rows,
+                            const int32_t *q_pos, int32_t *out_idx,
+                            void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Core attention ([P1] CSA step three, HCA dense attention and the tricks; [P4] 3.1).
+ * For query i of sequence b at position pos = q_pos[b][i], per head h:
+ *   q_h  = RoPE(RMSNorm(q[b][i][h]) * gamma_q, pos)
+ *   rows = compressed rows (CSA: kv_cache[idx[b][i][r]] for idx >= 0, r < k;
+ *                           HCA: kv_cache[0 .. floor((pos+1)/m')) )
+ *          followed by the window rows of tokens max(0,pos-W+1)..pos, read from
+ *          win_kv[b][t mod win_cap]; every row is both key and value (MQA);
+ *   p_r  = exp(scale q_h.row_r) / (exp(sink[h]) + sum_r' exp(scale q_h.row_r'))
+ *   out[b][i][h] = RoPE(sum_r p_r row_r, -pos)   (bf16)
+ *   lse[b][i][h] = log(exp(sink[h]) + sum_r exp(scale q_h.row_r))   (fp32, optional)
+ * q [batch][n_q][H][c] bf16; gamma_q [c] fp32; sink [H] fp32; out [batch][n_q][H][c] bf16.
+ * Rows in the caches already carry RMSNorm and RoPE at their own positions.
+ * Supported: c in {128, 256, 512}, H <= 64, W <= 4096.
+ * The workspace holds split-K partial results; its size comes from *_attend_workspace.
+ * ------------------------------------------------------------------------------- */
+size_t csa_attend_workspace(const lca_attn_params *p, int batch, int n_q);
+size_t hca_attend_workspace(const lca_attn_params *p, int batch, int n_q, int64_t cache_rows);
+lca_status csa_attend(const lca_attn_params *p, int batch, int n_q,
+                      const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                      const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                      const int32_t *idx,
+                      const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                      const float *sink, lca_bf16 *out, float *lse,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+lca_status hca_attend(const lca_attn_params *p, int batch, int n_q,
+                      const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                      const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                      const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                      const float *sink, lca_bf16 *out, float *lse,
+                      void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Grouped output projection ([P1] CSA step four): the H heads of each token are split
+ * into `groups` groups of H/groups heads; group g is projected by Wg[g] (d_g rows of
+ * (H/groups)*c) to d_g values, the groups' results are concatenated (bf16, in `mid`)
+ * and projected by Wm (d_model rows of groups*d_g) to y.
+ *   o   [batch][H*c] bf16;  Wg [groups*d_g][(H/groups)*c] bf16;  Wm [d_model][groups*d_g];
+ *   mid [batch][groups*d_g] bf16 (caller-owned scratch);  y [batch][d_model] bf16.
+ * Supported: batch <= 16, every row length a multiple of 8.
+ * lca_gemm_bf16 is the plain product it is built from: C[M][N] = A[M][K] . B[N][K]^T
+ * (fp32 accumulation, bf16 out), M <= 16 (activations), B the weight rows.
+ * ------------------------------------------------------------------------------- */
+lca_status lca_grouped_oproj(int batch, int heads, int head_dim, int groups, int d_g, int d_model,
+                             const lca_bf16 *o, const lca_bf16 *Wg, const lca_bf16 *Wm,
+                             lca_bf16 *mid, lca_bf16 *y, cudaStream_t stream);
+lca_status lca_gemm_bf16(int M, int N, int K, const lca_bf16 *A, int64_t lda,
+                         const lca_bf16 *B, int64_t ldb, lca_bf16 *C, int64_t ldc,
+                         cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
+ * Diagnostics.
+ * ------------------------------------------------------------------------------- */
+const char *lca_status_string(lca_status s);
+/* Description of the last failure on the calling thread ("" if none). */
+const char *lca_last_error(void);
+/* Waits for `stream`, then reads and clears the device error word of the current device
+ * into *word (LCA_DEVERR_* bits).  Returns LCA_ERR_TIMEOUT if a timeout bit is set,
+ * LCA_ERR_DEVICE for any other bit, LCA_OK when the word is zero. */
+lca_status lca_device_error(cudaStream_t stream, uint32_t *word);
+/* Library version string. */
+const char *lca_version(void);
+
+#if defined(__GNUC__)
+#pragma GCC visibility pop
+#endif
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LCA_H */

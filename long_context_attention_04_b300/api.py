@@ -1,0 +1,255 @@
+"""Python binding of liblca with the C ABI's names: argument marshalling only.
+
+Every function takes torch CUDA tensors (torch provides the memory and the stream), checks
+dtypes and layouts, and passes raw pointers, strides and sizes to the library; all
+arithmetic runs in the library's CUDA kernels.  A failure status raises LcaError with the
+library's message.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+
+import torch
+
+from . import _lib
+
+
+class LcaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("lca status %d: %s" % (status, message))
+        self.status = status
+
+
+@dataclasses.dataclass
+class AttnParams:
+    """Mirror of lca_attn_params (names follow the pages' notation)."""
+    heads: int = 64
+    head_dim: int = 512
+    rope_dims: int = 64
+    rope_base: float = 10000.0
+    rms_eps: float = 1e-6
+    softmax_scale: float = 0.0      # 0 -> 1/sqrt(head_dim)
+    window: int = 128
+    ratio: int = 4
+    topk: int = 512
+    idx_heads: int = 64
+    idx_dim: int = 128
+
+    def c(self) -> _lib.lca_attn_params:
+        return _lib.lca_attn_params(self.heads, self.head_dim, self.rope_dims, self.rope_base, self.rms_eps,
+                                    self.softmax_scale, self.window, self.ratio, self.topk, self.idx_heads,
+                                    self.idx_dim)
+
+    @property
+    def scale(self) -> float:
+        return self.softmax_scale if self.softmax_scale > 0 else 1.0 / math.sqrt(self.head_dim)
+
+
+def params_from(shape, **over) -> AttnParams:
+    """AttnParams from any object with the same field names (e.g. a workload's layer shape)."""
+    kw = {f.name: getattr(shape, f.name) for f in dataclasses.fields(AttnParams) if hasattr(shape, f.name)}
+    kw.update(over)
+    return AttnParams(**kw)
+
+
+def _check(status: int):
+    if status != 0:
+        lib = _lib.load()
+        raise LcaError(status, lib.lca_last_error().decode())
+
+
+def _ptr(t: torch.Tensor | None, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _rows(t: torch.Tensor, name: str) -> int:
+    """Batch stride (elements) of a [B, rows, width] tensor whose rows are dense."""
+    if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != t.shape[2]:
+        raise ValueError("%s must be [B, rows, width] with dense rows" % name)
+    return t.stride(0)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _i32(t, name):
+    if t.dtype != torch.int32 or not t.is_contiguous():
+        raise TypeError("%s must be a contiguous int32 tensor" % name)
+    return _ptr(t, torch.int32, name)
+
+
+def _compress(fn, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache, stream):
+    B, n_tok, width = tok_v.shape
+    if tok_z.dim() != 2 or tok_z.stride(1) != 1 or tok_z.shape[0] != B:
+        raise ValueError("tok_z must be [B, n_tok] with unit inner stride")
+    if cache.shape[0] != B or cache.shape[2] != width:
+        raise ValueError("cache must be [B, rows, width]")
+    st = fn(ctypes.byref(p.c()), B, width,
+            _ptr(tok_v, torch.bfloat16, "tok_v"), _rows(tok_v, "tok_v"), n_tok,
+            _ptr(tok_z, torch.float32, "tok_z"), tok_z.stride(0), _i32(tok_pos0, "tok_pos0"),
+            _ptr(pos_bias, torch.float32, "pos_bias"), _ptr(gamma, torch.float32, "gamma"), int(apply_rope),
+            _i32(first_entry, "first_entry"), int(n_new),
+            _ptr(cache, torch.bfloat16, "cache"), _rows(cache, "cache"), cache.shape[1], _stream(stream))
+    _check(st)
+
+
+def csa_compress_kv(p: AttnParams, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new,
+                    cache, stream=None):
+    """CSA compression (windows of 2m, stride m) of entries first_entry[b] .. +n_new into cache."""
+    _compress(_lib.load().csa_compress_kv, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope,
+              first_entry, n_new, cache, stream)
+
+
+def hca_compress_kv(p: AttnParams, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new,
+                    cache, stream=None):
+    """HCA compression (non-overlapping windows of m') of entries first_entry[b] .. +n_new into cache."""
+    _compress(_lib.load().hca_compress_kv, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope,
+              first_entry, n_new, cache, stream)
+
+
+def lca_window_update(p: AttnParams, tok_v, tok_pos0, gamma, win_kv, stream=None):
+    """Write RoPE(RMSNorm(v)*gamma, pos) of each token to ring row pos mod win_cap."""
+    B, n_tok, _ = tok_v.shape
+    st = _lib.load().lca_window_update(
+        ctypes.byref(p.c()), B, _ptr(tok_v, torch.bfloat16, "tok_v"), _rows(tok_v, "tok_v"), n_tok,
+        _i32(tok_pos0, "tok_pos0"), _ptr(gamma, torch.float32, "gamma"),
+        _ptr(win_kv, torch.bfloat16, "win_kv"), _rows(win_kv, "win_kv"), win_kv.shape[1], _stream(stream))
+    _check(st)
+
+
+def _idx_q(q_idx, w_idx, p):
+    if q_idx.dim() != 4 or not q_idx.is_contiguous():
+        raise ValueError("q_idx must be a contiguous [B, n_q, H_I, d_I] tensor")
+    B, n_q, hi, di = q_idx.shape
+    if (hi, di) != (p.idx_heads, p.idx_dim):
+        raise ValueError("q_idx heads/dim do not match params")
+    if tuple(w_idx.shape) != (B, n_q, hi) or not w_idx.is_contiguous():
+        raise ValueError("w_idx must be a contiguous [B, n_q, H_I] tensor")
+    return B, n_q
+
+
+def csa_indexer_scores(p: AttnParams, q_idx, w_idx, k_cache, q_pos, scores, stream=None):
+    """scores[b, i, j] = sum_h w[b,i,h] ReLU(q[b,i,h] . k[b,j]) for j < n_vis(i), -inf beyond."""
+    B, n_q = _idx_q(q_idx, w_idx, p)
+    if scores.dim() != 3 or scores.stride(2) != 1 or scores.stride(1) != scores.shape[2] or \
+            scores.stride(0) != n_q * scores.shape[2]:
+        raise ValueError("scores must be a dense [B, n_q, stride] tensor")
+    st = _lib.load().csa_indexer_scores(
+        ctypes.byref(p.c()), B, n_q, _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w_idx, torch.float32, "w_idx"),
+        _ptr(k_cache, torch.bfloat16, "k_cache"), _rows(k_cache, "k_cache"), k_cache.shape[1],
+        _i32(q_pos, "q_pos"), _ptr(scores, torch.float32, "scores"), scores.shape[2], _stream(stream))
+    _check(st)
+
+
+def lca_topk(p: AttnParams, scores, q_pos, max_entries, out_idx, stream=None):
+    """Top-k (score desc, index asc), ascending indices, -1 padded, per query row of scores."""
+    B, n_q, stride = scores.shape
+    if tuple(out_idx.shape) != (B, n_q, p.topk):
+        raise ValueError("out_idx must be [B, n_q, topk]")
+    st = _lib.load().lca_topk(ctypes.byref(p.c()), B, n_q, _ptr(scores, torch.float32, "scores"), stride,
+                              _i32(q_pos, "q_pos"), int(max_entries), _i32(out_idx, "out_idx"), _stream(stream))
+    _check(st)
+
+
+def csa_indexer_workspace(p: AttnParams, batch: int, n_q: int, cache_rows: int) -> int:
+    return int(_lib.load().csa_indexer_workspace(ctypes.byref(p.c()), batch, n_q, cache_rows))
+
+
+def csa_indexer_topk(p: AttnParams, q_idx, w_idx, k_cache, q_pos, out_idx, workspace, stream=None):
+    """Indexer scores into the workspace, then top-k into out_idx [B, n_q, k]."""
+    B, n_q = _idx_q(q_idx, w_idx, p)
+    st = _lib.load().csa_indexer_topk(
+        ctypes.byref(p.c()), B, n_q, _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w_idx, torch.float32, "w_idx"),
+        _ptr(k_cache, torch.bfloat16, "k_cache"), _rows(k_cache, "k_cache"), k_cache.shape[1],
+        _i32(q_pos, "q_pos"), _i32(out_idx, "out_idx"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+
+
+def csa_attend_workspace(p: AttnParams, batch: int, n_q: int) -> int:
+    return int(_lib.load().csa_attend_workspace(ctypes.byref(p.c()), batch, n_q))
+
+
+def hca_attend_workspace(p: AttnParams, batch: int, n_q: int, cache_rows: int) -> int:
+    return int(_lib.load().hca_attend_workspace(ctypes.byref(p.c()), batch, n_q, cache_rows))
+
+
+def _attend_common(q, p):
+    if q.dim() != 4 or not q.is_contiguous() or tuple(q.shape[2:]) != (p.heads, p.head_dim):
+        raise ValueError("q must be a contiguous [B, n_q, H, c] tensor matching params")
+    return q.shape[0], q.shape[1]
+
+
+def csa_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse=None,
+               stream=None):
+    """Core attention over kv_cache[idx] plus the window rows (see include/lca.h)."""
+    B, n_q = _attend_common(q, p)
+    if tuple(idx.shape) != (B, n_q, p.topk):
+        raise ValueError("idx must be [B, n_q, topk]")
+    st = _lib.load().csa_attend(
+        ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
+        _i32(q_pos, "q_pos"), _ptr(kv_cache, torch.bfloat16, "kv_cache"), _rows(kv_cache, "kv_cache"),
+        kv_cache.shape[1], _i32(idx, "idx"), _ptr(win_kv, torch.bfloat16, "win_kv"), _rows(win_kv, "win_kv"),
+        win_kv.shape[1], _ptr(sink, torch.float32, "sink"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+
+
+def hca_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None, stream=None):
+    """Dense core attention over the visible entries of kv_cache plus the window rows."""
+    B, n_q = _attend_common(q, p)
+    st = _lib.load().hca_attend(
+        ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
+        _i32(q_pos, "q_pos"), _ptr(kv_cache, torch.bfloat16, "kv_cache"), _rows(kv_cache, "kv_cache"),
+        kv_cache.shape[1], _ptr(win_kv, torch.bfloat16, "win_kv"), _rows(win_kv, "win_kv"), win_kv.shape[1],
+        _ptr(sink, torch.float32, "sink"), _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+
+
+def lca_grouped_oproj(o, Wg, Wm, groups: int, mid, y, stream=None):
+    """y = Wm . concat_g(Wg[g] . o_g) for o [B, H, c]; mid [B, groups*d_g] is scratch."""
+    B, H, c = o.shape
+    d_g = Wg.shape[0] // groups
+    d_model = Wm.shape[0]
+    for t, n in ((o, "o"), (Wg, "Wg"), (Wm, "Wm"), (mid, "mid"), (y, "y")):
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % n)
+    st = _lib.load().lca_grouped_oproj(B, H, c, groups, d_g, d_model, _ptr(o, torch.bfloat16, "o"),
+                                       _ptr(Wg, torch.bfloat16, "Wg"), _ptr(Wm, torch.bfloat16, "Wm"),
+                                       _ptr(mid, torch.bfloat16, "mid"), _ptr(y, torch.bfloat16, "y"),
+                                       _stream(stream))
+    _check(st)
+
+
+def lca_gemm_bf16(A, B, C, stream=None):
+    """C[M, N] = A[M, K] . B[N, K]^T (bf16 in/out, fp32 accumulation)."""
+    M, K = A.shape
+    N = B.shape[0]
+    st = _lib.load().lca_gemm_bf16(M, N, K, _ptr(A, torch.bfloat16, "A"), A.stride(0),
+                                   _ptr(B, torch.bfloat16, "B"), B.stride(0), _ptr(C, torch.bfloat16, "C"),
+                                   C.stride(0), _stream(stream))
+    _check(st)
+
+
+def lca_device_error(stream=None) -> int:
+    """Synchronise the stream, read and clear the device error word; returns the word."""
+    w = ctypes.c_uint32(0)
+    _lib.load().lca_device_error(_stream(stream), ctypes.byref(w))
+    return int(w.value)
+
+
+def lca_version() -> str:
+    return _lib.load().lca_version().decode()

@@ -1,0 +1,233 @@
+// attend_common.cuh -- pieces shared by the core-attention kernels: the key-row list of a
+// query (compressed rows + window rows), the split of that list across CTAs, the query
+// prologue (RMSNorm + RoPE), and the split-K combine with the sink and the output RoPE(-i).
+//
+// DeepSeek-V4 hybrid attention (gxgjx.lffhtl.com/lxrt/355279.html, section 混肃穆力机制):
+// CSA step three (Multi-Query Attention over the top-k compressed blocks), HCA (dense
+// attention over all compressed entries), and the tricks list: Q/KV normalization,
+// Partial RoPE with the output rotated at -i, the sliding-window branch over the most
+// recent uncompressed tokens, and the attention sink in the softmax denominator.
+// [P4] zhinnengdao.top section 3.1: one learnable sink logit per head.
+#pragma once
+
+#include "common.cuh"
+
+namespace lca {
+
+// Everything an attention kernel needs about one call.
+struct AttendArgs {
+    int H, C, R;                  // heads, head dim, rope dims
+    float rope_base, eps;
+    float scale_log2;             // softmax scale * log2(e): logits are kept in base 2
+    int W;                        // window tokens
+    int ratio;                    // m' for the dense (HCA) row list
+    int n_idx;                    // k for the gathered (CSA) row list; 0 selects dense
+    int n_q;                      // queries per sequence
+    int splits;                   // CTAs per query
+    const __nv_bfloat16 *q;       // [B][n_q][H][C]
+    const float *gamma_q;         // [C]
+    const int32_t *q_pos;         // [B][n_q]
+    const __nv_bfloat16 *kv; int64_t kv_bs; int64_t cache_rows;
+    const int32_t *idx;           // [B][n_q][n_idx] or nullptr
+    const __nv_bfloat16 *win; int64_t win_bs; int win_cap;
+    const float *sink;            // [H]
+    // split-K partials: O [unit][split][H][C] fp32 (unnormalised), m/l [unit][split][H] (base 2)
+    float *part_o, *part_m, *part_l;
+    __nv_bfloat16 *out;           // [B][n_q][H][C]
+    float *lse;                   // [B][n_q][H] or nullptr
+};
+
+// The row list of one query: n_comp compressed rows (CSA: idx list, HCA: entries 0..n_vis)
+// followed by n_win window rows (tokens win_begin .. pos).
+struct RowList {
+    int64_t pos;
+    int64_t n_comp;
+    int64_t win_begin;
+    int n_win;
+    const int32_t *idx;              // CSA list for this query, or nullptr (dense)
+    const __nv_bfloat16 *kv;         // this sequence's compressed cache
+    const __nv_bfloat16 *win;        // this sequence's window ring
+    __device__ __forceinline__ int64_t total() const { return n_comp + n_win; }
+};
+
+__device__ __forceinline__ RowList make_row_list(const AttendArgs &a, int b, int qi) {
+    RowList L;
+    L.pos = a.q_pos[(int64_t)b * a.n_q + qi];
+    if (L.pos < 0) {
+        raise_error(LCA_DEVERR_NEGATIVE_POS);
+        L.pos = -1;
+    }
+    L.kv = a.kv + (int64_t)b * a.kv_bs;
+    L.win = a.win + (int64_t)b * a.win_bs;
+    if (a.n_idx > 0) {
+        L.idx = a.idx + ((int64_t)b * a.n_q + qi) * a.n_idx;
+        L.n_comp = a.n_idx;
+    } else {
+        L.idx = nullptr;
+        int64_t n_vis = (L.pos + 1) / a.ratio;
+        if (n_vis > a.cache_rows) {
+            raise_error(LCA_DEVERR_VISIBLE_RANGE);
+            n_vis = a.cache_rows;
+        }
+        L.n_comp = n_vis;
+    }
+    L.win_begin = L.pos - a.W + 1 < 0 ? 0 : L.pos - a.W + 1;
+    L.n_win = (int)(L.pos - L.win_begin + 1);
+    return L;
+}
+
+// Source of row r of the list, or nullptr when the row is masked (idx == -1 or out of range).
+__device__ __forceinline__ const __nv_bfloat16 *row_source(const AttendArgs &a, const RowList &L, int64_t r,
+                                                            bool report) {
+    if (r < L.n_comp) {
+        int64_t j = L.idx ? (int64_t)L.idx[r] : r;
+        if (j < 0) return nullptr;
+        if (j >= a.cache_rows) {
+            if (report) raise_error(LCA_DEVERR_INDEX_RANGE);
+            return nullptr;
+        }
+        return L.kv + j * a.C;
+    }
+    if (r < L.total()) {
+        const int64_t t = L.win_begin + (r - L.n_comp);
+        return L.win + (t % a.win_cap) * a.C;
+    }
+    return nullptr;
+}
+
+// Tiles [t0, t1) of `tile_rows` rows handled by split s of S.
+__device__ __forceinline__ void split_range(int64_t n_rows, int tile_rows, int s, int S, int64_t &t0, int64_t &t1) {
+    const int64_t T = (n_rows + tile_rows - 1) / tile_rows;
+    t0 = T * s / S;
+    t1 = T * (s + 1) / S;
+}
+
+// Query prologue for head h (one warp): RMSNorm over C with gamma_q, then RoPE(pos) on the
+// trailing R dims.  Lane l holds elements [l*EPL, l*EPL+EPL) in v[] on return.
+template <int C>
+__device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const __nv_bfloat16 *qh, int64_t pos,
+                                           float *v) {
+    constexpr int EPL = C / 32;   // elements per lane (4, 8 or 16)
+    const int lane = threadIdx.x & 31;
+    const uint4 *src = reinterpret_cast<const uint4 *>(qh + lane * EPL);
+#pragma unroll
+    for (int u = 0; u < EPL / 8; ++u) unpack8(__ldg(src + u), v + 8 * u);
+    float ss = 0.f;
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) ss += v[u] * v[u];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / (float)C + a.eps);
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) v[u] = v[u] * inv * __ldg(a.gamma_q + lane * EPL + u);
+    if (a.R > 0) {
+        const int half = a.R / 2, first = C - a.R;
+        const int hl = half / EPL;        // lanes per half (R/2 is a multiple of EPL)
+        const int lane0 = first / EPL;
+        const bool in_rope = lane >= lane0;
+        const bool lower = lane < lane0 + hl;
+        const int partner = lower ? lane + hl : lane - hl;
+#pragma unroll
+        for (int u = 0; u < EPL; ++u) {
+            const float other = __shfl_sync(0xffffffffu, v[u], in_rope ? partner : lane);
+            if (in_rope) {
+                const int e = lane * EPL + u;
+                const int d = lower ? e - first : e - first - half;
+                float cs, sn;
+                rope_angle((double)pos, d, a.R, (double)a.rope_base, cs, sn);
+                v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
+            }
+        }
+    }
+}
+
+// Specialisation helper for C = 128 (4 elements per lane: one 8-byte load).
+template <>
+__device__ __forceinline__ void q_hat_warp<128>(const AttendArgs &a, const __nv_bfloat16 *qh, int64_t pos,
+                                                float *v) {
+    constexpr int C = 128, EPL = 4;
+    const int lane = threadIdx.x & 31;
+    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(qh + lane * EPL));
+    v[0] = bf16_lo(raw.x); v[1] = bf16_hi(raw.x); v[2] = bf16_lo(raw.y); v[3] = bf16_hi(raw.y);
+    float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+    ss = warp_sum(ss);
+    const float inv = rsqrtf(ss / (float)C + a.eps);
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) v[u] = v[u] * inv * __ldg(a.gamma_q + lane * EPL + u);
+    if (a.R > 0) {
+        const int half = a.R / 2, first = C - a.R;
+        const int hl = half / EPL, lane0 = first / EPL;
+        const bool in_rope = lane >= lane0;
+        const bool lower = lane < lane0 + hl;
+        const int partner = lower ? lane + hl : lane - hl;
+#pragma unroll
+        for (int u = 0; u < EPL; ++u) {
+            const float other = __shfl_sync(0xffffffffu, v[u], in_rope ? partner : lane);
+            if (in_rope) {
+                const int e = lane * EPL + u;
+                const int d = lower ? e - first : e - first - half;
+                float cs, sn;
+                rope_angle((double)pos, d, a.R, (double)a.rope_base, cs, sn);
+                v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
+            }
+        }
+    }
+}
+
+constexpr int kCombineThreads = 256;
+
+// Split-K combine: one CTA per (unit, head).  Merges the splits' (m, l, O) with the sink,
+// normalises, rotates the trailing R dims by -pos and stores bf16 (+ lse).
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttendArgs a) {
+    extern __shared__ float cw[];     // [splits] weights, then the row [C]
+    const int64_t unit = blockIdx.x;
+    const int h = blockIdx.y;
+    const int S = a.splits;
+    float *wts = cw;
+    float *row = cw + ((S + 3) & ~3);
+    __shared__ float Lsh;
+    const int64_t pos = a.q_pos[unit] < 0 ? 0 : a.q_pos[unit];
+    if (threadIdx.x == 0) {
+        const float sink2 = a.sink[h] * kLog2e;
+        float M = sink2;
+        for (int s = 0; s < S; ++s) {
+            const float l = a.part_l[(unit * S + s) * a.H + h];
+            if (l > 0.f) M = fmaxf(M, a.part_m[(unit * S + s) * a.H + h]);
+        }
+        float L = exp2f(sink2 - M);
+        for (int s = 0; s < S; ++s) {
+            const float l = a.part_l[(unit * S + s) * a.H + h];
+            const float w = l > 0.f ? exp2f(a.part_m[(unit * S + s) * a.H + h] - M) : 0.f;
+            wts[s] = w;
+            L += w * l;
+        }
+        Lsh = L;
+        if (a.lse) a.lse[unit * a.H + h] = (M + log2f(L)) * kLn2;
+    }
+    __syncthreads();
+    const float invL = 1.f / Lsh;
+    for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
+        float acc = 0.f;
+        for (int s = 0; s < S; ++s) {
+            const float w = wts[s];
+            if (w != 0.f) acc = fmaf(w, a.part_o[((unit * S + s) * a.H + h) * a.C + i], acc);
+        }
+        row[i] = acc * invL;
+    }
+    __syncthreads();
+    if (a.R > 0) {
+        const int half = a.R / 2, first = a.C - a.R;
+        for (int d = threadIdx.x; d < half; d += blockDim.x) {
+            float cs, sn;
+            rope_angle(-(double)pos, d, a.R, (double)a.rope_base, cs, sn);
+            const float x = row[first + d], y = row[first + d + half];
+            row[first + d] = x * cs - y * sn;
+            row[first + d + half] = x * sn + y * cs;
+        }
+    }
+    __syncthreads();
+    __nv_bfloat16 *dst = a.out + (unit * a.H + h) * a.C;
+    for (int k = threadIdx.x; k < a.C / 8; k += blockDim.x)
+        reinterpret_cast<uint4 *>(dst)[k] = pack8(row + 8 * k);
+}
+
+}  // namespace lca

@@ -1,0 +1,96 @@
+// common.cuh -- device helpers shared by the kernels of liblca (bf16 packing, the device
+// error word, block reductions, RoPE angles).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/lca.h"
+
+namespace lca {
+
+// One error word per device (the library is a single translation unit).  Kernels OR
+// LCA_DEVERR_* bits into it; lca_device_error() reads and clears it.
+__device__ unsigned int g_error_word;
+
+__device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_error_word, bits); }
+
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Round two fp32 values to bf16 (round to nearest even) and pack them (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Unpack 8 bf16 values held in a 16-byte vector.
+__device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float *f) {
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// Sum over the whole block (blockDim.x a multiple of 32, <= 1024); every thread gets it.
+__device__ __forceinline__ float block_sum(float v, float *scratch32) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_sum(v);
+    __syncthreads();
+    if (lane == 0) scratch32[warp] = v;
+    __syncthreads();
+    float t = lane < nw ? scratch32[lane] : 0.f;
+    return warp_sum(t);
+}
+
+__device__ __forceinline__ float block_max(float v, float *scratch32) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    v = warp_max(v);
+    __syncthreads();
+    if (lane == 0) scratch32[warp] = v;
+    __syncthreads();
+    float t = lane < nw ? scratch32[lane] : -INFINITY;
+    return warp_max(t);
+}
+
+// cos/sin of the RoPE angle of pair d at position pos: angle = pos * base^(-2d/R).
+// The product is formed and reduced modulo 2*pi in double (positions reach 2^20 and
+// beyond, where an fp32 product would lose the angle), then evaluated in fp32.
+__device__ __forceinline__ void rope_angle(double pos, int d, int R, double base, float &cs, float &sn) {
+    double inv_freq = pow(base, -2.0 * (double)d / (double)R);
+    double a = remainder(pos * inv_freq, kTwoPi);
+    sincosf((float)a, &sn, &cs);
+}
+
+// Order-preserving map of a float to uint32 (larger float -> larger key); -0 maps like +0.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+    if (f == 0.0f) f = 0.0f;
+    uint32_t u = __float_as_uint(f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__host__ __device__ __forceinline__ int64_t ceil_div64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+}  // namespace lca

@@ -1,0 +1,532 @@
+// lca.cu -- the C ABI of liblca (declared in include/lca.h): host-side validation, work
+// planning and kernel launches.  The library is built as one translation unit so that the
+// device error word is a single object per device.
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/lca.h"
+#include "common.cuh"
+#include "compress.cuh"
+#include "topk.cuh"
+#include "indexer_simt.cuh"
+#include "attend_common.cuh"
+#include "attend_simt.cuh"
+#include "gemv.cuh"
+
+using namespace lca;
+
+namespace {
+
+thread_local std::string t_last_error;
+
+lca_status fail(lca_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    t_last_error = buf;
+    return s;
+}
+
+lca_status ok() {
+    t_last_error.clear();
+    return LCA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
+
+lca_status check_launch(const char *what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+    return LCA_OK;
+}
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+    return n;
+}
+
+#define LCA_REQUIRE(cond, status, ...) \
+    do {                                \
+        if (!(cond)) return fail(status, __VA_ARGS__); \
+    } while (0)
+
+RowNormRope make_nr(const lca_attn_params *p, const float *gamma, int apply_rope) {
+    RowNormRope nr;
+    nr.gamma = gamma;
+    nr.eps = p->rms_eps;
+    nr.rope_dims = apply_rope ? p->rope_dims : 0;
+    nr.rope_base = p->rope_base;
+    return nr;
+}
+
+lca_status compress_impl(const char *name, bool overlap, const lca_attn_params *p, int batch, int width,
+                         const lca_bf16 *tok_v, int64_t tok_v_bs, int n_tok, const float *tok_z,
+                         int64_t tok_z_bs, const int32_t *tok_pos0, const float *pos_bias,
+                         const float *gamma, int apply_rope, const int32_t *first_entry, int n_new,
+                         lca_bf16 *cache, int64_t cache_bs, int64_t cache_rows, cudaStream_t stream) {
+    LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
+    LCA_REQUIRE(batch > 0 && n_tok > 0 && n_new >= 0, LCA_ERR_INVALID_ARG,
+                "%s: batch (%d) and n_tok (%d) must be positive, n_new (%d) >= 0", name, batch, n_tok, n_new);
+    LCA_REQUIRE(width >= 8 && width <= kMaxRowWidth && width % 8 == 0, LCA_ERR_UNSUPPORTED,
+                "%s: width %d must be a multiple of 8 in [8, %d]", name, width, kMaxRowWidth);
+    LCA_REQUIRE(p->ratio > 0, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
+    const int span = overlap ? 2 * p->ratio : p->ratio;
+    LCA_REQUIRE(span <= kMaxSpan, LCA_ERR_UNSUPPORTED, "%s: window of %d tokens exceeds %d", name, span, kMaxSpan);
+    LCA_REQUIRE(tok_v && tok_z && tok_pos0 && pos_bias && first_entry && cache, LCA_ERR_INVALID_ARG,
+                "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(tok_v) && aligned16(cache), LCA_ERR_INVALID_ARG,
+                "%s: tok_v and cache must be 16-byte aligned", name);
+    LCA_REQUIRE(tok_v_bs % 8 == 0 && cache_bs % 8 == 0, LCA_ERR_INVALID_ARG,
+                "%s: batch strides must be multiples of 8 elements", name);
+    LCA_REQUIRE(batch == 1 || (tok_v_bs >= (int64_t)n_tok * width && tok_z_bs >= n_tok &&
+                               cache_bs >= cache_rows * width),
+                LCA_ERR_INVALID_ARG, "%s: batch strides smaller than one sequence", name);
+    LCA_REQUIRE(cache_rows > 0, LCA_ERR_INVALID_ARG, "%s: cache_rows must be positive", name);
+    if (apply_rope)
+        LCA_REQUIRE(p->rope_dims > 0 && p->rope_dims % 2 == 0 && p->rope_dims <= width, LCA_ERR_INVALID_ARG,
+                    "%s: rope_dims %d must be even and in (0, width]", name, p->rope_dims);
+    if (n_new == 0) return ok();
+    CompressArgs a;
+    a.span = span;
+    a.stride = p->ratio;
+    a.width = width;
+    a.tok_v = reinterpret_cast<const __nv_bfloat16 *>(tok_v);
+    a.tok_v_bs = tok_v_bs;
+    a.n_tok = n_tok;
+    a.tok_z = tok_z;
+    a.tok_z_bs = tok_z_bs;
+    a.tok_pos0 = tok_pos0;
+    a.bias = pos_bias;
+    a.first_entry = first_entry;
+    a.n_new = n_new;
+    a.cache = reinterpret_cast<__nv_bfloat16 *>(cache);
+    a.cache_bs = cache_bs;
+    a.cache_rows = cache_rows;
+    a.nr = make_nr(p, gamma, apply_rope);
+    compress_kernel<<<dim3(n_new, batch), kRowThreads, 0, stream>>>(a);
+    lca_status s = check_launch(name);
+    return s == LCA_OK ? ok() : s;
+}
+
+// ---- attention planning ----
+struct AttendPlan {
+    int splits;
+    int64_t units;
+    size_t part_bytes;       // O partials
+    size_t ml_bytes;         // m and l partials
+    size_t total;
+};
+
+constexpr int kPlanTileRows = kSimtTile;
+
+AttendPlan plan_attend(const lca_attn_params *p, int batch, int n_q, int64_t max_rows) {
+    AttendPlan pl;
+    pl.units = (int64_t)batch * n_q;
+    const int64_t tiles = ceil_div64(max_rows, kPlanTileRows);
+    const int sms = device_sm_count();
+    int64_t s = ceil_div64(sms, pl.units);
+    if (s > tiles) s = tiles;
+    if (s < 1) s = 1;
+    if (s > 64) s = 64;
+    pl.splits = (int)s;
+    pl.part_bytes = (size_t)pl.units * pl.splits * p->heads * p->head_dim * sizeof(float);
+    pl.ml_bytes = (size_t)pl.units * pl.splits * p->heads * sizeof(float);
+    pl.total = pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255);
+    return pl;
+}
+
+lca_status attend_validate(const char *name, const lca_attn_params *p, int batch, int n_q) {
+    LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
+    LCA_REQUIRE(batch > 0 && n_q > 0, LCA_ERR_INVALID_ARG, "%s: batch and n_q must be positive", name);
+    LCA_REQUIRE(p->head_dim == 128 || p->head_dim == 256 || p->head_dim == 512, LCA_ERR_UNSUPPORTED,
+                "%s: head_dim %d not in {128, 256, 512}", name, p->head_dim);
+    LCA_REQUIRE(p->heads >= 1 && p->heads <= 64, LCA_ERR_UNSUPPORTED, "%s: heads %d not in [1, 64]", name, p->heads);
+    const int epl = p->head_dim / 32;
+    LCA_REQUIRE(p->rope_dims >= 0 && p->rope_dims <= p->head_dim && p->rope_dims % 2 == 0 &&
+                    (p->rope_dims / 2) % epl == 0,
+                LCA_ERR_UNSUPPORTED, "%s: rope_dims %d must be even, <= c and R/2 a multiple of c/32", name,
+                p->rope_dims);
+    LCA_REQUIRE(p->window >= 1 && p->window <= 4096, LCA_ERR_UNSUPPORTED, "%s: window %d not in [1, 4096]", name,
+                p->window);
+    return LCA_OK;
+}
+
+lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q,
+                       const float *gamma_q, const int32_t *q_pos, const lca_bf16 *kv, int64_t kv_bs,
+                       int64_t cache_rows, const int32_t *idx, const lca_bf16 *win, int64_t win_bs,
+                       int win_cap, const float *sink, lca_bf16 *out, float *lse, void *ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+    lca_status st = attend_validate(name, p, batch, n_q);
+    if (st != LCA_OK) return st;
+    const bool csa = idx != nullptr;
+    if (csa) LCA_REQUIRE(p->topk >= 1, LCA_ERR_INVALID_ARG, "%s: topk must be positive", name);
+    else LCA_REQUIRE(p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
+    LCA_REQUIRE(q && gamma_q && q_pos && kv && win && sink && out, LCA_ERR_INVALID_ARG,
+                "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(q) && aligned16(kv) && aligned16(win) && aligned16(out), LCA_ERR_INVALID_ARG,
+                "%s: q, kv_cache, win_kv and out must be 16-byte aligned", name);
+    LCA_REQUIRE(kv_bs % 8 == 0 && win_bs % 8 == 0, LCA_ERR_INVALID_ARG,
+                "%s: batch strides must be multiples of 8 elements", name);
+    LCA_REQUIRE(cache_rows > 0, LCA_ERR_INVALID_ARG, "%s: cache_rows must be positive", name);
+    LCA_REQUIRE(win_cap >= p->window, LCA_ERR_INVALID_ARG, "%s: win_cap %d < window %d", name, win_cap, p->window);
+    LCA_REQUIRE(batch == 1 || (kv_bs >= cache_rows * p->head_dim && win_bs >= (int64_t)win_cap * p->head_dim),
+                LCA_ERR_INVALID_ARG, "%s: batch strides smaller than one sequence", name);
+    const int64_t max_rows = (csa ? p->topk : cache_rows) + p->window;
+    AttendPlan pl = plan_attend(p, batch, n_q, max_rows);
+    LCA_REQUIRE(ws && aligned16(ws) && ws_bytes >= pl.total, LCA_ERR_WORKSPACE,
+                "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu", name, pl.total, ws_bytes);
+    AttendArgs a;
+    a.H = p->heads;
+    a.C = p->head_dim;
+    a.R = p->rope_dims;
+    a.rope_base = p->rope_base;
+    a.eps = p->rms_eps;
+    const float scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf((float)p->head_dim);
+    a.scale_log2 = scale * kLog2e;
+    a.W = p->window;
+    a.ratio = p->ratio;
+    a.n_idx = csa ? p->topk : 0;
+    a.n_q = n_q;
+    a.splits = pl.splits;
+    a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
+    a.gamma_q = gamma_q;
+    a.q_pos = q_pos;
+    a.kv = reinterpret_cast<const __nv_bfloat16 *>(kv);
+    a.kv_bs = kv_bs;
+    a.cache_rows = cache_rows;
+    a.idx = idx;
+    a.win = reinterpret_cast<const __nv_bfloat16 *>(win);
+    a.win_bs = win_bs;
+    a.win_cap = win_cap;
+    a.sink = sink;
+    char *w = static_cast<char *>(ws);
+    a.part_o = reinterpret_cast<float *>(w);
+    a.part_m = reinterpret_cast<float *>(w + pl.part_bytes);
+    a.part_l = reinterpret_cast<float *>(w + pl.part_bytes + ((pl.ml_bytes + 255) & ~(size_t)255));
+    a.out = reinterpret_cast<__nv_bfloat16 *>(out);
+    a.lse = lse;
+    LCA_REQUIRE(pl.units <= 0x7fffffff, LCA_ERR_UNSUPPORTED, "%s: too many queries", name);
+    dim3 grid((unsigned)pl.units, pl.splits);
+    switch (p->head_dim) {
+    case 128: {
+        size_t smem = sizeof(SimtSmem<128>);
+        cudaFuncSetAttribute(attend_simt_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attend_simt_kernel<128><<<grid, kSimtThreads, smem, stream>>>(a);
+        break;
+    }
+    case 256: {
+        size_t smem = sizeof(SimtSmem<256>);
+        cudaFuncSetAttribute(attend_simt_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attend_simt_kernel<256><<<grid, kSimtThreads, smem, stream>>>(a);
+        break;
+    }
+    default: {
+        size_t smem = sizeof(SimtSmem<512>);
+        cudaFuncSetAttribute(attend_simt_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attend_simt_kernel<512><<<grid, kSimtThreads, smem, stream>>>(a);
+        break;
+    }
+    }
+    st = check_launch(name);
+    if (st != LCA_OK) return st;
+    const size_t csmem = (size_t)(((pl.splits + 3) & ~3) + p->head_dim) * sizeof(float);
+    combine_kernel<<<dim3((unsigned)pl.units, p->heads), kCombineThreads, csmem, stream>>>(a);
+    st = check_launch(name);
+    return st == LCA_OK ? ok() : st;
+}
+
+lca_status indexer_validate(const char *name, const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q_idx,
+                            const float *w_idx, const lca_bf16 *k_cache, int64_t k_bs, int64_t cache_rows,
+                            const int32_t *q_pos) {
+    LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
+    LCA_REQUIRE(batch > 0 && n_q > 0 && cache_rows > 0, LCA_ERR_INVALID_ARG,
+                "%s: batch, n_q and cache_rows must be positive", name);
+    LCA_REQUIRE(p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
+    LCA_REQUIRE(p->idx_heads >= 1 && p->idx_heads <= 64 && p->idx_dim >= 8 && p->idx_dim <= 256 &&
+                    p->idx_dim % 8 == 0,
+                LCA_ERR_UNSUPPORTED, "%s: indexer heads %d / dim %d unsupported", name, p->idx_heads, p->idx_dim);
+    LCA_REQUIRE(q_idx && w_idx && k_cache && q_pos, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(q_idx) && aligned16(k_cache), LCA_ERR_INVALID_ARG,
+                "%s: q_idx and k_cache must be 16-byte aligned", name);
+    LCA_REQUIRE(k_bs % 8 == 0 && (batch == 1 || k_bs >= cache_rows * p->idx_dim), LCA_ERR_INVALID_ARG,
+                "%s: bad k_batch_stride", name);
+    return LCA_OK;
+}
+
+lca_status indexer_launch(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q_idx, const float *w_idx,
+                          const lca_bf16 *k_cache, int64_t k_bs, int64_t cache_rows, const int32_t *q_pos,
+                          float *scores, int64_t s_stride, cudaStream_t stream) {
+    IndexerArgs a;
+    a.HI = p->idx_heads;
+    a.DI = p->idx_dim;
+    a.ratio = p->ratio;
+    a.n_q = n_q;
+    a.q = reinterpret_cast<const __nv_bfloat16 *>(q_idx);
+    a.w = w_idx;
+    a.k = reinterpret_cast<const __nv_bfloat16 *>(k_cache);
+    a.k_bs = k_bs;
+    a.cache_rows = cache_rows;
+    a.q_pos = q_pos;
+    a.scores = scores;
+    a.s_stride = s_stride;
+    const size_t smem = (size_t)(a.HI * a.DI + a.HI + a.DI * kIdxSimtRows) * sizeof(float);
+    cudaFuncSetAttribute(indexer_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    dim3 grid((unsigned)ceil_div64(cache_rows, kIdxSimtRows), n_q, batch);
+    indexer_simt_kernel<<<grid, kIdxSimtRows, smem, stream>>>(a);
+    return check_launch("csa_indexer_scores");
+}
+
+lca_status topk_launch(const lca_attn_params *p, int batch, int n_q, const float *scores, int64_t s_stride,
+                       const int32_t *q_pos, int64_t max_entries, int32_t *out_idx, cudaStream_t stream) {
+    TopkArgs a;
+    a.scores = scores;
+    a.row_stride = s_stride;
+    a.q_pos = q_pos;
+    a.ratio = p->ratio;
+    a.max_entries = max_entries;
+    a.k = p->topk;
+    a.out = out_idx;
+    topk_kernel<<<(unsigned)((int64_t)batch * n_q), kTopkThreads, 0, stream>>>(a);
+    return check_launch("lca_topk");
+}
+
+size_t indexer_ws_bytes(int batch, int n_q, int64_t cache_rows) {
+    const int64_t stride = (cache_rows + 3) & ~(int64_t)3;
+    return (size_t)batch * n_q * stride * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *lca_version(void) { return "lca 0.1 (sm_103a)"; }
+
+const char *lca_status_string(lca_status s) {
+    switch (s) {
+    case LCA_OK: return "ok";
+    case LCA_ERR_INVALID_ARG: return "invalid argument";
+    case LCA_ERR_UNSUPPORTED: return "unsupported shape";
+    case LCA_ERR_WORKSPACE: return "workspace too small";
+    case LCA_ERR_CUDA: return "CUDA error";
+    case LCA_ERR_TIMEOUT: return "kernel wait timed out";
+    case LCA_ERR_DEVICE: return "device-side check failed";
+    }
+    return "unknown status";
+}
+
+const char *lca_last_error(void) { return t_last_error.c_str(); }
+
+lca_status lca_device_error(cudaStream_t stream, uint32_t *word) {
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_device_error: %s", cudaGetErrorString(e));
+    unsigned int w = 0, zero = 0;
+    e = cudaMemcpyFromSymbol(&w, g_error_word, sizeof w);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof zero);
+    if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_device_error: %s", cudaGetErrorString(e));
+    if (word) *word = w;
+    if (w & LCA_DEVERR_TIMEOUT) return fail(LCA_ERR_TIMEOUT, "a bounded wait inside a kernel ran out (0x%x)", w);
+    if (w) return fail(LCA_ERR_DEVICE, "device-side check failed (0x%x)", w);
+    return ok();
+}
+
+lca_status csa_compress_kv(const lca_attn_params *p, int batch, int width, const lca_bf16 *tok_v,
+                           int64_t tok_v_batch_stride, int n_tok, const float *tok_z, int64_t tok_z_batch_stride,
+                           const int32_t *tok_pos0, const float *pos_bias, const float *gamma, int apply_rope,
+                           const int32_t *first_entry, int n_new, lca_bf16 *cache, int64_t cache_batch_stride,
+                           int64_t cache_rows, cudaStream_t stream) {
+    return compress_impl("csa_compress_kv", true, p, batch, width, tok_v, tok_v_batch_stride, n_tok, tok_z,
+                         tok_z_batch_stride, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache,
+                         cache_batch_stride, cache_rows, stream);
+}
+
+lca_status hca_compress_kv(const lca_attn_params *p, int batch, int width, const lca_bf16 *tok_v,
+                           int64_t tok_v_batch_stride, int n_tok, const float *tok_z, int64_t tok_z_batch_stride,
+                           const int32_t *tok_pos0, const float *pos_bias, const float *gamma, int apply_rope,
+                           const int32_t *first_entry, int n_new, lca_bf16 *cache, int64_t cache_batch_stride,
+                           int64_t cache_rows, cudaStream_t stream) {
+    return compress_impl("hca_compress_kv", false, p, batch, width, tok_v, tok_v_batch_stride, n_tok, tok_z,
+                         tok_z_batch_stride, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache,
+                         cache_batch_stride, cache_rows, stream);
+}
+
+lca_status lca_window_update(const lca_attn_params *p, int batch, const lca_bf16 *tok_v, int64_t tok_v_batch_stride,
+                             int n_tok, const int32_t *tok_pos0, const float *gamma, lca_bf16 *win_kv,
+                             int64_t win_batch_stride, int win_cap, cudaStream_t stream) {
+    const char *name = "lca_window_update";
+    LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
+    const int width = p->head_dim;
+    LCA_REQUIRE(batch > 0 && n_tok >= 0 && win_cap > 0, LCA_ERR_INVALID_ARG,
+                "%s: batch and win_cap must be positive", name);
+    LCA_REQUIRE(width >= 8 && width <= kMaxRowWidth && width % 8 == 0, LCA_ERR_UNSUPPORTED,
+                "%s: head_dim %d unsupported", name, width);
+    LCA_REQUIRE(tok_v && tok_pos0 && gamma && win_kv, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(tok_v) && aligned16(win_kv) && tok_v_batch_stride % 8 == 0 && win_batch_stride % 8 == 0,
+                LCA_ERR_INVALID_ARG, "%s: misaligned pointer or stride", name);
+    LCA_REQUIRE(p->rope_dims >= 0 && p->rope_dims % 2 == 0 && p->rope_dims <= width, LCA_ERR_INVALID_ARG,
+                "%s: bad rope_dims", name);
+    if (n_tok == 0) return ok();
+    WindowArgs a;
+    a.width = width;
+    a.tok_v = reinterpret_cast<const __nv_bfloat16 *>(tok_v);
+    a.tok_v_bs = tok_v_batch_stride;
+    a.n_tok = n_tok;
+    a.tok_pos0 = tok_pos0;
+    a.win = reinterpret_cast<__nv_bfloat16 *>(win_kv);
+    a.win_bs = win_batch_stride;
+    a.win_cap = win_cap;
+    a.nr = make_nr(p, gamma, p->rope_dims > 0);
+    window_kernel<<<dim3(n_tok, batch), kRowThreads, 0, stream>>>(a);
+    lca_status s = check_launch(name);
+    return s == LCA_OK ? ok() : s;
+}
+
+lca_status csa_indexer_scores(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q_idx,
+                              const float *w_idx, const lca_bf16 *k_cache, int64_t k_batch_stride,
+                              int64_t cache_rows, const int32_t *q_pos, float *scores, int64_t scores_stride,
+                              cudaStream_t stream) {
+    const char *name = "csa_indexer_scores";
+    lca_status st = indexer_validate(name, p, batch, n_q, q_idx, w_idx, k_cache, k_batch_stride, cache_rows, q_pos);
+    if (st != LCA_OK) return st;
+    LCA_REQUIRE(scores && aligned16(scores) && scores_stride >= cache_rows && scores_stride % 4 == 0,
+                LCA_ERR_INVALID_ARG, "%s: scores must be 16-byte aligned with a stride >= cache_rows, %% 4", name);
+    st = indexer_launch(p, batch, n_q, q_idx, w_idx, k_cache, k_batch_stride, cache_rows, q_pos, scores,
+                        scores_stride, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+lca_status lca_topk(const lca_attn_params *p, int batch, int n_q, const float *scores, int64_t scores_stride,
+                    const int32_t *q_pos, int64_t max_entries, int32_t *out_idx, cudaStream_t stream) {
+    const char *name = "lca_topk";
+    LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
+    LCA_REQUIRE(batch > 0 && n_q > 0 && max_entries >= 0, LCA_ERR_INVALID_ARG, "%s: bad sizes", name);
+    LCA_REQUIRE(p->topk >= 1 && p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: topk and ratio must be positive", name);
+    LCA_REQUIRE(scores && q_pos && out_idx, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned4(scores) && scores_stride >= max_entries, LCA_ERR_INVALID_ARG,
+                "%s: scores_stride must be >= max_entries", name);
+    lca_status st = topk_launch(p, batch, n_q, scores, scores_stride, q_pos, max_entries, out_idx, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+size_t csa_indexer_workspace(const lca_attn_params *p, int batch, int n_q, int64_t cache_rows) {
+    (void)p;
+    if (batch <= 0 || n_q <= 0 || cache_rows <= 0) return 0;
+    return indexer_ws_bytes(batch, n_q, cache_rows);
+}
+
+lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q_idx, const float *w_idx,
+                            const lca_bf16 *k_cache, int64_t k_batch_stride, int64_t cache_rows,
+                            const int32_t *q_pos, int32_t *out_idx, void *workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+    const char *name = "csa_indexer_topk";
+    lca_status st = indexer_validate(name, p, batch, n_q, q_idx, w_idx, k_cache, k_batch_stride, cache_rows, q_pos);
+    if (st != LCA_OK) return st;
+    LCA_REQUIRE(p->topk >= 1, LCA_ERR_INVALID_ARG, "%s: topk must be positive", name);
+    LCA_REQUIRE(out_idx, LCA_ERR_INVALID_ARG, "%s: out_idx is NULL", name);
+    const size_t need = indexer_ws_bytes(batch, n_q, cache_rows);
+    LCA_REQUIRE(workspace && aligned16(workspace) && workspace_bytes >= need, LCA_ERR_WORKSPACE,
+                "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu", name, need, workspace_bytes);
+    const int64_t stride = (cache_rows + 3) & ~(int64_t)3;
+    float *scores = static_cast<float *>(workspace);
+    st = indexer_launch(p, batch, n_q, q_idx, w_idx, k_cache, k_batch_stride, cache_rows, q_pos, scores, stride,
+                        stream);
+    if (st != LCA_OK) return st;
+    st = topk_launch(p, batch, n_q, scores, stride, q_pos, cache_rows, out_idx, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+size_t csa_attend_workspace(const lca_attn_params *p, int batch, int n_q) {
+    if (!p || batch <= 0 || n_q <= 0 || p->topk < 1) return 0;
+    return plan_attend(p, batch, n_q, (int64_t)p->topk + p->window).total;
+}
+
+size_t hca_attend_workspace(const lca_attn_params *p, int batch, int n_q, int64_t cache_rows) {
+    if (!p || batch <= 0 || n_q <= 0 || cache_rows <= 0) return 0;
+    return plan_attend(p, batch, n_q, cache_rows + p->window).total;
+}
+
+lca_status csa_attend(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                      const int32_t *q_pos, const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                      const int32_t *idx, const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                      const float *sink, lca_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
+                      cudaStream_t stream) {
+    if (!idx) return fail(LCA_ERR_INVALID_ARG, "csa_attend: idx is NULL");
+    return attend_impl("csa_attend", p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride, cache_rows, idx,
+                       win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream);
+}
+
+lca_status hca_attend(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                      const int32_t *q_pos, const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                      const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap, const float *sink,
+                      lca_bf16 *out, float *lse, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return attend_impl("hca_attend", p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride, cache_rows, nullptr,
+                       win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream);
+}
+
+static lca_status gemv_launch(const char *name, int M, int N, int K, const lca_bf16 *A, int64_t lda, int64_t a_off,
+                              const lca_bf16 *B, int64_t ldb, int64_t b_off, lca_bf16 *C, int64_t ldc, int64_t c_off,
+                              int batches, cudaStream_t stream) {
+    GemvArgs a;
+    a.M = M;
+    a.N = N;
+    a.K = K;
+    a.A = reinterpret_cast<const __nv_bfloat16 *>(A);
+    a.lda = lda;
+    a.a_batch_off = a_off;
+    a.B = reinterpret_cast<const __nv_bfloat16 *>(B);
+    a.ldb = ldb;
+    a.b_batch_off = b_off;
+    a.C = reinterpret_cast<__nv_bfloat16 *>(C);
+    a.ldc = ldc;
+    a.c_batch_off = c_off;
+    const int rows_per_block = (kGemvThreads / 32) * kGemvRowsPerWarp;
+    dim3 grid((unsigned)ceil_div64(N, rows_per_block), batches);
+    if (M <= 1) gemv_kernel<1><<<grid, kGemvThreads, 0, stream>>>(a);
+    else if (M <= 2) gemv_kernel<2><<<grid, kGemvThreads, 0, stream>>>(a);
+    else if (M <= 4) gemv_kernel<4><<<grid, kGemvThreads, 0, stream>>>(a);
+    else if (M <= 8) gemv_kernel<8><<<grid, kGemvThreads, 0, stream>>>(a);
+    else gemv_kernel<16><<<grid, kGemvThreads, 0, stream>>>(a);
+    return check_launch(name);
+}
+
+lca_status lca_gemm_bf16(int M, int N, int K, const lca_bf16 *A, int64_t lda, const lca_bf16 *B, int64_t ldb,
+                         lca_bf16 *C, int64_t ldc, cudaStream_t stream) {
+    const char *name = "lca_gemm_bf16";
+    LCA_REQUIRE(M >= 1 && M <= 16 && N >= 1 && K >= 8 && K % 8 == 0, LCA_ERR_UNSUPPORTED,
+                "%s: need 1 <= M <= 16, N >= 1, K a positive multiple of 8 (M=%d N=%d K=%d)", name, M, N, K);
+    LCA_REQUIRE(A && B && C, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(A) && aligned16(B) && lda % 8 == 0 && ldb % 8 == 0 && lda >= K && ldb >= K && ldc >= N,
+                LCA_ERR_INVALID_ARG, "%s: A and B must be 16-byte aligned with strides >= K, multiples of 8", name);
+    lca_status st = gemv_launch(name, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+lca_status lca_grouped_oproj(int batch, int heads, int head_dim, int groups, int d_g, int d_model, const lca_bf16 *o,
+                             const lca_bf16 *Wg, const lca_bf16 *Wm, lca_bf16 *mid, lca_bf16 *y,
+                             cudaStream_t stream) {
+    const char *name = "lca_grouped_oproj";
+    LCA_REQUIRE(batch >= 1 && batch <= 16, LCA_ERR_UNSUPPORTED, "%s: batch %d not in [1, 16]", name, batch);
+    LCA_REQUIRE(heads >= 1 && groups >= 1 && heads % groups == 0 && head_dim >= 1 && d_g >= 1 && d_model >= 1,
+                LCA_ERR_INVALID_ARG, "%s: heads must divide into groups", name);
+    const int64_t in_g = (int64_t)(heads / groups) * head_dim;
+    LCA_REQUIRE(in_g % 8 == 0 && ((int64_t)groups * d_g) % 8 == 0 && d_g % 8 == 0, LCA_ERR_UNSUPPORTED,
+                "%s: group input and output widths must be multiples of 8", name);
+    LCA_REQUIRE(o && Wg && Wm && mid && y, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(o) && aligned16(Wg) && aligned16(Wm) && aligned16(mid), LCA_ERR_INVALID_ARG,
+                "%s: o, Wg, Wm and mid must be 16-byte aligned", name);
+    const int64_t hc = (int64_t)heads * head_dim;
+    const int64_t gd = (int64_t)groups * d_g;
+    lca_status st = gemv_launch(name, batch, d_g, (int)in_g, o, hc, in_g, Wg, in_g, (int64_t)d_g * in_g, mid, gd, d_g,
+                                groups, stream);
+    if (st != LCA_OK) return st;
+    st = gemv_launch(name, batch, d_model, (int)gd, mid, gd, 0, Wm, gd, 0, y, d_model, 0, 1, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+}  // extern "C"

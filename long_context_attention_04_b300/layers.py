@@ -1,0 +1,97 @@
+"""Per-layer orchestration of the attention path: the order of the C-ABI calls of one CSA or
+HCA layer step, over device buffers the caller (or the layer object) owns.
+
+The order follows the pages' description of a layer (DeepSeek-V4 hybrid attention,
+gxgjx.lffhtl.com/lxrt/355279.html section 混肃穆力机制): compress the block the new token
+completes (CSA step one / HCA), refresh the window ring with the new token's row, score and
+select entries (CSA step two), run the core attention with window and sink (CSA step three /
+HCA), and, in a full block, the grouped output projection (CSA step four).  No arithmetic
+happens here; every step is a library call.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+from . import api
+from .api import AttnParams
+
+
+@dataclasses.dataclass
+class LayerWeights:
+    gamma_kv: torch.Tensor        # [c] fp32
+    gamma_q: torch.Tensor         # [c] fp32
+    bias_kv: torch.Tensor         # [2m] (CSA) or [m'] (HCA) fp32
+    sink: torch.Tensor            # [H] fp32
+    bias_idx: torch.Tensor | None = None   # [2m] fp32 (CSA only)
+
+
+class CsaLayer:
+    """One CSA layer for B sequences: KV cache [B, rows, c], indexer keys [B, rows, d_I],
+    window ring [B, win_cap, c], plus the index buffer and workspaces of a step of n_q queries."""
+
+    def __init__(self, p: AttnParams, weights: LayerWeights, kv_cache, idx_cache, win_kv, n_q: int = 1):
+        self.p = p
+        self.w = weights
+        self.kv_cache, self.idx_cache, self.win_kv = kv_cache, idx_cache, win_kv
+        B, rows = kv_cache.shape[:2]
+        dev = kv_cache.device
+        self.idx = torch.empty((B, n_q, p.topk), dtype=torch.int32, device=dev)
+        self.ws_idx = torch.empty(api.csa_indexer_workspace(p, B, n_q, rows), dtype=torch.uint8, device=dev)
+        self.ws_att = torch.empty(api.csa_attend_workspace(p, B, n_q), dtype=torch.uint8, device=dev)
+
+    def compress(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, stream=None):
+        """Compress n_new entries per sequence into both caches (KV: RMSNorm + RoPE; keys: neither)."""
+        api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
+                            n_new, self.kv_cache, stream)
+        api.csa_compress_kv(self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
+                            self.idx_cache, stream)
+
+    def window(self, new_tok_v, new_pos0, stream=None):
+        api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, stream)
+
+    def select(self, q_idx, w_idx, q_pos, stream=None):
+        api.csa_indexer_topk(self.p, q_idx, w_idx, self.idx_cache, q_pos, self.idx, self.ws_idx, stream)
+        return self.idx
+
+    def attend(self, q, q_pos, out, lse=None, stream=None):
+        api.csa_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.idx, self.win_kv, self.w.sink, out,
+                       self.ws_att, lse, stream)
+
+    def step(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, new_tok_v, new_pos0,
+             q, q_idx, w_idx, q_pos, out, stream=None):
+        if n_new:
+            self.compress(tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, stream)
+        self.window(new_tok_v, new_pos0, stream)
+        self.select(q_idx, w_idx, q_pos, stream)
+        self.attend(q, q_pos, out, stream=stream)
+
+
+class HcaLayer:
+    """One HCA layer for B sequences: KV cache [B, rows, c] and window ring [B, win_cap, c]."""
+
+    def __init__(self, p: AttnParams, weights: LayerWeights, kv_cache, win_kv, n_q: int = 1):
+        self.p = p
+        self.w = weights
+        self.kv_cache, self.win_kv = kv_cache, win_kv
+        B, rows = kv_cache.shape[:2]
+        self.ws_att = torch.empty(api.hca_attend_workspace(p, B, n_q, rows), dtype=torch.uint8,
+                                  device=kv_cache.device)
+
+    def compress(self, tok_v, tok_z, tok_pos0, first_entry, n_new, stream=None):
+        api.hca_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
+                            n_new, self.kv_cache, stream)
+
+    def window(self, new_tok_v, new_pos0, stream=None):
+        api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, stream)
+
+    def attend(self, q, q_pos, out, lse=None, stream=None):
+        api.hca_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.win_kv, self.w.sink, out,
+                       self.ws_att, lse, stream)
+
+    def step(self, tok_v, tok_z, tok_pos0, first_entry, n_new, new_tok_v, new_pos0, q, q_pos, out, stream=None):
+        if n_new:
+            self.compress(tok_v, tok_z, tok_pos0, first_entry, n_new, stream)
+        self.window(new_tok_v, new_pos0, stream)
+        self.attend(q, q_pos, out, stream=stream)

@@ -1,0 +1,284 @@
+"""GPU parity of every step of the path against the CPU oracle, through the C ABI.
+
+Sizes are small enough for the oracle to finish in seconds but span several 128-row tiles
+and end in a ragged tail.  Tolerances: attention outputs max |err| <= 2e-2 * RMS(oracle);
+stored rows within bf16 rounding; top-k sets equal except at near-ties (1e-5 relative).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import (assert_close_rms, bf16_to_f64, check_topk, f32, oracle_attend_batch, u16)
+from long_context_attention_04_b300 import api, build as lca_build
+from long_context_attention_04_b300.api import AttnParams
+from workloads import Rng, bits_to_bf16
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lca_build.build()
+    api.lca_device_error()   # clear any stale device error bits
+    yield
+
+
+def dev(t):
+    return t.to(DEV)
+
+
+def assert_rows_close(got_bf16, ref, what=""):
+    """A stored bf16 row equals the oracle's fp64 row up to bf16 rounding (+ fp32 arithmetic)."""
+    got = bf16_to_f64(got_bf16)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    bound = 2.0 ** -8 * np.abs(ref) + 2e-3 * rms
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), "%s: worst %.3e at %s" % (what, float((err - bound).max()), np.argmax(err - bound))
+
+
+# ------------------------------------------------------------------ compress -------
+
+@pytest.mark.parametrize("overlap,ratio,width,rope,norm", [
+    (True, 4, 512, True, True),      # CSA KV entries
+    (True, 4, 128, False, False),    # CSA indexer keys
+    (False, 128, 512, True, True),   # HCA KV entries
+    (False, 8, 256, True, True),
+])
+def test_compress_matches_oracle(overlap, ratio, width, rope, norm):
+    rng = Rng(10)
+    B = 3
+    span = 2 * ratio if overlap else ratio
+    n_tok = 6 * ratio + (ratio if overlap else 0)
+    p = AttnParams(heads=8, head_dim=width, rope_dims=64, ratio=ratio)
+    tok_v = rng.normal_bf16((B, n_tok, width))
+    tok_z = rng.normal_f32((B, n_tok))
+    bias = rng.normal_f32((span,), 0.5)
+    gamma = (0.5 + torch.rand(width, generator=rng.g)).float()
+    # sequence 0 starts at position 0 (entry 0's window is clipped); the others deep in a sequence
+    pos0 = [0, 40 * ratio, 3000 * ratio]
+    first = [0 if p0 == 0 else p0 // ratio + (1 if overlap else 0) for p0 in pos0]
+    n_new = 6
+    rows = max(first) + n_new + 3
+    cache = torch.zeros((B, rows, width), dtype=torch.bfloat16)
+    cache_d = dev(cache)
+    fn = api.csa_compress_kv if overlap else api.hca_compress_kv
+    fn(p, dev(tok_v), dev(tok_z), dev(torch.tensor(pos0, dtype=torch.int32)), dev(bias),
+       dev(gamma) if norm else None, rope, dev(torch.tensor(first, dtype=torch.int32)), n_new, cache_d)
+    assert api.lca_device_error() == 0
+    got = cache_d.cpu()
+    for b in range(B):
+        ref = oracle.compress(u16(tok_v[b]), f32(tok_z[b]), pos0[b], f32(bias), f32(gamma) if norm else None,
+                              p.rms_eps, 64 if rope else 0, p.rope_base, span, ratio, first[b], n_new)
+        assert_rows_close(got[b, first[b]:first[b] + n_new], ref, "compress b=%d" % b)
+        # rows outside the written range stay untouched
+        assert (got[b, :first[b]] == 0).all() and (got[b, first[b] + n_new:] == 0).all()
+
+
+def test_compress_missing_tokens_sets_device_error_and_skips():
+    rng = Rng(11)
+    p = AttnParams(head_dim=128, ratio=4)
+    tok_v = dev(rng.normal_bf16((1, 8, 128)))
+    cache = torch.zeros((1, 10, 128), dtype=torch.bfloat16, device=DEV)
+    # entry 3 needs tokens 8..15 but the staging holds 0..7
+    api.csa_compress_kv(p, tok_v, dev(rng.normal_f32((1, 8))), dev(torch.tensor([0], dtype=torch.int32)),
+                        dev(torch.zeros(8)), None, 0, dev(torch.tensor([3], dtype=torch.int32)), 1, cache)
+    assert api.lca_device_error() & 0x1
+    assert (cache == 0).all()
+    assert api.lca_device_error() == 0     # read clears it
+
+
+def test_window_update_matches_oracle():
+    rng = Rng(12)
+    B, n_tok, c, cap = 2, 5, 512, 8
+    p = AttnParams(head_dim=c, rope_dims=64)
+    tok_v = rng.normal_bf16((B, n_tok, c))
+    gamma = (0.5 + torch.rand(c, generator=rng.g)).float()
+    pos0 = [6, 1048570]          # wraps around the ring of 8
+    win = torch.zeros((B, cap, c), dtype=torch.bfloat16, device=DEV)
+    api.lca_window_update(p, dev(tok_v), dev(torch.tensor(pos0, dtype=torch.int32)), dev(gamma), win)
+    got = win.cpu()
+    for b in range(B):
+        for t in range(n_tok):
+            pos = pos0[b] + t
+            ref = oracle.window_row(u16(tok_v[b, t]), f32(gamma), p.rms_eps, 64, p.rope_base, pos)
+            assert_rows_close(got[b, pos % cap], ref, "window b=%d pos=%d" % (b, pos))
+
+
+# ------------------------------------------------------------ indexer + top-k -------
+
+@pytest.mark.parametrize("HI,DI,rows,k", [(64, 128, 1000, 100), (4, 32, 300, 64), (32, 64, 777, 512)])
+def test_indexer_scores_and_topk_match_oracle(HI, DI, rows, k):
+    rng = Rng(13)
+    B, n_q, m = 2, 3, 4
+    p = AttnParams(idx_heads=HI, idx_dim=DI, ratio=m, topk=k)
+    q = rng.normal_bf16((B, n_q, HI, DI))
+    w = rng.normal_f32((B, n_q, HI), 1.0 / math.sqrt(HI))
+    keys = rng.normal_bf16((B, rows, DI))
+    # visible entries: all rows, a ragged middle, fewer than k, and zero
+    pos = torch.tensor([[m * rows - 1, m * 517 + 2, m * (k // 2) - 1],
+                        [m * rows + 50, m * 128 - 1, 0]], dtype=torch.int32)
+    stride = (rows + 3) // 4 * 4
+    scores = torch.full((B, n_q, stride), 7.0, device=DEV)
+    api.csa_indexer_scores(p, dev(q), dev(w), dev(keys), dev(pos), scores)
+    err = api.lca_device_error()
+    assert err == 0x4   # position (rows + 50) sees more entries than the cache holds: clamped, reported
+    out_idx = torch.empty((B, n_q, k), dtype=torch.int32, device=DEV)
+    api.lca_topk(p, scores, dev(pos), rows, out_idx)
+    assert api.lca_device_error() == 0x4
+    s_gpu = scores.cpu().numpy()
+    i_gpu = out_idx.cpu().numpy()
+    for b in range(B):
+        for i in range(n_q):
+            n_vis = min(oracle.visible_entries(int(pos[b, i]), m), rows)
+            ref = oracle.indexer_scores(u16(q[b, i]), f32(w[b, i]), u16(keys[b]), n_vis)
+            got = s_gpu[b, i, :n_vis].astype(np.float64)
+            scale = max(np.abs(ref).max(), 1e-30) if n_vis else 1.0
+            np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-5 * scale)
+            assert np.isneginf(s_gpu[b, i, n_vis:rows]).all()
+            check_topk(i_gpu[b, i], ref, k, "b=%d i=%d" % (b, i))
+    # the combined call gives the same lists
+    ws = torch.empty(api.csa_indexer_workspace(p, B, n_q, rows), dtype=torch.uint8, device=DEV)
+    out2 = torch.empty_like(out_idx)
+    api.csa_indexer_topk(p, dev(q), dev(w), dev(keys), dev(pos), out2, ws)
+    api.lca_device_error()
+    assert torch.equal(out2, out_idx)
+
+
+@pytest.mark.parametrize("n,k", [(5000, 300), (262144, 1024), (1023, 1024), (32768, 512)])
+def test_topk_exact_on_given_scores_with_ties(n, k):
+    """Scores given (not computed): the GPU selection must equal the oracle's exactly, ties included."""
+    g = np.random.default_rng(14)
+    rows = []
+    rows.append(g.integers(-20, 20, n).astype(np.float32))           # heavy ties
+    rows.append(np.zeros(n, np.float32))                              # all equal
+    r = g.standard_normal(n).astype(np.float32)
+    r[g.integers(0, n, n // 10)] = np.sort(r)[-k] if n > k else 0.0   # ties at the boundary
+    rows.append(r)
+    rows.append(-np.abs(g.standard_normal(n)).astype(np.float32))    # all negative, with -0.0
+    rows[-1][::7] = -0.0
+    rows[-1][3::7] = 0.0
+    S = np.stack(rows)[None]                   # [1, 4, n]
+    stride = (n + 3) // 4 * 4
+    Sp = np.full((1, 4, stride), -np.inf, np.float32)
+    Sp[..., :n] = S
+    p = AttnParams(topk=k, ratio=1)
+    pos = torch.full((1, 4), n - 1, dtype=torch.int32)
+    out = torch.empty((1, 4, k), dtype=torch.int32, device=DEV)
+    api.lca_topk(p, dev(torch.from_numpy(Sp)), dev(pos), n, out)
+    got = out.cpu().numpy()
+    for r in range(4):
+        np.testing.assert_array_equal(got[0, r], oracle.topk(S[0, r].astype(np.float64), k))
+
+
+# ------------------------------------------------------------------- attention -------
+
+def _attend_inputs(rng, B, n_q, H, c, rows, W, cap):
+    return dict(
+        q=rng.normal_bf16((B, n_q, H, c)),
+        kv=rng.normal_bf16((B, rows, c)),
+        win=rng.normal_bf16((B, cap, c)),
+        gamma=(0.5 + torch.rand(c, generator=rng.g)).float(),
+        sink=rng.normal_f32((H,)),
+    )
+
+
+@pytest.mark.parametrize("H,c,R,W", [(64, 512, 64, 128), (8, 128, 64, 16), (16, 256, 32, 40), (1, 512, 64, 128)])
+def test_hca_attend_matches_oracle(H, c, R, W):
+    rng = Rng(15)
+    B, n_q, m, rows = 3, 2, 4, 700
+    cap = W + 8
+    p = AttnParams(heads=H, head_dim=c, rope_dims=R, window=W, ratio=m)
+    d = _attend_inputs(rng, B, n_q, H, c, rows, W, cap)
+    # visible entries: 650 (ragged), 700 (all), 1 (tiny), 0 with a short window, deep positions
+    pos = torch.tensor([[m * 650 - 1, m * 700 - 1], [4, 0], [m * 333 + 1, m * 129 - 2]], dtype=torch.int32)
+    out = torch.empty((B, n_q, H, c), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, n_q, H), dtype=torch.float32, device=DEV)
+    ws = torch.empty(api.hca_attend_workspace(p, B, n_q, rows), dtype=torch.uint8, device=DEV)
+    api.hca_attend(p, dev(d["q"]), dev(d["gamma"]), dev(pos), dev(d["kv"]), dev(d["win"]), dev(d["sink"]), out,
+                   ws, lse)
+    assert api.lca_device_error() == 0
+    ref = oracle_attend_batch(p, d["q"], d["gamma"], pos, d["kv"], d["win"], d["sink"])
+    o = out.cpu().float().numpy()
+    l = lse.cpu().numpy()
+    for (b, i), (ro, rl) in ref.items():
+        assert_close_rms(o[b, i], ro, what="hca b=%d i=%d" % (b, i))
+        np.testing.assert_allclose(l[b, i], rl, rtol=0, atol=2e-3 * max(1.0, np.abs(rl).max()))
+
+
+@pytest.mark.parametrize("H,c,k,W", [(64, 512, 512, 128), (8, 128, 64, 16), (64, 512, 300, 1)])
+def test_csa_attend_with_injected_indices_matches_oracle(H, c, k, W):
+    rng = Rng(16)
+    B, n_q, rows = 2, 2, 3000
+    cap = W + 5
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=4, topk=k)
+    d = _attend_inputs(rng, B, n_q, H, c, rows, W, cap)
+    g = np.random.default_rng(17)
+    idx = np.full((B, n_q, k), -1, np.int32)
+    counts = [[k, k - 37], [k // 3, 0]]
+    for b in range(B):
+        for i in range(n_q):
+            sel = np.sort(g.choice(rows, counts[b][i], replace=False))
+            idx[b, i, :len(sel)] = sel
+    idx_t = torch.from_numpy(idx)
+    pos = torch.tensor([[4 * rows - 1, 9000], [3, 700]], dtype=torch.int32)
+    out = torch.empty((B, n_q, H, c), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, n_q, H), dtype=torch.float32, device=DEV)
+    ws = torch.empty(api.csa_attend_workspace(p, B, n_q), dtype=torch.uint8, device=DEV)
+    api.csa_attend(p, dev(d["q"]), dev(d["gamma"]), dev(pos), dev(d["kv"]), dev(idx_t), dev(d["win"]),
+                   dev(d["sink"]), out, ws, lse)
+    assert api.lca_device_error() == 0
+    ref = oracle_attend_batch(p, d["q"], d["gamma"], pos, d["kv"], d["win"], d["sink"], idx=idx_t)
+    o = out.cpu().float().numpy()
+    l = lse.cpu().numpy()
+    for (b, i), (ro, rl) in ref.items():
+        assert_close_rms(o[b, i], ro, what="csa b=%d i=%d" % (b, i))
+        np.testing.assert_allclose(l[b, i], rl, rtol=0, atol=2e-3 * max(1.0, np.abs(rl).max()))
+
+
+def test_attend_reports_out_of_range_indices():
+    rng = Rng(18)
+    p = AttnParams(heads=8, head_dim=128, window=4, ratio=4, topk=8)
+    d = _attend_inputs(rng, 1, 1, 8, 128, 50, 4, 4)
+    idx = torch.tensor([[[0, 1, 2, 60, -1, -1, -1, -1]]], dtype=torch.int32)
+    out = torch.empty((1, 1, 8, 128), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(api.csa_attend_workspace(p, 1, 1), dtype=torch.uint8, device=DEV)
+    api.csa_attend(p, dev(d["q"]), dev(d["gamma"]), dev(torch.tensor([[10]], dtype=torch.int32)), dev(d["kv"]),
+                   dev(idx), dev(d["win"]), dev(d["sink"]), out, ws)
+    assert api.lca_device_error() & 0x2
+    # the bad index is skipped: same as the list without it
+    ref = oracle_attend_batch(p, d["q"], d["gamma"], torch.tensor([[10]]), d["kv"], d["win"], d["sink"],
+                              idx=torch.tensor([[[0, 1, 2, -1, -1, -1, -1, -1]]], dtype=torch.int32))
+    assert_close_rms(out.cpu().float().numpy()[0, 0], ref[(0, 0)][0], what="skip bad index")
+
+
+# ------------------------------------------------------------- output projection ----
+
+def test_grouped_oproj_matches_oracle():
+    rng = Rng(19)
+    B, H, c, G, d_g, d = 4, 64, 512, 8, 1024, 4096
+    o = rng.normal_bf16((B, H, c))
+    Wg = rng.normal_bf16((G * d_g, (H // G) * c), 0.02)
+    Wm = rng.normal_bf16((d, G * d_g), 0.02)
+    mid = torch.empty((B, G * d_g), dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((B, d), dtype=torch.bfloat16, device=DEV)
+    api.lca_grouped_oproj(dev(o), dev(Wg), dev(Wm), G, mid, y)
+    got = y.cpu().float().numpy()
+    for b in range(B):
+        ref = oracle.grouped_oproj(u16(o[b]), u16(Wg), u16(Wm), G)
+        assert_close_rms(got[b], ref, what="oproj b=%d" % b)
+
+
+def test_gemm_matches_oracle():
+    rng = Rng(20)
+    for M, N, K in ((1, 37, 64), (4, 1000, 256), (16, 515, 4096), (3, 8, 8)):
+        A = rng.normal_bf16((M, K))
+        Bm = rng.normal_bf16((N, K))
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+        api.lca_gemm_bf16(dev(A), dev(Bm), C)
+        ref = oracle.gemm_bf16(u16(A), u16(Bm))
+        assert_close_rms(C.cpu().float().numpy(), ref, tol=1e-2, what="gemm %dx%dx%d" % (M, N, K))
