@@ -33,6 +33,7 @@ struct AttendArgs {
     const float *sink;            // [H]
     // split-K partials: O [unit][split][H][C] fp32 (unnormalised), m/l [unit][split][H] (base 2)
     float *part_o, *part_m, *part_l;
+    uint8_t *q_lo_img;            // per-CTA image of the query's bf16 lo part (tensor-core kernel)
     __nv_bfloat16 *out;           // [B][n_q][H][C]
     float *lse;                   // [B][n_q][H] or nullptr
 };

@@ -1,17 +1,20 @@
 // lca.cu -- the C ABI of liblca (declared in include/lca.h): host-side validation, work
 // planning and kernel launches.  The library is built as one translation unit so that the
 // device error word is a single object per device.
+#include <cudaTypedefs.h>
+
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <string>
 
 #include "../../include/lca.h"
 #include "common.cuh"
 #include "compress.cuh"
 #include "topk.cuh"
-#include "indexer_simt.cuh"
+#include "indexer_tc.cuh"
 #include "attend_common.cuh"
-#include "attend_simt.cuh"
+#include "attend_tc.cuh"
 #include "gemv.cuh"
 
 using namespace lca;
@@ -50,6 +53,38 @@ int device_sm_count() {
     int n = 0;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
     return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// A bf16 tensor map of rank 2 or 3 (dims innermost first, strides in bytes for dims 1..),
+// tiled boxes with the given swizzle; out-of-range elements read as zero.
+bool make_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
+                     const uint32_t *box, CUtensorMapSwizzle swizzle) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t gd[3], gs[2];
+    cuuint32_t bd[3], es[3] = {1, 1, 1};
+    for (int i = 0; i < rank; ++i) {
+        gd[i] = dims[i];
+        bd[i] = box[i];
+    }
+    for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gd, gs, bd, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 #define LCA_REQUIRE(cond, status, ...) \
@@ -121,24 +156,28 @@ struct AttendPlan {
     int64_t units;
     size_t part_bytes;       // O partials
     size_t ml_bytes;         // m and l partials
+    size_t lo_bytes;         // per-CTA query lo images
     size_t total;
 };
 
-constexpr int kPlanTileRows = kSimtTile;
+constexpr int kPlanTileRows = kAtTile;
 
+// Split-K plan: one CTA per (query, split) and one CTA per SM, so a query gets as many splits
+// as keep all SMs busy in one wave (and never more splits than tiles).
 AttendPlan plan_attend(const lca_attn_params *p, int batch, int n_q, int64_t max_rows) {
     AttendPlan pl;
     pl.units = (int64_t)batch * n_q;
     const int64_t tiles = ceil_div64(max_rows, kPlanTileRows);
     const int sms = device_sm_count();
-    int64_t s = ceil_div64(sms, pl.units);
+    int64_t s = sms / pl.units;
     if (s > tiles) s = tiles;
     if (s < 1) s = 1;
     if (s > 64) s = 64;
     pl.splits = (int)s;
     pl.part_bytes = (size_t)pl.units * pl.splits * p->heads * p->head_dim * sizeof(float);
     pl.ml_bytes = (size_t)pl.units * pl.splits * p->heads * sizeof(float);
-    pl.total = pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255);
+    pl.lo_bytes = (size_t)pl.units * pl.splits * (p->head_dim / 128) * kAtLoChunkBytes;
+    pl.total = pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255) + pl.lo_bytes;
     return pl;
 }
 
@@ -210,29 +249,27 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     a.part_o = reinterpret_cast<float *>(w);
     a.part_m = reinterpret_cast<float *>(w + pl.part_bytes);
     a.part_l = reinterpret_cast<float *>(w + pl.part_bytes + ((pl.ml_bytes + 255) & ~(size_t)255));
+    a.q_lo_img = reinterpret_cast<uint8_t *>(w + pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255));
     a.out = reinterpret_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
     LCA_REQUIRE(pl.units <= 0x7fffffff, LCA_ERR_UNSUPPORTED, "%s: too many queries", name);
     dim3 grid((unsigned)pl.units, pl.splits);
     switch (p->head_dim) {
-    case 128: {
-        size_t smem = sizeof(SimtSmem<128>);
-        cudaFuncSetAttribute(attend_simt_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attend_simt_kernel<128><<<grid, kSimtThreads, smem, stream>>>(a);
+    case 128:
+        cudaFuncSetAttribute(attend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttendTcConfig<128>::SMEM_BYTES);
+        attend_tc_kernel<128><<<grid, kAtThreads, AttendTcConfig<128>::SMEM_BYTES, stream>>>(a);
         break;
-    }
-    case 256: {
-        size_t smem = sizeof(SimtSmem<256>);
-        cudaFuncSetAttribute(attend_simt_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attend_simt_kernel<256><<<grid, kSimtThreads, smem, stream>>>(a);
+    case 256:
+        cudaFuncSetAttribute(attend_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttendTcConfig<256>::SMEM_BYTES);
+        attend_tc_kernel<256><<<grid, kAtThreads, AttendTcConfig<256>::SMEM_BYTES, stream>>>(a);
         break;
-    }
-    default: {
-        size_t smem = sizeof(SimtSmem<512>);
-        cudaFuncSetAttribute(attend_simt_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attend_simt_kernel<512><<<grid, kSimtThreads, smem, stream>>>(a);
+    default:
+        cudaFuncSetAttribute(attend_tc_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttendTcConfig<512>::SMEM_BYTES);
+        attend_tc_kernel<512><<<grid, kAtThreads, AttendTcConfig<512>::SMEM_BYTES, stream>>>(a);
         break;
-    }
     }
     st = check_launch(name);
     if (st != LCA_OK) return st;
@@ -249,9 +286,10 @@ lca_status indexer_validate(const char *name, const lca_attn_params *p, int batc
     LCA_REQUIRE(batch > 0 && n_q > 0 && cache_rows > 0, LCA_ERR_INVALID_ARG,
                 "%s: batch, n_q and cache_rows must be positive", name);
     LCA_REQUIRE(p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
-    LCA_REQUIRE(p->idx_heads >= 1 && p->idx_heads <= 64 && p->idx_dim >= 8 && p->idx_dim <= 256 &&
-                    p->idx_dim % 8 == 0,
-                LCA_ERR_UNSUPPORTED, "%s: indexer heads %d / dim %d unsupported", name, p->idx_heads, p->idx_dim);
+    LCA_REQUIRE((p->idx_dim == 128 && p->idx_heads == 64) || (p->idx_dim == 64 && p->idx_heads == 32) ||
+                    (p->idx_dim == 32 && p->idx_heads == 4),
+                LCA_ERR_UNSUPPORTED, "%s: indexer (heads %d, dim %d) not in {(64, 128), (32, 64), (4, 32)}", name,
+                p->idx_heads, p->idx_dim);
     LCA_REQUIRE(q_idx && w_idx && k_cache && q_pos, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
     LCA_REQUIRE(aligned16(q_idx) && aligned16(k_cache), LCA_ERR_INVALID_ARG,
                 "%s: q_idx and k_cache must be 16-byte aligned", name);
@@ -260,27 +298,53 @@ lca_status indexer_validate(const char *name, const lca_attn_params *p, int batc
     return LCA_OK;
 }
 
+template <int DI, int HI, int QPT>
+lca_status indexer_tc_launch(int batch, int n_q, const lca_bf16 *q_idx, const lca_bf16 *k_cache, int64_t k_bs,
+                             IndexerTcArgs &a, cudaStream_t stream) {
+    using Cfg = IndexerTcConfig<DI, HI, QPT>;
+    const CUtensorMapSwizzle sw = Cfg::ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    CUtensorMap kmap, qmap;
+    const uint64_t kd[3] = {(uint64_t)DI, (uint64_t)a.cache_rows, (uint64_t)batch};
+    const uint64_t ks[2] = {(uint64_t)DI * 2, (uint64_t)k_bs * 2};
+    const uint32_t kb[3] = {(uint32_t)Cfg::BOX, 128u, 1u};
+    if (!make_tensor_map(&kmap, k_cache, 3, kd, ks, kb, sw))
+        return fail(LCA_ERR_CUDA, "csa_indexer_scores: key tensor map rejected by the driver");
+    const uint64_t qd[2] = {(uint64_t)DI, (uint64_t)batch * n_q * HI};
+    const uint64_t qs[1] = {(uint64_t)DI * 2};
+    const uint32_t qb[2] = {(uint32_t)Cfg::BOX, (uint32_t)Cfg::N};
+    if (!make_tensor_map(&qmap, q_idx, 2, qd, qs, qb, sw))
+        return fail(LCA_ERR_CUDA, "csa_indexer_scores: query tensor map rejected by the driver");
+    a.groups = (n_q + QPT - 1) / QPT;
+    a.tiles = (int)ceil_div64(a.cache_rows, 128);
+    a.items = (int64_t)batch * a.groups * a.tiles;
+    const int grid = (int)std::min<int64_t>(a.items, device_sm_count());
+    cudaFuncSetAttribute(indexer_tc_kernel<DI, HI, QPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         Cfg::SMEM_BYTES);
+    indexer_tc_kernel<DI, HI, QPT><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(kmap, qmap, a);
+    return check_launch("csa_indexer_scores");
+}
+
 lca_status indexer_launch(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q_idx, const float *w_idx,
                           const lca_bf16 *k_cache, int64_t k_bs, int64_t cache_rows, const int32_t *q_pos,
                           float *scores, int64_t s_stride, cudaStream_t stream) {
-    IndexerArgs a;
-    a.HI = p->idx_heads;
-    a.DI = p->idx_dim;
-    a.ratio = p->ratio;
+    IndexerTcArgs a;
     a.n_q = n_q;
-    a.q = reinterpret_cast<const __nv_bfloat16 *>(q_idx);
-    a.w = w_idx;
-    a.k = reinterpret_cast<const __nv_bfloat16 *>(k_cache);
-    a.k_bs = k_bs;
+    a.ratio = p->ratio;
     a.cache_rows = cache_rows;
+    a.w = w_idx;
     a.q_pos = q_pos;
     a.scores = scores;
-    a.s_stride = s_stride;
-    const size_t smem = (size_t)(a.HI * a.DI + a.HI + a.DI * kIdxSimtRows) * sizeof(float);
-    cudaFuncSetAttribute(indexer_simt_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    dim3 grid((unsigned)ceil_div64(cache_rows, kIdxSimtRows), n_q, batch);
-    indexer_simt_kernel<<<grid, kIdxSimtRows, smem, stream>>>(a);
-    return check_launch("csa_indexer_scores");
+    a.stride = s_stride;
+    if (p->idx_dim == 128) {
+        if (n_q == 1) return indexer_tc_launch<128, 64, 1>(batch, n_q, q_idx, k_cache, k_bs, a, stream);
+        if (n_q == 2) return indexer_tc_launch<128, 64, 2>(batch, n_q, q_idx, k_cache, k_bs, a, stream);
+        return indexer_tc_launch<128, 64, 4>(batch, n_q, q_idx, k_cache, k_bs, a, stream);
+    }
+    if (p->idx_dim == 64) {
+        if (n_q == 1) return indexer_tc_launch<64, 32, 1>(batch, n_q, q_idx, k_cache, k_bs, a, stream);
+        return indexer_tc_launch<64, 32, 8>(batch, n_q, q_idx, k_cache, k_bs, a, stream);
+    }
+    return indexer_tc_launch<32, 4, 4>(batch, n_q, q_idx, k_cache, k_bs, a, stream);
 }
 
 lca_status topk_launch(const lca_attn_params *p, int batch, int n_q, const float *scores, int64_t s_stride,
