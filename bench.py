@@ -114,7 +114,10 @@ class Workload:
     dominant = ""              # name of the dominant kernel
     bound = "hbm"
 
-    def step(self, ev=None):   # ev: optional (start, end) events around the dominant kernel
+    def step(self):
+        raise NotImplementedError
+
+    def dominant_call(self):   # the dominant kernel's launch alone
         raise NotImplementedError
 
     def e2e_step(self):
@@ -158,15 +161,15 @@ class CsaDecode(Workload):
         self.dom_bytes = B * (n_vis * s.idx_dim * 2 + s.idx_heads * s.idx_dim * 2 + s.idx_heads * 4 + n_vis * 4)
         self.dom_flops = 2.0 * B * n_vis * s.idx_heads * s.idx_dim
 
-    def step(self, ev=None):
+    def dominant_call(self):
+        d = self.d
+        self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], self.layer.idx_cache, self.q_pos, self.scores)
+
+    def step(self):
         api, L, d = self.api, self.layer, self.d
         L.compress(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, 1)
         L.window(d["tok_v"][:, -1:], self.new_pos)
-        if ev:
-            ev[0].record()
         api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
-        if ev:
-            ev[1].record()
         api.lca_topk(self.p, self.scores, self.q_pos, self.entries, L.idx)
         L.attend(d["q"], self.q_pos, self.out)
 
@@ -260,15 +263,15 @@ class HcaDecode(Workload):
         self.dom_bytes = B * (rows * s.head_dim * 2 + 2 * s.heads * s.head_dim * 2)
         self.dom_flops = 4.0 * B * rows * s.heads * s.head_dim
 
-    def step(self, ev=None):
+    def dominant_call(self):
+        # the attention kernel and its split-K combine
+        self.layer.attend(self.d["q"], self.q_pos, self.out)
+
+    def step(self):
         L, d = self.layer, self.d
         L.compress(d["tok_v"], d["tok_z"], self.tok_pos0, self.first, 1)
         L.window(d["tok_v"][:, -1:], self.new_pos)
-        if ev:
-            ev[0].record()
         L.attend(d["q"], self.q_pos, self.out)
-        if ev:
-            ev[1].record()
 
     def e2e_step(self):
         d = self.d
@@ -352,15 +355,15 @@ class CsaPrefill(Workload):
         self.dom_flops = float(2.0 * n_vis.sum() * s.idx_heads * s.idx_dim)
         self.dom_bytes = entries * s.idx_dim * 2 + Tq * s.idx_heads * (s.idx_dim * 2 + 4) + float(n_vis.sum()) * 4
 
-    def step(self, ev=None):
+    def dominant_call(self):
+        d = self.d
+        self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], self.layer.idx_cache, self.q_pos, self.scores)
+
+    def step(self):
         api, L, d = self.api, self.layer, self.d
         L.compress(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, self.Tq // self.s.ratio)
         L.window(d["tok_v"][:, self.s.ratio:], self.new_pos)
-        if ev:
-            ev[0].record()
         api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
-        if ev:
-            ev[1].record()
         api.lca_topk(self.p, self.scores, self.q_pos, self.entries, L.idx)
         L.attend(d["q"], self.q_pos, self.out)
 
@@ -460,31 +463,54 @@ def barrier(world: int):
 
 # --------------------------------------------------------------------------- main -----
 
-def time_steps(wk: Workload, steps: int, warmup: int, flush: torch.Tensor, e2e: bool, world: int):
-    """Per-step device times (ms) of `steps` steps after `warmup`, L2 flushed before each step."""
-    stream = torch.cuda.current_stream()
-    fn = wk.e2e_step if e2e else wk.step
-    for _ in range(warmup):
+def capture(fn) -> torch.cuda.CUDAGraph:
+    """Capture fn()'s launches (all on the current stream) into a CUDA graph."""
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
         fn()
     torch.cuda.synchronize()
+    return g
+
+
+def time_replays(graph: torch.cuda.CUDAGraph, steps: int, flush: torch.Tensor, world: int):
+    """Device time (ms) of each of `steps` replays, L2 flushed (outside the timed span) before each."""
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    dom_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for i in range(steps):
         flush.zero_()
-        step_ev[i][0].record(stream)
-        if e2e:
-            fn()
-        else:
-            wk.step(dom_ev[i])
-        step_ev[i][1].record(stream)
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    dom_ms = [a.elapsed_time(b) for a, b in dom_ev] if not e2e else []
-    return step_ms, dom_ms
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def time_eager(fn, steps: int, flush: torch.Tensor, world: int):
+    stream = torch.cuda.current_stream()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
 
 
 def run_ours(args):
@@ -504,9 +530,19 @@ def run_ours(args):
     if do_cpu:
         wk.snapshot_host()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    for _ in range(args.warmup):
+        wk.step()
+    torch.cuda.synchronize()
+    step_graph = capture(wk.step)            # the whole step: every launch of the layer
+    dom_graph = capture(wk.dominant_call)    # the dominant kernel alone
+    step_graph.replay()
+    dom_graph.replay()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        step_ms, dom_ms = time_steps(wk, args.steps, args.warmup, flush, False, world)
-    e2e_ms, _ = time_steps(wk, args.steps, max(1, args.warmup // 2), flush, True, world)
+        step_ms = time_replays(step_graph, args.steps, flush, world)
+        dom_ms = time_replays(dom_graph, args.steps, flush, world)
+    for _ in range(max(1, args.warmup // 2)):
+        wk.e2e_step()
+    e2e_ms = time_eager(wk.e2e_step, args.steps, flush, world)
     ms = float(np.mean(step_ms))
     ms_all = max_over_ranks(ms, world, device)
     e2e_all = max_over_ranks(float(np.mean(e2e_ms)), world, device)
@@ -531,7 +567,9 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded N(0,1) caches, tokens, queries; N(0,0.02) biases (workloads.py)",
         "config": {"workload": cfg["name"], "name": args.workload, "batch": cfg.get("B", 1),
-                   "l2": "caches larger than L2, and L2 flushed (512 MiB write) before every timed step"},
+                   "l2": "caches larger than L2, and L2 flushed (512 MiB write) before every timed step",
+                   "timing": "device: CUDA-graph replays of the step, CUDA events; e2e: eager calls with "
+                             "pinned-host inputs copied in and the output copied out inside the timed span"},
         "roofline": roof,
         "e2e": {"value": round(world * wk.tokens / (e2e_all * 1e-3), 1), "unit": "tokens/s",
                 "h2d_bytes_per_step": wk.h2d_bytes, "d2h_bytes_per_step": wk.d2h_bytes},

@@ -17,7 +17,8 @@ namespace lca {
 // Everything an attention kernel needs about one call.
 struct AttendArgs {
     int H, C, R;                  // heads, head dim, rope dims
-    float rope_base, eps;
+    float eps;
+    RopeTable rope;
     float scale_log2;             // softmax scale * log2(e): logits are kept in base 2
     int W;                        // window tokens
     int ratio;                    // m' for the dense (HCA) row list
@@ -44,6 +45,7 @@ struct RowList {
     int64_t pos;
     int64_t n_comp;
     int64_t win_begin;
+    int64_t win_slot0;               // ring row of token win_begin
     int n_win;
     const int32_t *idx;              // CSA list for this query, or nullptr (dense)
     const __nv_bfloat16 *kv;         // this sequence's compressed cache
@@ -73,6 +75,7 @@ __device__ __forceinline__ RowList make_row_list(const AttendArgs &a, int b, int
         L.n_comp = n_vis;
     }
     L.win_begin = L.pos - a.W + 1 < 0 ? 0 : L.pos - a.W + 1;
+    L.win_slot0 = L.win_begin % a.win_cap;
     L.n_win = (int)(L.pos - L.win_begin + 1);
     return L;
 }
@@ -90,8 +93,9 @@ __device__ __forceinline__ const __nv_bfloat16 *row_source(const AttendArgs &a, 
         return L.kv + j * a.C;
     }
     if (r < L.total()) {
-        const int64_t t = L.win_begin + (r - L.n_comp);
-        return L.win + (t % a.win_cap) * a.C;
+        int64_t slot = L.win_slot0 + (r - L.n_comp);      // at most one wrap: n_win <= W <= win_cap
+        if (slot >= a.win_cap) slot -= a.win_cap;
+        return L.win + slot * a.C;
     }
     return nullptr;
 }
@@ -134,7 +138,7 @@ __device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const __nv_bfloa
                 const int e = lane * EPL + u;
                 const int d = lower ? e - first : e - first - half;
                 float cs, sn;
-                rope_angle((double)pos, d, a.R, (double)a.rope_base, cs, sn);
+                rope_cs(a.rope, d, pos, cs, sn);
                 v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
             }
         }
@@ -167,59 +171,80 @@ __device__ __forceinline__ void q_hat_warp<128>(const AttendArgs &a, const __nv_
                 const int e = lane * EPL + u;
                 const int d = lower ? e - first : e - first - half;
                 float cs, sn;
-                rope_angle((double)pos, d, a.R, (double)a.rope_base, cs, sn);
+                rope_cs(a.rope, d, pos, cs, sn);
                 v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
             }
         }
     }
 }
 
-constexpr int kCombineThreads = 256;
+constexpr int kCombineThreads = 128;
+constexpr int kMaxSplits = 128;
 
 // Split-K combine: one CTA per (unit, head).  Merges the splits' (m, l, O) with the sink,
 // normalises, rotates the trailing R dims by -pos and stores bf16 (+ lse).
+//   M = max(sink, max_s m_s);  w_s = 2^(m_s - M);  L = 2^(sink - M) + sum_s w_s l_s;
+//   o = sum_s w_s O_s / L   (m, sink in base-2 logit units)
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttendArgs a) {
-    extern __shared__ float cw[];     // [splits] weights, then the row [C]
+    __shared__ float wts[kMaxSplits];
+    __shared__ __align__(16) float row[1024];
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float Lsh;
     const int64_t unit = blockIdx.x;
     const int h = blockIdx.y;
     const int S = a.splits;
-    float *wts = cw;
-    float *row = cw + ((S + 3) & ~3);
-    __shared__ float Lsh;
     const int64_t pos = a.q_pos[unit] < 0 ? 0 : a.q_pos[unit];
+    const float sink2 = a.sink[h] * kLog2e;
+    // each thread owns at most one split (S <= kCombineThreads)
+    float m = -INFINITY, l = 0.f;
+    if (threadIdx.x < S) {
+        l = a.part_l[(unit * S + threadIdx.x) * a.H + h];
+        m = l > 0.f ? a.part_m[(unit * S + threadIdx.x) * a.H + h] : -INFINITY;
+    }
+    float M = warp_max(fmaxf(m, sink2));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
+    __syncthreads();
+    M = red[0];
+    for (int w = 1; w < kCombineThreads / 32; ++w) M = fmaxf(M, red[w]);
+    const float wgt = threadIdx.x < S && l > 0.f ? exp2f(m - M) : 0.f;
+    if (threadIdx.x < S) wts[threadIdx.x] = wgt;
+    float part = warp_sum(wgt * l);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
+    __syncthreads();
     if (threadIdx.x == 0) {
-        const float sink2 = a.sink[h] * kLog2e;
-        float M = sink2;
-        for (int s = 0; s < S; ++s) {
-            const float l = a.part_l[(unit * S + s) * a.H + h];
-            if (l > 0.f) M = fmaxf(M, a.part_m[(unit * S + s) * a.H + h]);
-        }
         float L = exp2f(sink2 - M);
-        for (int s = 0; s < S; ++s) {
-            const float l = a.part_l[(unit * S + s) * a.H + h];
-            const float w = l > 0.f ? exp2f(a.part_m[(unit * S + s) * a.H + h] - M) : 0.f;
-            wts[s] = w;
-            L += w * l;
-        }
+        for (int w = 0; w < kCombineThreads / 32; ++w) L += red[w];
         Lsh = L;
         if (a.lse) a.lse[unit * a.H + h] = (M + log2f(L)) * kLn2;
     }
     __syncthreads();
     const float invL = 1.f / Lsh;
-    for (int i = threadIdx.x; i < a.C; i += blockDim.x) {
-        float acc = 0.f;
-        for (int s = 0; s < S; ++s) {
-            const float w = wts[s];
-            if (w != 0.f) acc = fmaf(w, a.part_o[((unit * S + s) * a.H + h) * a.C + i], acc);
+    const float *po = a.part_o + (unit * S * a.H + h) * (int64_t)a.C;
+    const int64_t split_stride = (int64_t)a.H * a.C;
+    for (int i = 4 * threadIdx.x; i < a.C; i += 4 * blockDim.x) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int s2 = 0; s2 < S; ++s2) {
+            const float w = wts[s2];
+            if (w != 0.f) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(po + s2 * split_stride + i));
+                acc.x = fmaf(w, v.x, acc.x);
+                acc.y = fmaf(w, v.y, acc.y);
+                acc.z = fmaf(w, v.z, acc.z);
+                acc.w = fmaf(w, v.w, acc.w);
+            }
         }
-        row[i] = acc * invL;
+        row[i] = acc.x * invL;
+        row[i + 1] = acc.y * invL;
+        row[i + 2] = acc.z * invL;
+        row[i + 3] = acc.w * invL;
     }
     __syncthreads();
     if (a.R > 0) {
         const int half = a.R / 2, first = a.C - a.R;
         for (int d = threadIdx.x; d < half; d += blockDim.x) {
             float cs, sn;
-            rope_angle(-(double)pos, d, a.R, (double)a.rope_base, cs, sn);
+            rope_cs(a.rope, d, -pos, cs, sn);
             const float x = row[first + d], y = row[first + d + half];
             row[first + d] = x * cs - y * sn;
             row[first + d + half] = x * sn + y * cs;

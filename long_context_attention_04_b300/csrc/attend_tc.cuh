@@ -19,17 +19,21 @@
 // and S^T accumulates KV.hi^T + KV.lo^T in fp32: a single bf16 query would put a relative
 // error of 2^-9 on every logit, comparable to the bf16 rounding of the output itself.
 // Shared memory holds the 64 KB hi tile and a ring of three 48 KB slots, each a 128-row x
-// 128-c KV chunk plus the matching 16 KB lo chunk (copied from this CTA's workspace image).
-// A 128-row tile at c = 512 does not fit twice, so each tile is streamed twice, once for S
-// and once for PV, the second time from L2.  HBM traffic stays one pass.
+// 128-c KV chunk plus the matching 16 KB lo chunk (bulk-copied from this CTA's workspace
+// image).  A 128-row tile at c = 512 does not fit twice next to the query, so each tile is
+// streamed twice, once for S and once for PV, the second time from L2; HBM sees one pass.
+//
+// Rows of a query: compressed rows (CSA: the selected entries; HCA: entries 0..n_vis), then
+// the window rows; tiles never mix the two.  All loads are TMA: contiguous compressed tiles
+// (HCA) as 2D boxes of 128 rows, indexed rows (CSA selections, window ring rows) with
+// 4-row gathers; masked rows are fetched at coordinate -1 and arrive as zeros.
 //
 // Roles (one CTA per (query, split), one CTA per SM):
-//   warps 0-3   producers: 16-byte cp.async gathers of rows (compressed entries by index or
-//               by position, window rows from the ring) into the swizzled slots
-//   warps 4-11  softmax: one TMEM lane (row) per thread, 32 heads per thread; online softmax
+//   warp 0      TMA producer
+//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warps 2-9   softmax: one TMEM lane (row) per thread, 32 heads per thread; online softmax
 //               in base 2 with a conditional rescale (the running max moves only when a
 //               logit exceeds it by more than 2^8), P^T rows to shared memory
-//   warp 12     TMEM allocator and MMA issuer
 // The split's unnormalised O, running max and row sum go to the workspace; combine_kernel
 // merges the splits with the sink and applies the output RoPE(-pos).
 // Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds.
@@ -40,23 +44,24 @@
 
 namespace lca {
 
-constexpr int kAtHP = 64;            // padded heads (MMA N)
-constexpr int kAtTile = 128;         // rows per tile (MMA M of S^T)
-constexpr int kAtSlots = 3;          // chunk slots in the ring
-constexpr int kAtChunkBytes = 128 * 128 * 2;            // KV chunk: 128 rows x 128 c
-constexpr int kAtLoChunkBytes = kAtHP * 128 * 2;        // q lo chunk: 64 heads x 128 c
+constexpr int kAtHP = 64;                                // padded heads (MMA N)
+constexpr int kAtTile = 128;                             // rows per tile (MMA M of S^T)
+constexpr int kAtSlots = 3;                              // chunk slots in the ring
+constexpr int kAtChunkBytes = 128 * 128 * 2;             // KV chunk: 128 rows x 128 c
+constexpr int kAtLoChunkBytes = kAtHP * 128 * 2;         // q lo chunk: 64 heads x 128 c
 constexpr int kAtSlotBytes = kAtChunkBytes + kAtLoChunkBytes;
-constexpr int kAtProducerWarps = 4;
+constexpr int kAtProducerWarp = 0;
+constexpr int kAtMmaWarp = 1;
+constexpr int kAtSoftmaxWarp0 = 2;
 constexpr int kAtSoftmaxWarps = 8;
-constexpr int kAtMmaWarp = kAtProducerWarps + kAtSoftmaxWarps;
-constexpr int kAtThreads = 32 * (kAtMmaWarp + 1);
-constexpr float kAtTau = 8.0f;       // log2 headroom before the running max must move
+constexpr int kAtThreads = 32 * (kAtSoftmaxWarp0 + kAtSoftmaxWarps);
+constexpr float kAtTau = 8.0f;                           // log2 headroom before the running max must move
 
 template <int C>
 struct AttendTcConfig {
     static constexpr int CC = C / 128;                        // c chunks per row
     static constexpr int Q_BYTES = kAtHP * C * 2;
-    static constexpr int P_BYTES = kAtTile * kAtHP * 2;       // one P^T buffer (16 KB)
+    static constexpr int P_BYTES = kAtTile * kAtHP * 2;       // the P^T buffer (16 KB)
     static constexpr int TMEM_S = 0;                          // two S^T buffers: columns 0..127
     static constexpr int TMEM_O = 2 * kAtHP;                  // O^T chunk j at TMEM_O + 64 j
     static constexpr int TMEM_NEED = TMEM_O + CC * kAtHP;
@@ -67,25 +72,38 @@ struct AttendTcConfig {
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
-// Row code of one row of a query's row list: entry index, 0x80000000 | ring slot for a
-// window row, or 0xffffffff for a masked row.
-__device__ __forceinline__ uint32_t row_code(const AttendArgs &a, const RowList &L, int64_t R, bool report) {
-    if (R >= L.total()) return 0xffffffffu;
-    if (R < L.n_comp) {
-        const int64_t j = L.idx ? (int64_t)__ldg(L.idx + R) : R;
-        if (j < 0) return 0xffffffffu;
-        if (j >= a.cache_rows) {
-            if (report) raise_error(LCA_DEVERR_INDEX_RANGE);
-            return 0xffffffffu;
-        }
-        return (uint32_t)j;
-    }
-    const int64_t t = L.win_begin + (R - L.n_comp);
-    return 0x80000000u | (uint32_t)(t % a.win_cap);
+// Where the rows of one query come from, in tiles: tiles [0, tc) hold compressed rows
+// [128 t, 128 t + 128) (masked at n_comp), tiles [tc, tc + tw) hold window rows.
+struct TileMap {
+    int tc, tw;
+    __device__ __forceinline__ int total() const { return tc + tw; }
+};
+
+__device__ __forceinline__ TileMap tile_map(const RowList &L) {
+    TileMap m;
+    m.tc = (int)((L.n_comp + kAtTile - 1) / kAtTile);
+    m.tw = (L.n_win + kAtTile - 1) / kAtTile;
+    return m;
 }
 
+// Whether row r of tile t is a real key/value row.
+__device__ __forceinline__ bool tile_row_valid(const AttendArgs &a, const RowList &L, const TileMap &m, int t, int r) {
+    if (t < m.tc) {
+        const int64_t R = (int64_t)t * kAtTile + r;
+        if (R >= L.n_comp) return false;
+        if (!L.idx) return true;
+        const int32_t j = __ldg(L.idx + R);
+        return j >= 0 && j < a.cache_rows;
+    }
+    return (t - m.tc) * kAtTile + r < L.n_win;
+}
+
+// Register cap: the register file is split across the four SM sub-partitions (16K each) and
+// 10 warps place 3 warps on two of them, so 3 x 32 x 168 <= 16384.
 template <int C>
-__global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) {
+__global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtensorMap kv_tile_map,
+                                                  const __grid_constant__ CUtensorMap kv_row_map,
+                                                  const __grid_constant__ CUtensorMap win_row_map, AttendArgs a) {
     using Cfg = AttendTcConfig<C>;
     constexpr int CC = Cfg::CC;
     extern __shared__ uint8_t smem_raw[];
@@ -113,8 +131,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
     const int unit = blockIdx.x, split = blockIdx.y;
     const int b = unit / a.n_q, qi = unit % a.n_q;
     const RowList L = make_row_list(a, b, qi);
-    int64_t t0, t1;
-    split_range(L.total(), kAtTile, split, a.splits, t0, t1);
+    const TileMap tm = tile_map(L);
+    const int64_t t0 = (int64_t)tm.total() * split / a.splits;
+    const int64_t t1 = (int64_t)tm.total() * (split + 1) / a.splits;
     const int64_t pidx0 = ((int64_t)unit * a.splits + split) * a.H;
     uint8_t *lo_img = a.q_lo_img + ((int64_t)unit * a.splits + split) * Cfg::LO_IMAGE_BYTES;
 
@@ -126,10 +145,10 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
         return;
     }
 
-    // ---- set-up: barriers, TMEM, the normalised and rotated query tile ----
+    // ---- set-up: barriers, TMEM, the normalised and rotated query (hi in smem, lo image) ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kAtSlots; ++s) {
-            ptx::mbar_init(&full[s], 32 * kAtProducerWarps);
+            ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -183,89 +202,97 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
                 make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
         }
     }
-    ptx::fence_proxy_async();
+    ptx::fence_proxy_async();          // hi tile: generic writes -> tensor-core reads
+    ptx::fence_proxy_async_global();   // lo image: generic writes -> bulk-copy reads
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int n_tiles = (int)(t1 - t0);
 
-    if (warp < kAtProducerWarps) {
-        // ------------------------------------------------------------ producers ----
-        const __nv_bfloat16 *kv_b = L.kv, *win_b = L.win;
-        const int sub_row = warp * 2 + (lane >> 4);   // row within an 8-row stripe
-        const int piece = lane & 15;                  // 16-byte piece of the 256-byte chunk row
-        uint32_t cur[16], nxt[16];
-        uint32_t issued = 0;                          // chunk loads issued
-        uint32_t arrived = 0;                         // chunk loads signalled complete
-        auto load_chunk = [&](const uint32_t *codes, int j, bool with_lo) -> bool {
-            const int s = issued % kAtSlots;
-            if (issued >= (uint32_t)kAtSlots && !ptx::mbar_wait(&empty[s], ((issued / kAtSlots) - 1) & 1))
-                return false;
-            uint8_t *slot = ring + s * kAtSlotBytes;
-            if (with_lo) {   // the lo part of query chunk j (16 KB, already swizzled)
-                const uint32_t lo_dst = ptx::smem_u32(slot + kAtChunkBytes);
-                const uint8_t *lo_src = lo_img + j * kAtLoChunkBytes;
-#pragma unroll
-                for (int i = 0; i < kAtLoChunkBytes / 16 / (32 * kAtProducerWarps); ++i) {
-                    const int piece16 = i * (32 * kAtProducerWarps) + threadIdx.x;
-                    ptx::cp_async16(lo_dst + piece16 * 16, lo_src + piece16 * 16, 16);
-                }
-            }
-            const uint32_t dst0 = ptx::smem_u32(slot) + (piece >> 3) * (128 * 128);
-#pragma unroll
-            for (int it = 0; it < 16; ++it) {
-                const int r = it * 8 + sub_row;
-                const uint32_t code = codes[it];
-                const __nv_bfloat16 *src = kv_b;
-                uint32_t bytes = 0;
-                if (code != 0xffffffffu) {
-                    src = (code & 0x80000000u) ? win_b + (int64_t)(code & 0x7fffffffu) * C
-                                               : kv_b + (int64_t)code * C;
-                    src += j * 128 + piece * 8;
-                    bytes = 16;
-                }
-                ptx::cp_async16(dst0 + ptx::sw128_offset(r, piece & 7), src, bytes);
-            }
-            ptx::cp_async_commit();
-            ++issued;
-            // signal the chunk issued two loads ago (its copies are complete now)
-            if (issued >= 3) {
-                ptx::cp_async_wait<2>();
-                ptx::fence_proxy_async();
-                ptx::mbar_arrive(&full[arrived % kAtSlots]);
-                ++arrived;
-            }
-            return true;
-        };
-        auto codes_of = [&](uint32_t *codes, int64_t t) {
-#pragma unroll
-            for (int it = 0; it < 16; ++it) codes[it] = row_code(a, L, t * kAtTile + it * 8 + sub_row, piece == 0);
-        };
+    if (warp == kAtProducerWarp) {
+        // ------------------------------------------------------------ producer ----
+        // Chunk loads in consumption order: S(t0), then per tile S(t), PV(t-1), finally PV(t1-1).
+        const int total_loads = CC * (2 * n_tiles);
+        const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
+        const int64_t win_row0 = (int64_t)b * (a.win_bs / C);
+        if (lane == 0) {
+            ptx::tma_prefetch(&kv_tile_map);
+            ptx::tma_prefetch(&kv_row_map);
+            ptx::tma_prefetch(&win_row_map);
+        }
         bool ok = true;
-        codes_of(cur, t0);
-        for (int j = 0; j < CC && ok; ++j) ok = load_chunk(cur, j, true);
-        for (int64_t t = t0 + 1; t < t1 && ok && !*abort_flag; ++t) {
-            codes_of(nxt, t);
-            for (int j = 0; j < CC && ok; ++j) ok = load_chunk(nxt, j, true);      // S(t)
-            for (int j = 0; j < CC && ok; ++j) ok = load_chunk(cur, j, false);     // PV(t-1)
+        for (int n = 0; n < total_loads && ok && !*abort_flag; ++n) {
+            const int j = n % CC;
+            const int g = n / CC;                 // 0 = S(t0); then pairs S(t0+k), PV(t0+k-1)
+            int t;
+            bool s_pass;
+            if (g == 0) {
+                t = (int)t0;
+                s_pass = true;
+            } else if (g == 2 * n_tiles - 1) {
+                t = (int)t1 - 1;
+                s_pass = false;
+            } else {
+                const int k = (g + 1) / 2;
+                s_pass = (g & 1) != 0;
+                t = (int)t0 + (s_pass ? k : k - 1);
+            }
+            const int s = n % kAtSlots;
+            if (n >= kAtSlots && !ptx::mbar_wait(&empty[s], ((n / kAtSlots) - 1) & 1)) {
+                ok = false;
+                break;
+            }
+            uint8_t *slot = ring + s * kAtSlotBytes;
+            if (lane == 0) ptx::mbar_arrive_expect_tx(&full[s], kAtChunkBytes + (s_pass ? kAtLoChunkBytes : 0));
+            __syncwarp();
+            const uint32_t dst = ptx::smem_u32(slot);
+            if (t < tm.tc && !L.idx) {
+                // contiguous compressed rows: two 64-c boxes of 128 rows
+                if (lane < 2)
+                    ptx::tma_load_2d(dst + lane * (128 * 128), &kv_tile_map, j * 128 + lane * 64,
+                                     (int)(kv_row0 + (int64_t)t * kAtTile), &full[s]);
+            } else {
+                // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, for both c boxes
+                int rc[4];
 #pragma unroll
-            for (int it = 0; it < 16; ++it) cur[it] = nxt[it];
+                for (int i = 0; i < 4; ++i) {
+                    const int r = 4 * lane + i;
+                    int coord = -1;
+                    if (t < tm.tc) {
+                        const int64_t R = (int64_t)t * kAtTile + r;
+                        if (R < L.n_comp) {
+                            const int32_t e = __ldg(L.idx + R);
+                            if (e >= 0 && e < a.cache_rows) coord = (int)(kv_row0 + e);
+                            else if (e >= a.cache_rows && s_pass && j == 0) raise_error(LCA_DEVERR_INDEX_RANGE);
+                        }
+                    } else {
+                        const int R = (t - tm.tc) * kAtTile + r;
+                        if (R < L.n_win) {
+                            int64_t slot_row = L.win_slot0 + R;       // at most one wrap: n_win <= W <= win_cap
+                            if (slot_row >= a.win_cap) slot_row -= a.win_cap;
+                            coord = (int)(win_row0 + slot_row);
+                        }
+                    }
+                    rc[i] = coord;
+                }
+                const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
+#pragma unroll
+                for (int bx = 0; bx < 2; ++bx)
+                    ptx::tma_gather4(dst + bx * (128 * 128) + lane * 512, map, j * 128 + bx * 64, rc[0], rc[1], rc[2],
+                                     rc[3], &full[s]);
+            }
+            if (s_pass && lane == 0)   // the lo part of query chunk j (16 KB, already swizzled)
+                ptx::bulk_load(dst + kAtChunkBytes, lo_img + j * kAtLoChunkBytes, kAtLoChunkBytes, &full[s]);
         }
-        for (int j = 0; j < CC && ok; ++j) ok = load_chunk(cur, j, false);         // PV(t1-1)
         if (!ok) *abort_flag = 1;
-        ptx::cp_async_wait_all();
-        ptx::fence_proxy_async();
-        while (arrived < issued) {
-            ptx::mbar_arrive(&full[arrived % kAtSlots]);
-            ++arrived;
-        }
     } else if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------- MMA issue ----
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::idesc_bf16(128, kAtHP, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(128, kAtHP, true, true);
             const uint32_t q_addr = ptx::smem_u32(q_tile);
+            const uint32_t p_addr = ptx::smem_u32(p_buf);
             uint32_t used = 0;   // chunk slots consumed
             bool ok = true;
             auto take = [&]() -> uint32_t {   // wait for the next chunk; returns its smem address
@@ -274,10 +301,11 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
                 ptx::tc_fence_after();
                 return ptx::smem_u32(ring + s * kAtSlotBytes);
             };
-            auto issue_s = [&](int u) -> bool {   // S^T of relative tile u
+            auto issue_s = [&](int u) -> bool {   // S^T of relative tile u: KV . (hi + lo)^T
                 const int buf = u & 1;
                 if (u >= 2 && !ptx::mbar_wait(&s_empty[buf], ((u >> 1) - 1) & 1)) return false;
                 ptx::tc_fence_after();
+                const uint32_t d = tmem + Cfg::TMEM_S + buf * kAtHP;
                 for (int j = 0; j < CC; ++j) {
                     const uint32_t slot = take();
                     if (!slot) return false;
@@ -291,7 +319,6 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
                         const uint64_t bl = ptx::smem_desc(slot + kAtChunkBytes + (kk >> 2) * (kAtHP * 128) +
                                                                (kk & 3) * 32,
                                                            16, 1024, ptx::kSwizzle128);
-                        const uint32_t d = tmem + Cfg::TMEM_S + buf * kAtHP;
                         ptx::mma_bf16(d, ad, bh, idesc_s, (j > 0 || kk > 0));
                         ptx::mma_bf16(d, ad, bl, idesc_s, 1);
                     }
@@ -305,7 +332,6 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
                 const int buf = u & 1;
                 if (!ptx::mbar_wait(&p_full[buf], (u >> 1) & 1)) return false;
                 ptx::tc_fence_after();
-                const uint32_t p_addr = ptx::smem_u32(p_buf);
                 for (int j = 0; j < CC; ++j) {
                     const uint32_t slot = take();
                     if (!slot) return false;
@@ -333,7 +359,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
         }
     } else {
         // -------------------------------------------------------------- softmax ----
-        const int sw = warp - kAtProducerWarps;      // 0..7
+        const int sw = warp - kAtSoftmaxWarp0;       // 0..7
         const int quarter = warp & 3;                // TMEM lane quarter
         const int half = sw >> 2;                    // heads [32 half, 32 half + 32)
         const int r = quarter * 32 + lane;           // row of the tile == TMEM lane
@@ -364,7 +390,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(&s_empty[buf]);
-            const bool valid = row_code(a, L, (t0 + u) * kAtTile + r, false) != 0xffffffffu;
+            const bool valid = tile_row_valid(a, L, tm, (int)t0 + u, r);
             bool need = false;
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
@@ -455,10 +481,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
                 pr[h] = exp2f(x[h] - ms);
                 l[h] += pr[h];
             }
-            uint8_t *prow = p_buf;
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4)
-                *reinterpret_cast<uint4 *>(prow + ptx::sw128_offset(r, half * 4 + c4)) = pack8(pr + 8 * c4);
+                *reinterpret_cast<uint4 *>(p_buf + ptx::sw128_offset(r, half * 4 + c4)) = pack8(pr + 8 * c4);
             ptx::fence_proxy_async();
             ptx::mbar_arrive(&p_full[buf]);
         }
@@ -467,7 +492,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
         if (ok && !*abort_flag &&
             ptx::mbar_wait(&pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1)) {
             ptx::tc_fence_after();
-            // row sums over the 128 rows; the P buffers are free now (every PV is done)
+            // row sums over the 128 rows; the P buffer is free now (every PV is done)
             float *lsum = reinterpret_cast<float *>(p_buf);
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
@@ -482,8 +507,11 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_tc_kernel(AttendArgs a) 
                     float s = 0.f;
 #pragma unroll
                     for (int w = 0; w < 4; ++w) s += lsum[(half * 4 + w) * 32 + lane];
+                    float mv = m[0];
+#pragma unroll
+                    for (int k = 1; k < 32; ++k) mv = lane == k ? m[k] : mv;
                     if (h < a.H) {
-                        a.part_m[pidx0 + h] = m[lane];
+                        a.part_m[pidx0 + h] = mv;
                         a.part_l[pidx0 + h] = s;
                     }
                 }

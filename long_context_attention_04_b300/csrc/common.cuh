@@ -16,7 +16,6 @@ __device__ unsigned int g_error_word;
 
 __device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_error_word, bits); }
 
-constexpr double kTwoPi = 6.283185307179586476925286766559;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -75,13 +74,22 @@ __device__ __forceinline__ float block_max(float v, float *scratch32) {
     return warp_max(t);
 }
 
-// cos/sin of the RoPE angle of pair d at position pos: angle = pos * base^(-2d/R).
-// The product is formed and reduced modulo 2*pi in double (positions reach 2^20 and
-// beyond, where an fp32 product would lose the angle), then evaluated in fp32.
-__device__ __forceinline__ void rope_angle(double pos, int d, int R, double base, float &cs, float &sn) {
-    double inv_freq = pow(base, -2.0 * (double)d / (double)R);
-    double a = remainder(pos * inv_freq, kTwoPi);
-    sincosf((float)a, &sn, &cs);
+// RoPE frequencies as fractions of a turn.  Pair d rotates by pos * theta_d radians with
+// theta_d = base^(-2d/R); f[d] = theta_d / (2 pi) in unsigned 0.64 fixed point, computed on
+// the host in extended precision.  The angle of position pos is then the 64-bit product
+// pos * f[d] taken modulo 2^64 (the whole turns fall off), exact up to the rounding of f[d]
+// (~2^-64 relative) even at positions of 2^20 and beyond, with no floating-point range
+// reduction on the device.
+constexpr int kMaxRopePairs = 64;
+struct RopeTable {
+    uint64_t f[kMaxRopePairs];
+};
+
+// cos/sin of the RoPE angle of pair d at (signed) position pos.
+__device__ __forceinline__ void rope_cs(const RopeTable &t, int d, int64_t pos, float &cs, float &sn) {
+    const uint64_t turns = (uint64_t)pos * t.f[d];
+    const float two_frac = (float)(uint32_t)(turns >> 40) * 0x1p-23f;   // 2 x fraction of a turn
+    sincospif(two_frac, &sn, &cs);
 }
 
 // Order-preserving map of a float to uint32 (larger float -> larger key); -0 maps like +0.

@@ -16,7 +16,7 @@
 
 namespace lca {
 
-constexpr int kRowThreads = 128;        // threads per row-building CTA
+constexpr int kRowThreads = 256;        // threads per row-building CTA
 constexpr int kMaxRowWidth = 1024;      // widest row (elements)
 constexpr int kMaxSpan = 256;           // widest compressor window (tokens)
 
@@ -24,12 +24,12 @@ struct RowNormRope {
     const float *gamma;   // [width] or nullptr (no RMSNorm)
     float eps;
     int rope_dims;        // 0: no RoPE
-    float rope_base;
+    RopeTable rope;
 };
 
 // Finish a row held in fp32 shared memory (row[0..width)): RMSNorm, RoPE at `pos`, store bf16.
 // Every thread of the CTA must call it.
-__device__ __forceinline__ void finish_row(float *row, int width, const RowNormRope &nr, double pos,
+__device__ __forceinline__ void finish_row(float *row, int width, const RowNormRope &nr, int64_t pos,
                                            __nv_bfloat16 *dst, float *scratch32) {
     if (nr.gamma) {
         float ss = 0.f;
@@ -43,7 +43,7 @@ __device__ __forceinline__ void finish_row(float *row, int width, const RowNormR
         const int half = nr.rope_dims / 2, base_i = width - nr.rope_dims;
         for (int d = threadIdx.x; d < half; d += blockDim.x) {
             float cs, sn;
-            rope_angle(pos, d, nr.rope_dims, (double)nr.rope_base, cs, sn);
+            rope_cs(nr.rope, d, pos, cs, sn);
             const float a = row[base_i + d], b = row[base_i + d + half];
             row[base_i + d] = a * cs - b * sn;
             row[base_i + d + half] = a * sn + b * cs;
@@ -71,6 +71,7 @@ struct CompressArgs {
 __global__ void __launch_bounds__(kRowThreads) compress_kernel(CompressArgs a) {
     __shared__ float weight[kMaxSpan];
     __shared__ __align__(16) float row[kMaxRowWidth];
+    __shared__ float partial[kRowThreads * 8];
     __shared__ float scratch[32];
     const int b = blockIdx.y, e = blockIdx.x;
     const int64_t j = (int64_t)a.first_entry[b] + e;
@@ -105,11 +106,16 @@ __global__ void __launch_bounds__(kRowThreads) compress_kernel(CompressArgs a) {
     }
     den = block_sum(den, scratch);   // contains __syncthreads: weights visible after it
     const float inv_den = 1.f / den;
-    // weighted sum, 8 channels per thread per step
+    // Weighted sum: thread (group g, chunk k) sums 8 channels of chunk k over the tokens
+    // g, g + groups, ...; the groups' partial sums are then added in shared memory.
     const __nv_bfloat16 *v = a.tok_v + (int64_t)b * a.tok_v_bs + (begin - p0) * a.width;
-    for (int k = threadIdx.x; k < a.width / 8; k += blockDim.x) {
-        float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int t = 0; t < n_win; ++t) {
+    const int kc = a.width / 8;                       // 16-byte chunks per row
+    const int groups = blockDim.x / kc;               // token groups (>= 2 for width <= 1024)
+    const int g = threadIdx.x / kc, k = threadIdx.x % kc;
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (g < groups) {
+#pragma unroll 4
+        for (int t = g; t < n_win; t += groups) {
             const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(v + (int64_t)t * a.width) + k);
             float f[8];
             unpack8(raw, f);
@@ -117,11 +123,20 @@ __global__ void __launch_bounds__(kRowThreads) compress_kernel(CompressArgs a) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) acc[u] = fmaf(w, f[u], acc[u]);
         }
+    }
+    float *part = partial;                            // [groups][width]
+    if (g < groups) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) row[8 * k + u] = acc[u] * inv_den;
+        for (int u = 0; u < 8; ++u) part[g * a.width + 8 * k + u] = acc[u];
     }
     __syncthreads();
-    finish_row(row, a.width, a.nr, (double)(end - 1), a.cache + (int64_t)b * a.cache_bs + j * a.width, scratch);
+    for (int i = threadIdx.x; i < a.width; i += blockDim.x) {
+        float sum = 0.f;
+        for (int gg = 0; gg < groups; ++gg) sum += part[gg * a.width + i];
+        row[i] = sum * inv_den;
+    }
+    __syncthreads();
+    finish_row(row, a.width, a.nr, end - 1, a.cache + (int64_t)b * a.cache_bs + j * a.width, scratch);
 }
 
 struct WindowArgs {
@@ -150,7 +165,7 @@ __global__ void __launch_bounds__(kRowThreads) window_kernel(WindowArgs a) {
         for (int u = 0; u < 8; ++u) row[8 * k + u] = f[u];
     }
     __syncthreads();
-    finish_row(row, a.width, a.nr, (double)pos,
+    finish_row(row, a.width, a.nr, pos,
                a.win + (int64_t)b * a.win_bs + (pos % a.win_cap) * a.width, scratch);
 }
 

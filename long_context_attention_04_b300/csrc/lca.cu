@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <algorithm>
+#include <cmath>
 #include <string>
 
 #include "../../include/lca.h"
@@ -92,12 +93,27 @@ bool make_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_
         if (!(cond)) return fail(status, __VA_ARGS__); \
     } while (0)
 
+// theta_d / (2 pi) for d < R/2 in unsigned 0.64 fixed point (see RopeTable), in long double.
+RopeTable make_rope_table(int rope_dims, float rope_base) {
+    RopeTable t;
+    const long double two_pi = 6.283185307179586476925286766559005768L;
+    for (int d = 0; d < kMaxRopePairs; ++d) {
+        t.f[d] = 0;
+        if (rope_dims > 0 && d < rope_dims / 2) {
+            const long double theta = powl((long double)rope_base, -2.0L * d / (long double)rope_dims);
+            const long double frac = theta / two_pi;                       // < 1
+            t.f[d] = (uint64_t)(frac * 18446744073709551616.0L);           // * 2^64
+        }
+    }
+    return t;
+}
+
 RowNormRope make_nr(const lca_attn_params *p, const float *gamma, int apply_rope) {
     RowNormRope nr;
     nr.gamma = gamma;
     nr.eps = p->rms_eps;
     nr.rope_dims = apply_rope ? p->rope_dims : 0;
-    nr.rope_base = p->rope_base;
+    nr.rope = make_rope_table(nr.rope_dims, p->rope_base);
     return nr;
 }
 
@@ -125,8 +141,10 @@ lca_status compress_impl(const char *name, bool overlap, const lca_attn_params *
                 LCA_ERR_INVALID_ARG, "%s: batch strides smaller than one sequence", name);
     LCA_REQUIRE(cache_rows > 0, LCA_ERR_INVALID_ARG, "%s: cache_rows must be positive", name);
     if (apply_rope)
-        LCA_REQUIRE(p->rope_dims > 0 && p->rope_dims % 2 == 0 && p->rope_dims <= width, LCA_ERR_INVALID_ARG,
-                    "%s: rope_dims %d must be even and in (0, width]", name, p->rope_dims);
+        LCA_REQUIRE(p->rope_dims > 0 && p->rope_dims % 2 == 0 && p->rope_dims <= width &&
+                        p->rope_dims <= 2 * kMaxRopePairs && p->rope_base > 1.0f,
+                    LCA_ERR_INVALID_ARG, "%s: rope_dims %d must be even, <= width and <= %d; base > 1", name,
+                    p->rope_dims, 2 * kMaxRopePairs);
     if (n_new == 0) return ok();
     CompressArgs a;
     a.span = span;
@@ -172,7 +190,7 @@ AttendPlan plan_attend(const lca_attn_params *p, int batch, int n_q, int64_t max
     int64_t s = sms / pl.units;
     if (s > tiles) s = tiles;
     if (s < 1) s = 1;
-    if (s > 64) s = 64;
+    if (s > kMaxSplits) s = kMaxSplits;
     pl.splits = (int)s;
     pl.part_bytes = (size_t)pl.units * pl.splits * p->heads * p->head_dim * sizeof(float);
     pl.ml_bytes = (size_t)pl.units * pl.splits * p->heads * sizeof(float);
@@ -189,7 +207,8 @@ lca_status attend_validate(const char *name, const lca_attn_params *p, int batch
     LCA_REQUIRE(p->heads >= 1 && p->heads <= 64, LCA_ERR_UNSUPPORTED, "%s: heads %d not in [1, 64]", name, p->heads);
     const int epl = p->head_dim / 32;
     LCA_REQUIRE(p->rope_dims >= 0 && p->rope_dims <= p->head_dim && p->rope_dims % 2 == 0 &&
-                    (p->rope_dims / 2) % epl == 0,
+                    (p->rope_dims / 2) % epl == 0 && p->rope_dims <= 2 * kMaxRopePairs &&
+                    (p->rope_dims == 0 || p->rope_base > 1.0f),
                 LCA_ERR_UNSUPPORTED, "%s: rope_dims %d must be even, <= c and R/2 a multiple of c/32", name,
                 p->rope_dims);
     LCA_REQUIRE(p->window >= 1 && p->window <= 4096, LCA_ERR_UNSUPPORTED, "%s: window %d not in [1, 4096]", name,
@@ -215,8 +234,12 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
                 "%s: batch strides must be multiples of 8 elements", name);
     LCA_REQUIRE(cache_rows > 0, LCA_ERR_INVALID_ARG, "%s: cache_rows must be positive", name);
     LCA_REQUIRE(win_cap >= p->window, LCA_ERR_INVALID_ARG, "%s: win_cap %d < window %d", name, win_cap, p->window);
-    LCA_REQUIRE(batch == 1 || (kv_bs >= cache_rows * p->head_dim && win_bs >= (int64_t)win_cap * p->head_dim),
-                LCA_ERR_INVALID_ARG, "%s: batch strides smaller than one sequence", name);
+    LCA_REQUIRE(batch == 1 || (kv_bs >= cache_rows * p->head_dim && win_bs >= (int64_t)win_cap * p->head_dim &&
+                               kv_bs % p->head_dim == 0 && win_bs % p->head_dim == 0),
+                LCA_ERR_INVALID_ARG, "%s: batch strides must cover a sequence and be multiples of head_dim", name);
+    LCA_REQUIRE((int64_t)(batch - 1) * (kv_bs / p->head_dim) + cache_rows < ((int64_t)1 << 31) &&
+                    (int64_t)(batch - 1) * (win_bs / p->head_dim) + win_cap < ((int64_t)1 << 31),
+                LCA_ERR_UNSUPPORTED, "%s: caches exceed 2^31 rows", name);
     const int64_t max_rows = (csa ? p->topk : cache_rows) + p->window;
     AttendPlan pl = plan_attend(p, batch, n_q, max_rows);
     LCA_REQUIRE(ws && aligned16(ws) && ws_bytes >= pl.total, LCA_ERR_WORKSPACE,
@@ -225,7 +248,7 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     a.H = p->heads;
     a.C = p->head_dim;
     a.R = p->rope_dims;
-    a.rope_base = p->rope_base;
+    a.rope = make_rope_table(p->rope_dims, p->rope_base);
     a.eps = p->rms_eps;
     const float scale = p->softmax_scale > 0.f ? p->softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     a.scale_log2 = scale * kLog2e;
@@ -254,27 +277,41 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     a.lse = lse;
     LCA_REQUIRE(pl.units <= 0x7fffffff, LCA_ERR_UNSUPPORTED, "%s: too many queries", name);
     dim3 grid((unsigned)pl.units, pl.splits);
-    switch (p->head_dim) {
+    // tensor maps: the caches as 2D [rows, c] views (sequence b starts at row b * bs / c)
+    const int C = p->head_dim;
+    const uint64_t kv_rows = (uint64_t)(batch - 1) * (uint64_t)(kv_bs / C) + (uint64_t)cache_rows;
+    const uint64_t win_rows = (uint64_t)(batch - 1) * (uint64_t)(win_bs / C) + (uint64_t)win_cap;
+    const uint64_t dims_kv[2] = {(uint64_t)C, kv_rows}, dims_win[2] = {(uint64_t)C, win_rows};
+    const uint64_t row_bytes[1] = {(uint64_t)C * 2};
+    const uint32_t box_tile[2] = {64, (uint32_t)kAtTile}, box_row[2] = {64, 1};
+    CUtensorMap kv_tile_map, kv_row_map, win_row_map;
+    if (!make_tensor_map(&kv_tile_map, kv, 2, dims_kv, row_bytes, box_tile, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&kv_row_map, kv, 2, dims_kv, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&win_row_map, win, 2, dims_win, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B))
+        return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
+    switch (C) {
     case 128:
         cudaFuncSetAttribute(attend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttendTcConfig<128>::SMEM_BYTES);
-        attend_tc_kernel<128><<<grid, kAtThreads, AttendTcConfig<128>::SMEM_BYTES, stream>>>(a);
+        attend_tc_kernel<128><<<grid, kAtThreads, AttendTcConfig<128>::SMEM_BYTES, stream>>>(kv_tile_map, kv_row_map,
+                                                                                            win_row_map, a);
         break;
     case 256:
         cudaFuncSetAttribute(attend_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttendTcConfig<256>::SMEM_BYTES);
-        attend_tc_kernel<256><<<grid, kAtThreads, AttendTcConfig<256>::SMEM_BYTES, stream>>>(a);
+        attend_tc_kernel<256><<<grid, kAtThreads, AttendTcConfig<256>::SMEM_BYTES, stream>>>(kv_tile_map, kv_row_map,
+                                                                                            win_row_map, a);
         break;
     default:
         cudaFuncSetAttribute(attend_tc_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttendTcConfig<512>::SMEM_BYTES);
-        attend_tc_kernel<512><<<grid, kAtThreads, AttendTcConfig<512>::SMEM_BYTES, stream>>>(a);
+        attend_tc_kernel<512><<<grid, kAtThreads, AttendTcConfig<512>::SMEM_BYTES, stream>>>(kv_tile_map, kv_row_map,
+                                                                                            win_row_map, a);
         break;
     }
     st = check_launch(name);
     if (st != LCA_OK) return st;
-    const size_t csmem = (size_t)(((pl.splits + 3) & ~3) + p->head_dim) * sizeof(float);
-    combine_kernel<<<dim3((unsigned)pl.units, p->heads), kCombineThreads, csmem, stream>>>(a);
+    combine_kernel<<<dim3((unsigned)pl.units, p->heads), kCombineThreads, 0, stream>>>(a);
     st = check_launch(name);
     return st == LCA_OK ? ok() : st;
 }
@@ -357,7 +394,14 @@ lca_status topk_launch(const lca_attn_params *p, int batch, int n_q, const float
     a.max_entries = max_entries;
     a.k = p->topk;
     a.out = out_idx;
-    topk_kernel<<<(unsigned)((int64_t)batch * n_q), kTopkThreads, 0, stream>>>(a);
+    const unsigned rows = (unsigned)((int64_t)batch * n_q);
+    if (max_entries <= kTopkSmemKeys) {
+        const int smem = (int)(((max_entries + 3) & ~(int64_t)3) * sizeof(uint32_t));
+        cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        topk_kernel<true><<<rows, kTopkThreads, smem, stream>>>(a);
+    } else {
+        topk_kernel<false><<<rows, kTopkThreads, 0, stream>>>(a);
+    }
     return check_launch("lca_topk");
 }
 
@@ -433,8 +477,9 @@ lca_status lca_window_update(const lca_attn_params *p, int batch, const lca_bf16
     LCA_REQUIRE(tok_v && tok_pos0 && gamma && win_kv, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
     LCA_REQUIRE(aligned16(tok_v) && aligned16(win_kv) && tok_v_batch_stride % 8 == 0 && win_batch_stride % 8 == 0,
                 LCA_ERR_INVALID_ARG, "%s: misaligned pointer or stride", name);
-    LCA_REQUIRE(p->rope_dims >= 0 && p->rope_dims % 2 == 0 && p->rope_dims <= width, LCA_ERR_INVALID_ARG,
-                "%s: bad rope_dims", name);
+    LCA_REQUIRE(p->rope_dims >= 0 && p->rope_dims % 2 == 0 && p->rope_dims <= width &&
+                    p->rope_dims <= 2 * kMaxRopePairs && (p->rope_dims == 0 || p->rope_base > 1.0f),
+                LCA_ERR_INVALID_ARG, "%s: bad rope_dims / rope_base", name);
     if (n_tok == 0) return ok();
     WindowArgs a;
     a.width = width;

@@ -10,8 +10,9 @@
 // select (11 + 11 + 10 bits, shared-memory histograms) finds the exact k-th key T and how
 // many keys equal to T are needed; a final pass in index order, with one block scan per
 // chunk, writes every key > T and the first `need` keys == T, which yields ascending
-// indices directly.  The scores are read four times; for decode rows (<= 1 MiB) the
-// re-reads hit L2.
+// indices directly.  Rows of up to kTopkSmemKeys entries (decode) are read from global
+// memory once and kept as keys in shared memory for all four passes; longer rows are read
+// four times.
 #pragma once
 
 #include "common.cuh"
@@ -20,6 +21,7 @@ namespace lca {
 
 constexpr int kTopkThreads = 512;
 constexpr int kTopkBins = 2048;
+constexpr int kTopkSmemKeys = 49152;      // 192 KB of keys in shared memory
 
 struct TopkArgs {
     const float *scores; int64_t row_stride;   // row (b*n_q + i)
@@ -55,7 +57,9 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_tot, int &t
     return x - v + (warp > 0 ? warp_tot[warp - 1] : 0);
 }
 
+template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
+    extern __shared__ uint32_t skeys[];        // SMEM: the row's keys
     __shared__ int hist[kTopkBins];
     __shared__ int warp_tot[kTopkThreads / 32];
     __shared__ int sel_bin, sel_above;
@@ -73,17 +77,36 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
         for (int i = threadIdx.x; i < k; i += blockDim.x) out[i] = i < n ? i : -1;
         return;
     }
+    const bool vec4 = ((a.row_stride & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15) == 0);
+    if constexpr (SMEM) {
+        const int64_t n4 = vec4 ? n / 4 : 0;
+        for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
+            const float4 f = __ldg(reinterpret_cast<const float4 *>(s) + i);
+            reinterpret_cast<uint4 *>(skeys)[i] =
+                make_uint4(ordered_key(f.x), ordered_key(f.y), ordered_key(f.z), ordered_key(f.w));
+        }
+        for (int64_t i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) skeys[i] = ordered_key(__ldg(s + i));
+        __syncthreads();
+    }
+    auto key_at = [&](int64_t i) -> uint32_t {
+        if constexpr (SMEM) return skeys[i];
+        else return ordered_key(__ldg(s + i));
+    };
     // ---- radix select of the k-th largest key ----
     uint32_t prefix = 0, mask = 0;
     int remaining = k;     // keys still to take among those matching prefix
     const int shifts[3] = {21, 10, 0};
     const int widths[3] = {11, 11, 10};
-    const bool vec4 = ((a.row_stride & 3) == 0) && ((reinterpret_cast<uintptr_t>(a.scores) & 15) == 0);
     for (int pass = 0; pass < 3; ++pass) {
         const int sh = shifts[pass], nb = 1 << widths[pass];
         for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
         __syncthreads();
-        if (vec4) {
+        if (SMEM) {
+            for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+                const uint32_t key = skeys[i];
+                if ((key & mask) == prefix) atomicAdd(&hist[(key >> sh) & (nb - 1)], 1);
+            }
+        } else if (vec4) {
             const int64_t n4 = n / 4;
             for (int64_t i = threadIdx.x; i < n4; i += blockDim.x) {
                 const float4 f = __ldg(reinterpret_cast<const float4 *>(s) + i);
@@ -140,7 +163,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
         int gt = 0, eq = 0;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            keys[u] = i0 + u < n ? ordered_key(__ldg(s + i0 + u)) : 0u;
+            keys[u] = i0 + u < n ? key_at(i0 + u) : 0u;
             const bool in = i0 + u < n;
             gt += (in && keys[u] > T);
             eq += (in && keys[u] == T);
