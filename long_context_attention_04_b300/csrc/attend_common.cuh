@@ -34,7 +34,7 @@ struct AttendArgs {
     const float *sink;            // [H]
     // split-K partials: O [unit][split][H][C] fp32 (unnormalised), m/l [unit][split][H] (base 2)
     float *part_o, *part_m, *part_l;
-    uint8_t *q_lo_img;            // per-CTA image of the query's bf16 lo part (tensor-core kernel)
+    uint8_t *q_img;               // per-query images of the prepared query: [unit][hi | lo] (q_prep_kernel)
     __nv_bfloat16 *out;           // [B][n_q][H][C]
     float *lse;                   // [B][n_q][H] or nullptr
 };
@@ -109,9 +109,14 @@ __device__ __forceinline__ void split_range(int64_t n_rows, int tile_rows, int s
 
 // Query prologue for head h (one warp): RMSNorm over C with gamma_q, then RoPE(pos) on the
 // trailing R dims.  Lane l holds elements [l*EPL, l*EPL+EPL) in v[] on return.
+// cos/sin of the R/2 RoPE angles at position pos, one pair per thread (threads [0, R/2)).
+__device__ __forceinline__ void rope_table_fill(const AttendArgs &a, int64_t pos, float *cs, float *sn) {
+    for (int d = threadIdx.x; d < a.R / 2; d += blockDim.x) rope_cs(a.rope, d, pos, cs[d], sn[d]);
+}
+
 template <int C>
-__device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const __nv_bfloat16 *qh, int64_t pos,
-                                           float *v) {
+__device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const __nv_bfloat16 *qh, const float *rcs,
+                                           const float *rsn, float *v) {
     constexpr int EPL = C / 32;   // elements per lane (4, 8 or 16)
     const int lane = threadIdx.x & 31;
     const uint4 *src = reinterpret_cast<const uint4 *>(qh + lane * EPL);
@@ -137,8 +142,7 @@ __device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const __nv_bfloa
             if (in_rope) {
                 const int e = lane * EPL + u;
                 const int d = lower ? e - first : e - first - half;
-                float cs, sn;
-                rope_cs(a.rope, d, pos, cs, sn);
+                const float cs = rcs[d], sn = rsn[d];
                 v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
             }
         }
@@ -147,8 +151,8 @@ __device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const __nv_bfloa
 
 // Specialisation helper for C = 128 (4 elements per lane: one 8-byte load).
 template <>
-__device__ __forceinline__ void q_hat_warp<128>(const AttendArgs &a, const __nv_bfloat16 *qh, int64_t pos,
-                                                float *v) {
+__device__ __forceinline__ void q_hat_warp<128>(const AttendArgs &a, const __nv_bfloat16 *qh, const float *rcs,
+                                                const float *rsn, float *v) {
     constexpr int C = 128, EPL = 4;
     const int lane = threadIdx.x & 31;
     const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(qh + lane * EPL));
@@ -170,8 +174,7 @@ __device__ __forceinline__ void q_hat_warp<128>(const AttendArgs &a, const __nv_
             if (in_rope) {
                 const int e = lane * EPL + u;
                 const int d = lower ? e - first : e - first - half;
-                float cs, sn;
-                rope_cs(a.rope, d, pos, cs, sn);
+                const float cs = rcs[d], sn = rsn[d];
                 v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
             }
         }

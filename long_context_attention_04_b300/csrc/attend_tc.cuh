@@ -9,19 +9,22 @@
 // Multi-Query Attention shares one key/value row set across all heads, so a 128-row tile
 // of rows against all (padded to 64) heads is a dense contraction.  Both products run
 // transposed so that every MMA has M = 128:
-//   S^T[row, head]  = KV[row, c] . Qhat[head, c]^T        (M = 128 rows,  N = 64, K = c)
+//   S^T[row, head]  = KV[row, c] . Qhat[head, c]^T        (M = 128 rows,  N = 2 x 64, K = c)
 //   O^T[c, head]   += KV[row, c]^T . P^T[row, head]       (M = 128 c,     N = 64, K = 128 rows)
 // The same 128-byte-swizzled shared-memory tile serves as the K-major A operand of the first
 // product and the MN-major A operand of the second.  S^T (two buffers) and O^T (c/128
 // chunks) live in TMEM; P^T goes through shared memory in bf16.
 //
-// The normalised, rotated query is split into bf16 hi + lo parts (q = hi + lo to ~16 bits)
-// and S^T accumulates KV.hi^T + KV.lo^T in fp32: a single bf16 query would put a relative
-// error of 2^-9 on every logit, comparable to the bf16 rounding of the output itself.
-// Shared memory holds the 64 KB hi tile and a ring of three 48 KB slots, each a 128-row x
-// 128-c KV chunk plus the matching 16 KB lo chunk (bulk-copied from this CTA's workspace
-// image).  A 128-row tile at c = 512 does not fit twice next to the query, so each tile is
-// streamed twice, once for S and once for PV, the second time from L2; HBM sees one pass.
+// The normalised, rotated query (q_prep_kernel) is split into bf16 hi + lo parts (q = hi + lo
+// to ~16 bits) and S^T accumulates KV.hi^T + KV.lo^T in fp32: a single bf16 query would put a
+// relative error of 2^-9 on every logit, comparable to the bf16 rounding of the output.
+// The query is not kept resident: each S chunk of KV (128 rows x 128 c) comes with the matching
+// 32 KB query chunk (hi and lo stacked as one 128-row B operand, from the L2-hot image), and one
+// N = 128 MMA per k step yields hi and lo logits side by side, summed by the softmax.  Shared
+// memory holds a ring of four 32 KB KV slots, a ring of two 32 KB query slots and two 16 KB
+// P^T buffers.  A 128-row tile at c = 512 does not fit twice next to the query,
+// so each tile is streamed twice, once for S and once for PV, the second time from L2; HBM
+// sees one pass, and upcoming contiguous tiles are prefetched into L2 two tiles ahead.
 //
 // Rows of a query: compressed rows (CSA: the selected entries; HCA: entries 0..n_vis), then
 // the window rows; tiles never mix the two.  All loads are TMA: contiguous compressed tiles
@@ -41,15 +44,16 @@
 
 #include "attend_common.cuh"
 #include "ptx.cuh"
+#include "q_prep.cuh"
 
 namespace lca {
 
 constexpr int kAtHP = 64;                                // padded heads (MMA N)
 constexpr int kAtTile = 128;                             // rows per tile (MMA M of S^T)
-constexpr int kAtSlots = 3;                              // chunk slots in the ring
+constexpr int kAtSlots = 4;                              // KV chunk slots: one whole tile (c = 512)
+constexpr int kAtQSlots = 2;                             // query chunk slots
 constexpr int kAtChunkBytes = 128 * 128 * 2;             // KV chunk: 128 rows x 128 c
-constexpr int kAtLoChunkBytes = kAtHP * 128 * 2;         // q lo chunk: 64 heads x 128 c
-constexpr int kAtSlotBytes = kAtChunkBytes + kAtLoChunkBytes;
+constexpr int kAtQChunkBytes = kQChunkBytes;             // query chunk: (64 hi + 64 lo) x 128 c
 constexpr int kAtProducerWarp = 0;
 constexpr int kAtMmaWarp = 1;
 constexpr int kAtSoftmaxWarp0 = 2;
@@ -60,15 +64,12 @@ constexpr float kAtTau = 8.0f;                           // log2 headroom before
 template <int C>
 struct AttendTcConfig {
     static constexpr int CC = C / 128;                        // c chunks per row
-    static constexpr int Q_BYTES = kAtHP * C * 2;
     static constexpr int P_BYTES = kAtTile * kAtHP * 2;       // the P^T buffer (16 KB)
-    static constexpr int TMEM_S = 0;                          // two S^T buffers: columns 0..127
+    static constexpr int TMEM_S = 0;                          // S^T: 128 columns (hi | lo)
     static constexpr int TMEM_O = 2 * kAtHP;                  // O^T chunk j at TMEM_O + 64 j
-    static constexpr int TMEM_NEED = TMEM_O + CC * kAtHP;
-    static constexpr int TMEM_COLS = TMEM_NEED <= 256 ? 256 : 512;
-    static constexpr int LO_IMAGE_BYTES = CC * kAtLoChunkBytes;  // per CTA, in the workspace
+    static constexpr int TMEM_COLS = 512;
     static constexpr int MISC = 1280;                          // barriers, votes, cross-warp maxima
-    static constexpr int SMEM_BYTES = MISC + 1024 + Q_BYTES + kAtSlots * kAtSlotBytes + P_BYTES;
+    static constexpr int SMEM_BYTES = MISC + 1024 + CC * kAtChunkBytes + kAtQSlots * kAtQChunkBytes + P_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
@@ -110,12 +111,14 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     uint8_t *misc = smem_raw;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw + Cfg::MISC) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *q_tile = base;                                   // hi: C/64 boxes of [64 heads x 128 B]
-    uint8_t *ring = q_tile + Cfg::Q_BYTES;                    // slots: KV [2 x 128 rows x 128 B] + lo chunk
-    uint8_t *p_buf = ring + kAtSlots * kAtSlotBytes;          // [128 rows x 128 B]
+    uint8_t *ring = base;                                     // KV slot j = chunk j: 2 boxes [128 rows x 128 B]
+    uint8_t *q_ring = ring + CC * kAtChunkBytes;              // query slots: 2 boxes [128 rows x 128 B]
+    uint8_t *p_buf = q_ring + kAtQSlots * kAtQChunkBytes;     // [128 rows x 128 B]
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + kAtSlots;
-    uint64_t *s_full = empty + kAtSlots;
+    uint64_t *q_full = empty + kAtSlots;
+    uint64_t *q_empty = q_full + kAtQSlots;
+    uint64_t *s_full = q_empty + kAtQSlots;
     uint64_t *s_empty = s_full + 2;
     uint64_t *p_full = s_empty + 2;
     uint64_t *pv_done = p_full + 2;
@@ -135,7 +138,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     const int64_t t0 = (int64_t)tm.total() * split / a.splits;
     const int64_t t1 = (int64_t)tm.total() * (split + 1) / a.splits;
     const int64_t pidx0 = ((int64_t)unit * a.splits + split) * a.H;
-    uint8_t *lo_img = a.q_lo_img + ((int64_t)unit * a.splits + split) * Cfg::LO_IMAGE_BYTES;
+    const uint8_t *qimg = q_img<C>(a, unit);
 
     if (t0 >= t1) {   // nothing to do for this split: mark it empty for the combine
         for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
@@ -145,11 +148,23 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         return;
     }
 
-    // ---- set-up: barriers, TMEM, the normalised and rotated query (hi in smem, lo image) ----
+    // Contiguous (HCA) tiles: start pulling the first two tiles into L2 now, behind the prologue.
+    constexpr int kPrefetchTiles = 2;
+    if (!L.idx && threadIdx.x == 32) {
+        const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
+        for (int64_t t = t0; t < t1 && t < t0 + kPrefetchTiles && t < tm.tc; ++t)
+            for (int x = 0; x < C; x += 64) ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + t * kAtTile));
+    }
+
+    // ---- set-up: barriers, TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kAtSlots; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < kAtQSlots; ++s) {
+            ptx::mbar_init(&q_full[s], 1);
+            ptx::mbar_init(&q_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(&s_full[s], 1);
@@ -167,43 +182,6 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         ptx::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
         ptx::tmem_relinquish();
     }
-    for (int h = warp; h < kAtHP; h += kAtThreads / 32) {
-        constexpr int EPL = C / 32;
-        float v[EPL];
-        if (h < a.H) {
-            q_hat_warp<C>(a, a.q + ((int64_t)unit * a.H + h) * C, L.pos, v);
-        } else {
-#pragma unroll
-            for (int u = 0; u < EPL; ++u) v[u] = 0.f;
-        }
-        // hi = bf16(q), lo = bf16(q - hi); lane holds elements [lane*EPL, lane*EPL + EPL)
-        float lo[EPL];
-#pragma unroll
-        for (int u = 0; u < EPL; ++u) {
-            const float hi = __bfloat162float(__float2bfloat16_rn(v[u]));
-            lo[u] = v[u] - hi;
-            v[u] = hi;
-        }
-        // hi -> resident tile (box e/64); lo -> image: chunk e/128, box (e%128)/64
-        if constexpr (EPL >= 8) {
-#pragma unroll
-            for (int u = 0; u < EPL; u += 8) {
-                const int e = lane * EPL + u;
-                const uint32_t off = ptx::sw128_offset(h, (e % 64) / 8);
-                *reinterpret_cast<uint4 *>(q_tile + (e / 64) * (kAtHP * 128) + off) = pack8(v + u);
-                *reinterpret_cast<uint4 *>(lo_img + (e / 64) * (kAtHP * 128) + off) = pack8(lo + u);
-            }
-        } else {
-            const int e = lane * EPL;   // 4 elements: half a chunk
-            const uint32_t off = ptx::sw128_offset(h, (e % 64) / 8) + (e % 8) * 2;
-            *reinterpret_cast<uint2 *>(q_tile + (e / 64) * (kAtHP * 128) + off) =
-                make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
-            *reinterpret_cast<uint2 *>(lo_img + (e / 64) * (kAtHP * 128) + off) =
-                make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
-        }
-    }
-    ptx::fence_proxy_async();          // hi tile: generic writes -> tensor-core reads
-    ptx::fence_proxy_async_global();   // lo image: generic writes -> bulk-copy reads
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
@@ -212,8 +190,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
 
     if (warp == kAtProducerWarp) {
         // ------------------------------------------------------------ producer ----
-        // Chunk loads in consumption order: S(t0), then per tile S(t), PV(t-1), finally PV(t1-1).
-        const int total_loads = CC * (2 * n_tiles);
+        // Per tile t: for each chunk j, query chunk j into the query ring and KV chunk j of
+        // tile t into slot j (once PV(t-1) has released it).
         const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
         const int64_t win_row0 = (int64_t)b * (a.win_bs / C);
         if (lane == 0) {
@@ -222,137 +200,127 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             ptx::tma_prefetch(&win_row_map);
         }
         bool ok = true;
-        for (int n = 0; n < total_loads && ok && !*abort_flag; ++n) {
-            const int j = n % CC;
-            const int g = n / CC;                 // 0 = S(t0); then pairs S(t0+k), PV(t0+k-1)
-            int t;
-            bool s_pass;
-            if (g == 0) {
-                t = (int)t0;
-                s_pass = true;
-            } else if (g == 2 * n_tiles - 1) {
-                t = (int)t1 - 1;
-                s_pass = false;
-            } else {
-                const int k = (g + 1) / 2;
-                s_pass = (g & 1) != 0;
-                t = (int)t0 + (s_pass ? k : k - 1);
+        int q_n = 0;   // query chunk loads issued
+        for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
+            const int t = (int)t0 + u;
+            if (!L.idx && lane == 1) {
+                const int tp = t + kPrefetchTiles;   // keep HBM reads two tiles ahead
+                if (tp < t1 && tp < tm.tc)
+                    for (int x = 0; x < C; x += 64)
+                        ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + (int64_t)tp * kAtTile));
             }
-            const int s = n % kAtSlots;
-            if (n >= kAtSlots && !ptx::mbar_wait(&empty[s], ((n / kAtSlots) - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            uint8_t *slot = ring + s * kAtSlotBytes;
-            if (lane == 0) ptx::mbar_arrive_expect_tx(&full[s], kAtChunkBytes + (s_pass ? kAtLoChunkBytes : 0));
-            __syncwarp();
-            const uint32_t dst = ptx::smem_u32(slot);
-            if (t < tm.tc && !L.idx) {
-                // contiguous compressed rows: two 64-c boxes of 128 rows
-                if (lane < 2)
-                    ptx::tma_load_2d(dst + lane * (128 * 128), &kv_tile_map, j * 128 + lane * 64,
-                                     (int)(kv_row0 + (int64_t)t * kAtTile), &full[s]);
-            } else {
-                // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, for both c boxes
-                int rc[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int r = 4 * lane + i;
-                    int coord = -1;
-                    if (t < tm.tc) {
-                        const int64_t R = (int64_t)t * kAtTile + r;
-                        if (R < L.n_comp) {
-                            const int32_t e = __ldg(L.idx + R);
-                            if (e >= 0 && e < a.cache_rows) coord = (int)(kv_row0 + e);
-                            else if (e >= a.cache_rows && s_pass && j == 0) raise_error(LCA_DEVERR_INDEX_RANGE);
-                        }
-                    } else {
-                        const int R = (t - tm.tc) * kAtTile + r;
-                        if (R < L.n_win) {
-                            int64_t slot_row = L.win_slot0 + R;       // at most one wrap: n_win <= W <= win_cap
-                            if (slot_row >= a.win_cap) slot_row -= a.win_cap;
-                            coord = (int)(win_row0 + slot_row);
-                        }
-                    }
-                    rc[i] = coord;
+            for (int j = 0; j < CC && ok; ++j) {
+                // query chunk j
+                const int qs = q_n % kAtQSlots;
+                if (q_n >= kAtQSlots && !ptx::mbar_wait(&q_empty[qs], ((q_n / kAtQSlots) - 1) & 1)) {
+                    ok = false;
+                    break;
                 }
-                const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(&q_full[qs], kAtQChunkBytes);
+                    ptx::bulk_load(ptx::smem_u32(q_ring + qs * kAtQChunkBytes), qimg + j * kAtQChunkBytes,
+                                   kAtQChunkBytes, &q_full[qs]);
+                }
+                ++q_n;
+                // KV chunk j of tile t
+                if (u > 0 && !ptx::mbar_wait(&empty[j], (u - 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t *slot = ring + j * kAtChunkBytes;
+                if (lane == 0) ptx::mbar_arrive_expect_tx(&full[j], kAtChunkBytes);
+                __syncwarp();
+                const uint32_t dst = ptx::smem_u32(slot);
+                if (t < tm.tc && !L.idx) {
+                    // contiguous compressed rows: two 64-c boxes of 128 rows
+                    if (lane < 2)
+                        ptx::tma_load_2d(dst + lane * (128 * 128), &kv_tile_map, j * 128 + lane * 64,
+                                         (int)(kv_row0 + (int64_t)t * kAtTile), &full[j]);
+                } else {
+                    // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, for both c boxes
+                    int rc[4];
 #pragma unroll
-                for (int bx = 0; bx < 2; ++bx)
-                    ptx::tma_gather4(dst + bx * (128 * 128) + lane * 512, map, j * 128 + bx * 64, rc[0], rc[1], rc[2],
-                                     rc[3], &full[s]);
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 4 * lane + i;
+                        int coord = -1;
+                        if (t < tm.tc) {
+                            const int64_t R = (int64_t)t * kAtTile + r;
+                            if (R < L.n_comp) {
+                                const int32_t e = __ldg(L.idx + R);
+                                if (e >= 0 && e < a.cache_rows) coord = (int)(kv_row0 + e);
+                                else if (e >= a.cache_rows && j == 0) raise_error(LCA_DEVERR_INDEX_RANGE);
+                            }
+                        } else {
+                            const int R = (t - tm.tc) * kAtTile + r;
+                            if (R < L.n_win) {
+                                int64_t slot_row = L.win_slot0 + R;   // at most one wrap: n_win <= W <= win_cap
+                                if (slot_row >= a.win_cap) slot_row -= a.win_cap;
+                                coord = (int)(win_row0 + slot_row);
+                            }
+                        }
+                        rc[i] = coord;
+                    }
+                    const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
+#pragma unroll
+                    for (int bx = 0; bx < 2; ++bx)
+                        ptx::tma_gather4(dst + bx * (128 * 128) + lane * 512, map, j * 128 + bx * 64, rc[0], rc[1],
+                                         rc[2], rc[3], &full[j]);
+                }
             }
-            if (s_pass && lane == 0)   // the lo part of query chunk j (16 KB, already swizzled)
-                ptx::bulk_load(dst + kAtChunkBytes, lo_img + j * kAtLoChunkBytes, kAtLoChunkBytes, &full[s]);
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------- MMA issue ----
+        // Per tile: S^T = KV . [hi | lo]^T chunk by chunk; then, once the softmax has written P,
+        // O^T += V^T P^T chunk by chunk, releasing each KV slot to the producer.  tcgen05 ops
+        // execute in issue order, so S(t+1) never overwrites S^T or P^T still in use.
         if (lane == 0) {
-            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, kAtHP, false, false);
+            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 2 * kAtHP, false, false);
             constexpr uint32_t idesc_o = ptx::idesc_bf16(128, kAtHP, true, true);
-            const uint32_t q_addr = ptx::smem_u32(q_tile);
             const uint32_t p_addr = ptx::smem_u32(p_buf);
-            uint32_t used = 0;   // chunk slots consumed
+            uint32_t q_used = 0;
             bool ok = true;
-            auto take = [&]() -> uint32_t {   // wait for the next chunk; returns its smem address
-                const int s = used % kAtSlots;
-                if (!ptx::mbar_wait(&full[s], (used / kAtSlots) & 1)) return 0;
-                ptx::tc_fence_after();
-                return ptx::smem_u32(ring + s * kAtSlotBytes);
-            };
-            auto issue_s = [&](int u) -> bool {   // S^T of relative tile u: KV . (hi + lo)^T
-                const int buf = u & 1;
-                if (u >= 2 && !ptx::mbar_wait(&s_empty[buf], ((u >> 1) - 1) & 1)) return false;
-                ptx::tc_fence_after();
-                const uint32_t d = tmem + Cfg::TMEM_S + buf * kAtHP;
-                for (int j = 0; j < CC; ++j) {
-                    const uint32_t slot = take();
-                    if (!slot) return false;
+            for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
+                const uint32_t d = tmem + Cfg::TMEM_S;
+                for (int j = 0; j < CC && ok; ++j) {
+                    const int qs = q_used % kAtQSlots;
+                    if (!ptx::mbar_wait(&full[j], u & 1) || !ptx::mbar_wait(&q_full[qs], (q_used / kAtQSlots) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t slot = ptx::smem_u32(ring + j * kAtChunkBytes);
+                    const uint32_t q_addr = ptx::smem_u32(q_ring + qs * kAtQChunkBytes);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t ad = ptx::smem_desc(slot + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024,
                                                            ptx::kSwizzle128);
-                        const uint64_t bh = ptx::smem_desc(q_addr + (2 * j + (kk >> 2)) * (kAtHP * 128) +
-                                                               (kk & 3) * 32,
-                                                           16, 1024, ptx::kSwizzle128);
-                        const uint64_t bl = ptx::smem_desc(slot + kAtChunkBytes + (kk >> 2) * (kAtHP * 128) +
-                                                               (kk & 3) * 32,
-                                                           16, 1024, ptx::kSwizzle128);
-                        ptx::mma_bf16(d, ad, bh, idesc_s, (j > 0 || kk > 0));
-                        ptx::mma_bf16(d, ad, bl, idesc_s, 1);
+                        const uint64_t bd = ptx::smem_desc(q_addr + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024,
+                                                           ptx::kSwizzle128);
+                        ptx::mma_bf16(d, ad, bd, idesc_s, (j > 0 || kk > 0));
                     }
-                    ptx::mma_commit(&empty[used % kAtSlots]);
-                    ++used;
+                    ptx::mma_commit(&q_empty[qs]);
+                    ++q_used;
                 }
-                ptx::mma_commit(&s_full[buf]);
-                return true;
-            };
-            auto issue_pv = [&](int u) -> bool {   // O^T += V^T P^T of relative tile u
-                const int buf = u & 1;
-                if (!ptx::mbar_wait(&p_full[buf], (u >> 1) & 1)) return false;
+                if (!ok) break;
+                ptx::mma_commit(&s_full[0]);
+                if (!ptx::mbar_wait(&p_full[0], u & 1)) {
+                    ok = false;
+                    break;
+                }
                 ptx::tc_fence_after();
                 for (int j = 0; j < CC; ++j) {
-                    const uint32_t slot = take();
-                    if (!slot) return false;
+                    const uint32_t slot = ptx::smem_u32(ring + j * kAtChunkBytes);
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t ad = ptx::smem_desc(slot + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
                         const uint64_t bd = ptx::smem_desc(p_addr + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
                         ptx::mma_bf16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bd, idesc_o, (u > 0 || kk > 0));
                     }
-                    ptx::mma_commit(&empty[used % kAtSlots]);
-                    ++used;
+                    ptx::mma_commit(&empty[j]);
                 }
-                ptx::mma_commit(&pv_done[buf]);
-                return true;
-            };
-            ok = issue_s(0);
-            for (int u = 1; u < n_tiles && ok && !*abort_flag; ++u) {
-                ok = issue_s(u);
-                if (ok) ok = issue_pv(u - 1);
+                ptx::mma_commit(&pv_done[0]);
             }
-            if (ok && !*abort_flag) ok = issue_pv(n_tiles - 1);
             if (!ok) *abort_flag = 1;
             ptx::mma_commit(teardown);
             ptx::mbar_wait(teardown, 0);
@@ -373,23 +341,21 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         uint32_t votes_done = 0, reds_done = 0;
         bool ok = true;
         for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
-            const int buf = u & 1;
-            if (!ptx::mbar_wait(&s_full[buf], (u >> 1) & 1)) {
+            if (!ptx::mbar_wait(&s_full[0], u & 1)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             float x[32];
             {
-                uint32_t v[32];
-                ptx::tmem_ld32(lane_addr + Cfg::TMEM_S + buf * kAtHP + half * 32, v);
+                uint32_t vh[32], vl[32];
+                ptx::tmem_ld32(lane_addr + Cfg::TMEM_S + half * 32, vh);
+                ptx::tmem_ld32(lane_addr + Cfg::TMEM_S + kAtHP + half * 32, vl);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(v[h]);
+                for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(vh[h]) + __uint_as_float(vl[h]);
             }
             ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&s_empty[buf]);
             const bool valid = tile_row_valid(a, L, tm, (int)t0 + u, r);
             bool need = false;
 #pragma unroll
@@ -427,14 +393,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                     break;
                 }
                 ++reds_done;
-                // O^T holds data once PV of the previous tile is done: wait for it, then rescale
-                if (u > 0) {
-                    if (!ptx::mbar_wait(&pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                }
+                // O^T: PV of the previous tile completed before S^T of this tile (in-order execution)
 #pragma unroll
                 for (int h0 = 0; h0 < 32; h0 += 16) {
                     float alpha[16];
@@ -466,14 +425,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 }
                 ptx::tc_fence_before();
             }
-            // probabilities of this row, written as a bf16 P^T row (32 heads = 4 chunks) into the
-            // single P buffer once PV of the previous tile has read it
-            if (u >= 1) {
-                if (!ptx::mbar_wait(&pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-            }
+            // probabilities of this row, written as a bf16 P^T row (32 heads = 4 chunks); PV of the
+            // previous tile, the last reader of P^T, completed before S^T of this tile
             float pr[32];
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
@@ -485,12 +438,11 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             for (int c4 = 0; c4 < 4; ++c4)
                 *reinterpret_cast<uint4 *>(p_buf + ptx::sw128_offset(r, half * 4 + c4)) = pack8(pr + 8 * c4);
             ptx::fence_proxy_async();
-            ptx::mbar_arrive(&p_full[buf]);
+            ptx::mbar_arrive(&p_full[0]);
         }
         if (!ok) *abort_flag = 1;
         // ---- the split's results: row sums, running max, unnormalised O ----
-        if (ok && !*abort_flag &&
-            ptx::mbar_wait(&pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1)) {
+        if (ok && !*abort_flag && ptx::mbar_wait(&pv_done[0], (n_tiles - 1) & 1)) {
             ptx::tc_fence_after();
             // row sums over the 128 rows; the P buffer is free now (every PV is done)
             float *lsum = reinterpret_cast<float *>(p_buf);

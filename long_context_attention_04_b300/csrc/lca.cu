@@ -174,7 +174,7 @@ struct AttendPlan {
     int64_t units;
     size_t part_bytes;       // O partials
     size_t ml_bytes;         // m and l partials
-    size_t lo_bytes;         // per-CTA query lo images
+    size_t img_bytes;        // per-query hi / lo images of the prepared query
     size_t total;
 };
 
@@ -194,8 +194,8 @@ AttendPlan plan_attend(const lca_attn_params *p, int batch, int n_q, int64_t max
     pl.splits = (int)s;
     pl.part_bytes = (size_t)pl.units * pl.splits * p->heads * p->head_dim * sizeof(float);
     pl.ml_bytes = (size_t)pl.units * pl.splits * p->heads * sizeof(float);
-    pl.lo_bytes = (size_t)pl.units * pl.splits * (p->head_dim / 128) * kAtLoChunkBytes;
-    pl.total = pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255) + pl.lo_bytes;
+    pl.img_bytes = (size_t)pl.units * (p->head_dim / 128) * kQChunkBytes;
+    pl.total = pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255) + pl.img_bytes;
     return pl;
 }
 
@@ -272,7 +272,7 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     a.part_o = reinterpret_cast<float *>(w);
     a.part_m = reinterpret_cast<float *>(w + pl.part_bytes);
     a.part_l = reinterpret_cast<float *>(w + pl.part_bytes + ((pl.ml_bytes + 255) & ~(size_t)255));
-    a.q_lo_img = reinterpret_cast<uint8_t *>(w + pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255));
+    a.q_img = reinterpret_cast<uint8_t *>(w + pl.part_bytes + 2 * ((pl.ml_bytes + 255) & ~(size_t)255));
     a.out = reinterpret_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
     LCA_REQUIRE(pl.units <= 0x7fffffff, LCA_ERR_UNSUPPORTED, "%s: too many queries", name);
@@ -289,6 +289,14 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
         !make_tensor_map(&kv_row_map, kv, 2, dims_kv, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&win_row_map, win, 2, dims_win, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B))
         return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
+    const dim3 prep_grid((unsigned)pl.units, kQImgHeads / kQPrepHeads);
+    switch (C) {
+    case 128: q_prep_kernel<128><<<prep_grid, 32 * kQPrepHeads, 0, stream>>>(a); break;
+    case 256: q_prep_kernel<256><<<prep_grid, 32 * kQPrepHeads, 0, stream>>>(a); break;
+    default: q_prep_kernel<512><<<prep_grid, 32 * kQPrepHeads, 0, stream>>>(a); break;
+    }
+    st = check_launch(name);
+    if (st != LCA_OK) return st;
     switch (C) {
     case 128:
         cudaFuncSetAttribute(attend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,

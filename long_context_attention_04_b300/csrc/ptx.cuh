@@ -105,6 +105,13 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Prefetch a 2D box of a tensor map into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 4-row gather: rows r0..r3 (x = first element) of a 2D tensor map whose box is one row
 // high land in four consecutive box rows at dst; out-of-range rows read as zero.
 __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *map, int x, int r0, int r1, int r2,

@@ -1,0 +1,77 @@
+// q_prep.cuh -- the query side of core attention, computed once per query for all its
+// split-K CTAs: RMSNorm over c with gamma_q ("Q/KV normalization"), RoPE at the query
+// position on the trailing R dims ("Partial RoPE"), then the split q = hi + lo into two bf16
+// parts (DeepSeek-V4 hybrid attention, gxgjx.lffhtl.com/lxrt/355279.html, section 混肃穆力机制).
+//
+// Output: per query, an image of [c/128 chunks][2 boxes of 64 c][128 rows][128 bytes], rows
+// 0-63 the hi parts of heads 0-63 and rows 64-127 their lo parts, 128-byte swizzled (16-byte
+// chunk index XOR row % 8): exactly the shared-memory layout of the K-major B operand the
+// attention kernel feeds to tcgen05.mma (N = 128), so the attention kernel bulk-copies one
+// 32 KB chunk next to each KV chunk it multiplies.  Heads past H are zero rows.
+#pragma once
+
+#include "attend_common.cuh"
+
+namespace lca {
+
+constexpr int kQPrepHeads = 8;              // heads (warps) per CTA
+constexpr int kQImgHeads = 64;              // padded heads of an image
+
+constexpr int kQChunkBytes = 2 * 128 * 128;   // one c chunk of the image: 2 boxes x 128 rows x 128 B
+
+template <int C>
+__device__ __forceinline__ uint8_t *q_img(const AttendArgs &a, int64_t unit) {
+    return a.q_img + unit * (int64_t)((C / 128) * kQChunkBytes);
+}
+
+__host__ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
+    return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
+}
+
+// grid (units, 64 / kQPrepHeads), block 32 * kQPrepHeads: warp w prepares head blockIdx.y*8 + w.
+template <int C>
+__global__ void __launch_bounds__(32 * kQPrepHeads) q_prep_kernel(AttendArgs a) {
+    __shared__ float rcs[64], rsn[64];
+    const int64_t unit = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = blockIdx.y * kQPrepHeads + warp;
+    int64_t pos = a.q_pos[unit];
+    if (pos < 0) pos = 0;
+    rope_table_fill(a, pos, rcs, rsn);
+    __syncthreads();
+    constexpr int EPL = C / 32;
+    float v[EPL];
+    if (h < a.H) {
+        q_hat_warp<C>(a, a.q + (unit * a.H + h) * C, rcs, rsn, v);
+    } else {
+#pragma unroll
+        for (int u = 0; u < EPL; ++u) v[u] = 0.f;
+    }
+    float lo[EPL];
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) {
+        const float hi = __bfloat162float(__float2bfloat16_rn(v[u]));
+        lo[u] = v[u] - hi;
+        v[u] = hi;
+    }
+    uint8_t *img = q_img<C>(a, unit);
+    // element e of head h: chunk e/128, box (e%128)/64, rows h (hi) and 64 + h (lo)
+    if constexpr (EPL >= 8) {
+#pragma unroll
+        for (int u = 0; u < EPL; u += 8) {
+            const int e = lane * EPL + u;
+            uint8_t *box = img + (e / 128) * kQChunkBytes + ((e % 128) / 64) * (128 * 128);
+            *reinterpret_cast<uint4 *>(box + sw128(h, (e % 64) / 8)) = pack8(v + u);
+            *reinterpret_cast<uint4 *>(box + sw128(kQImgHeads + h, (e % 64) / 8)) = pack8(lo + u);
+        }
+    } else {
+        const int e = lane * EPL;   // 4 elements: half a 16-byte chunk
+        uint8_t *box = img + (e / 128) * kQChunkBytes + ((e % 128) / 64) * (128 * 128) + (e % 8) * 2;
+        *reinterpret_cast<uint2 *>(box + sw128(h, (e % 64) / 8)) =
+            make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        *reinterpret_cast<uint2 *>(box + sw128(kQImgHeads + h, (e % 64) / 8)) =
+            make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
+    }
+}
+
+}  // namespace lca
