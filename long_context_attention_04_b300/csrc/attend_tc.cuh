@@ -32,7 +32,8 @@
 // 4-row gathers; masked rows are fetched at coordinate -1 and arrive as zeros.
 //
 // Roles (one CTA per (query, split), one CTA per SM):
-//   warp 0      TMA producer
+//   warp 0      TMA producer of KV chunks
+//   warp 10     bulk-copy producer of query chunks
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-9   softmax: one TMEM lane (row) per thread, 32 heads per thread; online softmax
 //               in base 2 with a conditional rescale (the running max moves only when a
@@ -58,7 +59,8 @@ constexpr int kAtProducerWarp = 0;
 constexpr int kAtMmaWarp = 1;
 constexpr int kAtSoftmaxWarp0 = 2;
 constexpr int kAtSoftmaxWarps = 8;
-constexpr int kAtThreads = 32 * (kAtSoftmaxWarp0 + kAtSoftmaxWarps);
+constexpr int kAtQWarp = kAtSoftmaxWarp0 + kAtSoftmaxWarps;
+constexpr int kAtThreads = 32 * (kAtQWarp + 1);
 constexpr float kAtTau = 8.0f;                           // log2 headroom before the running max must move
 
 template <int C>
@@ -100,7 +102,7 @@ __device__ __forceinline__ bool tile_row_valid(const AttendArgs &a, const RowLis
 }
 
 // Register cap: the register file is split across the four SM sub-partitions (16K each) and
-// 10 warps place 3 warps on two of them, so 3 x 32 x 168 <= 16384.
+// 11 warps place 3 warps on three of them, so 3 x 32 x 168 <= 16384.
 template <int C>
 __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtensorMap kv_tile_map,
                                                   const __grid_constant__ CUtensorMap kv_row_map,
@@ -190,8 +192,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
 
     if (warp == kAtProducerWarp) {
         // ------------------------------------------------------------ producer ----
-        // Per tile t: for each chunk j, query chunk j into the query ring and KV chunk j of
-        // tile t into slot j (once PV(t-1) has released it).
+        // Per tile t: KV chunk j of tile t into slot j, once PV(t-1) has released it.
         const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
         const int64_t win_row0 = (int64_t)b * (a.win_bs / C);
         if (lane == 0) {
@@ -200,7 +201,6 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             ptx::tma_prefetch(&win_row_map);
         }
         bool ok = true;
-        int q_n = 0;   // query chunk loads issued
         for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
             const int t = (int)t0 + u;
             if (!L.idx && lane == 1) {
@@ -210,18 +210,6 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                         ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + (int64_t)tp * kAtTile));
             }
             for (int j = 0; j < CC && ok; ++j) {
-                // query chunk j
-                const int qs = q_n % kAtQSlots;
-                if (q_n >= kAtQSlots && !ptx::mbar_wait(&q_empty[qs], ((q_n / kAtQSlots) - 1) & 1)) {
-                    ok = false;
-                    break;
-                }
-                if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&q_full[qs], kAtQChunkBytes);
-                    ptx::bulk_load(ptx::smem_u32(q_ring + qs * kAtQChunkBytes), qimg + j * kAtQChunkBytes,
-                                   kAtQChunkBytes, &q_full[qs]);
-                }
-                ++q_n;
                 // KV chunk j of tile t
                 if (u > 0 && !ptx::mbar_wait(&empty[j], (u - 1) & 1)) {
                     ok = false;
@@ -324,6 +312,22 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             if (!ok) *abort_flag = 1;
             ptx::mma_commit(teardown);
             ptx::mbar_wait(teardown, 0);
+        }
+    } else if (warp == kAtQWarp) {
+        // ---------------------------------------------------------- query chunks ----
+        // Query chunk j (hi | lo, 32 KB) for every S chunk, in consumption order.
+        if (lane == 0) {
+            const int total = CC * n_tiles;
+            for (int n = 0; n < total && !*abort_flag; ++n) {
+                const int qs = n % kAtQSlots, j = n % CC;
+                if (n >= kAtQSlots && !ptx::mbar_wait(&q_empty[qs], ((n / kAtQSlots) - 1) & 1)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                ptx::mbar_arrive_expect_tx(&q_full[qs], kAtQChunkBytes);
+                ptx::bulk_load(ptx::smem_u32(q_ring + qs * kAtQChunkBytes), qimg + j * kAtQChunkBytes, kAtQChunkBytes,
+                               &q_full[qs]);
+            }
         }
     } else {
         // -------------------------------------------------------------- softmax ----
