@@ -195,6 +195,23 @@ lca_status hca_attend(const lca_attn_params *p, int batch, int n_q,
                       const float *sink, lca_bf16 *out, float *lse,
                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* hca_attend with no workspace argument and no allocation of any kind: the split-K
+ * partials and query images go to a 32 MiB array that the library reserves in device
+ * memory when its module loads.  Same arguments, layout and result as hca_attend.
+ * The paper has no counterpart; it serves callers that cannot allocate device memory.
+ *  - The first call on a device (with that device current) looks up the array's address;
+ *    make that first call before capturing the stream into a graph.
+ *  - A call that would need more than 32 MiB (batch * n_q > 127 queries at c = 512,
+ *    H = 64 on 148 SMs) returns LCA_ERR_WORKSPACE and launches nothing; use hca_attend.
+ *  - Every call on a device shares the one array: calls that overlap in time on one
+ *    device (two streams, two host threads) corrupt each other's results.  Serialise them.
+ *  - Nothing in the array needs to start at zero. */
+lca_status hca_attend_noalloc(const lca_attn_params *p, int batch, int n_q,
+                              const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                              const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                              const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                              const float *sink, lca_bf16 *out, float *lse, cudaStream_t stream);
+
 /* ---------------------------------------------------------------------------------
  * Grouped output projection ([P1] CSA step four): the H heads of each token are split
  * into `groups` groups of H/groups heads; group g is projected by Wg[g] (d_g rows of

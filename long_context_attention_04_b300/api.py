@@ -219,6 +219,18 @@ def hca_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, wo
     _check(st)
 
 
+def hca_attend_noalloc(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, lse=None, stream=None):
+    """hca_attend with its scratch in the library's static device array (no workspace)."""
+    B, n_q = _attend_common(q, p)
+    st = _lib.load().hca_attend_noalloc(
+        ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
+        _i32(q_pos, "q_pos"), _ptr(kv_cache, torch.bfloat16, "kv_cache"), _rows(kv_cache, "kv_cache"),
+        kv_cache.shape[1], _ptr(win_kv, torch.bfloat16, "win_kv"), _rows(win_kv, "win_kv"), win_kv.shape[1],
+        _ptr(sink, torch.float32, "sink"), _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
+        _stream(stream))
+    _check(st)
+
+
 def lca_grouped_oproj(o, Wg, Wm, groups: int, mid, y, stream=None):
     """y = Wm . concat_g(Wg[g] . o_g) for o [B, H, c]; mid [B, groups*d_g] is scratch."""
     B, H, c = o.shape

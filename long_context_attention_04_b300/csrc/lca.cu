@@ -7,6 +7,7 @@
 #include <cstdio>
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <string>
 
 #include "../../include/lca.h"
@@ -586,6 +587,46 @@ lca_status hca_attend(const lca_attn_params *p, int batch, int n_q, const lca_bf
                        win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream);
 }
 
+// ---- hca_attend_noalloc: the dense attention with its scratch in a static device array ----
+//
+// Some callers cannot hand the library a workspace: a host program with no device allocator
+// of its own, or a serving runtime that sizes its device memory once at start-up and may not
+// allocate (or free) anything while it serves.  For them the split-K partials and the
+// prepared query images live in one file-scope device array, reserved with the module, and
+// the entry point makes no allocation of any kind.  Its address is looked up once per
+// device, with that device current, on the first call made on it.  Every call on a device
+// shares the one array, so two calls in flight at once on that device (on two streams, or
+// from two host threads) overwrite each other's partials; calls must be ordered on one
+// stream or otherwise serialised.  No byte of it needs to start at zero: each call writes
+// every partial it later reads.
+namespace {
+constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;   // 32 MiB
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices];
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// The array's device address on the current device, looked up on first use.
+static lca_status noalloc_scratch(const char *name, void **addr) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "%s: cudaGetDevice: %s", name, cudaGetErrorString(e));
+    LCA_REQUIRE(dev >= 0 && dev < kNoAllocMaxDevices, LCA_ERR_UNSUPPORTED, "%s: device ordinal %d >= %d", name, dev,
+                kNoAllocMaxDevices);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void *a = nullptr;
+        e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+        if (e != cudaSuccess || !a)
+            return fail(LCA_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", name, cudaGetErrorString(e));
+        g_noalloc_addr[dev] = a;
+    }
+    *addr = g_noalloc_addr[dev];
+    return LCA_OK;
+}
+
 static lca_status gemv_launch(const char *name, int M, int N, int K, const lca_bf16 *A, int64_t lda, int64_t a_off,
                               const lca_bf16 *B, int64_t ldb, int64_t b_off, lca_bf16 *C, int64_t ldc, int64_t c_off,
                               int batches, cudaStream_t stream) {
@@ -610,6 +651,26 @@ static lca_status gemv_launch(const char *name, int M, int N, int K, const lca_b
     else if (M <= 8) gemv_kernel<8><<<grid, kGemvThreads, 0, stream>>>(a);
     else gemv_kernel<16><<<grid, kGemvThreads, 0, stream>>>(a);
     return check_launch(name);
+}
+
+lca_status hca_attend_noalloc(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q,
+                              const float *gamma_q, const int32_t *q_pos, const lca_bf16 *kv_cache,
+                              int64_t kv_batch_stride, int64_t cache_rows, const lca_bf16 *win_kv,
+                              int64_t win_batch_stride, int win_cap, const float *sink, lca_bf16 *out, float *lse,
+                              cudaStream_t stream) {
+    const char *name = "hca_attend_noalloc";
+    lca_status st = attend_validate(name, p, batch, n_q);
+    if (st != LCA_OK) return st;
+    LCA_REQUIRE(cache_rows > 0, LCA_ERR_INVALID_ARG, "%s: cache_rows must be positive", name);
+    const size_t need = plan_attend(p, batch, n_q, cache_rows + p->window).total;
+    LCA_REQUIRE(need <= kNoAllocScratchBytes, LCA_ERR_WORKSPACE,
+                "%s: this call needs %zu bytes of scratch, more than the %zu-byte static array "
+                "(use hca_attend with a workspace)", name, need, kNoAllocScratchBytes);
+    void *scratch = nullptr;
+    st = noalloc_scratch(name, &scratch);
+    if (st != LCA_OK) return st;
+    return attend_impl(name, p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride, cache_rows, nullptr, win_kv,
+                       win_batch_stride, win_cap, sink, out, lse, scratch, kNoAllocScratchBytes, stream);
 }
 
 lca_status lca_gemm_bf16(int M, int N, int K, const lca_bf16 *A, int64_t lda, const lca_bf16 *B, int64_t ldb,
