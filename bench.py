@@ -19,7 +19,6 @@ import argparse
 import json
 import math
 import os
-import subprocess
 import sys
 import threading
 import time
@@ -49,59 +48,118 @@ def measured_peaks() -> dict:
 
 # ------------------------------------------------------------------------- clocks -----
 
-class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
-    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
-             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-             "clocks_event_reasons.sw_power_cap")
+class _Nvml:
+    """The few read-only NVML queries the clock sampler needs, through ctypes on the driver's
+    libnvidia-ml (no Python NVML package is required)."""
+    CLOCK_SM = 0
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
+    def __init__(self):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._check(self.lib.nvmlInit_v2())
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def _check(self, rc):
+        if rc != 0:
+            raise RuntimeError("NVML error %d" % rc)
+
+    def handle(self, bus_id: str, index: int):
+        h = self.ct.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), self.ct.byref(h)) != 0:
+            self._check(self.lib.nvmlDeviceGetHandleByIndex_v2(self.ct.c_uint(index), self.ct.byref(h)))
+        return h
+
+    def sm_clock(self, h) -> int:
+        v = self.ct.c_uint()
+        self._check(self.lib.nvmlDeviceGetClockInfo(h, self.CLOCK_SM, self.ct.byref(v)))
+        return v.value
+
+    def sm_max_clock(self, h) -> int:
+        v = self.ct.c_uint()
+        self._check(self.lib.nvmlDeviceGetMaxClockInfo(h, self.CLOCK_SM, self.ct.byref(v)))
+        return v.value
+
+    def reasons(self, h) -> int:
+        v = self.ct.c_ulonglong()
+        self._check(self.reasons_fn(h, self.ct.byref(v)))
+        return v.value
+
+    def shutdown(self):
+        self.lib.nvmlShutdown()
+
+
+class ClockSampler:
+    """SM clock and clock-event (throttle) reasons, read through NVML about every millisecond
+    on a background thread while the timed region runs (a 200 ms nvidia-smi loop would miss
+    a timed region of a few milliseconds).  Read-only: no clock or other setting is touched."""
+
+    # NVML clock-event reason bits
+    REASONS = (("sw_power_cap", 0x4), ("hw_slowdown", 0x8), ("sw_thermal_slowdown", 0x20),
+               ("hw_thermal_slowdown", 0x40), ("hw_power_brake_slowdown", 0x80))
+
+    def __init__(self, device_index: int, period_s: float = 0.001):
+        self.device_index = device_index
+        self.period = period_s
+        self.samples = []          # (sm_mhz, reason bits)
+        self.max_mhz = None
+        self.nv = None
+        self.handle = None
+        self.stop = threading.Event()
+        self.thread = None
+        self.error = None
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.nv = _Nvml()
+            pr = torch.cuda.get_device_properties(self.device_index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            vis = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip().isdigit()]
+            idx = int(vis[self.device_index]) if self.device_index < len(vis) else self.device_index
+            self.handle = self.nv.handle(bus, idx)
+            self.max_mhz = float(self.nv.sm_max_clock(self.handle))
+            self._sample()
+            self.thread = threading.Thread(target=self._loop, daemon=True)
             self.thread.start()
-        except (OSError, ValueError):
-            self.proc = None
+        except Exception as e:     # no NVML: the line reports zero samples and why
+            self.handle = None
+            self.error = "%s: %s" % (type(e).__name__, e)
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def _sample(self):
+        self.samples.append((float(self.nv.sm_clock(self.handle)), int(self.nv.reasons(self.handle))))
+
+    def _loop(self):
+        while not self.stop.is_set():
+            try:
+                self._sample()
+            except Exception as e:
+                self.error = "%s: %s" % (type(e).__name__, e)
+                return
+            time.sleep(self.period)
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self.stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        if self.nv is not None:
             try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+                self.nv.shutdown()
+            except Exception:
+                pass
 
     def summary(self) -> dict:
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 7:
-                continue
-            try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[3:7]):
-                if v.lower().startswith("active"):
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "nvml",
+                    "error": self.error}
+        reasons = set()
+        for _, bits in self.samples:
+            for name, bit in self.REASONS:
+                if bits & bit:
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([m for m, _ in self.samples])), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml"}
 
 
 # ---------------------------------------------------------------------- workloads -----

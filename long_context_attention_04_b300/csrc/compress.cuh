@@ -16,7 +16,8 @@
 
 namespace lca {
 
-constexpr int kRowThreads = 256;        // threads per row-building CTA
+constexpr int kRowThreads = 256;        // threads per window-row CTA
+constexpr int kMaxCompressThreads = 1024;  // compressor CTAs: 128..1024 threads, by window size
 constexpr int kMaxRowWidth = 1024;      // widest row (elements)
 constexpr int kMaxSpan = 256;           // widest compressor window (tokens)
 
@@ -67,11 +68,21 @@ struct CompressArgs {
     RowNormRope nr;
 };
 
-// grid (n_new, batch), block kRowThreads.
-__global__ void __launch_bounds__(kRowThreads) compress_kernel(CompressArgs a) {
+// Threads for a compressor CTA: enough that every thread loads about one 16-byte chunk of
+// the window (width/8 chunks per token, span tokens), between 128 and 1024.
+inline int compress_threads(int width, int span) {
+    const int want = (width / 8) * span;
+    int t = 128;
+    while (t < want && t < kMaxCompressThreads) t *= 2;
+    return t;
+}
+
+// grid (n_new, batch), block compress_threads(width, span), dynamic shared memory
+// blockDim.x * 8 floats (the token groups' partial sums).
+__global__ void __launch_bounds__(kMaxCompressThreads) compress_kernel(CompressArgs a) {
     __shared__ float weight[kMaxSpan];
     __shared__ __align__(16) float row[kMaxRowWidth];
-    __shared__ float partial[kRowThreads * 8];
+    extern __shared__ float partial[];
     __shared__ float scratch[32];
     const int b = blockIdx.y, e = blockIdx.x;
     const int64_t j = (int64_t)a.first_entry[b] + e;
@@ -110,7 +121,7 @@ __global__ void __launch_bounds__(kRowThreads) compress_kernel(CompressArgs a) {
     // g, g + groups, ...; the groups' partial sums are then added in shared memory.
     const __nv_bfloat16 *v = a.tok_v + (int64_t)b * a.tok_v_bs + (begin - p0) * a.width;
     const int kc = a.width / 8;                       // 16-byte chunks per row
-    const int groups = blockDim.x / kc;               // token groups (>= 2 for width <= 1024)
+    const int groups = blockDim.x / kc;               // token groups (>= 1 for width <= 1024)
     const int g = threadIdx.x / kc, k = threadIdx.x % kc;
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if (g < groups) {

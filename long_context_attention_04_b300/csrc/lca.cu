@@ -164,7 +164,8 @@ lca_status compress_impl(const char *name, bool overlap, const lca_attn_params *
     a.cache_bs = cache_bs;
     a.cache_rows = cache_rows;
     a.nr = make_nr(p, gamma, apply_rope);
-    compress_kernel<<<dim3(n_new, batch), kRowThreads, 0, stream>>>(a);
+    const int threads = compress_threads(width, a.span);
+    compress_kernel<<<dim3(n_new, batch), threads, threads * 8 * sizeof(float), stream>>>(a);
     lca_status s = check_launch(name);
     return s == LCA_OK ? ok() : s;
 }
