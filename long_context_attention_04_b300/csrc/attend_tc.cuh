@@ -12,19 +12,23 @@
 //   S^T[row, head]  = KV[row, c] . Qhat[head, c]^T        (M = 128 rows,  N = 2 x 64, K = c)
 //   O^T[c, head]   += KV[row, c]^T . P^T[row, head]       (M = 128 c,     N = 64, K = 128 rows)
 // The same 128-byte-swizzled shared-memory tile serves as the K-major A operand of the first
-// product and the MN-major A operand of the second.  S^T (two buffers) and O^T (c/128
-// chunks) live in TMEM; P^T goes through shared memory in bf16.
+// product and the MN-major A operand of the second.  S^T (128 columns) and O^T (c/128 chunks
+// of 64 columns) live in TMEM.
 //
-// The normalised, rotated query (q_prep_kernel) is split into bf16 hi + lo parts (q = hi + lo
-// to ~16 bits) and S^T accumulates KV.hi^T + KV.lo^T in fp32: a single bf16 query would put a
-// relative error of 2^-9 on every logit, comparable to the bf16 rounding of the output.
-// The query is not kept resident: each S chunk of KV (128 rows x 128 c) comes with the matching
-// 32 KB query chunk (hi and lo stacked as one 128-row B operand, from the L2-hot image), and one
-// N = 128 MMA per k step yields hi and lo logits side by side, summed by the softmax.  Shared
-// memory holds a ring of four 32 KB KV slots, a ring of two 32 KB query slots and two 16 KB
-// P^T buffers.  A 128-row tile at c = 512 does not fit twice next to the query,
-// so each tile is streamed twice, once for S and once for PV, the second time from L2; HBM
-// sees one pass, and upcoming contiguous tiles are prefetched into L2 two tiles ahead.
+// Precision.  The normalised, rotated query (q_prep_kernel) is split into bf16 hi + lo parts
+// (q = hi + lo to ~16 bits) and S^T accumulates KV.hi^T and KV.lo^T side by side (one
+// N = 128 MMA per k step), summed by the softmax.  The probabilities are split the same way,
+// P = hi + lo, and O^T accumulates both products.  A single bf16 query or a single bf16 P
+// each put a relative error of up to 2^-9 on every weight, as large as the bf16 rounding of
+// the output itself.
+//
+// Shared memory holds the KV tile as four 32 KB slots (128 rows x 128 c each, the whole tile
+// at c = 512), a ring of two 32 KB query slots and the two 16 KB P^T buffers.  The query is
+// not resident: each S chunk comes with the matching 32 KB query chunk (hi and lo stacked as
+// one 128-row B operand, bulk-copied from the L2-hot image).  The KV tile stays resident
+// across both products; slot j is released when its PV chunk completes, and the producer
+// refills it with the next tile's chunk j.  HBM sees one pass over the rows; contiguous tiles
+// are prefetched into L2 two tiles ahead.
 //
 // Rows of a query: compressed rows (CSA: the selected entries; HCA: entries 0..n_vis), then
 // the window rows; tiles never mix the two.  All loads are TMA: contiguous compressed tiles
@@ -66,7 +70,8 @@ constexpr float kAtTau = 8.0f;                           // log2 headroom before
 template <int C>
 struct AttendTcConfig {
     static constexpr int CC = C / 128;                        // c chunks per row
-    static constexpr int P_BYTES = kAtTile * kAtHP * 2;       // the P^T buffer (16 KB)
+    static constexpr int P_HALF = kAtTile * kAtHP * 2;        // one bf16 P^T buffer (16 KB)
+    static constexpr int P_BYTES = 2 * P_HALF;                // P^T = hi + lo
     static constexpr int TMEM_S = 0;                          // S^T: 128 columns (hi | lo)
     static constexpr int TMEM_O = 2 * kAtHP;                  // O^T chunk j at TMEM_O + 64 j
     static constexpr int TMEM_COLS = 512;
@@ -115,7 +120,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                                                 ~uintptr_t(1023));
     uint8_t *ring = base;                                     // KV slot j = chunk j: 2 boxes [128 rows x 128 B]
     uint8_t *q_ring = ring + CC * kAtChunkBytes;              // query slots: 2 boxes [128 rows x 128 B]
-    uint8_t *p_buf = q_ring + kAtQSlots * kAtQChunkBytes;     // [128 rows x 128 B]
+    uint8_t *p_buf = q_ring + kAtQSlots * kAtQChunkBytes;     // hi, then lo: [128 rows x 128 B] each
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + kAtSlots;
     uint64_t *q_full = empty + kAtSlots;
@@ -302,8 +307,11 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t ad = ptx::smem_desc(slot + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
-                        const uint64_t bd = ptx::smem_desc(p_addr + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
-                        ptx::mma_bf16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bd, idesc_o, (u > 0 || kk > 0));
+                        const uint64_t bh = ptx::smem_desc(p_addr + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
+                        const uint64_t bl = ptx::smem_desc(p_addr + Cfg::P_HALF + kk * 2048, 128 * 128, 1024,
+                                                           ptx::kSwizzle128);
+                        ptx::mma_bf16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bh, idesc_o, (u > 0 || kk > 0));
+                        ptx::mma_bf16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bl, idesc_o, true);
                     }
                     ptx::mma_commit(&empty[j]);
                 }
@@ -429,18 +437,24 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 }
                 ptx::tc_fence_before();
             }
-            // probabilities of this row, written as a bf16 P^T row (32 heads = 4 chunks); PV of the
-            // previous tile, the last reader of P^T, completed before S^T of this tile
-            float pr[32];
+            // probabilities of this row, written as two bf16 P^T rows, hi = bf16(p) and
+            // lo = bf16(p - hi) (32 heads = 4 chunks each), so that hi + lo carries p to ~2^-16;
+            // PV of the previous tile, the last reader of P^T, completed before S^T of this tile.
+            float pr[32], plo[32];
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
                 const float ms = m[h] == -INFINITY ? 0.f : m[h];
-                pr[h] = exp2f(x[h] - ms);
-                l[h] += pr[h];
+                const float pv = exp2f(x[h] - ms);
+                pr[h] = __bfloat162float(__float2bfloat16_rn(pv));
+                plo[h] = pv - pr[h];
+                l[h] += pv;
             }
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
+            for (int c4 = 0; c4 < 4; ++c4) {
                 *reinterpret_cast<uint4 *>(p_buf + ptx::sw128_offset(r, half * 4 + c4)) = pack8(pr + 8 * c4);
+                *reinterpret_cast<uint4 *>(p_buf + Cfg::P_HALF + ptx::sw128_offset(r, half * 4 + c4)) =
+                    pack8(plo + 8 * c4);
+            }
             ptx::fence_proxy_async();
             ptx::mbar_arrive(&p_full[0]);
         }

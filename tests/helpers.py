@@ -39,6 +39,22 @@ def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float = OUT_TOL, wha
     return err / rms if rms > 0 else 0.0
 
 
+def assert_rows_close(got_bf16, ref, what=""):
+    """A stored bf16 row equals the oracle's fp64 row up to bf16 rounding (+ fp32 arithmetic)."""
+    got = bf16_to_f64(got_bf16)
+    ref = np.asarray(ref, np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    bound = 2.0 ** -8 * np.abs(ref) + 2e-3 * rms
+    err = np.abs(got - ref)
+    assert (err <= bound).all(), "%s: worst %.3e at %s" % (what, float((err - bound).max()), np.argmax(err - bound))
+
+
+def round_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """The oracle's fp64 values rounded to bf16 (nearest even) as uint16 bit patterns: how a
+    row the oracle computed is stored in a bf16 cache."""
+    return bf16_bits(torch.from_numpy(np.asarray(x, np.float64)).to(torch.bfloat16))
+
+
 def check_topk(gpu_idx: np.ndarray, ref_scores: np.ndarray, k: int, what: str = ""):
     """GPU top-k list vs the oracle's fp64 scores: ascending, -1 padded, and equal to the oracle's
     set except for entries within NEAR_TIE of the k-th score."""

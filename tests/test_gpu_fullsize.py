@@ -1,0 +1,146 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py times.
+
+Each test builds a bench workload (same batch, caches, split plan and kernels), runs one
+step of the whole path on the GPU, and compares sampled outputs with the oracle computed
+one by one on the host from the same seeded inputs:
+  * the rows the step writes (the new compressed entries and window rows) within bf16 rounding;
+  * the top-k lists (sets equal except at near-ties of the k-th score);
+  * the attention outputs within 2e-2 x RMS wherever the top-k set equals the oracle's
+    (a near-tie swap changes which rows are attended, so that output is not comparable).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+from helpers import assert_close_rms, assert_rows_close, check_topk, round_bf16_bits
+from long_context_attention_04_b300 import api, build as lca_build
+from workloads import WORKLOADS, bf16_bits
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lca_build.build()
+    api.lca_device_error()
+    yield
+
+
+def _host(t):
+    return t.detach().cpu()
+
+
+def test_csa_decode_128k_sampled_sequences():
+    wk = bench.CsaDecode(WORKLOADS["csa_decode_128k"], seed=0)
+    s, d, pos, E = wk.s, wk.d, wk.pos, wk.entries
+    samples = [0, 17, wk.B - 1]
+    before = {b: (bf16_bits(_host(d["kv_cache"][b])), bf16_bits(_host(d["idx_cache"][b])),
+                  bf16_bits(_host(d["win_kv"][b]))) for b in samples}
+    wk.step()
+    torch.cuda.synchronize()
+    assert api.lca_device_error() == 0
+    cap = d["win_kv"].shape[1]
+    g = d["gamma_kv"].cpu().numpy()
+    compared = 0
+    for b in samples:
+        kvb, ixb, winb = before[b]
+        tv, tz = bf16_bits(_host(d["tok_v"][b])), _host(d["tok_z"][b]).numpy()
+        tvi, tzi = bf16_bits(_host(d["tok_vi"][b])), _host(d["tok_zi"][b]).numpy()
+        kv_new = oracle.compress(tv, tz, d["tok_pos0"], d["bias_kv"].cpu().numpy(), g, s.rms_eps, s.rope_dims,
+                                 s.rope_base, 2 * s.ratio, s.ratio, E - 1, 1)[0]
+        k_new = oracle.compress(tvi, tzi, d["tok_pos0"], d["bias_idx"].cpu().numpy(), None, s.rms_eps, 0,
+                                s.rope_base, 2 * s.ratio, s.ratio, E - 1, 1)[0]
+        w_new = oracle.window_row(tv[-1], g, s.rms_eps, s.rope_dims, s.rope_base, pos)
+        assert_rows_close(wk.layer.kv_cache[b, E - 1], kv_new, "kv entry b=%d" % b)
+        assert_rows_close(wk.layer.idx_cache[b, E - 1], k_new, "key entry b=%d" % b)
+        assert_rows_close(wk.layer.win_kv[b, pos % cap], w_new, "window row b=%d" % b)
+        kvb[E - 1] = round_bf16_bits(kv_new)
+        ixb[E - 1] = round_bf16_bits(k_new)
+        winb[pos % cap] = round_bf16_bits(w_new)
+        n_vis = oracle.visible_entries(pos, s.ratio)
+        sc = oracle.indexer_scores(bf16_bits(_host(d["q_idx"][b, 0])), _host(d["w_idx"][b, 0]).numpy(), ixb, n_vis)
+        ref_idx = oracle.topk(sc, s.topk)
+        gpu_idx = _host(wk.layer.idx[b, 0]).numpy()
+        if check_topk(gpu_idx, sc, s.topk, what="topk b=%d" % b) == 0:
+            ro, _ = oracle.attend(bf16_bits(_host(d["q"][b, 0])), d["gamma_q"].cpu().numpy(), pos, kvb,
+                                  d["sink"].cpu().numpy(), winb, cap, s.window, s.rope_dims, s.rope_base, s.rms_eps,
+                                  wk.p.scale, idx=ref_idx)
+            assert_close_rms(_host(wk.out[b, 0]).float().numpy(), ro, what="csa out b=%d" % b)
+            compared += 1
+    assert compared >= len(samples) - 1
+
+
+def test_hca_decode_1m_sampled_sequences():
+    wk = bench.HcaDecode(WORKLOADS["hca_decode_1m"], seed=0)
+    s, d, pos, E = wk.s, wk.d, wk.pos, wk.entries
+    samples = [0, 9, wk.B - 1]
+    before = {b: (bf16_bits(_host(d["kv_cache"][b])), bf16_bits(_host(d["win_kv"][b]))) for b in samples}
+    wk.step()
+    torch.cuda.synchronize()
+    assert api.lca_device_error() == 0
+    cap = d["win_kv"].shape[1]
+    g = d["gamma_kv"].cpu().numpy()
+    for b in samples:
+        kvb, winb = before[b]
+        tv, tz = bf16_bits(_host(d["tok_v"][b])), _host(d["tok_z"][b]).numpy()
+        kv_new = oracle.compress(tv, tz, d["tok_pos0"], d["bias_kv"].cpu().numpy(), g, s.rms_eps, s.rope_dims,
+                                 s.rope_base, s.ratio, s.ratio, E - 1, 1)[0]
+        w_new = oracle.window_row(tv[-1], g, s.rms_eps, s.rope_dims, s.rope_base, pos)
+        assert_rows_close(wk.layer.kv_cache[b, E - 1], kv_new, "kv entry b=%d" % b)
+        assert_rows_close(wk.layer.win_kv[b, pos % cap], w_new, "window row b=%d" % b)
+        kvb[E - 1] = round_bf16_bits(kv_new)
+        winb[pos % cap] = round_bf16_bits(w_new)
+        ro, _ = oracle.attend(bf16_bits(_host(d["q"][b, 0])), d["gamma_q"].cpu().numpy(), pos, kvb,
+                              d["sink"].cpu().numpy(), winb, cap, s.window, s.rope_dims, s.rope_base, s.rms_eps,
+                              wk.p.scale, n_dense=oracle.visible_entries(pos, s.ratio))
+        assert_close_rms(_host(wk.out[b, 0]).float().numpy(), ro, what="hca out b=%d" % b)
+
+
+def test_csa_prefill_1m_sampled_queries():
+    wk = bench.CsaPrefill(WORKLOADS["csa_prefill_1m"], seed=0)
+    s, d = wk.s, wk.d
+    Tq, E, q0, m = wk.Tq, wk.entries, wk.q_begin, s.ratio
+    kvb = bf16_bits(_host(d["kv_cache"][0]))
+    ixb = bf16_bits(_host(d["idx_cache"][0]))
+    winb = bf16_bits(_host(d["win_kv"][0]))
+    wk.step()
+    torch.cuda.synchronize()
+    assert api.lca_device_error() == 0
+    cap = winb.shape[0]
+    g = d["gamma_kv"].cpu().numpy()
+    tv, tz = bf16_bits(_host(d["tok_v"][0])), _host(d["tok_z"][0]).numpy()
+    tvi, tzi = bf16_bits(_host(d["tok_vi"][0])), _host(d["tok_zi"][0]).numpy()
+    first, n_new = d["first_entry"], Tq // m
+    kv_new = oracle.compress(tv, tz, d["tok_pos0"], d["bias_kv"].cpu().numpy(), g, s.rms_eps, s.rope_dims,
+                             s.rope_base, 2 * m, m, first, n_new)
+    k_new = oracle.compress(tvi, tzi, d["tok_pos0"], d["bias_idx"].cpu().numpy(), None, s.rms_eps, 0, s.rope_base,
+                            2 * m, m, first, n_new)
+    for j in (0, 1, n_new // 2, n_new - 1):
+        assert_rows_close(wk.layer.kv_cache[0, first + j], kv_new[j], "kv entry %d" % (first + j))
+        assert_rows_close(wk.layer.idx_cache[0, first + j], k_new[j], "key entry %d" % (first + j))
+    kvb[first:first + n_new] = round_bf16_bits(kv_new)
+    ixb[first:first + n_new] = round_bf16_bits(k_new)
+    # window rows of the chunk's tokens (the staging rows start m tokens before the chunk)
+    for i in range(Tq):
+        t = q0 + i
+        row = oracle.window_row(tv[m + i], g, s.rms_eps, s.rope_dims, s.rope_base, t)
+        if i in (0, Tq // 2, Tq - 1):
+            assert_rows_close(wk.layer.win_kv[0, t % cap], row, "window row %d" % t)
+        winb[t % cap] = round_bf16_bits(row)
+    compared = 0
+    samples = [0, Tq // 2 + 3, Tq - 1]
+    for i in samples:
+        t = q0 + i
+        n_vis = oracle.visible_entries(t, m)
+        sc = oracle.indexer_scores(bf16_bits(_host(d["q_idx"][0, i])), _host(d["w_idx"][0, i]).numpy(), ixb, n_vis)
+        ref_idx = oracle.topk(sc, s.topk)
+        gpu_idx = _host(wk.layer.idx[0, i]).numpy()
+        if check_topk(gpu_idx, sc, s.topk, what="topk query %d" % t) == 0:
+            ro, _ = oracle.attend(bf16_bits(_host(d["q"][0, i])), d["gamma_q"].cpu().numpy(), t, kvb,
+                                  d["sink"].cpu().numpy(), winb, cap, s.window, s.rope_dims, s.rope_base, s.rms_eps,
+                                  wk.p.scale, idx=ref_idx)
+            assert_close_rms(_host(wk.out[0, i]).float().numpy(), ro, what="prefill out query %d" % t)
+            compared += 1
+    assert compared >= len(samples) - 1

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import (assert_close_rms, bf16_to_f64, check_topk, f32, oracle_attend_batch, u16)
+from helpers import (assert_close_rms, assert_rows_close, bf16_to_f64, check_topk, f32, oracle_attend_batch, u16)
 from long_context_attention_04_b300 import api, build as lca_build
 from long_context_attention_04_b300.api import AttnParams
 from workloads import Rng, bits_to_bf16
@@ -29,16 +29,6 @@ def _built():
 
 def dev(t):
     return t.to(DEV)
-
-
-def assert_rows_close(got_bf16, ref, what=""):
-    """A stored bf16 row equals the oracle's fp64 row up to bf16 rounding (+ fp32 arithmetic)."""
-    got = bf16_to_f64(got_bf16)
-    ref = np.asarray(ref, np.float64)
-    rms = float(np.sqrt(np.mean(ref * ref)))
-    bound = 2.0 ** -8 * np.abs(ref) + 2e-3 * rms
-    err = np.abs(got - ref)
-    assert (err <= bound).all(), "%s: worst %.3e at %s" % (what, float((err - bound).max()), np.argmax(err - bound))
 
 
 # ------------------------------------------------------------------ compress -------
