@@ -404,14 +404,30 @@ lca_status topk_launch(const lca_attn_params *p, int batch, int n_q, const float
     a.max_entries = max_entries;
     a.k = p->topk;
     a.out = out_idx;
-    const unsigned rows = (unsigned)((int64_t)batch * n_q);
-    if (max_entries <= kTopkSmemKeys) {
-        const int smem = (int)(((max_entries + 3) & ~(int64_t)3) * sizeof(uint32_t));
-        cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        topk_kernel<true><<<rows, kTopkThreads, smem, stream>>>(a);
-    } else {
-        topk_kernel<false><<<rows, kTopkThreads, 0, stream>>>(a);
-    }
+    const int64_t rows = (int64_t)batch * n_q;
+    // CTAs per row: enough to cover the SMs when rows are few (decode), one otherwise
+    int cl = (int)std::min<int64_t>(kTopkMaxCluster, std::max<int64_t>(1, device_sm_count() / rows));
+    while (cl > 1 && (int64_t)cl * (cl - 1) >= max_entries) cl /= 2;   // slices of at least a few keys
+    a.cl = cl;
+    const int64_t slice = ((max_entries + cl - 1) / cl + 3) & ~(int64_t)3;
+    const bool smem_keys = slice <= kTopkSmemKeys;
+    const int smem = (int)topk_smem_bytes(smem_keys, slice);
+    auto kern = smem_keys ? topk_kernel<true> : topk_kernel<false>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(rows * cl));
+    cfg.blockDim = dim3(kTopkThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_topk: launch failed: %s", cudaGetErrorString(e));
     return check_launch("lca_topk");
 }
 

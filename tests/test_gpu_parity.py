@@ -139,7 +139,7 @@ def test_indexer_scores_and_topk_match_oracle(HI, DI, rows, k):
     assert torch.equal(out2, out_idx)
 
 
-@pytest.mark.parametrize("n,k", [(5000, 300), (262144, 1024), (1023, 1024), (32768, 512)])
+@pytest.mark.parametrize("n,k", [(5000, 300), (262144, 1024), (1023, 1024), (32768, 512), (100003, 64)])
 def test_topk_exact_on_given_scores_with_ties(n, k):
     """Scores given (not computed): the GPU selection must equal the oracle's exactly, ties included."""
     g = np.random.default_rng(14)
@@ -152,16 +152,18 @@ def test_topk_exact_on_given_scores_with_ties(n, k):
     rows.append(-np.abs(g.standard_normal(n)).astype(np.float32))    # all negative, with -0.0
     rows[-1][::7] = -0.0
     rows[-1][3::7] = 0.0
-    S = np.stack(rows)[None]                   # [1, 4, n]
+    rows.append((8.0 * g.standard_normal(n)).astype(np.float32))      # no ties (indexer-like spread)
+    R = len(rows)
+    S = np.stack(rows)[None]                   # [1, R, n]
     stride = (n + 3) // 4 * 4
-    Sp = np.full((1, 4, stride), -np.inf, np.float32)
+    Sp = np.full((1, R, stride), -np.inf, np.float32)
     Sp[..., :n] = S
     p = AttnParams(topk=k, ratio=1)
-    pos = torch.full((1, 4), n - 1, dtype=torch.int32)
-    out = torch.empty((1, 4, k), dtype=torch.int32, device=DEV)
+    pos = torch.full((1, R), n - 1, dtype=torch.int32)
+    out = torch.empty((1, R, k), dtype=torch.int32, device=DEV)
     api.lca_topk(p, dev(torch.from_numpy(Sp)), dev(pos), n, out)
     got = out.cpu().numpy()
-    for r in range(4):
+    for r in range(R):
         np.testing.assert_array_equal(got[0, r], oracle.topk(S[0, r].astype(np.float64), k))
 
 
