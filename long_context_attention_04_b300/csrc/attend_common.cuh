@@ -189,6 +189,8 @@ constexpr int kMaxSplits = 128;
 //   M = max(sink, max_s m_s);  w_s = 2^(m_s - M);  L = 2^(sink - M) + sum_s w_s l_s;
 //   o = sum_s w_s O_s / L   (m, sink in base-2 logit units)
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(AttendArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float wts[kMaxSplits];
     __shared__ __align__(16) float row[1024];
     __shared__ float red[kCombineThreads / 32];

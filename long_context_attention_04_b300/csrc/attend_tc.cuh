@@ -114,6 +114,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                                                   const __grid_constant__ CUtensorMap win_row_map, AttendArgs a) {
     using Cfg = AttendTcConfig<C>;
     constexpr int CC = Cfg::CC;
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *misc = smem_raw;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw + Cfg::MISC) + 1023) &
@@ -138,31 +139,6 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     float *red = reinterpret_cast<float *>(misc + 256);                // [8][32]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int unit = blockIdx.x, split = blockIdx.y;
-    const int b = unit / a.n_q, qi = unit % a.n_q;
-    const RowList L = make_row_list(a, b, qi);
-    const TileMap tm = tile_map(L);
-    const int64_t t0 = (int64_t)tm.total() * split / a.splits;
-    const int64_t t1 = (int64_t)tm.total() * (split + 1) / a.splits;
-    const int64_t pidx0 = ((int64_t)unit * a.splits + split) * a.H;
-    const uint8_t *qimg = q_img<C>(a, unit);
-
-    if (t0 >= t1) {   // nothing to do for this split: mark it empty for the combine
-        for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
-            a.part_m[pidx0 + h] = -INFINITY;
-            a.part_l[pidx0 + h] = 0.f;
-        }
-        return;
-    }
-
-    // Contiguous (HCA) tiles: start pulling the first two tiles into L2 now, behind the prologue.
-    constexpr int kPrefetchTiles = 2;
-    if (!L.idx && threadIdx.x == 32) {
-        const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
-        for (int64_t t = t0; t < t1 && t < t0 + kPrefetchTiles && t < tm.tc; ++t)
-            for (int x = 0; x < C; x += 64) ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + t * kAtTile));
-    }
-
     // ---- set-up: barriers, TMEM ----
     if (threadIdx.x == 0) {
         for (int s = 0; s < kAtSlots; ++s) {
@@ -193,6 +169,39 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // the set-up above touches no global memory; everything below may
+
+    const int unit = blockIdx.x, split = blockIdx.y;
+    const int b = unit / a.n_q, qi = unit % a.n_q;
+    const RowList L = make_row_list(a, b, qi);
+    const TileMap tm = tile_map(L);
+    const int64_t t0 = (int64_t)tm.total() * split / a.splits;
+    const int64_t t1 = (int64_t)tm.total() * (split + 1) / a.splits;
+    const int64_t pidx0 = ((int64_t)unit * a.splits + split) * a.H;
+    const uint8_t *qimg = q_img<C>(a, unit);
+
+    if (t0 >= t1) {   // nothing to do for this split: mark it empty for the combine
+        for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
+            a.part_m[pidx0 + h] = -INFINITY;
+            a.part_l[pidx0 + h] = 0.f;
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (warp == kAtMmaWarp) {
+            ptx::tc_fence_after();
+            ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+        }
+        return;
+    }
+
+    // Contiguous (HCA) tiles: start pulling the first two tiles into L2 now.
+    constexpr int kPrefetchTiles = 2;
+    if (!L.idx && threadIdx.x == 32) {
+        const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
+        for (int64_t t = t0; t < t1 && t < t0 + kPrefetchTiles && t < tm.tc; ++t)
+            for (int x = 0; x < C; x += 64) ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + t * kAtTile));
+    }
+
     const int n_tiles = (int)(t1 - t0);
 
     if (warp == kAtProducerWarp) {

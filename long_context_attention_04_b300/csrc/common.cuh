@@ -16,6 +16,16 @@ __device__ unsigned int g_error_word;
 
 __device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_error_word, bits); }
 
+// Programmatic dependent launch.  Every kernel of the library is launched so that the next
+// kernel in the stream may be scheduled while it runs (its CTAs then wait on the SMs instead
+// of behind a launch).  Each kernel calls pdl_trigger() first, to let the next one launch,
+// and pdl_wait() before its first access to global memory, on every path: pdl_wait returns
+// once the previous kernel in the stream has completed and its writes are visible, and
+// because every kernel waits before it can complete, completion stays ordered along the
+// whole stream.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

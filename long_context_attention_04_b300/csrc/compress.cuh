@@ -80,6 +80,8 @@ inline int compress_threads(int width, int span) {
 // grid (n_new, batch), block compress_threads(width, span), dynamic shared memory
 // blockDim.x * 8 floats (the token groups' partial sums).
 __global__ void __launch_bounds__(kMaxCompressThreads) compress_kernel(CompressArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float weight[kMaxSpan];
     __shared__ __align__(16) float row[kMaxRowWidth];
     extern __shared__ float partial[];
@@ -160,6 +162,8 @@ struct WindowArgs {
 
 // grid (n_tok, batch), block kRowThreads: one window row per CTA.
 __global__ void __launch_bounds__(kRowThreads) window_kernel(WindowArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ __align__(16) float row[kMaxRowWidth];
     __shared__ float scratch[32];
     const int b = blockIdx.y, t = blockIdx.x;

@@ -25,6 +25,8 @@ struct GemvArgs {
 // grid (ceil(N / (8 warps * 4 rows)), batches), block 256.
 template <int MT>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(GemvArgs a) {
+    pdl_trigger();
+    pdl_wait();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n0 = ((int64_t)blockIdx.x * (kGemvThreads / 32) + warp) * kGemvRowsPerWarp;
     if (n0 >= a.N) return;

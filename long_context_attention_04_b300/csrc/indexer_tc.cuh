@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                       IndexerTcArgs a) {
     using Cfg = IndexerTcConfig<DI, HI, QPT>;
     constexpr int N = Cfg::N, STAGES = Cfg::STAGES;
+    pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_tile = base;
@@ -110,6 +111,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    pdl_wait();   // the set-up above touches no global memory; everything below may
 
     // Visible entries of the query group (max over its real queries), same in every role.
     auto group_visible = [&](int b, int g) -> int64_t {

@@ -9,6 +9,7 @@
 #include <cmath>
 #include <mutex>
 #include <string>
+#include <utility>
 
 #include "../../include/lca.h"
 #include "common.cuh"
@@ -47,6 +48,24 @@ lca_status check_launch(const char *what) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
     return LCA_OK;
+}
+
+// Launch with programmatic dependent launch allowed: the kernel may be scheduled while the
+// previous kernel in the stream runs; it waits for it (pdl_wait) before touching memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 int device_sm_count() {
@@ -165,7 +184,7 @@ lca_status compress_impl(const char *name, bool overlap, const lca_attn_params *
     a.cache_rows = cache_rows;
     a.nr = make_nr(p, gamma, apply_rope);
     const int threads = compress_threads(width, a.span);
-    compress_kernel<<<dim3(n_new, batch), threads, threads * 8 * sizeof(float), stream>>>(a);
+    launch_pdl(compress_kernel, dim3(n_new, batch), dim3(threads), threads * 8 * sizeof(float), stream, a);
     lca_status s = check_launch(name);
     return s == LCA_OK ? ok() : s;
 }
@@ -293,9 +312,9 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
         return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
     const dim3 prep_grid((unsigned)pl.units, kQImgHeads / kQPrepHeads);
     switch (C) {
-    case 128: q_prep_kernel<128><<<prep_grid, 32 * kQPrepHeads, 0, stream>>>(a); break;
-    case 256: q_prep_kernel<256><<<prep_grid, 32 * kQPrepHeads, 0, stream>>>(a); break;
-    default: q_prep_kernel<512><<<prep_grid, 32 * kQPrepHeads, 0, stream>>>(a); break;
+    case 128: launch_pdl(q_prep_kernel<128>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
+    case 256: launch_pdl(q_prep_kernel<256>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
+    default: launch_pdl(q_prep_kernel<512>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
     }
     st = check_launch(name);
     if (st != LCA_OK) return st;
@@ -303,25 +322,25 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     case 128:
         cudaFuncSetAttribute(attend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttendTcConfig<128>::SMEM_BYTES);
-        attend_tc_kernel<128><<<grid, kAtThreads, AttendTcConfig<128>::SMEM_BYTES, stream>>>(kv_tile_map, kv_row_map,
-                                                                                            win_row_map, a);
+        launch_pdl(attend_tc_kernel<128>, grid, dim3(kAtThreads), AttendTcConfig<128>::SMEM_BYTES, stream, kv_tile_map,
+                   kv_row_map, win_row_map, a);
         break;
     case 256:
         cudaFuncSetAttribute(attend_tc_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttendTcConfig<256>::SMEM_BYTES);
-        attend_tc_kernel<256><<<grid, kAtThreads, AttendTcConfig<256>::SMEM_BYTES, stream>>>(kv_tile_map, kv_row_map,
-                                                                                            win_row_map, a);
+        launch_pdl(attend_tc_kernel<256>, grid, dim3(kAtThreads), AttendTcConfig<256>::SMEM_BYTES, stream, kv_tile_map,
+                   kv_row_map, win_row_map, a);
         break;
     default:
         cudaFuncSetAttribute(attend_tc_kernel<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              AttendTcConfig<512>::SMEM_BYTES);
-        attend_tc_kernel<512><<<grid, kAtThreads, AttendTcConfig<512>::SMEM_BYTES, stream>>>(kv_tile_map, kv_row_map,
-                                                                                            win_row_map, a);
+        launch_pdl(attend_tc_kernel<512>, grid, dim3(kAtThreads), AttendTcConfig<512>::SMEM_BYTES, stream, kv_tile_map,
+                   kv_row_map, win_row_map, a);
         break;
     }
     st = check_launch(name);
     if (st != LCA_OK) return st;
-    combine_kernel<<<dim3((unsigned)pl.units, p->heads), kCombineThreads, 0, stream>>>(a);
+    launch_pdl(combine_kernel, dim3((unsigned)pl.units, p->heads), dim3(kCombineThreads), 0, stream, a);
     st = check_launch(name);
     return st == LCA_OK ? ok() : st;
 }
@@ -367,7 +386,7 @@ lca_status indexer_tc_launch(int batch, int n_q, const lca_bf16 *q_idx, const lc
     const int grid = (int)std::min<int64_t>(a.items, device_sm_count());
     cudaFuncSetAttribute(indexer_tc_kernel<DI, HI, QPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg::SMEM_BYTES);
-    indexer_tc_kernel<DI, HI, QPT><<<grid, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(kmap, qmap, a);
+    launch_pdl(indexer_tc_kernel<DI, HI, QPT>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, kmap, qmap, a);
     return check_launch("csa_indexer_scores");
 }
 
@@ -419,13 +438,15 @@ lca_status topk_launch(const lca_attn_params *p, int batch, int n_q, const float
     cfg.blockDim = dim3(kTopkThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_topk: launch failed: %s", cudaGetErrorString(e));
     return check_launch("lca_topk");
@@ -517,7 +538,7 @@ lca_status lca_window_update(const lca_attn_params *p, int batch, const lca_bf16
     a.win_bs = win_batch_stride;
     a.win_cap = win_cap;
     a.nr = make_nr(p, gamma, p->rope_dims > 0);
-    window_kernel<<<dim3(n_tok, batch), kRowThreads, 0, stream>>>(a);
+    launch_pdl(window_kernel, dim3(n_tok, batch), dim3(kRowThreads), 0, stream, a);
     lca_status s = check_launch(name);
     return s == LCA_OK ? ok() : s;
 }
@@ -662,11 +683,11 @@ static lca_status gemv_launch(const char *name, int M, int N, int K, const lca_b
     a.c_batch_off = c_off;
     const int rows_per_block = (kGemvThreads / 32) * kGemvRowsPerWarp;
     dim3 grid((unsigned)ceil_div64(N, rows_per_block), batches);
-    if (M <= 1) gemv_kernel<1><<<grid, kGemvThreads, 0, stream>>>(a);
-    else if (M <= 2) gemv_kernel<2><<<grid, kGemvThreads, 0, stream>>>(a);
-    else if (M <= 4) gemv_kernel<4><<<grid, kGemvThreads, 0, stream>>>(a);
-    else if (M <= 8) gemv_kernel<8><<<grid, kGemvThreads, 0, stream>>>(a);
-    else gemv_kernel<16><<<grid, kGemvThreads, 0, stream>>>(a);
+    if (M <= 1) launch_pdl(gemv_kernel<1>, grid, dim3(kGemvThreads), 0, stream, a);
+    else if (M <= 2) launch_pdl(gemv_kernel<2>, grid, dim3(kGemvThreads), 0, stream, a);
+    else if (M <= 4) launch_pdl(gemv_kernel<4>, grid, dim3(kGemvThreads), 0, stream, a);
+    else if (M <= 8) launch_pdl(gemv_kernel<8>, grid, dim3(kGemvThreads), 0, stream, a);
+    else launch_pdl(gemv_kernel<16>, grid, dim3(kGemvThreads), 0, stream, a);
     return check_launch(name);
 }
 

@@ -31,6 +31,8 @@ __host__ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk)
 // grid (units, 64 / kQPrepHeads), block 32 * kQPrepHeads: warp w prepares head blockIdx.y*8 + w.
 template <int C>
 __global__ void __launch_bounds__(32 * kQPrepHeads) q_prep_kernel(AttendArgs a) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float rcs[64], rsn[64];
     const int64_t unit = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

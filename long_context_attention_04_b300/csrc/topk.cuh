@@ -303,6 +303,8 @@ __device__ __forceinline__ void topk_write(TopkShared &sh, const TopkSrc &s, int
 // grid (rows * cl), cluster (cl), block kTopkThreads; dynamic shared memory topk_smem_bytes.
 template <bool SMEM>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
+    pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(16) uint32_t dyn[];   // SMEM: slice keys; else candidate keys + indices
     __shared__ TopkShared sh;
     const int cl = a.cl;
