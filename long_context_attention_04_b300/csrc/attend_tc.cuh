@@ -38,6 +38,8 @@
 // Roles (one CTA per (query, split), one CTA per SM):
 //   warp 0      TMA producer of KV chunks
 //   warp 10     bulk-copy producer of query chunks
+//   warp 11     second issuer of row gathers (c box 1 of gathered chunks; the producer issues
+//               box 0): TMA gathers from one warp reach about half the rate of two
 //   warp 1      TMEM allocator and MMA issuer (one thread)
 //   warps 2-9   softmax: one TMEM lane (row) per thread, 32 heads per thread; online softmax
 //               in base 2 with a conditional rescale (the running max moves only when a
@@ -64,7 +66,8 @@ constexpr int kAtMmaWarp = 1;
 constexpr int kAtSoftmaxWarp0 = 2;
 constexpr int kAtSoftmaxWarps = 8;
 constexpr int kAtQWarp = kAtSoftmaxWarp0 + kAtSoftmaxWarps;
-constexpr int kAtThreads = 32 * (kAtQWarp + 1);
+constexpr int kAtGatherWarp = kAtQWarp + 1;              // second issuer of row gathers
+constexpr int kAtThreads = 32 * (kAtGatherWarp + 1);
 constexpr float kAtTau = 8.0f;                           // log2 headroom before the running max must move
 
 template <int C>
@@ -75,7 +78,7 @@ struct AttendTcConfig {
     static constexpr int TMEM_S = 0;                          // S^T: 128 columns (hi | lo)
     static constexpr int TMEM_O = 2 * kAtHP;                  // O^T chunk j at TMEM_O + 64 j
     static constexpr int TMEM_COLS = 512;
-    static constexpr int MISC = 1280;                          // barriers, votes, cross-warp maxima
+    static constexpr int MISC = 1344;                          // barriers, votes, cross-warp maxima
     static constexpr int SMEM_BYTES = MISC + 1024 + CC * kAtChunkBytes + kAtQSlots * kAtQChunkBytes + P_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -137,6 +140,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     int *votes = reinterpret_cast<int *>(misc + 192);                  // [2][8]
     float *red = reinterpret_cast<float *>(misc + 256);                // [8][32]
+    uint64_t *gather_go = reinterpret_cast<uint64_t *>(misc + 1280);  // [kAtSlots]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // ---- set-up: barriers, TMEM ----
@@ -144,6 +148,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         for (int s = 0; s < kAtSlots; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&gather_go[s], 1);
         }
         for (int s = 0; s < kAtQSlots; ++s) {
             ptx::mbar_init(&q_full[s], 1);
@@ -203,12 +208,36 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     }
 
     const int n_tiles = (int)(t1 - t0);
+    const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
+    const int64_t win_row0 = (int64_t)b * (a.win_bs / C);
+    // Rows 4 lane .. 4 lane + 3 of gathered tile t as 2D-map row coordinates (-1: masked, read as 0).
+    auto gather_rows = [&](int t, int j, int *rc) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int r = 4 * lane + i;
+            int coord = -1;
+            if (t < tm.tc) {
+                const int64_t R = (int64_t)t * kAtTile + r;
+                if (R < L.n_comp) {
+                    const int32_t e = __ldg(L.idx + R);
+                    if (e >= 0 && e < a.cache_rows) coord = (int)(kv_row0 + e);
+                    else if (e >= a.cache_rows && j == 0 && warp == kAtProducerWarp) raise_error(LCA_DEVERR_INDEX_RANGE);
+                }
+            } else {
+                const int R = (t - tm.tc) * kAtTile + r;
+                if (R < L.n_win) {
+                    int64_t slot_row = L.win_slot0 + R;   // at most one wrap: n_win <= W <= win_cap
+                    if (slot_row >= a.win_cap) slot_row -= a.win_cap;
+                    coord = (int)(win_row0 + slot_row);
+                }
+            }
+            rc[i] = coord;
+        }
+    };
 
     if (warp == kAtProducerWarp) {
         // ------------------------------------------------------------ producer ----
         // Per tile t: KV chunk j of tile t into slot j, once PV(t-1) has released it.
-        const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
-        const int64_t win_row0 = (int64_t)b * (a.win_bs / C);
         if (lane == 0) {
             ptx::tma_prefetch(&kv_tile_map);
             ptx::tma_prefetch(&kv_row_map);
@@ -239,34 +268,14 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                         ptx::tma_load_2d(dst + lane * (128 * 128), &kv_tile_map, j * 128 + lane * 64,
                                          (int)(kv_row0 + (int64_t)t * kAtTile), &full[j]);
                 } else {
-                    // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, for both c boxes
+                    // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, c box 0; the gather
+                    // warp, released through gather_go[j], issues box 1 (one warp's TMA gathers run
+                    // at about half the rate of two)
+                    if (lane == 0) ptx::mbar_arrive(&gather_go[j]);
                     int rc[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int r = 4 * lane + i;
-                        int coord = -1;
-                        if (t < tm.tc) {
-                            const int64_t R = (int64_t)t * kAtTile + r;
-                            if (R < L.n_comp) {
-                                const int32_t e = __ldg(L.idx + R);
-                                if (e >= 0 && e < a.cache_rows) coord = (int)(kv_row0 + e);
-                                else if (e >= a.cache_rows && j == 0) raise_error(LCA_DEVERR_INDEX_RANGE);
-                            }
-                        } else {
-                            const int R = (t - tm.tc) * kAtTile + r;
-                            if (R < L.n_win) {
-                                int64_t slot_row = L.win_slot0 + R;   // at most one wrap: n_win <= W <= win_cap
-                                if (slot_row >= a.win_cap) slot_row -= a.win_cap;
-                                coord = (int)(win_row0 + slot_row);
-                            }
-                        }
-                        rc[i] = coord;
-                    }
+                    gather_rows(t, j, rc);
                     const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
-#pragma unroll
-                    for (int bx = 0; bx < 2; ++bx)
-                        ptx::tma_gather4(dst + bx * (128 * 128) + lane * 512, map, j * 128 + bx * 64, rc[0], rc[1],
-                                         rc[2], rc[3], &full[j]);
+                    ptx::tma_gather4(dst + lane * 512, map, j * 128, rc[0], rc[1], rc[2], rc[3], &full[j]);
                 }
             }
         }
@@ -330,6 +339,29 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             ptx::mma_commit(teardown);
             ptx::mbar_wait(teardown, 0);
         }
+    } else if (warp == kAtGatherWarp) {
+        // ------------------------------------------------------- second gatherer ----
+        // c box 1 of every gathered chunk, after the producer has seen its slot free (gather_go
+        // is arrived on once per gathered chunk of the slot, so its phases count those alone).
+        uint32_t go_count[kAtSlots] = {};
+        bool ok = true;
+        for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
+            const int t = (int)t0 + u;
+            if (t < tm.tc && !L.idx) continue;   // contiguous tile: the producer loads it alone
+            for (int j = 0; j < CC; ++j) {
+                if (!ptx::mbar_wait(&gather_go[j], go_count[j] & 1)) {
+                    ok = false;
+                    break;
+                }
+                ++go_count[j];
+                int rc[4];
+                gather_rows(t, j, rc);
+                const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
+                ptx::tma_gather4(ptx::smem_u32(ring + j * kAtChunkBytes) + 128 * 128 + lane * 512, map,
+                                 j * 128 + 64, rc[0], rc[1], rc[2], rc[3], &full[j]);
+            }
+        }
+        if (!ok) *abort_flag = 1;
     } else if (warp == kAtQWarp) {
         // ---------------------------------------------------------- query chunks ----
         // Query chunk j (hi | lo, 32 KB) for every S chunk, in consumption order.
