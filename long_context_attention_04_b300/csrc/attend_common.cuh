@@ -114,57 +114,48 @@ __device__ __forceinline__ void rope_table_fill(const AttendArgs &a, int64_t pos
     for (int d = threadIdx.x; d < a.R / 2; d += blockDim.x) rope_cs(a.rope, d, pos, cs[d], sn[d]);
 }
 
+// One head's query for the calling warp: lane l holds elements [l EPL, l EPL + EPL) of q and
+// gamma_q (loaded by q_load_warp, before the position is known, so that the loads overlap).
 template <int C>
-__device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const __nv_bfloat16 *qh, const float *rcs,
-                                           const float *rsn, float *v) {
+struct QLane {
+    float v[C / 32];
+    float g[C / 32];
+};
+
+template <int C>
+__device__ __forceinline__ void q_load_warp(const AttendArgs &a, const __nv_bfloat16 *qh, QLane<C> &q) {
     constexpr int EPL = C / 32;   // elements per lane (4, 8 or 16)
     const int lane = threadIdx.x & 31;
-    const uint4 *src = reinterpret_cast<const uint4 *>(qh + lane * EPL);
+    if constexpr (EPL >= 8) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(qh + lane * EPL);
 #pragma unroll
-    for (int u = 0; u < EPL / 8; ++u) unpack8(__ldg(src + u), v + 8 * u);
+        for (int u = 0; u < EPL / 8; ++u) unpack8(__ldg(src + u), q.v + 8 * u);
+    } else {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(qh + lane * EPL));
+        q.v[0] = bf16_lo(raw.x); q.v[1] = bf16_hi(raw.x); q.v[2] = bf16_lo(raw.y); q.v[3] = bf16_hi(raw.y);
+    }
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) q.g[u] = __ldg(a.gamma_q + lane * EPL + u);
+}
+
+// RMSNorm with gamma_q, then RoPE (table rcs/rsn at the query position) on the trailing R
+// dims: the half-split pairs (first + d, first + d + R/2) sit R/2 / EPL lanes apart.
+template <int C>
+__device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const QLane<C> &q, const float *rcs,
+                                           const float *rsn, float *v) {
+    constexpr int EPL = C / 32;
+    const int lane = threadIdx.x & 31;
     float ss = 0.f;
 #pragma unroll
-    for (int u = 0; u < EPL; ++u) ss += v[u] * v[u];
+    for (int u = 0; u < EPL; ++u) ss += q.v[u] * q.v[u];
     ss = warp_sum(ss);
     const float inv = rsqrtf(ss / (float)C + a.eps);
 #pragma unroll
-    for (int u = 0; u < EPL; ++u) v[u] = v[u] * inv * __ldg(a.gamma_q + lane * EPL + u);
+    for (int u = 0; u < EPL; ++u) v[u] = q.v[u] * inv * q.g[u];
     if (a.R > 0) {
         const int half = a.R / 2, first = C - a.R;
         const int hl = half / EPL;        // lanes per half (R/2 is a multiple of EPL)
         const int lane0 = first / EPL;
-        const bool in_rope = lane >= lane0;
-        const bool lower = lane < lane0 + hl;
-        const int partner = lower ? lane + hl : lane - hl;
-#pragma unroll
-        for (int u = 0; u < EPL; ++u) {
-            const float other = __shfl_sync(0xffffffffu, v[u], in_rope ? partner : lane);
-            if (in_rope) {
-                const int e = lane * EPL + u;
-                const int d = lower ? e - first : e - first - half;
-                const float cs = rcs[d], sn = rsn[d];
-                v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
-            }
-        }
-    }
-}
-
-// Specialisation helper for C = 128 (4 elements per lane: one 8-byte load).
-template <>
-__device__ __forceinline__ void q_hat_warp<128>(const AttendArgs &a, const __nv_bfloat16 *qh, const float *rcs,
-                                                const float *rsn, float *v) {
-    constexpr int C = 128, EPL = 4;
-    const int lane = threadIdx.x & 31;
-    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(qh + lane * EPL));
-    v[0] = bf16_lo(raw.x); v[1] = bf16_hi(raw.x); v[2] = bf16_lo(raw.y); v[3] = bf16_hi(raw.y);
-    float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
-    ss = warp_sum(ss);
-    const float inv = rsqrtf(ss / (float)C + a.eps);
-#pragma unroll
-    for (int u = 0; u < EPL; ++u) v[u] = v[u] * inv * __ldg(a.gamma_q + lane * EPL + u);
-    if (a.R > 0) {
-        const int half = a.R / 2, first = C - a.R;
-        const int hl = half / EPL, lane0 = first / EPL;
         const bool in_rope = lane >= lane0;
         const bool lower = lane < lane0 + hl;
         const int partner = lower ? lane + hl : lane - hl;

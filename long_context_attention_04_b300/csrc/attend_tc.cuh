@@ -199,13 +199,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         return;
     }
 
-    // Contiguous (HCA) tiles: start pulling the first two tiles into L2 now.
-    constexpr int kPrefetchTiles = 2;
-    if (!L.idx && threadIdx.x == 32) {
-        const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
-        for (int64_t t = t0; t < t1 && t < t0 + kPrefetchTiles && t < tm.tc; ++t)
-            for (int x = 0; x < C; x += 64) ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + t * kAtTile));
-    }
+    constexpr int kPrefetchTiles = 2;   // contiguous (HCA) tiles are pulled into L2 this far ahead
 
     const int n_tiles = (int)(t1 - t0);
     const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
@@ -246,12 +240,6 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         bool ok = true;
         for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
             const int t = (int)t0 + u;
-            if (!L.idx && lane == 1) {
-                const int tp = t + kPrefetchTiles;   // keep HBM reads two tiles ahead
-                if (tp < t1 && tp < tm.tc)
-                    for (int x = 0; x < C; x += 64)
-                        ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + (int64_t)tp * kAtTile));
-            }
             for (int j = 0; j < CC && ok; ++j) {
                 // KV chunk j of tile t
                 if (u > 0 && !ptx::mbar_wait(&empty[j], (u - 1) & 1)) {
@@ -277,6 +265,14 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                     const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
                     ptx::tma_gather4(dst + lane * 512, map, j * 128, rc[0], rc[1], rc[2], rc[3], &full[j]);
                 }
+            }
+            // L2 prefetch of the next contiguous tiles, issued behind this tile's own loads so that
+            // HBM serves those first (at the first tile: the next two)
+            if (!L.idx && lane == 1) {
+                for (int tp = t + (u == 0 ? 1 : kPrefetchTiles); tp <= t + kPrefetchTiles; ++tp)
+                    if (tp < t1 && tp < tm.tc)
+                        for (int x = 0; x < C; x += 64)
+                            ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + (int64_t)tp * kAtTile));
             }
         }
         if (!ok) *abort_flag = 1;

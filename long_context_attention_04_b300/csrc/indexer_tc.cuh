@@ -14,7 +14,7 @@
 //             K = d_I.
 // Persistent, warp-specialised, one CTA per SM:
 //   warp 0     TMA producer: query tile per (sequence, query group), key tiles into a ring
-//   warp 1     TMEM allocator and MMA issuer (one thread), double-buffered accumulators
+//   warp 1     TMEM allocator and MMA issuer (one thread), 2-4 accumulator buffers
 //   warps 2..  epilogue: TMEM -> registers, weighted ReLU sum per query, fp32 score store
 // Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds.
 #pragma once
@@ -50,7 +50,10 @@ struct IndexerTcConfig {
     static constexpr int EPI_WARPS = N > 64 ? 8 : 4;
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int COLS_PER_WG = N / (EPI_WARPS / 4);  // columns one epilogue warp group owns
-    static constexpr int TMEM_COLS = 2 * N < 32 ? 32 : 2 * N;
+    // accumulator buffers in TMEM: the MMA runs up to ACC_BUFS tiles ahead of the epilogue
+    static constexpr int ACC_BUFS = 4 * N <= 512 ? 4 : 2;
+    static constexpr int TMEM_COLS = ACC_BUFS * N <= 32 ? 32 : ACC_BUFS * N <= 64 ? 64 : ACC_BUFS * N <= 128 ? 128
+                                   : ACC_BUFS * N <= 256 ? 256 : 512;
     static constexpr int SMEM_LIMIT = 227 * 1024;
     static constexpr int FIXED = Q_BYTES + 1024;             // query tile + barriers
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED - 1024) / TILE_BYTES;
@@ -59,6 +62,7 @@ struct IndexerTcConfig {
     static_assert(N >= 16 && N <= 256 && N % 16 == 0, "MMA N");
     static_assert(COLS_PER_WG % HI == 0, "a warp group owns whole queries");
     static_assert(STAGES >= 2, "ring");
+    static_assert(ACC_BUFS * N <= 512, "TMEM");
 };
 
 template <int DI, int HI, int QPT>
@@ -76,8 +80,8 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;
-    uint64_t *acc_empty = acc_full + 2;
-    uint64_t *q_full = acc_empty + 2;
+    uint64_t *acc_empty = acc_full + Cfg::ACC_BUFS;
+    uint64_t *q_full = acc_empty + Cfg::ACC_BUFS;
     uint64_t *q_empty = q_full + 1;
     uint64_t *teardown = q_empty + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(teardown + 1);
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < Cfg::ACC_BUFS; ++s) {
             ptx::mbar_init(&acc_full[s], 1);
             ptx::mbar_init(&acc_empty[s], Cfg::EPI_WARPS);
         }
@@ -174,7 +178,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             constexpr uint32_t idesc = ptx::idesc_bf16(128, N, false, false);
             int64_t cur = -1;
             int64_t vis = 0;
-            uint32_t use = 0, groups_seen = 0, acc_use[2] = {0, 0};
+            uint32_t use = 0, groups_seen = 0, acc_use[Cfg::ACC_BUFS] = {};
             int acc = 0;
             bool issued = false;
             const uint32_t q_addr = ptx::smem_u32(q_tile);
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                 ptx::mma_commit(&empty[s]);
                 ptx::mma_commit(&acc_full[acc]);
                 ++acc_use[acc];
-                acc ^= 1;
+                acc = acc + 1 == Cfg::ACC_BUFS ? 0 : acc + 1;
                 ++use;
             }
             if (issued) {
@@ -237,7 +241,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
         int64_t vis = 0;
         int64_t nv[QW];
         float wr[Cfg::COLS_PER_WG];                      // head weights of this group's queries
-        uint32_t acc_use[2] = {0, 0};
+        uint32_t acc_use[Cfg::ACC_BUFS] = {};
         int acc = 0;
         for (int64_t it = it0; it < it1 && !*abort_flag; ++it) {
             const int t = (int)(it % a.tiles);
@@ -275,20 +279,23 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                 }
                 ptx::tc_fence_after();
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * N + col0;
+                // several columns per TMEM round trip (all loads issued before one wait)
+                constexpr int CB = Cfg::COLS_PER_WG <= 64 ? Cfg::COLS_PER_WG : 32;
 #pragma unroll
-                for (int c = 0; c < Cfg::COLS_PER_WG; c += 16) {
-                    uint32_t r[16];
-                    ptx::tmem_ld16(taddr + c, r);
+                for (int c0 = 0; c0 < Cfg::COLS_PER_WG; c0 += CB) {
+                    uint32_t r[CB];
+#pragma unroll
+                    for (int c = 0; c < CB; c += 16) ptx::tmem_ld16(taddr + c0 + c, r + c);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        sc[(c + u) / HI] = fmaf(wr[c + u], fmaxf(__uint_as_float(r[u]), 0.f), sc[(c + u) / HI]);
+                    for (int u = 0; u < CB; ++u)
+                        sc[(c0 + u) / HI] = fmaf(wr[c0 + u], fmaxf(__uint_as_float(r[u]), 0.f), sc[(c0 + u) / HI]);
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
                 ++acc_use[acc];
-                acc ^= 1;
+                acc = acc + 1 == Cfg::ACC_BUFS ? 0 : acc + 1;
             }
             if (j < a.cache_rows) {
 #pragma unroll

@@ -37,14 +37,16 @@ __global__ void __launch_bounds__(32 * kQPrepHeads) q_prep_kernel(AttendArgs a) 
     const int64_t unit = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = blockIdx.y * kQPrepHeads + warp;
+    constexpr int EPL = C / 32;
+    QLane<C> ql;
+    if (h < a.H) q_load_warp<C>(a, a.q + (unit * a.H + h) * C, ql);   // in flight during the RoPE table
     int64_t pos = a.q_pos[unit];
     if (pos < 0) pos = 0;
     rope_table_fill(a, pos, rcs, rsn);
     __syncthreads();
-    constexpr int EPL = C / 32;
     float v[EPL];
     if (h < a.H) {
-        q_hat_warp<C>(a, a.q + (unit * a.H + h) * C, rcs, rsn, v);
+        q_hat_warp<C>(a, ql, rcs, rsn, v);
     } else {
 #pragma unroll
         for (int u = 0; u < EPL; ++u) v[u] = 0.f;
