@@ -494,7 +494,96 @@ def _round_bits(x: np.ndarray) -> np.ndarray:
     return bf16_bits(torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.bfloat16))
 
 
-WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill}
+class BlockDecode(Workload):
+    """A V4-Flash-style attention block at decode: alternating CSA and HCA layers, each with its
+    own caches, followed by the grouped output projection of its heads.  Layers start from the
+    projected per-token inputs (the input projections are not part of the path)."""
+
+    def __init__(self, cfg: dict, seed: int = 0):
+        from long_context_attention_04_b300 import api
+        self.api = api
+        self.cfg = cfg
+        B, pos = cfg["B"], cfg["pos"]
+        self.B, self.pos = B, pos
+        self.layers = []
+        n_csa = n_hca = 0
+        for i in range(cfg["n_csa"] + cfg["n_hca"]):
+            # alternate CSA and HCA layers, CSA first, while both kinds remain
+            csa = n_hca >= cfg["n_hca"] or (n_csa < cfg["n_csa"] and n_csa <= n_hca)
+            n_csa, n_hca = n_csa + csa, n_hca + (not csa)
+            if csa:
+                sub = dict(name="CSA layer", B=B, pos=pos, entries=cfg["csa_entries"], shape=cfg["csa"])
+                self.layers.append(CsaDecode(sub, seed=seed * 1000 + i))
+            else:
+                sub = dict(name="HCA layer", B=B, pos=pos, entries=cfg["hca_entries"], shape=cfg["hca"])
+                self.layers.append(HcaDecode(sub, seed=seed * 1000 + i))
+        s = cfg["csa"]
+        G, d_g, d_model = cfg["groups"], cfg["d_g"], cfg["d_model"]
+        self.G = G
+        rng = wl.Rng(seed * 1000 + 999, device="cuda")
+        self.W = [wl.oproj_weights(rng, s.heads, s.head_dim, G, d_g, d_model) for _ in self.layers]
+        self.mid = torch.empty((B, G * d_g), dtype=torch.bfloat16, device="cuda")
+        self.y = [torch.empty((B, d_model), dtype=torch.bfloat16, device="cuda") for _ in self.layers]
+        self.tokens = B
+        self.launches = sum(L.launches for L in self.layers) + 2 * len(self.layers)
+        self.dominant = "indexer"
+        csa0 = self.layers[0]
+        self.dom_bytes, self.dom_flops = csa0.dom_bytes, csa0.dom_flops
+        self.host_out = [torch.empty(y.shape, dtype=torch.bfloat16).pin_memory() for y in self.y]
+        self.h2d_bytes = sum(L.h2d_bytes for L in self.layers)
+        self.d2h_bytes = sum(y.numel() * y.element_size() for y in self.y)
+
+    def dominant_call(self):
+        # the indexer of one CSA layer (the largest single read of the block)
+        self.layers[0].dominant_call()
+
+    def _oproj(self, i):
+        L = self.layers[i]
+        self.api.lca_grouped_oproj(L.out.view(self.B, L.s.heads, L.s.head_dim), self.W[i]["Wg"], self.W[i]["Wm"],
+                                   self.G, self.mid, self.y[i])
+
+    def step(self):
+        for i, L in enumerate(self.layers):
+            L.step()
+            self._oproj(i)
+
+    def e2e_step(self):
+        for i, L in enumerate(self.layers):
+            for k, t in L.host_in.items():
+                L.d[k].copy_(t, non_blocking=True)
+            L.step()
+            self._oproj(i)
+            self.host_out[i].copy_(self.y[i], non_blocking=True)
+
+    def snapshot_host(self):
+        self.layers[0].snapshot_host()
+        self.layers[1].snapshot_host()
+        self.W_host = [{k: v.cpu() for k, v in W.items()} for W in self.W[:2]]
+
+    def cpu_sample(self, budget_s: float) -> dict:
+        """The oracle on one sequence of the first CSA and the first HCA layer (with their output
+        projections), extrapolated to the whole block: every CSA layer costs the same, and so does
+        every HCA layer."""
+        import oracle
+        from workloads import bf16_bits
+        t0 = time.perf_counter()
+        c = self.layers[0].cpu_sample(0.0)          # one sequence each (a zero budget stops after one)
+        h = self.layers[1].cpu_sample(0.0)
+        t1 = time.perf_counter()
+        o = np.zeros((64, 512), np.uint16)
+        for i in range(2):
+            oracle.grouped_oproj(o, bf16_bits(self.W_host[i]["Wg"]), bf16_bits(self.W_host[i]["Wm"]), self.G)
+        t2 = time.perf_counter()
+        n_csa, n_hca = self.cfg["n_csa"], self.cfg["n_hca"]
+        per_token = n_csa / c["value"] + n_hca / h["value"] + (n_csa + n_hca) * (t2 - t1) / 2
+        return dict(value=1.0 / per_token, unit="tokens/s", cores=1, kind="oracle",
+                    sample="one sequence through the first CSA and the first HCA layer and two output projections "
+                           "(%.1f s), extrapolated to %d CSA + %d HCA layers; single-threaded fp64"
+                           % (t2 - t0, n_csa, n_hca))
+
+
+WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill,
+             "block_decode_1m": BlockDecode}
 
 
 # ------------------------------------------------------------------- distributed -----
@@ -650,14 +739,32 @@ def run_reference(args):
     if rank != 0:
         return
     cfg = wl.WORKLOADS[args.workload]
-    wk = _HostOnly(args.workload, cfg, args.seed)
+    if args.workload == "block_decode_1m":
+        # one token through one CSA and one HCA layer per step, scaled to the block's layer count
+        parts = [_HostOnly("csa_decode_128k", dict(entries=cfg["csa_entries"], pos=cfg["pos"], shape=cfg["csa"]),
+                           args.seed),
+                 _HostOnly("hca_decode_1m", dict(entries=cfg["hca_entries"], pos=cfg["pos"], shape=cfg["hca"]),
+                           args.seed)]
+        scale = float(cfg["n_csa"])        # n_csa == n_hca: each step covers 1/n_csa of the block
+
+        class _Pair:
+            sample = ("one CSA layer (%d entries) and one HCA layer (%d entries), scaled to %d + %d layers"
+                      % (cfg["csa_entries"], cfg["hca_entries"], cfg["n_csa"], cfg["n_hca"]))
+
+            def one_unit(self):
+                for p in parts:
+                    p.one_unit()
+        wk = _Pair()
+    else:
+        wk = _HostOnly(args.workload, cfg, args.seed)
+        scale = 1.0
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
         wk.one_unit()
         if i >= args.warmup:
             times.append(time.perf_counter() - t0)
-    per_unit = float(np.mean(times))
+    per_unit = float(np.mean(times)) * scale
     value = 1.0 / per_unit
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": world,
