@@ -5,7 +5,8 @@
 // merged to d).  At decode batch sizes the product streams the weight matrix B once from
 // HBM and does M multiply-adds per weight, far below the tensor-core ridge, so it stays on
 // the CUDA cores: each warp owns 4 weight rows, reads them with 16-byte loads (a warp reads
-// 512 contiguous bytes of a row per step) and keeps M x 4 fp32 accumulators.
+// 512 contiguous bytes of a row per step, several steps loaded before the first multiply)
+// and keeps M x 4 fp32 accumulators.
 #pragma once
 
 #include "common.cuh"
@@ -14,6 +15,10 @@ namespace lca {
 
 constexpr int kGemvThreads = 256;
 constexpr int kGemvRowsPerWarp = 4;
+
+// 256-element steps loaded ahead per iteration: fewer for larger M (registers)
+template <int MT>
+__host__ __device__ constexpr int gemv_unroll() { return MT <= 4 ? 4 : MT <= 8 ? 2 : 1; }
 
 struct GemvArgs {
     int M, N, K;
@@ -27,6 +32,7 @@ template <int MT>
 __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(GemvArgs a) {
     pdl_trigger();
     pdl_wait();
+    constexpr int U = gemv_unroll<MT>();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n0 = ((int64_t)blockIdx.x * (kGemvThreads / 32) + warp) * kGemvRowsPerWarp;
     if (n0 >= a.N) return;
@@ -39,27 +45,33 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(GemvArgs a) {
 #pragma unroll
         for (int r = 0; r < kGemvRowsPerWarp; ++r) acc[m][r] = 0.f;
     const int nrows = (a.N - n0) < kGemvRowsPerWarp ? (int)(a.N - n0) : kGemvRowsPerWarp;
-    for (int k = lane * 8; k < a.K; k += 32 * 8) {
-        float bw[kGemvRowsPerWarp][8];
+    for (int k0 = lane * 8; k0 < a.K; k0 += 32 * 8 * U) {
+        uint4 wv[U][kGemvRowsPerWarp], av[U][MT];
 #pragma unroll
-        for (int r = 0; r < kGemvRowsPerWarp; ++r) {
-            if (r < nrows) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(B + (n0 + r) * a.ldb + k));
-                unpack8(v, bw[r]);
-            } else {
+        for (int s = 0; s < U; ++s) {
+            const int k = k0 + s * 32 * 8;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) bw[r][u] = 0.f;
-            }
+            for (int r = 0; r < kGemvRowsPerWarp; ++r)
+                wv[s][r] = (k < a.K && r < nrows) ? __ldg(reinterpret_cast<const uint4 *>(B + (n0 + r) * a.ldb + k))
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+                av[s][m] = (k < a.K && m < a.M) ? __ldg(reinterpret_cast<const uint4 *>(A + m * a.lda + k))
+                                                : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int m = 0; m < MT; ++m) {
-            if (m < a.M) {
-                float av[8];
-                unpack8(__ldg(reinterpret_cast<const uint4 *>(A + m * a.lda + k)), av);
+        for (int s = 0; s < U; ++s) {
 #pragma unroll
-                for (int r = 0; r < kGemvRowsPerWarp; ++r)
+            for (int r = 0; r < kGemvRowsPerWarp; ++r) {
+                float bw[8];
+                unpack8(wv[s][r], bw);
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) acc[m][r] = fmaf(av[u], bw[r][u], acc[m][r]);
+                for (int m = 0; m < MT; ++m) {
+                    float x[8];
+                    unpack8(av[s][m], x);
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) acc[m][r] = fmaf(x[u], bw[u], acc[m][r]);
+                }
             }
         }
     }
@@ -68,8 +80,11 @@ __global__ void __launch_bounds__(kGemvThreads) gemv_kernel(GemvArgs a) {
 #pragma unroll
         for (int r = 0; r < kGemvRowsPerWarp; ++r) acc[m][r] = warp_sum(acc[m][r]);
     if (lane == 0) {
-        for (int m = 0; m < a.M; ++m)
-            for (int r = 0; r < nrows; ++r) C[m * a.ldc + n0 + r] = __float2bfloat16_rn(acc[m][r]);
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int r = 0; r < kGemvRowsPerWarp; ++r)
+                if (m < a.M && r < nrows) C[m * a.ldc + n0 + r] = __float2bfloat16_rn(acc[m][r]);
     }
 }
 
