@@ -224,12 +224,10 @@ class CsaDecode(Workload):
         self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], self.layer.idx_cache, self.q_pos, self.scores)
 
     def step(self):
-        api, L, d = self.api, self.layer, self.d
-        L.compress(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, 1)
-        L.window(d["tok_v"][:, -1:], self.new_pos)
-        api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
-        api.lca_topk(self.p, self.scores, self.q_pos, self.entries, L.idx)
-        L.attend(d["q"], self.q_pos, self.out)
+        d = self.d
+        self.layer.step_overlapped(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, 1,
+                                   d["tok_v"][:, -1:], self.new_pos, d["q"], d["q_idx"], d["w_idx"], self.q_pos,
+                                   self.out)
 
     def e2e_step(self):
         d = self.d
@@ -326,10 +324,9 @@ class HcaDecode(Workload):
         self.layer.attend(self.d["q"], self.q_pos, self.out)
 
     def step(self):
-        L, d = self.layer, self.d
-        L.compress(d["tok_v"], d["tok_z"], self.tok_pos0, self.first, 1)
-        L.window(d["tok_v"][:, -1:], self.new_pos)
-        L.attend(d["q"], self.q_pos, self.out)
+        d = self.d
+        self.layer.step_overlapped(d["tok_v"], d["tok_z"], self.tok_pos0, self.first, 1, d["tok_v"][:, -1:],
+                                   self.new_pos, d["q"], self.q_pos, self.out)
 
     def e2e_step(self):
         d = self.d

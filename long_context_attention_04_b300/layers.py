@@ -18,6 +18,13 @@ from . import api
 from .api import AttnParams
 
 
+def _side_stream(layer) -> torch.cuda.Stream:
+    """The layer's second stream (created on first use, on the layer's device)."""
+    if getattr(layer, "_side", None) is None:
+        layer._side = torch.cuda.Stream(device=layer.kv_cache.device)
+    return layer._side
+
+
 @dataclasses.dataclass
 class LayerWeights:
     gamma_kv: torch.Tensor        # [c] fp32
@@ -67,6 +74,28 @@ class CsaLayer:
         self.select(q_idx, w_idx, q_pos, stream)
         self.attend(q, q_pos, out, stream=stream)
 
+    def step_overlapped(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, new_tok_v, new_pos0,
+                        q, q_idx, w_idx, q_pos, out):
+        """The same step on the current stream, with the parts that do not feed the selection (the
+        KV entries and the window rows) on a side stream, overlapping the key entries, indexer and
+        top-k; the attention waits for both."""
+        main = torch.cuda.current_stream()
+        side = _side_stream(self)
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+        if n_new:
+            api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
+                                n_new, self.kv_cache, side)
+        api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, side)
+        join.record(side)
+        if n_new:
+            api.csa_compress_kv(self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
+                                self.idx_cache, main)
+        self.select(q_idx, w_idx, q_pos, main)
+        main.wait_event(join)
+        self.attend(q, q_pos, out, stream=main)
+
 
 class HcaLayer:
     """One HCA layer for B sequences: KV cache [B, rows, c] and window ring [B, win_cap, c]."""
@@ -95,3 +124,18 @@ class HcaLayer:
             self.compress(tok_v, tok_z, tok_pos0, first_entry, n_new, stream)
         self.window(new_tok_v, new_pos0, stream)
         self.attend(q, q_pos, out, stream=stream)
+
+    def step_overlapped(self, tok_v, tok_z, tok_pos0, first_entry, n_new, new_tok_v, new_pos0, q, q_pos, out):
+        """The same step on the current stream, with the window rows on a side stream next to the
+        compression; the attention waits for both."""
+        main = torch.cuda.current_stream()
+        side = _side_stream(self)
+        fork, join = torch.cuda.Event(), torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+        api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, side)
+        join.record(side)
+        if n_new:
+            self.compress(tok_v, tok_z, tok_pos0, first_entry, n_new, main)
+        main.wait_event(join)
+        self.attend(q, q_pos, out, stream=main)
