@@ -139,3 +139,61 @@ class HcaLayer:
             self.compress(tok_v, tok_z, tok_pos0, first_entry, n_new, main)
         main.wait_event(join)
         self.attend(q, q_pos, out, stream=main)
+
+
+class StepGraph:
+    """A decode step captured once as a CUDA graph and replayed for every token.
+
+    `fn` issues, on the current stream, everything a step does: the host-to-device copies of the
+    step's inputs (from pinned buffers the caller refills), the layer calls, and the copy of the
+    result back to pinned host memory.  Replaying the graph runs all of it with one launch from
+    the host; the library's calls are plain stream work, so they capture like any other."""
+
+    def __init__(self, fn, warmup: int = 1):
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(warmup):
+                fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            fn()
+        torch.cuda.synchronize()
+
+    def __call__(self):
+        self.graph.replay()
+
+
+class StagingBuffer:
+    """Per-step inputs packed into one device buffer with a pinned host mirror, so that a step
+    uploads them with a single copy (each host-to-device transfer pays a fixed latency of tens
+    of microseconds, more than a few MB of payload at link speed).
+
+    `tensors` maps names to device tensors; they are replaced, in place in the dict, by views of
+    the packed buffer (16-byte aligned, values copied), and `host[name]` is the matching view of
+    the pinned mirror.  Fill `host[...]`, then `upload()` on the stream of the step."""
+
+    def __init__(self, tensors: dict):
+        offs, total = {}, 0
+        for k, t in tensors.items():
+            offs[k] = total
+            total += (t.numel() * t.element_size() + 15) // 16 * 16
+        dev = next(iter(tensors.values())).device
+        self.dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+        self.host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        self.host = {}
+        for k, t in tensors.items():
+            n = t.numel() * t.element_size()
+            view = self.dev_buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+            view.copy_(t)
+            tensors[k] = view
+            self.host[k] = self.host_buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+            self.host[k].copy_(t)
+        self.nbytes = total
+
+    def upload(self, stream=None):
+        with torch.cuda.stream(stream or torch.cuda.current_stream()):
+            self.dev_buf.copy_(self.host_buf, non_blocking=True)
+
