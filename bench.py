@@ -36,6 +36,36 @@ METRIC = "CSA/HCA attention tokens/s per layer at 128K–1M ctx; % of HBM/tensor
 L2_FLUSH_BYTES = 512 << 20
 
 
+def source_hash() -> str:
+    """sha1 over the library sources (csrc/* and include/lca.h), first 16 hex digits."""
+    import glob
+    import hashlib
+    root = os.path.dirname(os.path.abspath(__file__))
+    files = sorted(glob.glob(os.path.join(root, "long_context_attention_04_b300", "csrc", "*")))
+    files.append(os.path.join(root, "include", "lca.h"))
+    h = hashlib.sha1()
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per dominant call from profiles/dram_traffic.md, if taken with these sources."""
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "profiles", "dram_traffic.md")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    h = source_hash()
+    for line in lines:
+        cols = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cols) == 7 and cols[0] == workload and cols[6] == h:
+            return int(cols[4])
+    return None
+
+
 def measured_peaks() -> dict:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -710,12 +740,14 @@ def run_ours(args):
     if wk.bound == "hbm":
         achieved = wk.dom_bytes / (dom * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None, "kernel": wk.dominant,
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": measured_traffic(args.workload),
+                "kernel": wk.dominant,
                 "kernel_ms": round(dom, 4), "peak_source": peaks["source"]}
     else:
         achieved = wk.dom_flops / (dom * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": None, "kernel": wk.dominant,
+                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": measured_traffic(args.workload),
+                "kernel": wk.dominant,
                 "kernel_ms": round(dom, 4), "peak_source": peaks["source"]}
     value = world * wk.tokens / (ms_all * 1e-3)
     line = {
