@@ -195,6 +195,40 @@ lca_status hca_attend(const lca_attn_params *p, int batch, int n_q,
                       const float *sink, lca_bf16 *out, float *lse,
                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* The two halves of an attention call, for callers that overlap the query preparation with
+ * other work (the selection, the cache updates) on another stream.  *_attend_prepare runs
+ * only the query preparation (RMSNorm + RoPE(i) of q, hi/lo query images) into the workspace;
+ * *_attend_prepared runs only the attention and the combine, reading those images.  Together,
+ * with the same arguments and workspace, and the prepare ordered before the attention (same
+ * stream, or an event), they compute exactly what *_attend computes.  The prepare reads q,
+ * gamma_q and q_pos only; the attention reads the images instead of q and gamma_q. */
+lca_status csa_attend_prepare(const lca_attn_params *p, int batch, int n_q,
+                              const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                              const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                              const int32_t *idx,
+                              const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                              const float *sink, lca_bf16 *out, float *lse,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
+lca_status csa_attend_prepared(const lca_attn_params *p, int batch, int n_q,
+                               const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                               const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                               const int32_t *idx,
+                               const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                               const float *sink, lca_bf16 *out, float *lse,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
+lca_status hca_attend_prepare(const lca_attn_params *p, int batch, int n_q,
+                              const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                              const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                              const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                              const float *sink, lca_bf16 *out, float *lse,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream);
+lca_status hca_attend_prepared(const lca_attn_params *p, int batch, int n_q,
+                               const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                               const lca_bf16 *kv_cache, int64_t kv_batch_stride, int64_t cache_rows,
+                               const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                               const float *sink, lca_bf16 *out, float *lse,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* hca_attend with no workspace argument and no allocation of any kind: the split-K
  * partials and query images go to a 32 MiB array that the library reserves in device
  * memory when its module loads.  Same arguments, layout and result as hca_attend.

@@ -42,6 +42,14 @@ SIGNATURES = {
                    c_int),
     "hca_attend": ([P, c_int, c_int, V, V, V, V, c_int64, c_int64, V, c_int64, c_int, V, V, V, V, c_size_t, V],
                    c_int),
+    "csa_attend_prepare": ([P, c_int, c_int, V, V, V, V, c_int64, c_int64, V, V, c_int64, c_int, V, V, V, V, c_size_t,
+                            V], c_int),
+    "csa_attend_prepared": ([P, c_int, c_int, V, V, V, V, c_int64, c_int64, V, V, c_int64, c_int, V, V, V, V, c_size_t,
+                             V], c_int),
+    "hca_attend_prepare": ([P, c_int, c_int, V, V, V, V, c_int64, c_int64, V, c_int64, c_int, V, V, V, V, c_size_t, V],
+                           c_int),
+    "hca_attend_prepared": ([P, c_int, c_int, V, V, V, V, c_int64, c_int64, V, c_int64, c_int, V, V, V, V, c_size_t,
+                             V], c_int),
     "hca_attend_noalloc": ([P, c_int, c_int, V, V, V, V, c_int64, c_int64, V, c_int64, c_int, V, V, V, V], c_int),
     "lca_grouped_oproj": ([c_int, c_int, c_int, c_int, c_int, c_int, V, V, V, V, V, V], c_int),
     "lca_gemm_bf16": ([c_int, c_int, c_int, V, c_int64, V, c_int64, V, c_int64, V], c_int),

@@ -192,12 +192,12 @@ def _attend_common(q, p):
 
 
 def csa_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse=None,
-               stream=None):
+               stream=None, entry="csa_attend"):
     """Core attention over kv_cache[idx] plus the window rows (see include/lca.h)."""
     B, n_q = _attend_common(q, p)
     if tuple(idx.shape) != (B, n_q, p.topk):
         raise ValueError("idx must be [B, n_q, topk]")
-    st = _lib.load().csa_attend(
+    st = getattr(_lib.load(), entry)(
         ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
         _i32(q_pos, "q_pos"), _ptr(kv_cache, torch.bfloat16, "kv_cache"), _rows(kv_cache, "kv_cache"),
         kv_cache.shape[1], _i32(idx, "idx"), _ptr(win_kv, torch.bfloat16, "win_kv"), _rows(win_kv, "win_kv"),
@@ -207,16 +207,39 @@ def csa_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, ou
     _check(st)
 
 
-def hca_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None, stream=None):
+def hca_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None, stream=None,
+               entry="hca_attend"):
     """Dense core attention over the visible entries of kv_cache plus the window rows."""
     B, n_q = _attend_common(q, p)
-    st = _lib.load().hca_attend(
+    st = getattr(_lib.load(), entry)(
         ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
         _i32(q_pos, "q_pos"), _ptr(kv_cache, torch.bfloat16, "kv_cache"), _rows(kv_cache, "kv_cache"),
         kv_cache.shape[1], _ptr(win_kv, torch.bfloat16, "win_kv"), _rows(win_kv, "win_kv"), win_kv.shape[1],
         _ptr(sink, torch.float32, "sink"), _ptr(out, torch.bfloat16, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(), _stream(stream))
     _check(st)
+
+
+def csa_attend_prepare(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse=None,
+                       stream=None):
+    """The query preparation of csa_attend alone, into the workspace (see include/lca.h)."""
+    csa_attend(p, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse, stream, "csa_attend_prepare")
+
+
+def csa_attend_prepared(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse=None,
+                        stream=None):
+    """The attention of csa_attend alone, on query images a csa_attend_prepare left in the workspace."""
+    csa_attend(p, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse, stream, "csa_attend_prepared")
+
+
+def hca_attend_prepare(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None,
+                       stream=None):
+    hca_attend(p, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse, stream, "hca_attend_prepare")
+
+
+def hca_attend_prepared(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None,
+                        stream=None):
+    hca_attend(p, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse, stream, "hca_attend_prepared")
 
 
 def hca_attend_noalloc(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, lse=None, stream=None):

@@ -237,11 +237,15 @@ lca_status attend_validate(const char *name, const lca_attn_params *p, int batch
     return LCA_OK;
 }
 
+// What an attention call launches: the query preparation and the attention (the usual call),
+// the attention alone (the query image is already in the workspace), or the preparation alone.
+enum AttendMode { kAttendAll = 0, kAttendPrepared = 1, kAttendPrepareOnly = 2 };
+
 lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q,
                        const float *gamma_q, const int32_t *q_pos, const lca_bf16 *kv, int64_t kv_bs,
                        int64_t cache_rows, const int32_t *idx, const lca_bf16 *win, int64_t win_bs,
                        int win_cap, const float *sink, lca_bf16 *out, float *lse, void *ws, size_t ws_bytes,
-                       cudaStream_t stream) {
+                       cudaStream_t stream, AttendMode mode = kAttendAll) {
     lca_status st = attend_validate(name, p, batch, n_q);
     if (st != LCA_OK) return st;
     const bool csa = idx != nullptr;
@@ -310,14 +314,17 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
         !make_tensor_map(&kv_row_map, kv, 2, dims_kv, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tensor_map(&win_row_map, win, 2, dims_win, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B))
         return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
-    const dim3 prep_grid((unsigned)pl.units, kQImgHeads / kQPrepHeads);
-    switch (C) {
-    case 128: launch_pdl(q_prep_kernel<128>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
-    case 256: launch_pdl(q_prep_kernel<256>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
-    default: launch_pdl(q_prep_kernel<512>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
+    if (mode != kAttendPrepared) {
+        const dim3 prep_grid((unsigned)pl.units, kQImgHeads / kQPrepHeads);
+        switch (C) {
+        case 128: launch_pdl(q_prep_kernel<128>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
+        case 256: launch_pdl(q_prep_kernel<256>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
+        default: launch_pdl(q_prep_kernel<512>, prep_grid, dim3(32 * kQPrepHeads), 0, stream, a); break;
+        }
+        st = check_launch(name);
+        if (st != LCA_OK) return st;
+        if (mode == kAttendPrepareOnly) return ok();
     }
-    st = check_launch(name);
-    if (st != LCA_OK) return st;
     switch (C) {
     case 128:
         cudaFuncSetAttribute(attend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -663,6 +670,48 @@ static lca_status noalloc_scratch(const char *name, void **addr) {
     }
     *addr = g_noalloc_addr[dev];
     return LCA_OK;
+}
+
+lca_status csa_attend_prepare(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                              const int32_t *q_pos, const lca_bf16 *kv_cache, int64_t kv_batch_stride,
+                              int64_t cache_rows, const int32_t *idx, const lca_bf16 *win_kv,
+                              int64_t win_batch_stride, int win_cap, const float *sink, lca_bf16 *out, float *lse,
+                              void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!idx) return fail(LCA_ERR_INVALID_ARG, "csa_attend_prepare: idx is NULL");
+    return attend_impl("csa_attend_prepare", p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride, cache_rows,
+                       idx, win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream,
+                       kAttendPrepareOnly);
+}
+
+lca_status csa_attend_prepared(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                               const int32_t *q_pos, const lca_bf16 *kv_cache, int64_t kv_batch_stride,
+                               int64_t cache_rows, const int32_t *idx, const lca_bf16 *win_kv,
+                               int64_t win_batch_stride, int win_cap, const float *sink, lca_bf16 *out, float *lse,
+                               void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    if (!idx) return fail(LCA_ERR_INVALID_ARG, "csa_attend_prepared: idx is NULL");
+    return attend_impl("csa_attend_prepared", p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride,
+                       cache_rows, idx, win_kv, win_batch_stride, win_cap, sink, out, lse, workspace,
+                       workspace_bytes, stream, kAttendPrepared);
+}
+
+lca_status hca_attend_prepare(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                              const int32_t *q_pos, const lca_bf16 *kv_cache, int64_t kv_batch_stride,
+                              int64_t cache_rows, const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                              const float *sink, lca_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+    return attend_impl("hca_attend_prepare", p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride, cache_rows,
+                       nullptr, win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream,
+                       kAttendPrepareOnly);
+}
+
+lca_status hca_attend_prepared(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                               const int32_t *q_pos, const lca_bf16 *kv_cache, int64_t kv_batch_stride,
+                               int64_t cache_rows, const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                               const float *sink, lca_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    return attend_impl("hca_attend_prepared", p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride,
+                       cache_rows, nullptr, win_kv, win_batch_stride, win_cap, sink, out, lse, workspace,
+                       workspace_bytes, stream, kAttendPrepared);
 }
 
 static lca_status gemv_launch(const char *name, int M, int N, int K, const lca_bf16 *A, int64_t lda, int64_t a_off,

@@ -62,9 +62,10 @@ class CsaLayer:
         api.csa_indexer_topk(self.p, q_idx, w_idx, self.idx_cache, q_pos, self.idx, self.ws_idx, stream)
         return self.idx
 
-    def attend(self, q, q_pos, out, lse=None, stream=None):
+    def attend(self, q, q_pos, out, lse=None, stream=None, part="csa_attend"):
+        """The attention; `part` may name csa_attend_prepare or csa_attend_prepared to run one half."""
         api.csa_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.idx, self.win_kv, self.w.sink, out,
-                       self.ws_att, lse, stream)
+                       self.ws_att, lse, stream, part)
 
     def step(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, new_tok_v, new_pos0,
              q, q_idx, w_idx, q_pos, out, stream=None):
@@ -77,8 +78,8 @@ class CsaLayer:
     def step_overlapped(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, new_tok_v, new_pos0,
                         q, q_idx, w_idx, q_pos, out):
         """The same step on the current stream, with the parts that do not feed the selection (the
-        KV entries and the window rows) on a side stream, overlapping the key entries, indexer and
-        top-k; the attention waits for both."""
+        KV entries, the window rows and the query preparation) on a side stream, overlapping the
+        key entries, indexer and top-k; the attention waits for both."""
         main = torch.cuda.current_stream()
         side = _side_stream(self)
         fork, join = torch.cuda.Event(), torch.cuda.Event()
@@ -88,13 +89,14 @@ class CsaLayer:
             api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
                                 n_new, self.kv_cache, side)
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, side)
+        self.attend(q, q_pos, out, stream=side, part="csa_attend_prepare")
         join.record(side)
         if n_new:
             api.csa_compress_kv(self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
                                 self.idx_cache, main)
         self.select(q_idx, w_idx, q_pos, main)
         main.wait_event(join)
-        self.attend(q, q_pos, out, stream=main)
+        self.attend(q, q_pos, out, stream=main, part="csa_attend_prepared")
 
 
 class HcaLayer:
@@ -115,9 +117,10 @@ class HcaLayer:
     def window(self, new_tok_v, new_pos0, stream=None):
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, stream)
 
-    def attend(self, q, q_pos, out, lse=None, stream=None):
+    def attend(self, q, q_pos, out, lse=None, stream=None, part="hca_attend"):
+        """The attention; `part` may name hca_attend_prepare or hca_attend_prepared to run one half."""
         api.hca_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.win_kv, self.w.sink, out,
-                       self.ws_att, lse, stream)
+                       self.ws_att, lse, stream, part)
 
     def step(self, tok_v, tok_z, tok_pos0, first_entry, n_new, new_tok_v, new_pos0, q, q_pos, out, stream=None):
         if n_new:
@@ -126,19 +129,20 @@ class HcaLayer:
         self.attend(q, q_pos, out, stream=stream)
 
     def step_overlapped(self, tok_v, tok_z, tok_pos0, first_entry, n_new, new_tok_v, new_pos0, q, q_pos, out):
-        """The same step on the current stream, with the window rows on a side stream next to the
-        compression; the attention waits for both."""
+        """The same step on the current stream, with the window rows and the query preparation on
+        a side stream next to the compression; the attention waits for both."""
         main = torch.cuda.current_stream()
         side = _side_stream(self)
         fork, join = torch.cuda.Event(), torch.cuda.Event()
         fork.record(main)
         side.wait_event(fork)
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, side)
+        self.attend(q, q_pos, out, stream=side, part="hca_attend_prepare")
         join.record(side)
         if n_new:
             self.compress(tok_v, tok_z, tok_pos0, first_entry, n_new, main)
         main.wait_event(join)
-        self.attend(q, q_pos, out, stream=main)
+        self.attend(q, q_pos, out, stream=main, part="hca_attend_prepared")
 
 
 class StepGraph:

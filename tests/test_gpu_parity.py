@@ -232,6 +232,42 @@ def test_csa_attend_with_injected_indices_matches_oracle(H, c, k, W):
         np.testing.assert_allclose(l[b, i], rl, rtol=0, atol=2e-3 * max(1.0, np.abs(rl).max()))
 
 
+@pytest.mark.parametrize("kind", ["csa", "hca"])
+def test_attend_prepare_then_prepared_equals_attend(kind):
+    """The query preparation on one stream and the attention on another (joined by an event) give
+    the same bits as the single call."""
+    rng = Rng(19)
+    B, n_q, rows, H, c, W, k = 2, 3, 900, 64, 512, 128, 512
+    cap = W + 3
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=4, topk=k)
+    d = _attend_inputs(rng, B, n_q, H, c, rows, W, cap)
+    pos = torch.tensor([[4 * rows - 1, 2000, 5], [3 * rows, 131, 4 * rows - 9]], dtype=torch.int32)
+    g = np.random.default_rng(20)
+    idx = torch.from_numpy(np.stack([np.stack([np.sort(g.choice(rows, k, replace=False)) for _ in range(n_q)])
+                                     for _ in range(B)]).astype(np.int32))
+    args = [dev(d["q"]), dev(d["gamma"]), dev(pos), dev(d["kv"])]
+    if kind == "csa":
+        args.append(dev(idx))
+        ws_bytes = api.csa_attend_workspace(p, B, n_q)
+    else:
+        ws_bytes = api.hca_attend_workspace(p, B, n_q, rows)
+    args += [dev(d["win"]), dev(d["sink"])]
+    whole, split = (torch.empty((B, n_q, H, c), dtype=torch.bfloat16, device=DEV) for _ in range(2))
+    lse_w, lse_s = (torch.empty((B, n_q, H), dtype=torch.float32, device=DEV) for _ in range(2))
+    ws_w, ws_s = (torch.empty(ws_bytes, dtype=torch.uint8, device=DEV) for _ in range(2))
+    getattr(api, kind + "_attend")(p, *args, whole, ws_w, lse_w)
+    side, ev = torch.cuda.Stream(), torch.cuda.Event()
+    side.wait_stream(torch.cuda.current_stream())
+    getattr(api, kind + "_attend_prepare")(p, *args, split, ws_s, lse_s, stream=side)
+    ev.record(side)
+    torch.cuda.current_stream().wait_event(ev)
+    getattr(api, kind + "_attend_prepared")(p, *args, split, ws_s, lse_s)
+    torch.cuda.synchronize()
+    assert api.lca_device_error() == 0
+    assert torch.equal(whole.view(torch.int16), split.view(torch.int16))
+    assert torch.equal(lse_w, lse_s)
+
+
 def test_attend_reports_out_of_range_indices():
     rng = Rng(18)
     p = AttnParams(heads=8, head_dim=128, window=4, ratio=4, topk=8)
