@@ -254,6 +254,9 @@ lca_status hca_attend_noalloc(const lca_attn_params *p, int batch, int n_q,
  *   o   [batch][H*c] bf16;  Wg [groups*d_g][(H/groups)*c] bf16;  Wm [d_model][groups*d_g];
  *   mid [batch][groups*d_g] bf16 (caller-owned scratch);  y [batch][d_model] bf16.
  * Supported: batch <= 16, every row length a multiple of 8.
+ * Wg and Wm are read from the moment the call's kernels start on the GPU, which may be
+ * before kernels issued earlier on the stream have finished (o and mid are read only after
+ * them): the weights must not be written by work still pending on the stream.
  * lca_gemm_bf16 is the plain product it is built from: C[M][N] = A[M][K] . B[N][K]^T
  * (fp32 accumulation, bf16 out), M <= 16 (activations), B the weight rows.
  * ------------------------------------------------------------------------------- */

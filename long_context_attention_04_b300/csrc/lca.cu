@@ -714,9 +714,65 @@ lca_status hca_attend_prepared(const lca_attn_params *p, int batch, int n_q, con
                        workspace_bytes, stream, kAttendPrepared);
 }
 
+extern "C++" {
+template <int MT, int KS, int NW>
+static void gemv_stream_launch(const GemvStreamArgs &a, int grid, cudaStream_t stream) {
+    constexpr int smem = gemv_stream_smem(KS * 256 * NW, MT, NW);
+    cudaFuncSetAttribute(gemv_stream_kernel<MT, KS, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    launch_pdl(gemv_stream_kernel<MT, KS, NW>, dim3(grid), dim3(32 * NW), smem, stream, a);
+}
+
+// The streaming product's variants: 8 warps (16 measured slower), K / 2048 slices of 256 per
+// warp, M x K / 2048 <= 16 activations per lane.  Returns false for shapes it does not cover.
+template <int MT>
+static bool gemv_stream_dispatch_mt(const GemvStreamArgs &a, int grid, cudaStream_t stream) {
+    switch (a.K) {
+    case 2048: gemv_stream_launch<MT, 1, 8>(a, grid, stream); return true;
+    case 4096: gemv_stream_launch<MT, 2, 8>(a, grid, stream); return true;
+    case 6144: if constexpr (MT <= 4) { gemv_stream_launch<MT, 3, 8>(a, grid, stream); return true; } return false;
+    case 8192: if constexpr (MT <= 4) { gemv_stream_launch<MT, 4, 8>(a, grid, stream); return true; } return false;
+    default: return false;
+    }
+}
+
+static bool gemv_stream_dispatch(const GemvStreamArgs &a, int mt, int grid, cudaStream_t stream) {
+    switch (mt) {
+    case 1: return gemv_stream_dispatch_mt<1>(a, grid, stream);
+    case 2: return gemv_stream_dispatch_mt<2>(a, grid, stream);
+    case 4: return gemv_stream_dispatch_mt<4>(a, grid, stream);
+    case 8: return gemv_stream_dispatch_mt<8>(a, grid, stream);
+    default: return false;
+    }
+}
+}  // extern "C++"
+
+// C = A . B^T for the batches' weight blocks.  The streaming kernel takes weight arrays stored
+// contiguously ([batches][N][K]) with K one of 2048, 4096, 6144, 8192, N a multiple of 4 and
+// few enough activations per lane (gemv_stream_dispatch); everything else takes gemv_kernel.
+// b_early: the weights may be read before the previous kernel in the stream has finished.
 static lca_status gemv_launch(const char *name, int M, int N, int K, const lca_bf16 *A, int64_t lda, int64_t a_off,
                               const lca_bf16 *B, int64_t ldb, int64_t b_off, lca_bf16 *C, int64_t ldc, int64_t c_off,
-                              int batches, cudaStream_t stream) {
+                              int batches, cudaStream_t stream, bool b_early = false) {
+    const int mt = M <= 1 ? 1 : M <= 2 ? 2 : M <= 4 ? 4 : M <= 8 ? 8 : 16;
+    if ((K == 2048 || K == 4096 || K == 6144 || K == 8192) && mt <= 8 && ldb == K &&
+        (batches == 1 || b_off == (int64_t)N * K) && N % 4 == 0 && aligned16(A) && aligned16(B) && lda % 8 == 0 &&
+        a_off % 8 == 0) {
+        GemvStreamArgs g;
+        g.M = M;
+        g.N = N;
+        g.K = K;
+        g.groups = (int64_t)batches * N / kGsRows;
+        g.A = reinterpret_cast<const __nv_bfloat16 *>(A);
+        g.lda = lda;
+        g.a_batch_off = a_off;
+        g.B = reinterpret_cast<const __nv_bfloat16 *>(B);
+        g.C = reinterpret_cast<__nv_bfloat16 *>(C);
+        g.ldc = ldc;
+        g.c_batch_off = c_off;
+        g.b_early = b_early ? 1 : 0;
+        const int grid = (int)std::min<int64_t>(g.groups, device_sm_count());
+        if (gemv_stream_dispatch(g, mt, grid, stream)) return check_launch(name);
+    }
     GemvArgs a;
     a.M = M;
     a.N = N;
@@ -788,9 +844,9 @@ lca_status lca_grouped_oproj(int batch, int heads, int head_dim, int groups, int
     const int64_t hc = (int64_t)heads * head_dim;
     const int64_t gd = (int64_t)groups * d_g;
     lca_status st = gemv_launch(name, batch, d_g, (int)in_g, o, hc, in_g, Wg, in_g, (int64_t)d_g * in_g, mid, gd, d_g,
-                                groups, stream);
+                                groups, stream, true);
     if (st != LCA_OK) return st;
-    st = gemv_launch(name, batch, d_model, (int)gd, mid, gd, 0, Wm, gd, 0, y, d_model, 0, 1, stream);
+    st = gemv_launch(name, batch, d_model, (int)gd, mid, gd, 0, Wm, gd, 0, y, d_model, 0, 1, stream, true);
     return st == LCA_OK ? ok() : st;
 }
 

@@ -39,6 +39,20 @@ def assert_close_rms(got: np.ndarray, ref: np.ndarray, tol: float = OUT_TOL, wha
     return err / rms if rms > 0 else 0.0
 
 
+def assert_close_bf16_out(got: np.ndarray, ref: np.ndarray, tol: float = 1e-3, what: str = ""):
+    """Element-wise bound for a product with fp32 accumulation and a bf16 result: half an ulp of
+    bf16 (2^-8 of the value: 8 significant bits) plus tol x RMS for the accumulation order."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    assert np.isfinite(got).all(), "%s: non-finite values" % what
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    bound = np.abs(ref) * 2.0 ** -8 + tol * rms
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), "%s: %d values outside half a bf16 ulp + %.0e x rms (first at %s)" % (
+        what, int(bad.sum()), tol, np.argwhere(bad)[0])
+
+
 def assert_rows_close(got_bf16, ref, what=""):
     """A stored bf16 row equals the oracle's fp64 row up to bf16 rounding (+ fp32 arithmetic)."""
     got = bf16_to_f64(got_bf16)
