@@ -197,7 +197,7 @@ lca_status hca_attend(const lca_attn_params *p, int batch, int n_q,
 
 /* The two halves of an attention call, for callers that overlap the query preparation with
  * other work (the selection, the cache updates) on another stream.  *_attend_prepare runs
- * only the query preparation (RMSNorm + RoPE(i) of q, hi/lo query images) into the workspace;
+ * only the query preparation (RMSNorm + RoPE(i) of q, fp16 hi/lo query images) into the workspace;
  * *_attend_prepared runs only the attention and the combine, reading those images.  Together,
  * with the same arguments and workspace, and the prepare ordered before the attention (same
  * stream, or an event), they compute exactly what *_attend computes.  The prepare reads q,

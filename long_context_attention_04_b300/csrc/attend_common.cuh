@@ -34,7 +34,7 @@ struct AttendArgs {
     const float *sink;            // [H]
     // split-K partials: O [unit][split][H][C] fp32 (unnormalised), m/l [unit][split][H] (base 2)
     float *part_o, *part_m, *part_l;
-    uint8_t *q_img;               // per-query images of the prepared query: [unit][hi | lo] (q_prep_kernel)
+    uint8_t *q_img;               // per-query images of the prepared query: [unit][hi | lo] fp16 (q_prep_kernel)
     __nv_bfloat16 *out;           // [B][n_q][H][C]
     float *lse;                   // [B][n_q][H] or nullptr
 };

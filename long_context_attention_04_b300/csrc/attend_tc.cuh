@@ -15,15 +15,17 @@
 // product and the MN-major A operand of the second.  S^T (128 columns) and O^T (c/128 chunks
 // of 64 columns) live in TMEM.
 //
-// Precision.  The normalised, rotated query (q_prep_kernel) is split into bf16 hi + lo parts
-// (q = hi + lo to ~16 bits) and S^T accumulates KV.hi^T and KV.lo^T side by side (one
-// N = 128 MMA per k step), summed by the softmax.  The probabilities are split the same way,
-// P = hi + lo, and O^T accumulates both products.  A single bf16 query or a single bf16 P
-// each put a relative error of up to 2^-9 on every weight, as large as the bf16 rounding of
-// the output itself.
+// Precision.  Both products run in fp16 with fp32 accumulation.  The KV tile is re-encoded
+// in shared memory from bf16 to fp16 as it lands (exact for normalised rows, see
+// bf16x8_to_f16x8).  The normalised, rotated query (q_prep_kernel) is split into fp16 hi + lo
+// parts (about 22 bits) and S^T accumulates KV.hi^T and KV.lo^T side by side (one N = 128 MMA
+// per k step), summed by the softmax: a single fp16 query moves the logits by up to 2^-12 of
+// |q||k|, enough to push outputs whose bf16 rounding already sits near the error bound past
+// it.  The probabilities, in [0, 1], need no split: fp16 P (relative error 2^-12) lands within
+// the output's own bf16 rounding, and the row sum adds the same rounded values.
 //
 // Shared memory holds the KV tile as four 32 KB slots (128 rows x 128 c each, the whole tile
-// at c = 512), a ring of two 32 KB query slots and the two 16 KB P^T buffers.  The query is
+// at c = 512), a ring of two 32 KB query slots and the 16 KB P^T buffer.  The query is
 // not resident: each S chunk comes with the matching 32 KB query chunk (hi and lo stacked as
 // one 128-row B operand, bulk-copied from the L2-hot image).  The KV tile stays resident
 // across both products; slot j is released when its PV chunk completes, and the producer
@@ -41,7 +43,8 @@
 //   warp 11     second issuer of row gathers (c box 1 of gathered chunks; the producer issues
 //               box 0): TMA gathers from one warp reach about half the rate of two
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-9   softmax: one TMEM lane (row) per thread, 32 heads per thread; online softmax
+//   warps 2-9   re-encoding of each landed KV chunk to fp16 (an eighth each), then the
+//               softmax: one TMEM lane (row) per thread, 32 heads per thread; online softmax
 //               in base 2 with a conditional rescale (the running max moves only when a
 //               logit exceeds it by more than 2^8), P^T rows to shared memory
 // The split's unnormalised O, running max and row sum go to the workspace; combine_kernel
@@ -73,12 +76,11 @@ constexpr float kAtTau = 8.0f;                           // log2 headroom before
 template <int C>
 struct AttendTcConfig {
     static constexpr int CC = C / 128;                        // c chunks per row
-    static constexpr int P_HALF = kAtTile * kAtHP * 2;        // one bf16 P^T buffer (16 KB)
-    static constexpr int P_BYTES = 2 * P_HALF;                // P^T = hi + lo
+    static constexpr int P_BYTES = kAtTile * kAtHP * 2;       // fp16 P^T (16 KB)
     static constexpr int TMEM_S = 0;                          // S^T: 128 columns (hi | lo)
     static constexpr int TMEM_O = 2 * kAtHP;                  // O^T chunk j at TMEM_O + 64 j
     static constexpr int TMEM_COLS = 512;
-    static constexpr int MISC = 1344;                          // barriers, votes, cross-warp maxima
+    static constexpr int MISC = 1408;                          // barriers, votes, cross-warp maxima
     static constexpr int SMEM_BYTES = MISC + 1024 + CC * kAtChunkBytes + kAtQSlots * kAtQChunkBytes + P_BYTES;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
@@ -124,10 +126,11 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                                                 ~uintptr_t(1023));
     uint8_t *ring = base;                                     // KV slot j = chunk j: 2 boxes [128 rows x 128 B]
     uint8_t *q_ring = ring + CC * kAtChunkBytes;              // query slots: 2 boxes [128 rows x 128 B]
-    uint8_t *p_buf = q_ring + kAtQSlots * kAtQChunkBytes;     // hi, then lo: [128 rows x 128 B] each
+    uint8_t *p_buf = q_ring + kAtQSlots * kAtQChunkBytes;     // P^T: [128 rows x 128 B] fp16
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + kAtSlots;
-    uint64_t *q_full = empty + kAtSlots;
+    uint64_t *conv = empty + kAtSlots;
+    uint64_t *q_full = conv + kAtSlots;
     uint64_t *q_empty = q_full + kAtQSlots;
     uint64_t *s_full = q_empty + kAtQSlots;
     uint64_t *s_empty = s_full + 2;
@@ -138,9 +141,10 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     uint64_t *teardown = red_bar + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(teardown + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    int *votes = reinterpret_cast<int *>(misc + 192);                  // [2][8]
-    float *red = reinterpret_cast<float *>(misc + 256);                // [8][32]
-    uint64_t *gather_go = reinterpret_cast<uint64_t *>(misc + 1280);  // [kAtSlots]
+    // misc: 27 barriers + TMEM slot + abort flag (224 B), votes, maxima, gather hand-offs
+    int *votes = reinterpret_cast<int *>(misc + 256);                  // [2][8]
+    float *red = reinterpret_cast<float *>(misc + 320);                // [8][32]
+    uint64_t *gather_go = reinterpret_cast<uint64_t *>(misc + 1344);  // [kAtSlots]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // ---- set-up: barriers, TMEM ----
@@ -148,6 +152,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         for (int s = 0; s < kAtSlots; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&conv[s], kAtSoftmaxWarps);
             ptx::mbar_init(&gather_go[s], 1);
         }
         for (int s = 0; s < kAtQSlots; ++s) {
@@ -278,12 +283,13 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         if (!ok) *abort_flag = 1;
     } else if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------- MMA issue ----
-        // Per tile: S^T = KV . [hi | lo]^T chunk by chunk; then, once the softmax has written P,
+        // Per tile: S^T = KV . [hi | lo]^T chunk by chunk as the re-encoded chunks become ready;
+        // then, once the softmax has written P,
         // O^T += V^T P^T chunk by chunk, releasing each KV slot to the producer.  tcgen05 ops
         // execute in issue order, so S(t+1) never overwrites S^T or P^T still in use.
         if (lane == 0) {
-            constexpr uint32_t idesc_s = ptx::idesc_bf16(128, 2 * kAtHP, false, false);
-            constexpr uint32_t idesc_o = ptx::idesc_bf16(128, kAtHP, true, true);
+            constexpr uint32_t idesc_s = ptx::idesc_f16(128, 2 * kAtHP, false, false);
+            constexpr uint32_t idesc_o = ptx::idesc_f16(128, kAtHP, true, true);
             const uint32_t p_addr = ptx::smem_u32(p_buf);
             uint32_t q_used = 0;
             bool ok = true;
@@ -291,7 +297,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 const uint32_t d = tmem + Cfg::TMEM_S;
                 for (int j = 0; j < CC && ok; ++j) {
                     const int qs = q_used % kAtQSlots;
-                    if (!ptx::mbar_wait(&full[j], u & 1) || !ptx::mbar_wait(&q_full[qs], (q_used / kAtQSlots) & 1)) {
+                    if (!ptx::mbar_wait(&conv[j], u & 1) || !ptx::mbar_wait(&q_full[qs], (q_used / kAtQSlots) & 1)) {
                         ok = false;
                         break;
                     }
@@ -304,7 +310,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                                                            ptx::kSwizzle128);
                         const uint64_t bd = ptx::smem_desc(q_addr + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024,
                                                            ptx::kSwizzle128);
-                        ptx::mma_bf16(d, ad, bd, idesc_s, (j > 0 || kk > 0));
+                        ptx::mma_f16(d, ad, bd, idesc_s, (j > 0 || kk > 0));
                     }
                     ptx::mma_commit(&q_empty[qs]);
                     ++q_used;
@@ -321,11 +327,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk) {
                         const uint64_t ad = ptx::smem_desc(slot + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
-                        const uint64_t bh = ptx::smem_desc(p_addr + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
-                        const uint64_t bl = ptx::smem_desc(p_addr + Cfg::P_HALF + kk * 2048, 128 * 128, 1024,
-                                                           ptx::kSwizzle128);
-                        ptx::mma_bf16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bh, idesc_o, (u > 0 || kk > 0));
-                        ptx::mma_bf16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bl, idesc_o, true);
+                        const uint64_t bd = ptx::smem_desc(p_addr + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
+                        ptx::mma_f16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bd, idesc_o, (u > 0 || kk > 0));
                     }
                     ptx::mma_commit(&empty[j]);
                 }
@@ -389,8 +392,26 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         }
         uint32_t votes_done = 0, reds_done = 0;
         bool ok = true;
+        const int ctid = sw * 32 + lane;             // 0..255 among the softmax warps
         for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
-            if (!ptx::mbar_wait(&s_full[0], u & 1)) {
+            // ---- re-encode tile u's KV chunks to fp16 as they land (an eighth per warp).  The
+            // slots were refilled after PV(u-1) released them, which needed this tile's P(u-1).
+            for (int j = 0; j < CC && ok; ++j) {
+                if (!ptx::mbar_wait(&full[j], u & 1)) {
+                    ok = false;
+                    break;
+                }
+                uint4 *chunk = reinterpret_cast<uint4 *>(ring + j * kAtChunkBytes);
+#pragma unroll
+                for (int k = 0; k < kAtChunkBytes / 16 / (32 * kAtSoftmaxWarps); ++k) {
+                    uint4 *p = chunk + ctid + k * (32 * kAtSoftmaxWarps);
+                    *p = bf16x8_to_f16x8(*p);
+                }
+                ptx::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&conv[j]);
+            }
+            if (!ok || !ptx::mbar_wait(&s_full[0], u & 1)) {
                 ok = false;
                 break;
             }
@@ -474,24 +495,19 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 }
                 ptx::tc_fence_before();
             }
-            // probabilities of this row, written as two bf16 P^T rows, hi = bf16(p) and
-            // lo = bf16(p - hi) (32 heads = 4 chunks each), so that hi + lo carries p to ~2^-16;
-            // PV of the previous tile, the last reader of P^T, completed before S^T of this tile.
-            float pr[32], plo[32];
+            // probabilities of this row as an fp16 P^T row (32 heads = 4 chunks); the row sum
+            // adds the rounded values, the weights PV applies.  PV of the previous tile, the last
+            // reader of P^T, completed before S^T of this tile.
+            float pr[32];
 #pragma unroll
             for (int h = 0; h < 32; ++h) {
                 const float ms = m[h] == -INFINITY ? 0.f : m[h];
-                const float pv = exp2f(x[h] - ms);
-                pr[h] = __bfloat162float(__float2bfloat16_rn(pv));
-                plo[h] = pv - pr[h];
-                l[h] += pv;
+                pr[h] = __half2float(__float2half_rn(exp2f(x[h] - ms)));
+                l[h] += pr[h];
             }
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-                *reinterpret_cast<uint4 *>(p_buf + ptx::sw128_offset(r, half * 4 + c4)) = pack8(pr + 8 * c4);
-                *reinterpret_cast<uint4 *>(p_buf + Cfg::P_HALF + ptx::sw128_offset(r, half * 4 + c4)) =
-                    pack8(plo + 8 * c4);
-            }
+            for (int c4 = 0; c4 < 4; ++c4)
+                *reinterpret_cast<uint4 *>(p_buf + ptx::sw128_offset(r, half * 4 + c4)) = pack8_f16(pr + 8 * c4);
             ptx::fence_proxy_async();
             ptx::mbar_arrive(&p_full[0]);
         }

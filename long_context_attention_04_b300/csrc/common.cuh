@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,6 +50,27 @@ __device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
 __device__ __forceinline__ uint4 pack8(const float *f) {
     return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
+// Two fp32 values as fp16 (round to nearest even, saturating at +-65504 instead of overflowing
+// to infinity), packed with `first` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float first, float second) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(second), "f"(first));
+    return r;
+}
+
+__device__ __forceinline__ uint4 pack8_f16(const float *f) {
+    return make_uint4(pack_f16x2(f[0], f[1]), pack_f16x2(f[2], f[3]), pack_f16x2(f[4], f[5]),
+                      pack_f16x2(f[6], f[7]));
+}
+
+// Eight bf16 values re-encoded as fp16.  Exact for magnitudes in [2^-14, 65504] (bf16 carries
+// 8 significant bits, fp16 11); smaller ones become fp16 subnormals (absolute error below
+// 2^-25), larger ones saturate.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 &v) {
+    return make_uint4(pack_f16x2(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
+                      pack_f16x2(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

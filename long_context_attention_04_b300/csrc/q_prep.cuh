@@ -1,13 +1,15 @@
 // q_prep.cuh -- the query side of core attention, computed once per query for all its
 // split-K CTAs: RMSNorm over c with gamma_q ("Q/KV normalization"), RoPE at the query
-// position on the trailing R dims ("Partial RoPE"), then the split q = hi + lo into two bf16
+// position on the trailing R dims ("Partial RoPE"), then the split q = hi + lo into two fp16
 // parts (DeepSeek-V4 hybrid attention, gxgjx.lffhtl.com/lxrt/355279.html, section 混肃穆力机制).
 //
 // Output: per query, an image of [c/128 chunks][2 boxes of 64 c][128 rows][128 bytes], rows
 // 0-63 the hi parts of heads 0-63 and rows 64-127 their lo parts, 128-byte swizzled (16-byte
 // chunk index XOR row % 8): exactly the shared-memory layout of the K-major B operand the
 // attention kernel feeds to tcgen05.mma (N = 128), so the attention kernel bulk-copies one
-// 32 KB chunk next to each KV chunk it multiplies.  Heads past H are zero rows.
+// 32 KB chunk next to each KV chunk it multiplies.  Heads past H are zero rows.  hi + lo
+// carries the normalised query to about 22 bits (fp16 keeps 11 each; the query's elements are
+// at most sqrt(c) max|gamma|, far inside fp16's range).
 #pragma once
 
 #include "attend_common.cuh"
@@ -54,7 +56,7 @@ __global__ void __launch_bounds__(32 * kQPrepHeads) q_prep_kernel(AttendArgs a) 
     float lo[EPL];
 #pragma unroll
     for (int u = 0; u < EPL; ++u) {
-        const float hi = __bfloat162float(__float2bfloat16_rn(v[u]));
+        const float hi = __half2float(__float2half_rn(v[u]));
         lo[u] = v[u] - hi;
         v[u] = hi;
     }
@@ -65,16 +67,16 @@ __global__ void __launch_bounds__(32 * kQPrepHeads) q_prep_kernel(AttendArgs a) 
         for (int u = 0; u < EPL; u += 8) {
             const int e = lane * EPL + u;
             uint8_t *box = img + (e / 128) * kQChunkBytes + ((e % 128) / 64) * (128 * 128);
-            *reinterpret_cast<uint4 *>(box + sw128(h, (e % 64) / 8)) = pack8(v + u);
-            *reinterpret_cast<uint4 *>(box + sw128(kQImgHeads + h, (e % 64) / 8)) = pack8(lo + u);
+            *reinterpret_cast<uint4 *>(box + sw128(h, (e % 64) / 8)) = pack8_f16(v + u);
+            *reinterpret_cast<uint4 *>(box + sw128(kQImgHeads + h, (e % 64) / 8)) = pack8_f16(lo + u);
         }
     } else {
         const int e = lane * EPL;   // 4 elements: half a 16-byte chunk
         uint8_t *box = img + (e / 128) * kQChunkBytes + ((e % 128) / 64) * (128 * 128) + (e % 8) * 2;
         *reinterpret_cast<uint2 *>(box + sw128(h, (e % 64) / 8)) =
-            make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+            make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
         *reinterpret_cast<uint2 *>(box + sw128(kQImgHeads + h, (e % 64) / 8)) =
-            make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
+            make_uint2(pack_f16x2(lo[0], lo[1]), pack_f16x2(lo[2], lo[3]));
     }
 }
 
