@@ -59,6 +59,7 @@ struct TopkShared {
     int n_cand[kTopkWarps];
     int cta_gt, cta_eq;          // this CTA's output counts (read by the other CTAs)
     int sel_bin, sel_above, overflow;
+    int g_total, g_over;         // this CTA's candidate count and overflow (read by the other CTAs)
 };
 
 __device__ __forceinline__ uint32_t smem_u32_of(const void *p) {
@@ -81,6 +82,13 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 // with reads after it, across the cluster.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// Store v to the shared memory of CTA `rank` of the cluster, at the address of `local`.
+__device__ __forceinline__ void dsmem_st(const void *local, uint32_t rank, uint32_t v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32_of(local)), "r"(rank));
+    asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(remote), "r"(v) : "memory");
 }
 
 // An int in the shared memory of CTA `rank` of the cluster, at the address of `local`.
@@ -152,6 +160,7 @@ __device__ __forceinline__ void topk_pick_bin(TopkShared &sh, const int *h, int 
 // row in global memory.  Keys are addressed by position in the CTA's slice.
 struct TopkSrc {
     const uint32_t *skeys;       // [len] shared keys, or nullptr
+    const int32_t *sidx;         // [len] row indices of skeys, or nullptr (index = base + position)
     const uint32_t *ckey;        // candidate keys [warps][kTopkCandPerWarp], or nullptr
     const int32_t *cidx;
     const float *g;              // global scores of the slice
@@ -227,7 +236,7 @@ __device__ __forceinline__ uint32_t topk_seg_key(const TopkShared &sh, const Top
     }
     const int j = warp * seg + i;
     valid = i < seg && j < s.len;
-    index = s.base + j;
+    index = s.sidx ? (valid ? s.sidx[j] : 0) : s.base + j;
     if (!valid) return 0u;
     return s.skeys ? s.skeys[j] : ordered_key(__ldg(s.g + j));
 }
@@ -355,6 +364,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
         __syncthreads();
         s.skeys = dyn;
     }
+    int cl_sel = cl;                             // CTAs taking part in the selection from here on
     // ---- first digit (bits 31..21) ----
     topk_hist(sh, s, 0u, 0u, 21, 2048);
     topk_merge_pick(sh, cl, 2048, k);
@@ -441,22 +451,68 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(TopkArgs a) {
             s.ckey = ckey;
             s.cidx = cidx;
         }
+        // ---- gather: when the whole row's candidates fit in CTA 0's key area, the other CTAs
+        // copy theirs there (in index order: CTA by CTA, warp by warp) and leave; CTA 0 finishes
+        // the selection alone, with no more cluster barriers.
+        if (SMEM && cl > 1) {
+            if (warp == 0) {
+                const int c = sh.n_cand[lane];
+                int x = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += y;
+                }
+                sh.pre_gt[lane] = x - c;                 // this warp's offset within the CTA
+                if (lane == 31) {
+                    sh.g_total = x;
+                    sh.g_over = sh.overflow;
+                }
+            }
+            cluster_sync();                              // every CTA's count is readable
+            int total = 0, before = 0, over = 0;
+            for (int r = 0; r < cl; ++r) {
+                const int t = dsmem_ld(&sh.g_total, (uint32_t)r);
+                over |= dsmem_ld(&sh.g_over, (uint32_t)r);
+                before += r < (int)rank ? t : 0;
+                total += t;
+            }
+            // CTA 0's key area ends where its candidate lists begin (its slice: [0, min(n, per)))
+            const int cap = (int)(topk_keys_words(min(n, per)) / 2);    // (key, index) pairs
+            if (!over && total <= cap) {
+                // CTA 0's key area: keys at [0, cap), indices at [cap, 2 cap)
+                const int o0 = before + sh.pre_gt[warp];
+                for (int i = lane; i < sh.n_cand[warp]; i += 32) {
+                    dsmem_st(dyn + o0 + i, 0u, ckey[warp * kTopkCandPerWarp + i]);
+                    dsmem_st(dyn + cap + o0 + i, 0u, (uint32_t)cidx[warp * kTopkCandPerWarp + i]);
+                }
+                cluster_sync();                          // the copies are in CTA 0
+                if (rank != 0) return;
+                s.skeys = dyn;
+                s.sidx = reinterpret_cast<const int32_t *>(dyn + cap);
+                s.ckey = nullptr;
+                s.cidx = nullptr;
+                s.len = total;
+                s.base = 0;
+                cl_sel = 1;
+            }
+        }
     }
     // ---- second and third digits, on keys whose higher digits match ----
     uint32_t prefix = bin1 << 21, mask = 0xFFE00000u;
     topk_hist(sh, s, prefix, mask, 10, 2048);
-    topk_merge_pick(sh, cl, 2048, remaining);
+    topk_merge_pick(sh, cl_sel, 2048, remaining);
     prefix |= (uint32_t)sh.sel_bin << 10;
     mask |= 0x001FFC00u;
     remaining -= sh.sel_above;
     __syncthreads();
     topk_hist(sh, s, prefix, mask, 0, 1024);
-    topk_merge_pick(sh, cl, 1024, remaining);
+    topk_merge_pick(sh, cl_sel, 1024, remaining);
     prefix |= (uint32_t)sh.sel_bin;
     remaining -= sh.sel_above;
     __syncthreads();
-    topk_write(sh, s, cl, rank, prefix, remaining, out, k);
-    if (cl > 1) cluster_sync();                  // keep this CTA's counts readable until all are done
+    topk_write(sh, s, cl_sel, cl_sel > 1 ? rank : 0u, prefix, remaining, out, k);
+    if (cl_sel > 1) cluster_sync();              // keep this CTA's counts readable until all are done
 }
 
 // Words of shared memory for a slice's keys, rounded to 16 bytes.

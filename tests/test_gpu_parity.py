@@ -154,6 +154,10 @@ def test_topk_exact_on_given_scores_with_ties(n, k):
     rows[-1][::7] = -0.0
     rows[-1][3::7] = 0.0
     rows.append((8.0 * g.standard_normal(n)).astype(np.float32))      # no ties (indexer-like spread)
+    r = (-1.0 - g.random(n)).astype(np.float32)                       # 60% share the selected first digit:
+    hot = g.random(n) < 0.6                                           # more candidates than one CTA holds
+    r[hot] = (1.0 + 0.25 * g.random(int(hot.sum()))).astype(np.float32)
+    rows.append(r)
     R = len(rows)
     S = np.stack(rows)[None]                   # [1, R, n]
     stride = (n + 3) // 4 * 4
