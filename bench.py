@@ -197,13 +197,13 @@ class ClockSampler:
 class Workload:
     """Common shape of a benchmark workload (device state + per-step inputs)."""
 
-    def _stage_inputs(self, keys, stage: bool):
+    def _stage_inputs(self, keys, stage: bool, groups: dict = None):
         """The per-step inputs as views of one packed device buffer with a pinned host mirror
-        (host_in), uploaded with one copy per step; without `stage`, plain pinned host copies."""
+        (host_in), uploaded group by group; without `stage`, plain pinned host copies."""
         from long_context_attention_04_b300.layers import StagingBuffer
         if stage:
             sub = {k: self.d[k] for k in keys}
-            self.stage = StagingBuffer(sub)
+            self.stage = StagingBuffer(sub, groups)
             self.d.update(sub)
             self.host_in = self.stage.host
         else:
@@ -252,7 +252,9 @@ class CsaDecode(Workload):
         self.launches = 7
         self.dominant = "indexer"
         # per-step inputs, pinned on the host for the end-to-end leg
-        self._stage_inputs(("tok_v", "tok_z", "tok_vi", "tok_zi", "q", "q_idx", "w_idx"), stage)
+        # (the selection's inputs first; the rest goes up on the side stream during the selection)
+        self.groups = {"main": ["tok_vi", "tok_zi", "q_idx", "w_idx"], "side": ["tok_v", "tok_z", "q"]}
+        self._stage_inputs(("tok_v", "tok_z", "tok_vi", "tok_zi", "q", "q_idx", "w_idx"), stage, self.groups)
         self.host_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
@@ -265,15 +267,15 @@ class CsaDecode(Workload):
         d = self.d
         self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], self.layer.idx_cache, self.q_pos, self.scores)
 
-    def step(self):
+    def step(self, side_prologue=None):
         d = self.d
         self.layer.step_overlapped(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, 1,
                                    d["tok_v"][:, -1:], self.new_pos, d["q"], d["q_idx"], d["w_idx"], self.q_pos,
-                                   self.out)
+                                   self.out, side_prologue)
 
     def e2e_step(self):
-        self.stage.upload()
-        self.step()
+        self.stage.upload(group="main")
+        self.step(lambda side: self.stage.upload(side, "side"))
         self.host_out.copy_(self.out, non_blocking=True)
 
     def cpu_sample(self, budget_s: float) -> dict:
@@ -350,7 +352,9 @@ class HcaDecode(Workload):
         self.tokens = B
         self.launches = 4
         self.dominant = "attend"
-        self._stage_inputs(("tok_v", "tok_z", "q"), stage)
+        # (the compression's inputs first; the query goes up on the side stream meanwhile)
+        self.groups = {"main": ["tok_v", "tok_z"], "side": ["q"]}
+        self._stage_inputs(("tok_v", "tok_z", "q"), stage, self.groups)
         self.host_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
@@ -363,14 +367,14 @@ class HcaDecode(Workload):
         # the attention kernel and its split-K combine
         self.layer.attend(self.d["q"], self.q_pos, self.out)
 
-    def step(self):
+    def step(self, side_prologue=None):
         d = self.d
         self.layer.step_overlapped(d["tok_v"], d["tok_z"], self.tok_pos0, self.first, 1, d["tok_v"][:, -1:],
-                                   self.new_pos, d["q"], self.q_pos, self.out)
+                                   self.new_pos, d["q"], self.q_pos, self.out, side_prologue)
 
     def e2e_step(self):
-        self.stage.upload()
-        self.step()
+        self.stage.upload(group="main")
+        self.step(lambda side: self.stage.upload(side, "side"))
         self.host_out.copy_(self.out, non_blocking=True)
 
     def snapshot_host(self):
@@ -549,10 +553,12 @@ class BlockDecode(Workload):
             else:
                 sub = dict(name="HCA layer", B=B, pos=pos, entries=cfg["hca_entries"], shape=cfg["hca"])
                 self.layers.append(HcaDecode(sub, seed=seed * 1000 + i, stage=False))
-        # every layer's per-step inputs in one staging buffer: one upload per block step
+        # every layer's per-step inputs in one staging buffer, one group per layer: a copy stream
+        # uploads the groups in layer order while the earlier layers compute
         from long_context_attention_04_b300.layers import StagingBuffer
         packed = {(i, k): L.d[k] for i, L in enumerate(self.layers) for k in L.host_in}
-        self.stage = StagingBuffer(packed)
+        self.stage = StagingBuffer(packed, {i: [(i, k) for k in L.host_in] for i, L in enumerate(self.layers)})
+        self.copy_stream = torch.cuda.Stream()
         for (i, k), t in packed.items():
             self.layers[i].d[k] = t
             self.layers[i].host_in[k] = self.stage.host[(i, k)]
@@ -587,11 +593,20 @@ class BlockDecode(Workload):
             self._oproj(i)
 
     def e2e_step(self):
-        self.stage.upload()
+        main, cs = torch.cuda.current_stream(), self.copy_stream
+        cs.wait_stream(main)
+        ready = []
+        for i in range(len(self.layers)):
+            self.stage.upload(cs, i)
+            ev = torch.cuda.Event()
+            ev.record(cs)
+            ready.append(ev)
         for i, L in enumerate(self.layers):
+            main.wait_event(ready[i])
             L.step()
             self._oproj(i)
             self.host_out[i].copy_(self.y[i], non_blocking=True)
+        main.wait_stream(cs)
 
     def snapshot_host(self):
         self.layers[0].snapshot_host()

@@ -76,15 +76,18 @@ class CsaLayer:
         self.attend(q, q_pos, out, stream=stream)
 
     def step_overlapped(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, new_tok_v, new_pos0,
-                        q, q_idx, w_idx, q_pos, out):
+                        q, q_idx, w_idx, q_pos, out, side_prologue=None):
         """The same step on the current stream, with the parts that do not feed the selection (the
         KV entries, the window rows and the query preparation) on a side stream, overlapping the
-        key entries, indexer and top-k; the attention waits for both."""
+        key entries, indexer and top-k; the attention waits for both.  `side_prologue(stream)`,
+        if given, is issued first on the side stream (e.g. the upload of the side's inputs)."""
         main = torch.cuda.current_stream()
         side = _side_stream(self)
         fork, join = torch.cuda.Event(), torch.cuda.Event()
         fork.record(main)
         side.wait_event(fork)
+        if side_prologue is not None:
+            side_prologue(side)
         if n_new:
             api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
                                 n_new, self.kv_cache, side)
@@ -128,14 +131,18 @@ class HcaLayer:
         self.window(new_tok_v, new_pos0, stream)
         self.attend(q, q_pos, out, stream=stream)
 
-    def step_overlapped(self, tok_v, tok_z, tok_pos0, first_entry, n_new, new_tok_v, new_pos0, q, q_pos, out):
+    def step_overlapped(self, tok_v, tok_z, tok_pos0, first_entry, n_new, new_tok_v, new_pos0, q, q_pos, out,
+                        side_prologue=None):
         """The same step on the current stream, with the window rows and the query preparation on
-        a side stream next to the compression; the attention waits for both."""
+        a side stream next to the compression; the attention waits for both.  `side_prologue(stream)`,
+        if given, is issued first on the side stream."""
         main = torch.cuda.current_stream()
         side = _side_stream(self)
         fork, join = torch.cuda.Event(), torch.cuda.Event()
         fork.record(main)
         side.wait_event(fork)
+        if side_prologue is not None:
+            side_prologue(side)
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, side)
         self.attend(q, q_pos, out, stream=side, part="hca_attend_prepare")
         join.record(side)
@@ -172,18 +179,30 @@ class StepGraph:
 
 class StagingBuffer:
     """Per-step inputs packed into one device buffer with a pinned host mirror, so that a step
-    uploads them with a single copy (each host-to-device transfer pays a fixed latency of tens
-    of microseconds, more than a few MB of payload at link speed).
+    uploads them with a few large copies (each host-to-device transfer pays a fixed latency of
+    tens of microseconds, more than a few MB of payload at link speed).
 
     `tensors` maps names to device tensors; they are replaced, in place in the dict, by views of
     the packed buffer (16-byte aligned, values copied), and `host[name]` is the matching view of
-    the pinned mirror.  Fill `host[...]`, then `upload()` on the stream of the step."""
+    the pinned mirror.  `groups` (optional) maps group names to lists of tensor names; each group
+    is packed contiguously and can be uploaded on its own, so that the work needing only the
+    first group starts while the rest is in flight.  Fill `host[...]`, then `upload(stream,
+    group)` (all groups when `group` is None)."""
 
-    def __init__(self, tensors: dict):
-        offs, total = {}, 0
-        for k, t in tensors.items():
-            offs[k] = total
-            total += (t.numel() * t.element_size() + 15) // 16 * 16
+    def __init__(self, tensors: dict, groups: dict = None):
+        if groups is None:
+            groups = {None: list(tensors)}
+        order = [k for g in groups.values() for k in g]
+        if sorted(map(repr, order)) != sorted(map(repr, tensors)):
+            raise ValueError("groups must partition the staged tensors")
+        offs, total, self.ranges = {}, 0, {}
+        for g, keys in groups.items():
+            start = total
+            for k in keys:
+                t = tensors[k]
+                offs[k] = total
+                total += (t.numel() * t.element_size() + 15) // 16 * 16
+            self.ranges[g] = (start, total)
         dev = next(iter(tensors.values())).device
         self.dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
         self.host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
@@ -197,7 +216,8 @@ class StagingBuffer:
             self.host[k].copy_(t)
         self.nbytes = total
 
-    def upload(self, stream=None):
+    def upload(self, stream=None, group=None):
+        a, b = (0, self.nbytes) if group is None else self.ranges[group]
         with torch.cuda.stream(stream or torch.cuda.current_stream()):
-            self.dev_buf.copy_(self.host_buf, non_blocking=True)
+            self.dev_buf[a:b].copy_(self.host_buf[a:b], non_blocking=True)
 
