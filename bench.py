@@ -249,7 +249,7 @@ class CsaDecode(Workload):
         self.out = torch.empty((B, 1, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
         self.scores = self.layer.ws_idx.view(torch.float32).view(B, 1, -1)
         self.tokens = B
-        self.launches = 7
+        self.launches = 8          # 2 compress, window, q prep, indexer, top-k, attention, combine
         self.dominant = "indexer"
         # per-step inputs, pinned on the host for the end-to-end leg
         # (the selection's inputs first; the rest goes up on the side stream during the selection)
@@ -350,7 +350,7 @@ class HcaDecode(Workload):
         self.q_pos = torch.full((B, 1), pos, **i32)
         self.out = torch.empty((B, 1, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
         self.tokens = B
-        self.launches = 4
+        self.launches = 5          # compress, window, q prep, attention, combine
         self.dominant = "attend"
         # (the compression's inputs first; the query goes up on the side stream meanwhile)
         self.groups = {"main": ["tok_v", "tok_z"], "side": ["q"]}
@@ -440,7 +440,7 @@ class CsaPrefill(Workload):
         self.out = torch.empty((1, Tq, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
         self.scores = self.layer.ws_idx.view(torch.float32).view(1, Tq, -1)
         self.tokens = Tq
-        self.launches = 7
+        self.launches = 8          # 2 compress, window, indexer, top-k, q prep, attention, combine
         self.dominant = "indexer"
         self.bound = "tensor"
         self._stage_inputs(("tok_v", "tok_z", "tok_vi", "tok_zi", "q", "q_idx", "w_idx"), stage)
