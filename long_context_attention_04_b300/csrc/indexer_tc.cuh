@@ -13,7 +13,8 @@
 //             N = QPT queries x H_I heads (B = query tile, K-major, loaded once per group),
 //             K = d_I.
 // Persistent, warp-specialised, one CTA per SM:
-//   warp 0     TMA producer: query tile per (sequence, query group), key tiles into a ring
+//   warp 0     TMA producer: query tile per (sequence, query group) (two buffers when the key
+//              ring keeps 6 stages beside them), key tiles into a ring
 //   warp 1     TMEM allocator and MMA issuer (one thread), 2-4 accumulator buffers
 //   warps 2..  epilogue: TMEM -> registers, weighted ReLU sum per query, fp32 score store
 // Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds.
@@ -55,10 +56,14 @@ struct IndexerTcConfig {
     static constexpr int TMEM_COLS = ACC_BUFS * N <= 32 ? 32 : ACC_BUFS * N <= 64 ? 64 : ACC_BUFS * N <= 128 ? 128
                                    : ACC_BUFS * N <= 256 ? 256 : 512;
     static constexpr int SMEM_LIMIT = 227 * 1024;
-    static constexpr int FIXED = Q_BYTES + 1024;             // query tile + barriers
+    // two query tiles where the key ring still keeps 6 stages (decode: the next sequence's query
+    // loads while the MMAs finish the current one, so the ring does not drain at the switch)
+    static constexpr int STAGES_2Q = (SMEM_LIMIT - 2 * Q_BYTES - 2048) / TILE_BYTES;
+    static constexpr int QBUF = STAGES_2Q >= 6 ? 2 : 1;
+    static constexpr int FIXED = QBUF * Q_BYTES + 1024;      // query tiles + barriers
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED - 1024) / TILE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr int SMEM_BYTES = 1024 + Q_BYTES + STAGES * TILE_BYTES + 1024;
+    static constexpr int SMEM_BYTES = 1024 + QBUF * Q_BYTES + STAGES * TILE_BYTES + 1024;
     static_assert(N >= 16 && N <= 256 && N % 16 == 0, "MMA N");
     static_assert(COLS_PER_WG % HI == 0, "a warp group owns whole queries");
     static_assert(STAGES >= 2, "ring");
@@ -75,15 +80,15 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_tile = base;
-    uint8_t *k_ring = base + Cfg::Q_BYTES;
+    uint8_t *k_ring = base + Cfg::QBUF * Cfg::Q_BYTES;
     uint8_t *misc = k_ring + STAGES * Cfg::TILE_BYTES;
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;
     uint64_t *acc_empty = acc_full + Cfg::ACC_BUFS;
     uint64_t *q_full = acc_empty + Cfg::ACC_BUFS;
-    uint64_t *q_empty = q_full + 1;
-    uint64_t *teardown = q_empty + 1;
+    uint64_t *q_empty = q_full + Cfg::QBUF;
+    uint64_t *teardown = q_empty + Cfg::QBUF;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(teardown + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -101,8 +106,10 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             ptx::mbar_init(&acc_full[s], 1);
             ptx::mbar_init(&acc_empty[s], Cfg::EPI_WARPS);
         }
-        ptx::mbar_init(q_full, 1);
-        ptx::mbar_init(q_empty, 1);
+        for (int s = 0; s < Cfg::QBUF; ++s) {
+            ptx::mbar_init(&q_full[s], 1);
+            ptx::mbar_init(&q_empty[s], 1);
+        }
         ptx::mbar_init(teardown, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -143,16 +150,18 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                 const int64_t bg = it / a.tiles;
                 const int b = (int)(bg / a.groups), g = (int)(bg % a.groups);
                 if (bg != cur) {
-                    if (groups_loaded > 0 && !ptx::mbar_wait(q_empty, (groups_loaded - 1) & 1)) {
+                    const int qb = (int)(groups_loaded % Cfg::QBUF);
+                    if (groups_loaded >= (uint32_t)Cfg::QBUF &&
+                        !ptx::mbar_wait(&q_empty[qb], ((groups_loaded / Cfg::QBUF) - 1) & 1)) {
                         *abort_flag = 1;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(q_full, Cfg::Q_BYTES);
+                    ptx::mbar_arrive_expect_tx(&q_full[qb], Cfg::Q_BYTES);
                     const int qrow = (int)(((int64_t)b * a.n_q + (int64_t)g * QPT) * HI);
 #pragma unroll
                     for (int bx = 0; bx < Cfg::NBOX; ++bx)
-                        ptx::tma_load_2d(ptx::smem_u32(q_tile + bx * N * Cfg::ROWB), &qmap, bx * Cfg::BOX, qrow,
-                                         q_full);
+                        ptx::tma_load_2d(ptx::smem_u32(q_tile + qb * Cfg::Q_BYTES + bx * N * Cfg::ROWB), &qmap,
+                                         bx * Cfg::BOX, qrow, &q_full[qb]);
                     ++groups_loaded;
                     cur = bg;
                     vis = group_visible(b, g);
@@ -181,16 +190,19 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             uint32_t use = 0, groups_seen = 0, acc_use[Cfg::ACC_BUFS] = {};
             int acc = 0;
             bool issued = false;
-            const uint32_t q_addr = ptx::smem_u32(q_tile);
+            uint32_t q_addr = ptx::smem_u32(q_tile);
             for (int64_t it = it0; it < it1 && !*abort_flag; ++it) {
                 const int t = (int)(it % a.tiles);
                 const int64_t bg = it / a.tiles;
                 if (bg != cur) {
-                    if (groups_seen > 0) ptx::mma_commit(q_empty);   // previous query tile free once MMAs finish
-                    if (!ptx::mbar_wait(q_full, groups_seen & 1)) {
+                    // the previous query tile is free once the MMAs issued so far finish
+                    if (groups_seen > 0) ptx::mma_commit(&q_empty[(groups_seen - 1) % Cfg::QBUF]);
+                    const int qb = (int)(groups_seen % Cfg::QBUF);
+                    if (!ptx::mbar_wait(&q_full[qb], (groups_seen / Cfg::QBUF) & 1)) {
                         *abort_flag = 1;
                         break;
                     }
+                    q_addr = ptx::smem_u32(q_tile + qb * Cfg::Q_BYTES);
                     ++groups_seen;
                     cur = bg;
                     vis = group_visible((int)(bg / a.groups), (int)(bg % a.groups));
