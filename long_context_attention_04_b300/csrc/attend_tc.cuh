@@ -245,6 +245,9 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         bool ok = true;
         for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
             const int t = (int)t0 + u;
+            // the tile's gathered rows, once for its c chunks (the index loads overlap the waits)
+            int rc[4] = {-1, -1, -1, -1};
+            if (t >= tm.tc || L.idx) gather_rows(t, 0, rc);
             for (int j = 0; j < CC && ok; ++j) {
                 // KV chunk j of tile t
                 if (u > 0 && !ptx::mbar_wait(&empty[j], (u - 1) & 1)) {
@@ -265,8 +268,6 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                     // warp, released through gather_go[j], issues box 1 (one warp's TMA gathers run
                     // at about half the rate of two)
                     if (lane == 0) ptx::mbar_arrive(&gather_go[j]);
-                    int rc[4];
-                    gather_rows(t, j, rc);
                     const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
                     ptx::tma_gather4(dst + lane * 512, map, j * 128, rc[0], rc[1], rc[2], rc[3], &full[j]);
                 }
@@ -347,14 +348,14 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
             const int t = (int)t0 + u;
             if (t < tm.tc && !L.idx) continue;   // contiguous tile: the producer loads it alone
+            int rc[4];
+            gather_rows(t, 1, rc);
             for (int j = 0; j < CC; ++j) {
                 if (!ptx::mbar_wait(&gather_go[j], go_count[j] & 1)) {
                     ok = false;
                     break;
                 }
                 ++go_count[j];
-                int rc[4];
-                gather_rows(t, j, rc);
                 const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
                 ptx::tma_gather4(ptx::smem_u32(ring + j * kAtChunkBytes) + 128 * 128 + lane * 512, map,
                                  j * 128 + 64, rc[0], rc[1], rc[2], rc[3], &full[j]);
