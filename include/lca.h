@@ -177,6 +177,10 @@ lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q,
  * q [batch][n_q][H][c] bf16; gamma_q [c] fp32; sink [H] fp32; out [batch][n_q][H][c] bf16.
  * Rows in the caches already carry RMSNorm and RoPE at their own positions.
  * Supported: c in {128, 256, 512}, H <= 64, W <= 4096.
+ * Arithmetic: both products on the tensor cores in fp16 with fp32 accumulation (the rows are
+ * re-encoded from bf16, exactly for magnitudes in [2^-14, 65504]; larger ones saturate; the
+ * query carries about 22 bits as two fp16 parts), softmax in fp32.  Against an fp64
+ * evaluation of the formulas above, max |error| <= 2e-2 x RMS of the output in the tests.
  * The workspace holds split-K partial results; its size comes from *_attend_workspace.
  * ------------------------------------------------------------------------------- */
 size_t csa_attend_workspace(const lca_attn_params *p, int batch, int n_q);

@@ -23,7 +23,9 @@ __device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_err
 // and pdl_wait() before its first access to global memory, on every path: pdl_wait returns
 // once the previous kernel in the stream has completed and its writes are visible, and
 // because every kernel waits before it can complete, completion stays ordered along the
-// whole stream.
+// whole stream.  One documented exception: the grouped output projection starts reading its
+// weight matrices before pdl_wait (lca_grouped_oproj: weights must not be written by work
+// still pending on the stream); everything it reads or writes besides them waits.
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 

@@ -24,7 +24,9 @@
 // kTopkSmemKeys entries are read from global memory once and kept as keys in shared memory;
 // longer slices (prefill, one CTA per row) are read twice, with 16-byte loads.  If a warp's
 // share of the list overflows (heavy ties), the CTA runs the remaining passes over all of
-// its keys instead.
+// its keys instead.  When the whole row's lists fit in the first CTA's key area, the other
+// CTAs copy theirs there (distributed shared-memory stores, index order kept) and leave, and
+// the first CTA runs the remaining passes and the write alone, with no cluster barriers.
 #pragma once
 
 #include "common.cuh"
