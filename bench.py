@@ -8,6 +8,7 @@ attention with split-K combine.  Workloads (sizes of the pages' V4-Flash configu
   csa_decode_128k (default)  batch 32, 128K context, one query per sequence
   hca_decode_1m              batch 16, 1M context, one query per sequence
   csa_prefill_1m             one 8192-query chunk at 1M context
+  csa_prefill_128k           one 2048-query chunk at 128K context (the same kernels, profiler-sized)
 Inputs are seeded synthetic tensors (workloads.py); the caches are larger than L2 and L2 is
 also flushed between timed steps.  Under torchrun each rank runs the workload on its own
 GPU (sequences shard with no exchange: weak scaling); the value is all ranks' tokens over
@@ -636,7 +637,7 @@ class BlockDecode(Workload):
 
 
 WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill,
-             "block_decode_1m": BlockDecode}
+             "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode}
 
 
 # ------------------------------------------------------------------- distributed -----

@@ -70,6 +70,30 @@ struct IndexerTcConfig {
     static_assert(ACC_BUFS * N <= 512, "TMEM");
 };
 
+// Position of a work item (sequence b, query group g, tile t) while a CTA walks its contiguous
+// range, advanced by increments (no 64-bit division per tile in the loops).
+struct ItemCursor {
+    int t, g, b;
+    int64_t bg;                  // b * groups + g
+    int tiles, groups;
+    __device__ __forceinline__ ItemCursor(int64_t it, int tiles_, int groups_) : tiles(tiles_), groups(groups_) {
+        t = (int)(it % tiles);
+        bg = it / tiles;
+        b = (int)(bg / groups);
+        g = (int)(bg % groups);
+    }
+    __device__ __forceinline__ void next() {
+        if (++t == tiles) {
+            t = 0;
+            ++bg;
+            if (++g == groups) {
+                g = 0;
+                ++b;
+            }
+        }
+    }
+};
+
 template <int DI, int HI, int QPT>
 __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
@@ -145,10 +169,11 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             int64_t cur = -1;
             int64_t vis = 0;
             uint32_t fill = 0, groups_loaded = 0;
-            for (int64_t it = it0; it < it1 && !*abort_flag; ++it) {
-                const int t = (int)(it % a.tiles);
-                const int64_t bg = it / a.tiles;
-                const int b = (int)(bg / a.groups), g = (int)(bg % a.groups);
+            ItemCursor ic(it0, a.tiles, a.groups);
+            for (int64_t it = it0; it < it1 && !*abort_flag; ++it, ic.next()) {
+                const int t = ic.t;
+                const int64_t bg = ic.bg;
+                const int b = ic.b, g = ic.g;
                 if (bg != cur) {
                     const int qb = (int)(groups_loaded % Cfg::QBUF);
                     if (groups_loaded >= (uint32_t)Cfg::QBUF &&
@@ -191,9 +216,10 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             int acc = 0;
             bool issued = false;
             uint32_t q_addr = ptx::smem_u32(q_tile);
-            for (int64_t it = it0; it < it1 && !*abort_flag; ++it) {
-                const int t = (int)(it % a.tiles);
-                const int64_t bg = it / a.tiles;
+            ItemCursor ic(it0, a.tiles, a.groups);
+            for (int64_t it = it0; it < it1 && !*abort_flag; ++it, ic.next()) {
+                const int t = ic.t;
+                const int64_t bg = ic.bg;
                 if (bg != cur) {
                     // the previous query tile is free once the MMAs issued so far finish
                     if (groups_seen > 0) ptx::mma_commit(&q_empty[(groups_seen - 1) % Cfg::QBUF]);
@@ -205,7 +231,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                     q_addr = ptx::smem_u32(q_tile + qb * Cfg::Q_BYTES);
                     ++groups_seen;
                     cur = bg;
-                    vis = group_visible((int)(bg / a.groups), (int)(bg % a.groups));
+                    vis = group_visible(ic.b, ic.g);
                 }
                 if ((int64_t)t * 128 >= vis) continue;
                 if (acc_use[acc] > 0 && !ptx::mbar_wait(&acc_empty[acc], (acc_use[acc] - 1) & 1)) {
@@ -255,10 +281,11 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
         float wr[Cfg::COLS_PER_WG];                      // head weights of this group's queries
         uint32_t acc_use[Cfg::ACC_BUFS] = {};
         int acc = 0;
-        for (int64_t it = it0; it < it1 && !*abort_flag; ++it) {
-            const int t = (int)(it % a.tiles);
-            const int64_t bg = it / a.tiles;
-            const int b = (int)(bg / a.groups), g = (int)(bg % a.groups);
+        ItemCursor ic(it0, a.tiles, a.groups);
+        for (int64_t it = it0; it < it1 && !*abort_flag; ++it, ic.next()) {
+            const int t = ic.t;
+            const int64_t bg = ic.bg;
+            const int b = ic.b, g = ic.g;
             if (bg != cur) {
                 cur = bg;
                 vis = group_visible(b, g);

@@ -76,7 +76,7 @@ class LayerShape:
         return 1.0 / math.sqrt(self.head_dim)
 
 
-# The five workloads.  Names say what each is and at which sizes.
+# The workloads.  Names say what each is and at which sizes.
 TINY_CSA_PREFILL = dict(
     name="tiny CSA prefill, 2048 tokens, hidden 256, H=8 c=128, H_I=4 d_I=32, k=64, W=16",
     kind="csa_prefill", B=1, n_tok=2048, hidden=256,
@@ -98,6 +98,13 @@ CSA_PREFILL_1M = dict(
     kind="csa_prefill_chunk", B=1, q_begin=1040384, Tq=8192, entries=262144,
     shape=LayerShape(ratio=4, topk=1024))
 
+# The same chunked prefill at 128K context: the 1M chunk's kernels at a size (0.4 GB on the
+# device) that a profiler can replay many times.
+CSA_PREFILL_128K = dict(
+    name="CSA chunked prefill, 2048 queries at 128K context (32768 entries), k=1024, W=128, H=64",
+    kind="csa_prefill_chunk", B=1, q_begin=129024, Tq=2048, entries=32768,
+    shape=LayerShape(ratio=4, topk=1024))
+
 BLOCK_DECODE_1M = dict(
     name="V4-Flash-style block decode, batch 4, 1M context, 8 CSA (k=512) + 8 HCA layers, "
          "grouped O-proj 64 heads -> 8 x 1024 -> 4096",
@@ -110,6 +117,7 @@ WORKLOADS = {
     "csa_decode_128k": CSA_DECODE_128K,
     "hca_decode_1m": HCA_DECODE_1M,
     "csa_prefill_1m": CSA_PREFILL_1M,
+    "csa_prefill_128k": CSA_PREFILL_128K,
     "block_decode_1m": BLOCK_DECODE_1M,
 }
 
