@@ -140,6 +140,32 @@ def test_indexer_scores_and_topk_match_oracle(HI, DI, rows, k):
     assert torch.equal(out2, out_idx)
 
 
+@pytest.mark.parametrize("B,rows", [(600, 100), (300, 200), (150, 300)])
+def test_indexer_many_short_sequences(B, rows):
+    """Decode-shaped calls (one query per sequence) with sequences of 1-3 tiles: every CTA walks
+    several sequences, so each query-tile buffer is refilled (after the MMAs release it)."""
+    rng = Rng(21)
+    m, k = 4, 64
+    p = AttnParams(idx_heads=64, idx_dim=128, ratio=m, topk=k)
+    q = rng.normal_bf16((B, 1, 64, 128))
+    w = rng.normal_f32((B, 1, 64), 0.125)
+    keys = rng.normal_bf16((B, rows, 128))
+    pos = torch.tensor([[m * (rows - (b % 7)) - 1] for b in range(B)], dtype=torch.int32)
+    stride = (rows + 3) // 4 * 4
+    scores = torch.full((B, 1, stride), 7.0, device=DEV)
+    api.csa_indexer_scores(p, dev(q), dev(w), dev(keys), dev(pos), scores)
+    assert api.lca_device_error() == 0
+    s_gpu = scores.cpu().numpy()
+    qb, wf, kb = u16(q), f32(w), u16(keys)
+    for b in range(B):
+        n_vis = oracle.visible_entries(int(pos[b, 0]), m)
+        ref = oracle.indexer_scores(qb[b, 0], wf[b, 0], kb[b], n_vis)
+        got = s_gpu[b, 0, :n_vis].astype(np.float64)
+        np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-5 * max(np.abs(ref).max(), 1e-30),
+                                   err_msg="sequence %d" % b)
+        assert np.isneginf(s_gpu[b, 0, n_vis:rows]).all()
+
+
 @pytest.mark.parametrize("n,k", [(5000, 300), (262144, 1024), (1023, 1024), (32768, 512), (100003, 64)])
 def test_topk_exact_on_given_scores_with_ties(n, k):
     """Scores given (not computed): the GPU selection must equal the oracle's exactly, ties included."""
