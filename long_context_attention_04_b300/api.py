@@ -193,7 +193,10 @@ def _attend_common(q, p):
 
 def csa_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse=None,
                stream=None, entry="csa_attend"):
-    """Core attention over kv_cache[idx] plus the window rows (see include/lca.h)."""
+    """Core attention over kv_cache[idx] plus the window rows (see include/lca.h).  `entry`
+    selects the whole call or one of its halves (csa_attend_prepare / csa_attend_prepared)."""
+    if entry not in ("csa_attend", "csa_attend_prepare", "csa_attend_prepared"):
+        raise ValueError("unknown attention entry %r" % (entry,))
     B, n_q = _attend_common(q, p)
     if tuple(idx.shape) != (B, n_q, p.topk):
         raise ValueError("idx must be [B, n_q, topk]")
@@ -209,7 +212,10 @@ def csa_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, ou
 
 def hca_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None, stream=None,
                entry="hca_attend"):
-    """Dense core attention over the visible entries of kv_cache plus the window rows."""
+    """Dense core attention over the visible entries of kv_cache plus the window rows.  `entry`
+    selects the whole call or one of its halves (hca_attend_prepare / hca_attend_prepared)."""
+    if entry not in ("hca_attend", "hca_attend_prepare", "hca_attend_prepared"):
+        raise ValueError("unknown attention entry %r" % (entry,))
     B, n_q = _attend_common(q, p)
     st = getattr(_lib.load(), entry)(
         ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
@@ -234,11 +240,13 @@ def csa_attend_prepared(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv,
 
 def hca_attend_prepare(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None,
                        stream=None):
+    """The query preparation of hca_attend alone, into the workspace (see include/lca.h)."""
     hca_attend(p, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse, stream, "hca_attend_prepare")
 
 
 def hca_attend_prepared(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse=None,
                         stream=None):
+    """The attention of hca_attend alone, on query images an hca_attend_prepare left in the workspace."""
     hca_attend(p, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, workspace, lse, stream, "hca_attend_prepared")
 
 

@@ -44,12 +44,12 @@ FAKE = ctypes.c_void_p(0x10000)        # aligned, never dereferenced: validation
 FAKE_ODD = ctypes.c_void_p(0x10002)
 
 
-def _attend(lib, p, **over):
+def _attend(lib, p, entry="csa_attend", **over):
     args = dict(p=ctypes.byref(p), batch=1, n_q=1, q=FAKE, gamma=FAKE, pos=FAKE, kv=FAKE, kv_bs=0,
                 rows=1000, idx=FAKE, win=FAKE, win_bs=0, win_cap=128, sink=FAKE, out=FAKE, lse=None,
                 ws=FAKE, ws_bytes=0, stream=None)
     args.update(over)
-    return lib.csa_attend(*args.values())
+    return getattr(lib, entry)(*args.values())
 
 
 def test_attend_rejects_bad_arguments(lib):
@@ -63,6 +63,15 @@ def test_attend_rejects_bad_arguments(lib):
     assert _attend(lib, _params(), ws_bytes=16) == 3                  # workspace too small
     assert b"workspace" in lib.lca_last_error()
     assert _attend(lib, _params(), idx=None) == 1
+
+
+@pytest.mark.parametrize("entry", ["csa_attend_prepare", "csa_attend_prepared"])
+def test_attention_halves_validate_like_the_whole_call(lib, entry):
+    assert _attend(lib, _params(), entry, q=None) == 1
+    assert _attend(lib, _params(head_dim=192), entry) == 2
+    assert _attend(lib, _params(), entry, ws_bytes=16) == 3
+    assert _attend(lib, _params(), entry, idx=None) == 1
+    assert entry.encode() in lib.lca_last_error()
 
 
 def test_workspace_sizes_are_positive_and_monotone(lib):
