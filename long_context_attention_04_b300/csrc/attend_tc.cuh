@@ -48,8 +48,7 @@
 //               in base 2 with a conditional rescale (the running max moves only when a
 //               logit exceeds it by more than 2^8), P^T rows to shared memory
 // The split's unnormalised O, running max and row sum go to the workspace; combine_kernel
-// merges the splits with the sink and applies the output RoPE(-pos).  With one split per
-// query (prefill) the kernel finishes the output itself and no combine runs.
+// merges the splits with the sink and applies the output RoPE(-pos).
 // Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds.
 #pragma once
 
@@ -195,12 +194,6 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         for (int h = threadIdx.x; h < a.H; h += blockDim.x) {
             a.part_m[pidx0 + h] = -INFINITY;
             a.part_l[pidx0 + h] = 0.f;
-        }
-        if (a.splits == 1) {   // no combine follows: the output is the sink's alone (zero)
-            for (int64_t i = threadIdx.x; i < (int64_t)a.H * C; i += blockDim.x)
-                a.out[(int64_t)unit * a.H * C + i] = __float2bfloat16_rn(0.f);
-            if (a.lse)
-                for (int h = threadIdx.x; h < a.H; h += blockDim.x) a.lse[(int64_t)unit * a.H + h] = a.sink[h];
         }
         ptx::tc_fence_before();
         __syncthreads();
@@ -532,74 +525,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(red_bar);
-            if (a.splits == 1 && ptx::mbar_wait(red_bar, reds_done & 1)) {
-                ++reds_done;
-                // One split: this CTA holds the whole row set, so it finishes the output itself
-                // (what combine_kernel does for several splits): weights against the sink,
-                // 1/L, RoPE(-pos) on the trailing R dims (pairs d, d + R/2 sit in other warps:
-                // those columns go through shared memory), bf16 store, lse.
-                const int64_t unit64 = unit;
-                const int64_t pos = L.pos < 0 ? 0 : L.pos;
-                float scale[32];
-                float lse_lane = 0.f;
-#pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    const int hh = half * 32 + h;
-                    float s = 0.f;
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) s += lsum[(half * 4 + w) * 32 + h];
-                    const float sink2 = hh < a.H ? a.sink[hh] * kLog2e : 0.f;
-                    const float M = fmaxf(m[h], sink2);
-                    const float wm = m[h] == -INFINITY ? 0.f : exp2f(m[h] - M);
-                    const float Lt = wm * s + exp2f(sink2 - M);
-                    scale[h] = wm / Lt;
-                    if (lane == h) lse_lane = (M + log2f(Lt)) * kLn2;
-                }
-                if (quarter == 0 && a.lse && half * 32 + lane < a.H) a.lse[unit64 * a.H + half * 32 + lane] = lse_lane;
-                const int first = C - a.R;                    // first rotated column
-                // [R][65]: column d of the rotated block, heads 0-63 plus one pad word so that
-                // neither the writes (lanes vary d) nor the reads conflict on banks.  Up to
-                // 128 x 65 x 4 B: the KV ring and the query slots behind it are free now.
-                constexpr int RS = kAtHP + 1;
-                static_assert(2 * kMaxRopePairs * RS * 4 <= CC * kAtChunkBytes + kAtQSlots * kAtQChunkBytes,
-                              "rotation staging");
-                float *rot = reinterpret_cast<float *>(ring);
-                for (int j = 0; j < CC; ++j) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(lane_addr + Cfg::TMEM_O + j * kAtHP + half * 32, v);
-                    ptx::tmem_ld_wait();
-                    const int c = j * 128 + r;
-#pragma unroll
-                    for (int h = 0; h < 32; ++h) {
-                        const int hh = half * 32 + h;
-                        const float o = __uint_as_float(v[h]) * scale[h];
-                        if (c >= first) rot[(c - first) * RS + hh] = o;
-                        else if (hh < a.H) a.out[(unit64 * a.H + hh) * C + c] = __float2bfloat16_rn(o);
-                    }
-                }
-                if (a.R > 0) {
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(red_bar);
-                    if (ptx::mbar_wait(red_bar, reds_done & 1)) {
-                        ++reds_done;
-                        const int hr = a.R / 2;
-                        for (int j = 0; j < CC; ++j) {
-                            const int c = j * 128 + r;
-                            if (c < first) continue;
-                            const int d = c - first, dd = d < hr ? d : d - hr;
-                            float cs, sn;
-                            rope_cs(a.rope, dd, -pos, cs, sn);
-#pragma unroll
-                            for (int h = 0; h < 32; ++h) {
-                                const int hh = half * 32 + h;
-                                const float x = rot[dd * RS + hh], y = rot[(dd + hr) * RS + hh];
-                                const float o = d < hr ? x * cs - y * sn : x * sn + y * cs;
-                                if (hh < a.H) a.out[(unit64 * a.H + hh) * C + c] = __float2bfloat16_rn(o);
-                            }
-                        }
-                    }
-                }
-            } else if (a.splits > 1 && ptx::mbar_wait(red_bar, reds_done & 1)) {
+            if (ptx::mbar_wait(red_bar, reds_done & 1)) {
                 if (quarter == 0) {   // one warp per head half writes m and l
                     const int h = half * 32 + lane;
                     float s = 0.f;

@@ -347,7 +347,6 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     }
     st = check_launch(name);
     if (st != LCA_OK) return st;
-    if (pl.splits == 1) return ok();   // the attention kernel wrote the output itself
     launch_pdl(combine_kernel, dim3((unsigned)pl.units, p->heads), dim3(kCombineThreads), 0, stream, a);
     st = check_launch(name);
     return st == LCA_OK ? ok() : st;
