@@ -866,7 +866,7 @@ class _HostOnly:
         self.s = s
         rng = wl.Rng(seed)
         self.kind = name
-        if name == "csa_decode_128k" or name == "csa_prefill_1m":
+        if name.startswith("csa_"):      # a CSA layer: compression, indexer, top-k, attention
             entries = cfg["entries"]
             pos = cfg.get("pos", cfg.get("q_begin", 0) + cfg.get("Tq", 1) - 1)
             self.pos = pos
