@@ -62,3 +62,45 @@ def test_reference_arm_under_two_ranks_prints_once():
     lines = _json_lines(p.stdout)
     assert len(lines) == 1
     assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_clock_summary_median_and_reason_bits():
+    c = bench.ClockSampler(0)
+    c.max_mhz = 2032.0
+    c.samples = [(1900.0, 0x4), (2000.0, 0), (1800.0, 0x8 | 0x4), (2032.0, 0x40)]
+    s = c.summary()
+    assert s["sm_mhz"] == 1950.0 and s["sm_max_mhz"] == 2032.0 and s["samples"] == 4
+    assert s["reasons"] == ["hw_slowdown", "hw_thermal_slowdown", "sw_power_cap"]
+
+
+def test_clock_summary_without_samples_says_why():
+    c = bench.ClockSampler(0)
+    c.error = "RuntimeError: NVML error 9"
+    s = c.summary()
+    assert s["samples"] == 0 and s["sm_mhz"] is None and s["error"] == c.error
+
+
+def _traffic_rows():
+    path = os.path.join(ROOT, "profiles", "dram_traffic.md")
+    rows = []
+    for line in open(path).read().splitlines():
+        cols = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cols) == 7 and cols[0] in bench.WORKLOADS:
+            rows.append(cols)
+    return rows
+
+
+def test_traffic_table_rows_add_up():
+    rows = _traffic_rows()
+    assert rows
+    for cols in rows:
+        assert int(cols[4]) == int(cols[2]) + int(cols[3]), cols[0]
+
+
+def test_traffic_counts_only_for_the_sources_it_was_taken_with(monkeypatch):
+    rows = _traffic_rows()
+    monkeypatch.setattr(bench, "source_hash", lambda: "0" * 16)
+    assert all(bench.measured_traffic(w) is None for w in bench.WORKLOADS)
+    name, h, traffic = rows[0][0], rows[0][6], int(rows[0][4])
+    monkeypatch.setattr(bench, "source_hash", lambda: h)
+    assert bench.measured_traffic(name) == traffic
