@@ -77,6 +77,16 @@ def _rows(t: torch.Tensor, name: str) -> int:
     return t.stride(0)
 
 
+def _holds(t, n: int, name: str, exact: bool = False):
+    """A dense tensor with at least (or exactly) n elements: the library indexes it as a flat
+    array of that length, and cannot see torch's strides or sizes."""
+    if t is None:
+        return
+    if not t.is_contiguous() or (t.numel() != n if exact else t.numel() < n):
+        raise ValueError("%s must be a contiguous tensor of %s%d elements, got shape %s"
+                         % (name, "" if exact else "at least ", n, tuple(t.shape)))
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -89,12 +99,16 @@ def _i32(t, name):
     return _ptr(t, torch.int32, name)
 
 
-def _compress(fn, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache, stream):
+def _compress(fn, span, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache, stream):
     B, n_tok, width = tok_v.shape
     if tok_z.dim() != 2 or tok_z.stride(1) != 1 or tok_z.shape[0] != B:
         raise ValueError("tok_z must be [B, n_tok] with unit inner stride")
     if cache.shape[0] != B or cache.shape[2] != width:
         raise ValueError("cache must be [B, rows, width]")
+    _holds(tok_pos0, B, "tok_pos0")
+    _holds(first_entry, B, "first_entry")
+    _holds(pos_bias, span, "pos_bias")
+    _holds(gamma, width, "gamma")
     st = fn(ctypes.byref(p.c()), B, width,
             _ptr(tok_v, torch.bfloat16, "tok_v"), _rows(tok_v, "tok_v"), n_tok,
             _ptr(tok_z, torch.float32, "tok_z"), tok_z.stride(0), _i32(tok_pos0, "tok_pos0"),
@@ -107,20 +121,22 @@ def _compress(fn, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_
 def csa_compress_kv(p: AttnParams, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new,
                     cache, stream=None):
     """CSA compression (windows of 2m, stride m) of entries first_entry[b] .. +n_new into cache."""
-    _compress(_lib.load().csa_compress_kv, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope,
+    _compress(_lib.load().csa_compress_kv, 2 * p.ratio, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope,
               first_entry, n_new, cache, stream)
 
 
 def hca_compress_kv(p: AttnParams, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new,
                     cache, stream=None):
     """HCA compression (non-overlapping windows of m') of entries first_entry[b] .. +n_new into cache."""
-    _compress(_lib.load().hca_compress_kv, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope,
+    _compress(_lib.load().hca_compress_kv, p.ratio, p, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope,
               first_entry, n_new, cache, stream)
 
 
 def lca_window_update(p: AttnParams, tok_v, tok_pos0, gamma, win_kv, stream=None):
     """Write RoPE(RMSNorm(v)*gamma, pos) of each token to ring row pos mod win_cap."""
     B, n_tok, _ = tok_v.shape
+    _holds(tok_pos0, B, "tok_pos0")
+    _holds(gamma, p.head_dim, "gamma")
     st = _lib.load().lca_window_update(
         ctypes.byref(p.c()), B, _ptr(tok_v, torch.bfloat16, "tok_v"), _rows(tok_v, "tok_v"), n_tok,
         _i32(tok_pos0, "tok_pos0"), _ptr(gamma, torch.float32, "gamma"),
@@ -145,6 +161,7 @@ def csa_indexer_scores(p: AttnParams, q_idx, w_idx, k_cache, q_pos, scores, stre
     if scores.dim() != 3 or scores.stride(2) != 1 or scores.stride(1) != scores.shape[2] or \
             scores.stride(0) != n_q * scores.shape[2]:
         raise ValueError("scores must be a dense [B, n_q, stride] tensor")
+    _holds(q_pos, B * n_q, "q_pos", exact=True)
     st = _lib.load().csa_indexer_scores(
         ctypes.byref(p.c()), B, n_q, _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w_idx, torch.float32, "w_idx"),
         _ptr(k_cache, torch.bfloat16, "k_cache"), _rows(k_cache, "k_cache"), k_cache.shape[1],
@@ -157,6 +174,8 @@ def lca_topk(p: AttnParams, scores, q_pos, max_entries, out_idx, stream=None):
     B, n_q, stride = scores.shape
     if tuple(out_idx.shape) != (B, n_q, p.topk):
         raise ValueError("out_idx must be [B, n_q, topk]")
+    _holds(scores, B * n_q * stride, "scores", exact=True)
+    _holds(q_pos, B * n_q, "q_pos", exact=True)
     st = _lib.load().lca_topk(ctypes.byref(p.c()), B, n_q, _ptr(scores, torch.float32, "scores"), stride,
                               _i32(q_pos, "q_pos"), int(max_entries), _i32(out_idx, "out_idx"), _stream(stream))
     _check(st)
@@ -169,6 +188,9 @@ def csa_indexer_workspace(p: AttnParams, batch: int, n_q: int, cache_rows: int) 
 def csa_indexer_topk(p: AttnParams, q_idx, w_idx, k_cache, q_pos, out_idx, workspace, stream=None):
     """Indexer scores into the workspace, then top-k into out_idx [B, n_q, k]."""
     B, n_q = _idx_q(q_idx, w_idx, p)
+    if tuple(out_idx.shape) != (B, n_q, p.topk):
+        raise ValueError("out_idx must be [B, n_q, topk]")
+    _holds(q_pos, B * n_q, "q_pos", exact=True)
     st = _lib.load().csa_indexer_topk(
         ctypes.byref(p.c()), B, n_q, _ptr(q_idx, torch.bfloat16, "q_idx"), _ptr(w_idx, torch.float32, "w_idx"),
         _ptr(k_cache, torch.bfloat16, "k_cache"), _rows(k_cache, "k_cache"), k_cache.shape[1],
@@ -185,10 +207,16 @@ def hca_attend_workspace(p: AttnParams, batch: int, n_q: int, cache_rows: int) -
     return int(_lib.load().hca_attend_workspace(ctypes.byref(p.c()), batch, n_q, cache_rows))
 
 
-def _attend_common(q, p):
+def _attend_common(q, p, gamma_q, q_pos, sink, out, lse):
     if q.dim() != 4 or not q.is_contiguous() or tuple(q.shape[2:]) != (p.heads, p.head_dim):
         raise ValueError("q must be a contiguous [B, n_q, H, c] tensor matching params")
-    return q.shape[0], q.shape[1]
+    B, n_q = q.shape[0], q.shape[1]
+    _holds(out, q.numel(), "out", exact=True)
+    _holds(lse, B * n_q * p.heads, "lse", exact=True)
+    _holds(q_pos, B * n_q, "q_pos", exact=True)
+    _holds(gamma_q, p.head_dim, "gamma_q")
+    _holds(sink, p.heads, "sink")
+    return B, n_q
 
 
 def csa_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse=None,
@@ -197,7 +225,7 @@ def csa_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, ou
     selects the whole call or one of its halves (csa_attend_prepare / csa_attend_prepared)."""
     if entry not in ("csa_attend", "csa_attend_prepare", "csa_attend_prepared"):
         raise ValueError("unknown attention entry %r" % (entry,))
-    B, n_q = _attend_common(q, p)
+    B, n_q = _attend_common(q, p, gamma_q, q_pos, sink, out, lse)
     if tuple(idx.shape) != (B, n_q, p.topk):
         raise ValueError("idx must be [B, n_q, topk]")
     st = getattr(_lib.load(), entry)(
@@ -216,7 +244,7 @@ def hca_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, wo
     selects the whole call or one of its halves (hca_attend_prepare / hca_attend_prepared)."""
     if entry not in ("hca_attend", "hca_attend_prepare", "hca_attend_prepared"):
         raise ValueError("unknown attention entry %r" % (entry,))
-    B, n_q = _attend_common(q, p)
+    B, n_q = _attend_common(q, p, gamma_q, q_pos, sink, out, lse)
     st = getattr(_lib.load(), entry)(
         ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
         _i32(q_pos, "q_pos"), _ptr(kv_cache, torch.bfloat16, "kv_cache"), _rows(kv_cache, "kv_cache"),
@@ -252,7 +280,7 @@ def hca_attend_prepared(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink
 
 def hca_attend_noalloc(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, lse=None, stream=None):
     """hca_attend with its scratch in the library's static device array (no workspace)."""
-    B, n_q = _attend_common(q, p)
+    B, n_q = _attend_common(q, p, gamma_q, q_pos, sink, out, lse)
     st = _lib.load().hca_attend_noalloc(
         ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
         _i32(q_pos, "q_pos"), _ptr(kv_cache, torch.bfloat16, "kv_cache"), _rows(kv_cache, "kv_cache"),
@@ -265,11 +293,17 @@ def hca_attend_noalloc(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink,
 def lca_grouped_oproj(o, Wg, Wm, groups: int, mid, y, stream=None):
     """y = Wm . concat_g(Wg[g] . o_g) for o [B, H, c]; mid [B, groups*d_g] is scratch."""
     B, H, c = o.shape
+    if groups < 1 or H % groups or Wg.shape[0] % groups:
+        raise ValueError("groups must divide the heads and the rows of Wg")
     d_g = Wg.shape[0] // groups
     d_model = Wm.shape[0]
     for t, n in ((o, "o"), (Wg, "Wg"), (Wm, "Wm"), (mid, "mid"), (y, "y")):
         if not t.is_contiguous():
             raise ValueError("%s must be contiguous" % n)
+    _holds(Wg, groups * d_g * (H // groups) * c, "Wg", exact=True)
+    _holds(Wm, d_model * groups * d_g, "Wm", exact=True)
+    _holds(mid, B * groups * d_g, "mid")
+    _holds(y, B * d_model, "y")
     st = _lib.load().lca_grouped_oproj(B, H, c, groups, d_g, d_model, _ptr(o, torch.bfloat16, "o"),
                                        _ptr(Wg, torch.bfloat16, "Wg"), _ptr(Wm, torch.bfloat16, "Wm"),
                                        _ptr(mid, torch.bfloat16, "mid"), _ptr(y, torch.bfloat16, "y"),
@@ -281,6 +315,13 @@ def lca_gemm_bf16(A, B, C, stream=None):
     """C[M, N] = A[M, K] . B[N, K]^T (bf16 in/out, fp32 accumulation)."""
     M, K = A.shape
     N = B.shape[0]
+    if B.dim() != 2 or B.shape[1] != K:
+        raise ValueError("B must be [N, K] with A's K")
+    if C.dim() != 2 or C.shape[0] < M or C.shape[1] < N:
+        raise ValueError("C must be at least [M, N]")
+    for t, n in ((A, "A"), (B, "B"), (C, "C")):
+        if t.stride(1) != 1:
+            raise ValueError("%s must have unit stride along its rows" % n)
     st = _lib.load().lca_gemm_bf16(M, N, K, _ptr(A, torch.bfloat16, "A"), A.stride(0),
                                    _ptr(B, torch.bfloat16, "B"), B.stride(0), _ptr(C, torch.bfloat16, "C"),
                                    C.stride(0), _stream(stream))
