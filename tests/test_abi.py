@@ -108,3 +108,18 @@ def test_projection_rejects_bad_arguments(lib):
     assert lib.lca_gemm_bf16(4, 8, 60, FAKE, 64, FAKE, 64, FAKE, 8, None) == 2      # K % 8
     assert lib.lca_grouped_oproj(4, 64, 512, 7, 1024, 4096, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
     assert lib.lca_status_string(3) == b"workspace too small"
+
+
+def test_null_and_zero_arguments_are_errors_not_crashes(lib):
+    """Every entry point called with NULL pointers and zero sizes returns an error status (or a
+    zero workspace size) from host validation, without touching memory."""
+    for name, (argtypes, restype) in sorted(_lib.SIGNATURES.items()):
+        if name in ("lca_version", "lca_status_string", "lca_last_error", "lca_device_error"):
+            continue
+        args = [None if t is ctypes.c_void_p or hasattr(t, "_type_") and not t.__name__.startswith("c_")
+                else 0 for t in argtypes]
+        r = getattr(lib, name)(*args)
+        if name.endswith("_workspace"):
+            assert r == 0, name
+        else:
+            assert r in (1, 2), (name, r)
