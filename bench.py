@@ -802,6 +802,9 @@ def run_ours(args):
     }
     if do_cpu:
         line["cpu_baseline"] = wk.cpu_sample(args.cpu_budget)
+        if args.all_core_budget > 0:
+            line["cpu_baseline"]["all_core"] = all_core_baseline(*oracle_units(args.workload, args.seed),
+                                                                 args.all_core_budget)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -809,18 +812,49 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_reference(args):
-    """The oracle (CPU, fp64, single thread) as the reference arm: each step is a bounded sample."""
-    rank, world, _ = dist_info()
-    if rank != 0:
-        return
-    cfg = wl.WORKLOADS[args.workload]
-    if args.workload == "block_decode_1m":
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:    # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def oracle_all_core(unit, budget_s: float, threads: int) -> float:
+    """Units per second of the oracle on `threads` host threads at once, each running `unit()`
+    (one token of the workload on shared read-only inputs) until `budget_s` of wall time has
+    passed.  The oracle's C calls release the interpreter lock, so the threads run in parallel."""
+    counts = [0] * threads
+    start = threading.Barrier(threads + 1)
+    stop_at = [0.0]
+
+    def work(i):
+        start.wait()
+        while time.perf_counter() < stop_at[0]:
+            unit()
+            counts[i] += 1
+
+    pool = [threading.Thread(target=work, args=(i,), daemon=True) for i in range(threads)]
+    for t in pool:
+        t.start()
+    t0 = time.perf_counter()
+    stop_at[0] = t0 + budget_s
+    start.wait()
+    for t in pool:
+        t.join()
+    return sum(counts) / (time.perf_counter() - t0)
+
+
+def oracle_units(workload: str, seed: int):
+    """One token of `workload` for the oracle on synthetic host inputs of the workload's shapes:
+    (object with one_unit() and sample, tokens a unit stands for)."""
+    cfg = wl.WORKLOADS[workload]
+    if workload == "block_decode_1m":
         # one token through one CSA and one HCA layer per step, scaled to the block's layer count
         parts = [_HostOnly("csa_decode_128k", dict(entries=cfg["csa_entries"], pos=cfg["pos"], shape=cfg["csa"]),
-                           args.seed),
+                           seed),
                  _HostOnly("hca_decode_1m", dict(entries=cfg["hca_entries"], pos=cfg["pos"], shape=cfg["hca"]),
-                           args.seed)]
+                           seed)]
         scale = float(cfg["n_csa"])        # n_csa == n_hca: each step covers 1/n_csa of the block
 
         class _Pair:
@@ -830,10 +864,26 @@ def run_reference(args):
             def one_unit(self):
                 for p in parts:
                     p.one_unit()
-        wk = _Pair()
-    else:
-        wk = _HostOnly(args.workload, cfg, args.seed)
-        scale = 1.0
+        return _Pair(), scale
+    return _HostOnly(workload, cfg, seed), 1.0
+
+
+def all_core_baseline(wk, scale: float, budget_s: float) -> dict:
+    """The oracle on every host core (threads over shared inputs), beside the single-thread figure."""
+    wk.one_unit()                       # warm: first-call set-up outside the timed span
+    n = host_cores()
+    value = oracle_all_core(wk.one_unit, budget_s, n) / scale
+    return {"value": round(value, 3), "unit": "tokens/s", "cores": n,
+            "sample": "%d threads, each one token at a time (%s) for %.0f s of wall time" % (n, wk.sample, budget_s)}
+
+
+def run_reference(args):
+    """The oracle (CPU, fp64, single thread) as the reference arm: each step is a bounded sample."""
+    rank, world, _ = dist_info()
+    if rank != 0:
+        return
+    cfg = wl.WORKLOADS[args.workload]
+    wk, scale = oracle_units(args.workload, args.seed)
     times = []
     for i in range(args.warmup + args.steps):
         t0 = time.perf_counter()
@@ -852,6 +902,8 @@ def run_reference(args):
                          "sample": "one token of the workload per step: " + wk.sample},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+    if args.all_core_budget > 0:
+        line["cpu_baseline"]["all_core"] = all_core_baseline(wk, scale, args.all_core_budget)
     print(json.dumps(line), flush=True)
 
 
@@ -923,6 +975,8 @@ def main(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--all-core-budget", type=float, default=6.0,
+                    help="seconds of wall time for the oracle on every host core (0: skip)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

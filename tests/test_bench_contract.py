@@ -29,7 +29,8 @@ def _run(args, timeout=240, env=None):
 
 @pytest.mark.parametrize("workload", sorted(bench.WORKLOADS))
 def test_reference_arm_prints_one_contract_line(workload):
-    p = _run(["bench.py", "--impl", "reference", "--workload", workload, "--steps", "1", "--warmup", "0"])
+    p = _run(["bench.py", "--impl", "reference", "--workload", workload, "--steps", "1", "--warmup", "0",
+              "--all-core-budget", "1"])
     assert p.returncode == 0, p.stderr[-2000:]
     lines = _json_lines(p.stdout)
     assert len(lines) == 1
@@ -41,7 +42,9 @@ def test_reference_arm_prints_one_contract_line(workload):
     assert d["value"] > 0 and d["ms_per_step"] > 0
     assert d["config"]["name"] == workload and d["config"]["workload"]
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["sample"] and cb["value"] == d["value"]
+    ac = cb["all_core"]
+    assert ac["cores"] == bench.host_cores() and ac["value"] > 0 and ac["unit"] == "tokens/s" and ac["sample"]
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
@@ -57,11 +60,28 @@ def test_reference_arm_under_two_ranks_prints_once():
     port = _free_port()
     p = _run(["-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr", "127.0.0.1",
               "--master-port", str(port), "bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1",
-              "--warmup", "0", "--workload", "hca_decode_1m"])
+              "--warmup", "0", "--workload", "hca_decode_1m", "--all-core-budget", "0"])
     assert p.returncode == 0, p.stderr[-2000:]
     lines = _json_lines(p.stdout)
     assert len(lines) == 1
     assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+    assert "all_core" not in lines[0]["cpu_baseline"]
+
+
+def test_all_core_timing_counts_units_over_wall_time():
+    import threading
+    import time
+    done = []
+    lock = threading.Lock()
+
+    def unit():
+        time.sleep(0.01)
+        with lock:
+            done.append(1)
+
+    rate = bench.oracle_all_core(unit, 0.2, 4)
+    # four threads of 10 ms units for 0.2 s: about 400 units/s, never more than the units run
+    assert 150 < rate < 450 and len(done) >= 40
 
 
 def test_clock_summary_median_and_reason_bits():
