@@ -34,6 +34,7 @@ if ROOT not in sys.path:
 import workloads as wl  # noqa: E402
 
 METRIC = "CSA/HCA attention tokens/s per layer at 128K–1M ctx; % of HBM/tensor roofline"
+DEFAULT_WORKLOAD = "csa_decode_128k"
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -195,6 +196,34 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------- workloads -----
 
+def csa_layer_work(s, B: int, n_vis, Tq: int, entries: int = 0):
+    """Algorithmic bytes and FLOPs of one CSA layer step: inputs read once, outputs written once,
+    workspace round trips (scores, split-K partials) left out.  Decode (Tq = 1): per sequence the
+    keys of the visible entries, the selected and window rows, the query and the output, the
+    tokens compressed into the new KV and key entries.  Prefill (one chunk): the keys of all
+    entries once (`entries`), each query's selected and window rows."""
+    m, c, dI, HI, H, k, W = s.ratio, s.head_dim, s.idx_dim, s.idx_heads, s.heads, s.topk, s.window
+    n_vis_sum = float(np.sum(n_vis)) * (B if np.ndim(n_vis) == 0 else 1)
+    n_new = max(1, Tq // m)
+    compress = B * n_new * ((2 * m) * (2 * c + 4) + 2 * c + (2 * m) * (2 * dI + 4) + 2 * dI)
+    window = B * Tq * 4 * c
+    keys = B * entries * 2 * dI if entries else n_vis_sum * 2 * dI
+    indexer = keys + B * Tq * HI * (2 * dI + 4)
+    attention = B * Tq * ((k + W) * 2 * c + 2 * H * c * 2 + 4 * k)
+    flops = 2.0 * n_vis_sum * HI * dI + 4.0 * B * Tq * (k + W) * H * c
+    return float(compress + window + indexer + attention), flops
+
+
+def hca_layer_work(s, B: int, n_vis: int):
+    """Algorithmic bytes and FLOPs of one HCA decode step: the block of m' tokens compressed into
+    the new entry, the window row, every visible entry and the window rows once, query and output."""
+    m, c, H, W = s.ratio, s.head_dim, s.heads, s.window
+    compress = B * (m * (2 * c + 4) + 2 * c)
+    window = B * 4 * c
+    attention = B * ((n_vis + W) * 2 * c + 2 * H * c * 2)
+    return float(compress + window + attention), 4.0 * B * (n_vis + W) * H * c
+
+
 class Workload:
     """Common shape of a benchmark workload (device state + per-step inputs)."""
 
@@ -259,10 +288,12 @@ class CsaDecode(Workload):
         self.host_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
         self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
         self.d2h_bytes = self.out.numel() * self.out.element_size()
-        # algorithmic bytes of one indexer launch: keys of the visible entries, queries, weights, scores
+        # algorithmic bytes of one indexer launch: keys of the visible entries, queries, weights (the
+        # scores it writes are a workspace round trip to the top-k, so they are not counted)
         n_vis = (pos + 1) // s.ratio
-        self.dom_bytes = B * (n_vis * s.idx_dim * 2 + s.idx_heads * s.idx_dim * 2 + s.idx_heads * 4 + n_vis * 4)
+        self.dom_bytes = B * (n_vis * s.idx_dim * 2 + s.idx_heads * s.idx_dim * 2 + s.idx_heads * 4)
         self.dom_flops = 2.0 * B * n_vis * s.idx_heads * s.idx_dim
+        self.step_bytes, self.step_flops = csa_layer_work(s, B, n_vis, 1)
 
     def dominant_call(self):
         d = self.d
@@ -363,6 +394,7 @@ class HcaDecode(Workload):
         rows = n_vis + s.window
         self.dom_bytes = B * (rows * s.head_dim * 2 + 2 * s.heads * s.head_dim * 2)
         self.dom_flops = 4.0 * B * rows * s.heads * s.head_dim
+        self.step_bytes, self.step_flops = hca_layer_work(s, B, n_vis)
 
     def dominant_call(self):
         # the attention kernel and its split-K combine
@@ -450,7 +482,8 @@ class CsaPrefill(Workload):
         self.d2h_bytes = self.out.numel() * self.out.element_size()
         n_vis = np.array([(q_begin + i + 1) // s.ratio for i in range(Tq)], dtype=np.float64)
         self.dom_flops = float(2.0 * n_vis.sum() * s.idx_heads * s.idx_dim)
-        self.dom_bytes = entries * s.idx_dim * 2 + Tq * s.idx_heads * (s.idx_dim * 2 + 4) + float(n_vis.sum()) * 4
+        self.dom_bytes = entries * s.idx_dim * 2 + Tq * s.idx_heads * (s.idx_dim * 2 + 4)
+        self.step_bytes, self.step_flops = csa_layer_work(s, 1, n_vis, Tq, entries=entries)
 
     def dominant_call(self):
         d = self.d
@@ -575,6 +608,11 @@ class BlockDecode(Workload):
         self.dominant = "indexer"
         csa0 = self.layers[0]
         self.dom_bytes, self.dom_flops = csa0.dom_bytes, csa0.dom_flops
+        # the layers' own work plus each layer's two projection weight matrices and activations
+        w_params = sum(int(W["Wg"].numel() + W["Wm"].numel()) for W in self.W)
+        self.step_bytes = sum(L.step_bytes for L in self.layers) + 2 * w_params + \
+            len(self.layers) * B * (s.heads * s.head_dim + d_model) * 2
+        self.step_flops = sum(L.step_flops for L in self.layers) + 2.0 * B * w_params
         self.host_out = [torch.empty(y.shape, dtype=torch.bfloat16).pin_memory() for y in self.y]
         self.h2d_bytes = sum(L.h2d_bytes for L in self.layers)
         self.d2h_bytes = sum(y.numel() * y.element_size() for y in self.y)
@@ -730,23 +768,43 @@ def time_eager(fn, steps: int, flush: L2Flush, world: int):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-def run_ours(args):
-    rank, world, local = dist_info()
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    device = torch.device("cuda", torch.cuda.current_device())
-    from long_context_attention_04_b300 import build as lca_build
-    if rank == 0:
-        lca_build.build()
-    barrier(world)
-    cfg = wl.WORKLOADS[args.workload]
-    wk = WORKLOADS[args.workload](cfg, seed=args.seed + rank)
-    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
-    if do_cpu:
+def roofline_of(wk, dom_ms: float, peaks: dict, workload: str) -> dict:
+    """The dominant call against its roofline (algorithmic bytes or FLOPs per launch / CUDA-event
+    time), with the DRAM traffic measured for it while the sources are unchanged."""
+    if wk.bound == "hbm":
+        achieved = wk.dom_bytes / (dom_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": measured_traffic(workload),
+                "kernel": wk.dominant, "algorithmic_bytes": int(wk.dom_bytes), "kernel_ms": round(dom_ms, 4),
+                "peak_source": peaks["source"]}
+    achieved = wk.dom_flops / (dom_ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+            "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": measured_traffic(workload),
+            "kernel": wk.dominant, "algorithmic_flops": wk.dom_flops, "kernel_ms": round(dom_ms, 4),
+            "peak_source": peaks["source"],
+            "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4)}
+
+
+def step_roofline_of(wk, step_ms: float, peaks: dict) -> dict:
+    """The whole step against its own roofline: all of its algorithmic bytes (or FLOPs, for a
+    tensor-bound step) at the measured peak, over the measured step time."""
+    if wk.bound == "hbm":
+        t = wk.step_bytes / (peaks["hbm_gbs"] * 1e9) * 1e3
+        return {"bound": "hbm", "algorithmic_bytes": int(wk.step_bytes), "roofline_ms": round(t, 4),
+                "frac": round(t / step_ms, 4)}
+    t = wk.step_flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+    return {"bound": "tensor", "algorithmic_flops": wk.step_flops, "roofline_ms": round(t, 4),
+            "frac": round(t / step_ms, 4)}
+
+
+def measure(name: str, args, flush, world: int, device, rank: int, seed: int, snapshot: bool = False) -> tuple:
+    """Builds workload `name`, warms it up and times its step, its dominant call and its end-to-end
+    step (CUDA events, L2 flushed before each step); returns (workload, result dict).  With
+    `snapshot`, host copies of the state the oracle needs are taken before the first step."""
+    cfg = wl.WORKLOADS[name]
+    wk = WORKLOADS[name](cfg, seed=seed)
+    if snapshot:
         wk.snapshot_host()
-    flush = L2Flush(device)
     for _ in range(args.warmup):
         wk.step()
     torch.cuda.synchronize()
@@ -762,30 +820,55 @@ def run_ours(args):
     from long_context_attention_04_b300.layers import StepGraph
     e2e = StepGraph(wk.e2e_step, warmup=max(1, args.warmup // 2))
     e2e_ms = time_eager(e2e, args.steps, flush, world)
-    ms = float(np.mean(step_ms))
-    ms_all = max_over_ranks(ms, world, device)
+    ms_all = max_over_ranks(float(np.mean(step_ms)), world, device)
     e2e_all = max_over_ranks(float(np.mean(e2e_ms)), world, device)
     dom = float(np.mean(dom_ms))
     from long_context_attention_04_b300 import api
-    dev_err = api.lca_device_error()
     peaks = measured_peaks()
-    if wk.bound == "hbm":
-        achieved = wk.dom_bytes / (dom * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": measured_traffic(args.workload),
-                "kernel": wk.dominant,
-                "kernel_ms": round(dom, 4), "peak_source": peaks["source"]}
-    else:
-        achieved = wk.dom_flops / (dom * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                "frac": round(achieved / peaks["bf16_tflops"], 4), "traffic": measured_traffic(args.workload),
-                "kernel": wk.dominant,
-                "kernel_ms": round(dom, 4), "peak_source": peaks["source"]}
-    value = world * wk.tokens / (ms_all * 1e-3)
+    res = {
+        "workload": cfg["name"],
+        "value": round(world * wk.tokens / (ms_all * 1e-3), 1), "unit": "tokens/s",
+        "ms_per_step": round(ms_all, 4),
+        "roofline": roofline_of(wk, dom, peaks, name),
+        "step_roofline": step_roofline_of(wk, ms_all, peaks),
+        "e2e": {"value": round(world * wk.tokens / (e2e_all * 1e-3), 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": wk.h2d_bytes, "d2h_bytes_per_step": wk.d2h_bytes},
+        "gpu_launches": wk.launches * args.steps,
+        "clocks": clk.summary(),
+        "device_error_word": api.lca_device_error(),
+    }
+    del step_graph, dom_graph, e2e
+    return wk, res
+
+
+# Target configurations timed beside the headline workload (one process, one GPU): HCA decode at
+# 1M context (HBM-bound), the 8192-query CSA prefill chunk at 1M (tensor-bound), and the block of
+# 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound).
+EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "block_decode_1m")
+
+
+def run_ours(args):
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    from long_context_attention_04_b300 import build as lca_build
+    if rank == 0:
+        lca_build.build()
+    barrier(world)
+    cfg = wl.WORKLOADS[args.workload]
+    do_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline
+    flush = L2Flush(device)
+    wk, res = measure(args.workload, args, flush, world, device, rank, args.seed + rank, snapshot=do_cpu)
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(ms_all, 4), "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
+        "dtype_note": "bf16 inputs, caches and outputs; attention products in fp16 (rows re-encoded exactly from "
+                      "bf16, the normalised query split into two fp16 parts), fp32 accumulation and softmax; "
+                      "indexer in bf16 with fp32 accumulation",
         "data": "synthetic: seeded N(0,1) caches, tokens, queries; N(0,0.02) biases (workloads.py)",
         "config": {"workload": cfg["name"], "name": args.workload, "batch": cfg.get("B", 1),
                    "l2": "caches larger than L2, and L2 flushed before every timed step (512 MiB written, "
@@ -793,18 +876,27 @@ def run_ours(args):
                    "timing": "device: CUDA-graph replays of the step, CUDA events; e2e: replays of the step "
                              "captured with its pinned-host input copies and its output copy (StepGraph), all "
                              "inside the timed span"},
-        "roofline": roof,
-        "e2e": {"value": round(world * wk.tokens / (e2e_all * 1e-3), 1), "unit": "tokens/s",
-                "h2d_bytes_per_step": wk.h2d_bytes, "d2h_bytes_per_step": wk.d2h_bytes},
-        "gpu_launches": wk.launches * args.steps,
-        "clocks": clk.summary(),
-        "device_error_word": dev_err,
+        "roofline": res["roofline"],
+        "step_roofline": res["step_roofline"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["gpu_launches"],
+        "clocks": res["clocks"],
+        "device_error_word": res["device_error_word"],
     }
     if do_cpu:
         line["cpu_baseline"] = wk.cpu_sample(args.cpu_budget)
         if args.all_core_budget > 0:
             line["cpu_baseline"]["all_core"] = all_core_baseline(*oracle_units(args.workload, args.seed),
                                                                  args.all_core_budget)
+    del wk
+    if world == 1 and not args.no_extra and args.workload == DEFAULT_WORKLOAD:
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            torch.cuda.empty_cache()
+            wk_x, res_x = measure(name, args, flush, world, device, rank, args.seed)
+            del wk_x
+            extra[name] = res_x
+        line["workloads"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -970,11 +1062,14 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="csa_decode_128k", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="time the chosen workload only (by default the headline run also times %s)"
+                    % ", ".join(EXTRA_WORKLOADS))
     ap.add_argument("--all-core-budget", type=float, default=6.0,
                     help="seconds of wall time for the oracle on every host core (0: skip)")
     args = ap.parse_args(argv)

@@ -61,6 +61,10 @@ typedef enum lca_status {
 #define LCA_DEVERR_INDEX_RANGE    0x2u  /* attend: an index outside [0, cache_rows) (not -1) */
 #define LCA_DEVERR_VISIBLE_RANGE  0x4u  /* visible entries exceed cache_rows; clamped */
 #define LCA_DEVERR_NEGATIVE_POS   0x8u  /* a negative position */
+#define LCA_DEVERR_FP16_RANGE     0x10u /* attend: a KV or window row element, or an element of
+                                         * the normalised, rotated query, outside fp16's finite
+                                         * range (|x| > 65504, inf, nan): the products saturate
+                                         * there, so that call's outputs are not accurate */
 #define LCA_DEVERR_TIMEOUT        0x100u /* a bounded wait inside a kernel ran out */
 
 /* Layer parameters (names follow the pages' notation). */
@@ -235,12 +239,19 @@ lca_status hca_attend_prepared(const lca_attn_params *p, int batch, int n_q,
 
 /* hca_attend with no workspace argument and no allocation of any kind: the split-K
  * partials and query images go to a 32 MiB array that the library reserves in device
- * memory when its module loads.  Same arguments, layout and result as hca_attend.
- * The paper has no counterpart; it serves callers that cannot allocate device memory.
- *  - The first call on a device (with that device current) looks up the array's address;
- *    make that first call before capturing the stream into a graph.
- *  - A call that would need more than 32 MiB (batch * n_q > 127 queries at c = 512,
- *    H = 64 on 148 SMs) returns LCA_ERR_WORKSPACE and launches nothing; use hca_attend.
+ * memory when its module loads (every device that loads the library holds it until the
+ * process exits).  Same arguments, layout and result as hca_attend, bit for bit.
+ * The paper has no counterpart; it serves callers that cannot allocate device memory: a
+ * host program without a device allocator of its own, or a serving runtime that fixes its
+ * device memory at start-up and may not allocate or free while it serves.
+ *  - The array's address is looked up on every call, in the calling thread's current
+ *    device and context (a context destroyed and created again, e.g. by cudaDeviceReset,
+ *    may place the array elsewhere).  The first call on a device may load the library's
+ *    module there: make that first call before capturing the stream into a graph.
+ *  - A call whose scratch, hca_attend_workspace(p, batch, n_q, cache_rows), exceeds 32 MiB
+ *    returns LCA_ERR_WORKSPACE and launches nothing; use hca_attend.  The size grows with
+ *    batch * n_q * splits * H * c * 4 bytes, the split count being about the SM count
+ *    divided by batch * n_q: on a 148-SM B300 at c = 512, H = 64, up to 127 queries fit.
  *  - Every call on a device shares the one array: calls that overlap in time on one
  *    device (two streams, two host threads) corrupt each other's results.  Serialise them.
  *  - Nothing in the array needs to start at zero. */
@@ -281,6 +292,13 @@ const char *lca_last_error(void);
  * into *word (LCA_DEVERR_* bits).  Returns LCA_ERR_TIMEOUT if a timeout bit is set,
  * LCA_ERR_DEVICE for any other bit, LCA_OK when the word is zero. */
 lca_status lca_device_error(cudaStream_t stream, uint32_t *word);
+/* For tests of the failure path only.  Sets, on the current device, the bound of every wait
+ * inside the kernels (SM clock cycles; <= 0 restores the default of 2e9, about a second) and
+ * a tile index (per CTA, counted from 0) whose rows the attention kernel leaves unloaded
+ * (< 0: none), so that the waits on that tile run out: the kernel then stops, frees its
+ * tensor memory, and lca_device_error reports LCA_ERR_TIMEOUT.  Affects every later launch
+ * on the device until reset with lca_test_hooks(0, -1). */
+lca_status lca_test_hooks(long long wait_limit_cycles, int attend_skip_tile);
 /* Library version string. */
 const char *lca_version(void);
 

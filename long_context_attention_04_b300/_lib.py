@@ -56,6 +56,7 @@ SIGNATURES = {
     "lca_status_string": ([c_int], ctypes.c_char_p),
     "lca_last_error": ([], ctypes.c_char_p),
     "lca_device_error": ([V, ctypes.POINTER(ctypes.c_uint32)], c_int),
+    "lca_test_hooks": ([ctypes.c_longlong, c_int], c_int),
     "lca_version": ([], ctypes.c_char_p),
 }
 

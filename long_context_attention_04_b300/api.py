@@ -335,5 +335,11 @@ def lca_device_error(stream=None) -> int:
     return int(w.value)
 
 
+def lca_test_hooks(wait_limit_cycles: int = 0, attend_skip_tile: int = -1):
+    """For failure-path tests only: the bound of every kernel wait (cycles; 0 = default) and a
+    tile the attention kernel leaves unloaded (-1 = none) on the current device."""
+    _check(_lib.load().lca_test_hooks(int(wait_limit_cycles), int(attend_skip_tile)))
+
+
 def lca_version() -> str:
     return _lib.load().lca_version().decode()

@@ -243,7 +243,11 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             ptx::tma_prefetch(&win_row_map);
         }
         bool ok = true;
+        const int skip = *(volatile int *)&g_test_skip_tile;   // -1 except in the timeout test
+        int issued[kAtSlots];                                    // last tile loaded into each slot
+        for (int j = 0; j < kAtSlots; ++j) issued[j] = -1;
         for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
+            if (u == skip) break;   // test hook: this tile's chunks are never loaded, so their waits run out
             const int t = (int)t0 + u;
             // the tile's gathered rows, once for its c chunks (the index loads overlap the waits)
             int rc[4] = {-1, -1, -1, -1};
@@ -255,6 +259,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                     break;
                 }
                 uint8_t *slot = ring + j * kAtChunkBytes;
+                issued[j] = u;
                 if (lane == 0) ptx::mbar_arrive_expect_tx(&full[j], kAtChunkBytes);
                 __syncwarp();
                 const uint32_t dst = ptx::smem_u32(slot);
@@ -282,6 +287,12 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             }
         }
         if (!ok) *abort_flag = 1;
+        // No copy may still be landing when the CTA exits: wait (bounded) for the last chunk
+        // issued into each slot.  Normally the softmax warps have already seen these phases
+        // complete, and the waits return at once.  A slot's phase covers the second gather
+        // issuer's box as well (its bytes are part of the expected count).
+        for (int j = 0; j < kAtSlots; ++j)
+            if (issued[j] >= 0) ptx::mbar_wait(&full[j], issued[j] & 1);
     } else if (warp == kAtMmaWarp) {
         // ------------------------------------------------------------- MMA issue ----
         // Per tile: S^T = KV . [hi | lo]^T chunk by chunk as the re-encoded chunks become ready;
@@ -367,7 +378,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         // Query chunk j (hi | lo, 32 KB) for every S chunk, in consumption order.
         if (lane == 0) {
             const int total = CC * n_tiles;
-            for (int n = 0; n < total && !*abort_flag; ++n) {
+            int n = 0;
+            for (; n < total && !*abort_flag; ++n) {
                 const int qs = n % kAtQSlots, j = n % CC;
                 if (n >= kAtQSlots && !ptx::mbar_wait(&q_empty[qs], ((n / kAtQSlots) - 1) & 1)) {
                     *abort_flag = 1;
@@ -377,6 +389,9 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 ptx::bulk_load(ptx::smem_u32(q_ring + qs * kAtQChunkBytes), qimg + j * kAtQChunkBytes, kAtQChunkBytes,
                                &q_full[qs]);
             }
+            // the last chunk issued into each slot has landed before the CTA exits (bounded)
+            for (int m = n - 1; m >= 0 && m >= n - kAtQSlots; --m)
+                ptx::mbar_wait(&q_full[m % kAtQSlots], (m / kAtQSlots) & 1);
         }
     } else {
         // -------------------------------------------------------------- softmax ----
@@ -393,6 +408,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         }
         uint32_t votes_done = 0, reds_done = 0;
         bool ok = true;
+        bool range_bad = false;                      // a row element outside fp16's range
         const int ctid = sw * 32 + lane;             // 0..255 among the softmax warps
         for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
             // ---- re-encode tile u's KV chunks to fp16 as they land (an eighth per warp).  The
@@ -406,7 +422,9 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
 #pragma unroll
                 for (int k = 0; k < kAtChunkBytes / 16 / (32 * kAtSoftmaxWarps); ++k) {
                     uint4 *p = chunk + ctid + k * (32 * kAtSoftmaxWarps);
-                    *p = bf16x8_to_f16x8(*p);
+                    const uint4 v = *p;
+                    range_bad |= bf16x8_exceeds_f16(v);
+                    *p = bf16x8_to_f16x8(v);
                 }
                 ptx::fence_proxy_async();
                 __syncwarp();
@@ -552,6 +570,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             }
             ptx::tc_fence_before();
         }
+        if (__any_sync(0xffffffffu, range_bad) && lane == 0) raise_error(LCA_DEVERR_FP16_RANGE);
     }
     __syncthreads();
     if (warp == kAtMmaWarp) {

@@ -17,6 +17,13 @@ __device__ unsigned int g_error_word;
 
 __device__ __forceinline__ void raise_error(unsigned int bits) { atomicOr(&g_error_word, bits); }
 
+// Bound of every mbarrier wait, in SM clock cycles (~1 s at 2 GHz by default), and a tile the
+// attention kernel's producer leaves unloaded (-1: none).  Both are changed only through
+// lca_test_hooks, which tests use to make a wait run out on purpose; kernels read them once
+// per launch (the skip) or once per slow wait (the bound).
+__device__ long long g_wait_limit_cycles = 2000000000LL;
+__device__ int g_test_skip_tile = -1;
+
 // Programmatic dependent launch.  Every kernel of the library is launched so that the next
 // kernel in the stream may be scheduled while it runs (its CTAs then wait on the SMs instead
 // of behind a launch).  Each kernel calls pdl_trigger() first, to let the next one launch,
@@ -73,6 +80,14 @@ __device__ __forceinline__ uint4 pack8_f16(const float *f) {
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 &v) {
     return make_uint4(pack_f16x2(bf16_lo(v.x), bf16_hi(v.x)), pack_f16x2(bf16_lo(v.y), bf16_hi(v.y)),
                       pack_f16x2(bf16_lo(v.z), bf16_hi(v.z)), pack_f16x2(bf16_lo(v.w), bf16_hi(v.w)));
+}
+
+// Whether any of the eight bf16 values in v lies outside fp16's finite range: |x| >= 2^16
+// (the largest bf16 below that, 65280, is an fp16 value), an infinity or a NaN.
+__device__ __forceinline__ bool bf16x8_exceeds_f16(const uint4 &v) {
+    const uint32_t mag = 0x7fff7fffu;
+    const uint32_t a = __vmaxu2(__vmaxu2(v.x & mag, v.y & mag), __vmaxu2(v.z & mag, v.w & mag));
+    return __vcmpgeu2(a, 0x47804780u) != 0;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

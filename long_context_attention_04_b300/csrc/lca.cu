@@ -7,7 +7,6 @@
 #include <cstdio>
 #include <algorithm>
 #include <cmath>
-#include <mutex>
 #include <string>
 #include <utility>
 
@@ -202,7 +201,11 @@ struct AttendPlan {
 constexpr int kPlanTileRows = kAtTile;
 
 // Split-K plan: one CTA per (query, split) and one CTA per SM, so a query gets as many splits
-// as keep all SMs busy in one wave (and never more splits than tiles).
+// as keep all SMs busy in one wave (and never more splits than tiles).  The byte counts cannot
+// wrap: attend_validate bounds batch * n_q by kMaxAttendUnits, so the largest total is below
+// 2^31 units x 128 splits x 64 heads x 512 x 4 bytes < 2^63 (the same bound keeps
+// *_attend_workspace from returning a wrapped size).
+constexpr int64_t kMaxAttendUnits = (int64_t)1 << 31;
 AttendPlan plan_attend(const lca_attn_params *p, int batch, int n_q, int64_t max_rows) {
     AttendPlan pl;
     pl.units = (int64_t)batch * n_q;
@@ -223,6 +226,8 @@ AttendPlan plan_attend(const lca_attn_params *p, int batch, int n_q, int64_t max
 lca_status attend_validate(const char *name, const lca_attn_params *p, int batch, int n_q) {
     LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
     LCA_REQUIRE(batch > 0 && n_q > 0, LCA_ERR_INVALID_ARG, "%s: batch and n_q must be positive", name);
+    LCA_REQUIRE((int64_t)batch * n_q < kMaxAttendUnits, LCA_ERR_UNSUPPORTED,
+                "%s: batch * n_q = %lld queries, at most 2^31 - 1 per call", name, (long long)batch * n_q);
     LCA_REQUIRE(p->head_dim == 128 || p->head_dim == 256 || p->head_dim == 512, LCA_ERR_UNSUPPORTED,
                 "%s: head_dim %d not in {128, 256, 512}", name, p->head_dim);
     LCA_REQUIRE(p->heads >= 1 && p->heads <= 64, LCA_ERR_UNSUPPORTED, "%s: heads %d not in [1, 64]", name, p->heads);
@@ -485,6 +490,15 @@ const char *lca_status_string(lca_status s) {
 
 const char *lca_last_error(void) { return t_last_error.c_str(); }
 
+lca_status lca_test_hooks(long long wait_limit_cycles, int attend_skip_tile) {
+    const long long limit = wait_limit_cycles > 0 ? wait_limit_cycles : 2000000000LL;
+    const int skip = attend_skip_tile >= 0 ? attend_skip_tile : -1;
+    cudaError_t e = cudaMemcpyToSymbol(g_wait_limit_cycles, &limit, sizeof limit);
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_test_skip_tile, &skip, sizeof skip);
+    if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_test_hooks: %s", cudaGetErrorString(e));
+    return ok();
+}
+
 lca_status lca_device_error(cudaStream_t stream, uint32_t *word) {
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_device_error: %s", cudaGetErrorString(e));
@@ -605,12 +619,12 @@ lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q, const 
 }
 
 size_t csa_attend_workspace(const lca_attn_params *p, int batch, int n_q) {
-    if (!p || batch <= 0 || n_q <= 0 || p->topk < 1) return 0;
+    if (!p || batch <= 0 || n_q <= 0 || p->topk < 1 || (int64_t)batch * n_q >= kMaxAttendUnits) return 0;
     return plan_attend(p, batch, n_q, (int64_t)p->topk + p->window).total;
 }
 
 size_t hca_attend_workspace(const lca_attn_params *p, int batch, int n_q, int64_t cache_rows) {
-    if (!p || batch <= 0 || n_q <= 0 || cache_rows <= 0) return 0;
+    if (!p || batch <= 0 || n_q <= 0 || cache_rows <= 0 || (int64_t)batch * n_q >= kMaxAttendUnits) return 0;
     return plan_attend(p, batch, n_q, cache_rows + p->window).total;
 }
 
@@ -638,37 +652,28 @@ lca_status hca_attend(const lca_attn_params *p, int batch, int n_q, const lca_bf
 // of its own, or a serving runtime that sizes its device memory once at start-up and may not
 // allocate (or free) anything while it serves.  For them the split-K partials and the
 // prepared query images live in one file-scope device array, reserved with the module, and
-// the entry point makes no allocation of any kind.  Its address is looked up once per
-// device, with that device current, on the first call made on it.  Every call on a device
-// shares the one array, so two calls in flight at once on that device (on two streams, or
-// from two host threads) overwrite each other's partials; calls must be ordered on one
-// stream or otherwise serialised.  No byte of it needs to start at zero: each call writes
-// every partial it later reads.
+// the entry point makes no allocation of any kind.  The array's address is looked up on
+// every call, with the calling thread's current device and context: a context that was torn
+// down and created again (cudaDeviceReset, or the primary context released and retained)
+// may map the module elsewhere, and a cached address would then point at memory the library
+// no longer owns.  The lookup is not a stream operation; on a device's first call it may load
+// the module, which is why that first call belongs before any stream capture.  Every call on
+// a device shares the one array, so two calls in flight at once on that device (on two
+// streams, or from two host threads) overwrite each other's partials; calls must be ordered
+// on one stream or otherwise serialised.  No byte of it needs to start at zero: each call
+// writes every partial and query image it later reads.
 namespace {
 constexpr size_t kNoAllocScratchBytes = (size_t)32 << 20;   // 32 MiB
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mu;
-void *g_noalloc_addr[kNoAllocMaxDevices];
 }  // namespace
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// The array's device address on the current device, looked up on first use.
+// The array's device address in the current context.
 static lca_status noalloc_scratch(const char *name, void **addr) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "%s: cudaGetDevice: %s", name, cudaGetErrorString(e));
-    LCA_REQUIRE(dev >= 0 && dev < kNoAllocMaxDevices, LCA_ERR_UNSUPPORTED, "%s: device ordinal %d >= %d", name, dev,
-                kNoAllocMaxDevices);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-        void *a = nullptr;
-        e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
-        if (e != cudaSuccess || !a)
-            return fail(LCA_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", name, cudaGetErrorString(e));
-        g_noalloc_addr[dev] = a;
-    }
-    *addr = g_noalloc_addr[dev];
+    void *a = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&a, g_noalloc_scratch);
+    if (e != cudaSuccess || !a) return fail(LCA_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", name, cudaGetErrorString(e));
+    *addr = a;
     return LCA_OK;
 }
 

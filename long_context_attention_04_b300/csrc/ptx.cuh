@@ -12,9 +12,6 @@
 namespace lca {
 namespace ptx {
 
-// ~1 s at 2 GHz: a wait that has not completed by then will not complete.
-constexpr long long kWaitLimitCycles = 2000000000LL;
-
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -49,16 +46,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Wait for the phase with the given parity to complete.  Gives up after kWaitLimitCycles,
-// raises LCA_DEVERR_TIMEOUT and returns false (the caller then abandons its loop).
+// Wait for the phase with the given parity to complete.  Gives up after g_wait_limit_cycles
+// (~1 s unless a test shortened it), raises LCA_DEVERR_TIMEOUT and returns false (the caller
+// then abandons its loop).
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    const long long limit = *(volatile long long *)&g_wait_limit_cycles;
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit) {
             raise_error(LCA_DEVERR_TIMEOUT);
             return false;
         }

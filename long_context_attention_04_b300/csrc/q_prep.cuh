@@ -53,6 +53,11 @@ __global__ void __launch_bounds__(32 * kQPrepHeads) q_prep_kernel(AttendArgs a) 
 #pragma unroll
         for (int u = 0; u < EPL; ++u) v[u] = 0.f;
     }
+    // an element outside fp16's finite range would saturate in the image: reported, not hidden
+    bool bad = false;
+#pragma unroll
+    for (int u = 0; u < EPL; ++u) bad |= !(fabsf(v[u]) <= 65504.f);
+    if (__any_sync(0xffffffffu, bad) && lane == 0) raise_error(LCA_DEVERR_FP16_RANGE);
     float lo[EPL];
 #pragma unroll
     for (int u = 0; u < EPL; ++u) {

@@ -345,3 +345,162 @@ def test_gemm_matches_oracle():
         api.lca_gemm_bf16(dev(A), dev(Bm), C)
         ref = oracle.gemm_bf16(u16(A), u16(Bm))
         assert_close_bf16_out(C.cpu().float().numpy(), ref, what="gemm %dx%dx%d" % (M, N, K))
+
+
+# ------------------------------------------------- every indexer dispatch branch ----
+
+@pytest.mark.parametrize("HI,DI,n_q", [(64, 128, 1), (64, 128, 2), (64, 128, 5), (32, 64, 1), (32, 64, 2),
+                                       (4, 32, 1)])
+def test_indexer_every_dispatch_shape(HI, DI, n_q):
+    """One case per kernel instantiation the library dispatches to (queries per tile 1, 2, 4 for
+    d_I = 128; 1, 8 for d_I = 64; 4 for d_I = 32), each with a ragged last tile, a query that
+    sees fewer entries than k and one that sees none."""
+    rng = Rng(22 + n_q)
+    B, m, rows, k = 3, 4, 651, 96
+    p = AttnParams(idx_heads=HI, idx_dim=DI, ratio=m, topk=k)
+    q = rng.normal_bf16((B, n_q, HI, DI))
+    w = rng.normal_f32((B, n_q, HI), 1.0 / math.sqrt(HI))
+    keys = rng.normal_bf16((B, rows, DI))
+    choices = [m * rows - 1, m * 389 + 3, m * (k // 3) + 1, 2, m * 129 - 1]
+    pos = torch.tensor([[choices[(b * n_q + i) % len(choices)] for i in range(n_q)] for b in range(B)],
+                       dtype=torch.int32)
+    stride = (rows + 3) // 4 * 4
+    scores = torch.full((B, n_q, stride), 7.0, device=DEV)
+    api.csa_indexer_scores(p, dev(q), dev(w), dev(keys), dev(pos), scores)
+    assert api.lca_device_error() == 0
+    out_idx = torch.empty((B, n_q, k), dtype=torch.int32, device=DEV)
+    api.lca_topk(p, scores, dev(pos), rows, out_idx)
+    assert api.lca_device_error() == 0
+    s_gpu, i_gpu = scores.cpu().numpy(), out_idx.cpu().numpy()
+    qb, wf, kb = u16(q), f32(w), u16(keys)
+    for b in range(B):
+        for i in range(n_q):
+            n_vis = oracle.visible_entries(int(pos[b, i]), m)
+            ref = oracle.indexer_scores(qb[b, i], wf[b, i], kb[b], n_vis)
+            got = s_gpu[b, i, :n_vis].astype(np.float64)
+            scale = max(np.abs(ref).max(), 1e-30) if n_vis else 1.0
+            np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-5 * scale, err_msg="b=%d i=%d" % (b, i))
+            assert np.isneginf(s_gpu[b, i, n_vis:rows]).all()
+            check_topk(i_gpu[b, i], ref, k, "b=%d i=%d" % (b, i))
+
+
+# ------------------------------------------- split count, batch position, decode ----
+
+def _attend_call(kind, p, d, pos, idx=None):
+    B, n_q = pos.shape
+    out = torch.empty((B, n_q, p.heads, p.head_dim), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, n_q, p.heads), dtype=torch.float32, device=DEV)
+    if kind == "csa":
+        ws = torch.empty(api.csa_attend_workspace(p, B, n_q), dtype=torch.uint8, device=DEV)
+        api.csa_attend(p, dev(d["q"]), dev(d["gamma"]), dev(pos), dev(d["kv"]), dev(idx), dev(d["win"]),
+                       dev(d["sink"]), out, ws, lse)
+    else:
+        ws = torch.empty(api.hca_attend_workspace(p, B, n_q, d["kv"].shape[1]), dtype=torch.uint8, device=DEV)
+        api.hca_attend(p, dev(d["q"]), dev(d["gamma"]), dev(pos), dev(d["kv"]), dev(d["win"]), dev(d["sink"]),
+                       out, ws, lse)
+    assert api.lca_device_error() == 0
+    return out.cpu().float().numpy(), lse.cpu().numpy()
+
+
+def _tile(t, reps):
+    return t.repeat(reps, *([1] * (t.dim() - 1)))
+
+
+@pytest.mark.parametrize("kind", ["csa", "hca"])
+def test_attend_independent_of_split_count(kind):
+    """The same two queries alone (each gets many split-K CTAs) and inside a batch of 75 copies
+    (one split each): both within the bar of the oracle, and their log-sum-exps agree."""
+    rng = Rng(23)
+    H, c, W, m, rows, k = 64, 512, 128, 4, 1400, 512
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=m, topk=k)
+    d1 = _attend_inputs(rng, 1, 2, H, c, rows, W, W + 4)
+    pos1 = torch.tensor([[m * rows - 1, m * 777 + 2]], dtype=torch.int32)
+    g = np.random.default_rng(24)
+    idx1 = torch.from_numpy(np.stack([np.sort(g.choice(rows, k, replace=False)) for _ in range(2)])
+                            .astype(np.int32)).view(1, 2, k)
+    reps = 75
+    dn = dict(d1, q=_tile(d1["q"], reps), kv=_tile(d1["kv"], reps), win=_tile(d1["win"], reps))
+    posn, idxn = _tile(pos1, reps), _tile(idx1, reps)
+    o1, l1 = _attend_call(kind, p, d1, pos1, idx1)
+    on, ln = _attend_call(kind, p, dn, posn, idxn)
+    ref = oracle_attend_batch(p, d1["q"], d1["gamma"], pos1, d1["kv"], d1["win"], d1["sink"],
+                              idx=idx1 if kind == "csa" else None)
+    for i in range(2):
+        ro, rl = ref[(0, i)]
+        assert_close_rms(o1[0, i], ro, what="alone i=%d" % i)
+        for b in (0, 37, reps - 1):
+            assert_close_rms(on[b, i], ro, what="batched b=%d i=%d" % (b, i))
+            np.testing.assert_allclose(ln[b, i], l1[0, i], rtol=0, atol=2e-3 * max(1.0, np.abs(rl).max()))
+        np.testing.assert_allclose(l1[0, i], rl, rtol=0, atol=2e-3 * max(1.0, np.abs(rl).max()))
+
+
+@pytest.mark.parametrize("kind", ["csa", "hca"])
+def test_attend_independent_of_batch_position(kind):
+    """A sequence's result does not depend on where it sits in the batch: the same query at
+    batch positions 0 and 5 (same call, same split plan) gives the same bits."""
+    rng = Rng(25)
+    H, c, W, m, rows, k, B = 64, 512, 128, 4, 900, 256, 6
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=m, topk=k)
+    d = _attend_inputs(rng, B, 1, H, c, rows, W, W + 2)
+    for key in ("q", "kv", "win"):
+        d[key][B - 1] = d[key][0]
+    pos = torch.tensor([[m * rows - 1 - 7 * b] for b in range(B)], dtype=torch.int32)
+    pos[B - 1, 0] = pos[0, 0]
+    g = np.random.default_rng(26)
+    idx = torch.from_numpy(np.stack([np.sort(g.choice(rows, k, replace=False)) for _ in range(B)])
+                           .astype(np.int32)).view(B, 1, k)
+    idx[B - 1] = idx[0]
+    o, l = _attend_call(kind, p, d, pos, idx)
+    assert np.array_equal(o[0], o[B - 1]) and np.array_equal(l[0], l[B - 1])
+    assert not np.array_equal(o[0], o[1])
+
+
+def test_csa_decode_equals_last_prefill_row():
+    """A prefill chunk's last query and a decode call for that same token (same selection, same
+    caches): the outputs agree within the bar, and each matches the oracle."""
+    rng = Rng(27)
+    H, c, W, m, k, T = 64, 512, 128, 4, 512, 40
+    rows, q0 = 2000, 4 * 2000 - 40
+    cap = T + W
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=m, topk=k)
+    d = _attend_inputs(rng, 1, T, H, c, rows, W, cap)
+    pos = torch.arange(q0, q0 + T, dtype=torch.int32).view(1, T)
+    g = np.random.default_rng(28)
+    idx = torch.from_numpy(np.stack([np.sort(g.choice(rows, k, replace=False)) for _ in range(T)])
+                           .astype(np.int32)).view(1, T, k)
+    o_pre, l_pre = _attend_call("csa", p, d, pos, idx)
+    d1 = dict(d, q=d["q"][:, T - 1:].contiguous())
+    o_dec, l_dec = _attend_call("csa", p, d1, pos[:, T - 1:].contiguous(), idx[:, T - 1:].contiguous())
+    ref = oracle_attend_batch(p, d1["q"], d["gamma"], pos[:, T - 1:], d["kv"], d["win"], d["sink"],
+                              idx=idx[:, T - 1:])[(0, 0)]
+    assert_close_rms(o_pre[0, T - 1], ref[0], what="prefill last row")
+    assert_close_rms(o_dec[0, 0], ref[0], what="decode")
+    assert_close_rms(o_dec[0, 0], o_pre[0, T - 1], what="decode vs prefill")
+    np.testing.assert_allclose(l_dec[0, 0], l_pre[0, T - 1], rtol=0, atol=2e-3 * max(1.0, np.abs(ref[1]).max()))
+
+
+# ------------------------------------------------------------ fp16 input domain ----
+
+@pytest.mark.parametrize("where", ["gamma_q", "kv_row", "window_row", "none"])
+def test_attend_reports_values_outside_fp16(where):
+    """The products run in fp16: a query or row element beyond 65504 would saturate.  Such a call
+    sets LCA_DEVERR_FP16_RANGE; an in-range call right at the edge of the inputs does not."""
+    rng = Rng(29)
+    H, c, W, m, rows = 8, 256, 16, 4, 300
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=m)
+    d = _attend_inputs(rng, 1, 1, H, c, rows, W, W)
+    pos = torch.tensor([[m * rows - 1]], dtype=torch.int32)
+    if where == "gamma_q":
+        d["gamma"] = torch.full((c,), 30000.0)     # normalised q ~ N(0, 1) x 30000: tails beyond 65504
+    elif where == "kv_row":
+        d["kv"][0, 123, 77] = 70000.0
+    elif where == "window_row":
+        d["win"][0, 5, 200] = -1e30
+    else:
+        d["gamma"] = torch.full((c,), 2000.0)      # |q| < 6 x 2000 < 65504
+        d["kv"][0, 123, 77] = 60000.0
+    out = torch.empty((1, 1, H, c), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(api.hca_attend_workspace(p, 1, 1, rows), dtype=torch.uint8, device=DEV)
+    api.hca_attend(p, dev(d["q"]), dev(d["gamma"]), dev(pos), dev(d["kv"]), dev(d["win"]), dev(d["sink"]), out, ws)
+    err = api.lca_device_error()
+    assert err == (0 if where == "none" else 0x10), hex(err)

@@ -1,14 +1,20 @@
-"""hca_attend_noalloc (scratch in the library's static device array) against hca_attend
-(caller workspace), through the C ABI, on two consecutive calls.
+"""hca_attend_noalloc, the entry point for callers that cannot allocate device memory (its
+scratch is the library's static device array), against hca_attend with a caller workspace,
+through the C ABI, on two consecutive calls.
+
+The two calls differ in inputs and in batch x queries, so the split count and the layout of
+the partials in the shared array change between them: the second call cannot pass by reading
+what the first one left there.  Each call must equal hca_attend on the same inputs bit for bit
+(same kernels, same split plan), and one is also compared with the oracle.
 
 Named so that it is collected last: it must pass both alone in a fresh process (where its
-first call does the per-device set-up) and after every other test has run.
+first call looks the array up on the device) and after every other test has run.
 """
 import numpy as np
 import pytest
 import torch
 
-from helpers import assert_close_rms
+from helpers import assert_close_rms, oracle_attend_batch
 from long_context_attention_04_b300 import api, build as lca_build
 from long_context_attention_04_b300.api import AttnParams, LcaError
 from workloads import Rng
@@ -32,32 +38,38 @@ def _case(seed, B, n_q, H, c, rows, W, m):
     g = np.random.default_rng(seed)
     pos = torch.from_numpy(g.integers(0, m * rows, size=(B, n_q), dtype=np.int32))
     pos[0, 0] = m * rows - 1            # every entry visible
-    return {k: v.to(DEV) for k, v in d.items()}, pos.to(DEV)
+    return d, pos
+
+
+def _run(fn, p, d, pos, ws=None):
+    B, n_q = pos.shape
+    out = torch.full((B, n_q, p.heads, p.head_dim), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse = torch.full((B, n_q, p.heads), float("nan"), dtype=torch.float32, device=DEV)
+    args = [d[k].to(DEV) for k in ("q", "gamma")] + [pos.to(DEV)] + [d[k].to(DEV) for k in ("kv", "win", "sink")]
+    if ws is None:
+        fn(p, *args, out, lse)
+    else:
+        fn(p, *args, out, ws, lse)
+    assert api.lca_device_error() == 0
+    return out.cpu(), lse.cpu()
 
 
 def test_noalloc_matches_workspace_entry_twice():
-    H, c, R, W, m = 64, 512, 64, 128, 128
-    B, n_q, rows = 4, 2, 1500
+    H, c, R, W, m, rows = 64, 512, 64, 128, 128, 1500
     p = AttnParams(heads=H, head_dim=c, rope_dims=R, window=W, ratio=m)
-    d, pos = _case(41, B, n_q, H, c, rows, W, m)
-    out_ws = torch.empty((B, n_q, H, c), dtype=torch.bfloat16, device=DEV)
-    lse_ws = torch.empty((B, n_q, H), dtype=torch.float32, device=DEV)
-    ws = torch.empty(api.hca_attend_workspace(p, B, n_q, rows), dtype=torch.uint8, device=DEV)
-    api.hca_attend(p, d["q"], d["gamma"], pos, d["kv"], d["win"], d["sink"], out_ws, ws, lse_ws)
-    ref_o = out_ws.float().cpu().numpy()
-    ref_l = lse_ws.cpu().numpy()
-    # two consecutive calls into the shared array, each compared with the workspace entry
-    for call in range(2):
-        out = torch.full((B, n_q, H, c), float("nan"), dtype=torch.bfloat16, device=DEV)
-        lse = torch.full((B, n_q, H), float("nan"), dtype=torch.float32, device=DEV)
-        api.hca_attend_noalloc(p, d["q"], d["gamma"], pos, d["kv"], d["win"], d["sink"], out, lse)
-        assert api.lca_device_error() == 0
-        o = out.float().cpu().numpy()
-        l = lse.cpu().numpy()
-        for b in range(B):
-            for i in range(n_q):
-                assert_close_rms(o[b, i], ref_o[b, i], what="noalloc call %d b=%d i=%d" % (call, b, i))
-        np.testing.assert_allclose(l, ref_l, rtol=0, atol=2e-3 * max(1.0, float(np.abs(ref_l).max())))
+    # call 1: 8 queries, 13 splits each (one per tile); call 2: other inputs, 15 queries, 9 splits each
+    for call, (seed, B, n_q) in enumerate(((41, 4, 2), (43, 5, 3))):
+        d, pos = _case(seed, B, n_q, H, c, rows, W, m)
+        ws = torch.empty(api.hca_attend_workspace(p, B, n_q, rows), dtype=torch.uint8, device=DEV)
+        ref_o, ref_l = _run(api.hca_attend, p, d, pos, ws)
+        o, l = _run(api.hca_attend_noalloc, p, d, pos)
+        assert torch.equal(o.view(torch.int16), ref_o.view(torch.int16)), "call %d: outputs differ" % call
+        assert torch.equal(l, ref_l), "call %d: lse differs" % call
+        if call == 1:
+            ref = oracle_attend_batch(p, d["q"], d["gamma"], pos, d["kv"], d["win"], d["sink"])
+            for (b, i), (ro, rl) in ref.items():
+                assert_close_rms(o[b, i].float().numpy(), ro, what="noalloc vs oracle b=%d i=%d" % (b, i))
+                np.testing.assert_allclose(l[b, i].numpy(), rl, rtol=0, atol=2e-3 * max(1.0, np.abs(rl).max()))
 
 
 def test_noalloc_rejects_calls_beyond_the_array():
@@ -68,6 +80,7 @@ def test_noalloc_rejects_calls_beyond_the_array():
     d, pos = _case(42, B, 1, H, c, rows, W, m)
     out = torch.empty((B, 1, H, c), dtype=torch.bfloat16, device=DEV)
     with pytest.raises(LcaError) as e:
-        api.hca_attend_noalloc(p, d["q"], d["gamma"], pos, d["kv"], d["win"], d["sink"], out)
+        api.hca_attend_noalloc(p, *[d[k].to(DEV) for k in ("q", "gamma")], pos.to(DEV),
+                               *[d[k].to(DEV) for k in ("kv", "win", "sink")], out)
     assert e.value.status == 3 and "static array" in str(e.value)
     assert api.lca_device_error() == 0
