@@ -6,50 +6,48 @@
 // window branch and the attention sink; [P4] zhinnengdao.top section 3.1 (c = 512, RoPE on
 // the last 64 dims, one sink logit per head).
 //
-// Multi-Query Attention shares one key/value row set across all heads, so a 128-row tile
-// of rows against all (padded to 64) heads is a dense contraction.  Both products run
-// transposed so that every MMA has M = 128:
-//   S^T[row, head]  = KV[row, c] . Qhat[head, c]^T        (M = 128 rows,  N = 2 x 64, K = c)
-//   O^T[c, head]   += KV[row, c]^T . P^T[row, head]       (M = 128 c,     N = 64, K = 128 rows)
-// The same 128-byte-swizzled shared-memory tile serves as the K-major A operand of the first
-// product and the MN-major A operand of the second.  S^T (128 columns) and O^T (c/128 chunks
-// of 64 columns) live in TMEM.
+// Multi-Query Attention shares one key/value row set across all heads, so a tile of rows
+// against all (padded to 64) heads is a dense contraction.  Per tile of 64 rows:
+//   S[q-row, row]   = Qhat[q-row, c] . KV[row, c]^T      (M = 128 query rows, N = 64, K = c)
+//   O^T[c, head]   += KV[row, c]^T . P^T[row, head]      (M = 128 c,  N = 64 heads, K = 64)
+// The 128 query rows are the 64 heads' normalised, rotated queries split into fp16 hi + lo
+// parts (about 22 bits; a single fp16 part moves the logits enough to push outputs whose
+// bf16 rounding already sits near the error bound past it).  Query row 32 g + i is the hi
+// part of head 16 g + i and row 32 g + 16 + i its lo part, so in S the two parts of a head
+// sit in one warp's lane quarter, 16 lanes apart, and a shuffle adds them.
 //
-// Precision.  Both products run in fp16 with fp32 accumulation.  The KV tile is re-encoded
-// in shared memory from bf16 to fp16 as it lands (exact for normalised rows, see
-// bf16x8_to_f16x8).  The normalised, rotated query (q_prep_kernel) is split into fp16 hi + lo
-// parts (about 22 bits) and S^T accumulates KV.hi^T and KV.lo^T side by side (one N = 128 MMA
-// per k step), summed by the softmax: a single fp16 query moves the logits by up to 2^-12 of
-// |q||k|, enough to push outputs whose bf16 rounding already sits near the error bound past
-// it.  The probabilities, in [0, 1], need no split: fp16 P (relative error 2^-12) lands within
-// the output's own bf16 rounding, and the row sum adds the same rounded values.
-//
-// Shared memory holds the KV tile as four 32 KB slots (128 rows x 128 c each, the whole tile
-// at c = 512), a ring of two 32 KB query slots and the 16 KB P^T buffer.  The query is
-// not resident: each S chunk comes with the matching 32 KB query chunk (hi and lo stacked as
-// one 128-row B operand, bulk-copied from the L2-hot image).  The KV tile stays resident
-// across both products; slot j is released when its PV chunk completes, and the producer
-// refills it with the next tile's chunk j.  HBM sees one pass over the rows; contiguous tiles
-// are prefetched into L2 two tiles ahead.
+// The query is resident for the whole split: its first c - 128 columns in tensor memory (the
+// A operand of the logit product read from TMEM), its last 128 columns in shared memory.  That
+// leaves shared memory to a ring of ten 16 KB slots of KV chunks (64 rows x 128 c): two and a
+// half tiles at c = 512, so the next tiles stream in while a tile's logits, softmax and PV
+// run.  Each chunk is re-encoded from bf16 to fp16 in place as it lands (exact for normalised
+// rows, see bf16x8_to_f16x8), serves as the K-major B operand of the logit product and then as
+// the MN-major A operand of PV, and is released when its PV completes.  The probabilities, in
+// [0, 2^8], go to shared memory as fp16 (relative error 2^-12, within the output's own bf16
+// rounding), double-buffered so that the softmax of one tile overlaps the PV of the previous.
+// TMEM columns: query C - 128 (c >= 256), S 64, O^T c/128 chunks of 64: C in all.
 //
 // Rows of a query: compressed rows (CSA: the selected entries; HCA: entries 0..n_vis), then
 // the window rows; tiles never mix the two.  All loads are TMA: contiguous compressed tiles
-// (HCA) as 2D boxes of 128 rows, indexed rows (CSA selections, window ring rows) with
-// 4-row gathers; masked rows are fetched at coordinate -1 and arrive as zeros.
+// (HCA) as 2D boxes of 64 rows, indexed rows (CSA selections, window ring rows) with 4-row
+// gathers; masked rows are fetched at coordinate -1 and arrive as zeros.
 //
-// Roles (one CTA per (query, split), one CTA per SM):
-//   warp 0      TMA producer of KV chunks
-//   warp 10     bulk-copy producer of query chunks
-//   warp 11     second issuer of row gathers (c box 1 of gathered chunks; the producer issues
-//               box 0): TMA gathers from one warp reach about half the rate of two
+// Roles (one CTA per (query, split), one CTA per SM, 12 warps):
+//   warp 0      TMA producer of KV chunks (box 0 of gathered chunks, both boxes of contiguous)
 //   warp 1      TMEM allocator and MMA issuer (one thread)
-//   warps 2-9   re-encoding of each landed KV chunk to fp16 (an eighth each), then the
-//               softmax: one TMEM lane (row) per thread, 32 heads per thread; online softmax
-//               in base 2 with a conditional rescale (the running max moves only when a
-//               logit exceeds it by more than 2^8), P^T rows to shared memory
+//   warp 2      second issuer of row gathers (box 1 of gathered chunks): TMA gathers from one
+//               warp reach about half the rate of two
+//   warp 3      bulk copy of the prepared query image (q_prep_kernel) into shared memory
+//   warps 4-7   softmax, one per TMEM lane quarter: the query's TMEM part at the start, then per
+//               tile one head per thread pair (hi lane + lo lane), 32 rows each, online base-2
+//               softmax with a conditional rescale (the running max moves only when a logit
+//               exceeds it by more than 2^8; the factors go through shared memory so each warp
+//               rescales its quarter of O^T), the P row of the head
+//   warps 8-11  fp16 re-encoding of each landed KV chunk (a quarter each)
 // The split's unnormalised O, running max and row sum go to the workspace; combine_kernel
 // merges the splits with the sink and applies the output RoPE(-pos).
-// Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds.
+// Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds
+// (issued copies drained, MMAs completed, TMEM freed).
 #pragma once
 
 #include "attend_common.cuh"
@@ -58,35 +56,41 @@
 
 namespace lca {
 
-constexpr int kAtHP = 64;                                // padded heads (MMA N)
-constexpr int kAtTile = 128;                             // rows per tile (MMA M of S^T)
-constexpr int kAtSlots = 4;                              // KV chunk slots: one whole tile (c = 512)
-constexpr int kAtQSlots = 2;                             // query chunk slots
-constexpr int kAtChunkBytes = 128 * 128 * 2;             // KV chunk: 128 rows x 128 c
-constexpr int kAtQChunkBytes = kQChunkBytes;             // query chunk: (64 hi + 64 lo) x 128 c
+constexpr int kAtHP = 64;                                // padded heads (MMA N of PV)
+constexpr int kAtTile = 64;                              // rows per tile (MMA N of the logit product)
+constexpr int kAtSlots = 10;                             // KV chunk slots in the ring
+constexpr int kAtChunkBytes = kAtTile * 128 * 2;         // KV chunk: 64 rows x 128 c (16 KB)
+constexpr int kAtBoxBytes = kAtTile * 128;               // one 64-c box of a chunk (8 KB)
+constexpr int kAtPBytes = kAtHP * kAtTile * 2;           // P: 64 heads x 64 rows, fp16 (8 KB)
 constexpr int kAtProducerWarp = 0;
 constexpr int kAtMmaWarp = 1;
-constexpr int kAtSoftmaxWarp0 = 2;
-constexpr int kAtSoftmaxWarps = 8;
-constexpr int kAtQWarp = kAtSoftmaxWarp0 + kAtSoftmaxWarps;
-constexpr int kAtGatherWarp = kAtQWarp + 1;              // second issuer of row gathers
-constexpr int kAtThreads = 32 * (kAtGatherWarp + 1);
+constexpr int kAtGatherWarp = 2;                         // second issuer of row gathers
+constexpr int kAtQWarp = 3;
+constexpr int kAtSoftmaxWarp0 = 4;                       // warps 4..7: lane quarters 0..3
+constexpr int kAtSoftmaxWarps = 4;
+constexpr int kAtConvWarp0 = 8;                          // warps 8..11
+constexpr int kAtConvWarps = 4;
+constexpr int kAtThreads = 32 * (kAtConvWarp0 + kAtConvWarps);
 constexpr float kAtTau = 8.0f;                           // log2 headroom before the running max must move
+constexpr int kPrefetchTiles = 2;                        // contiguous (HCA) tiles pulled into L2 this far ahead
 
 template <int C>
 struct AttendTcConfig {
     static constexpr int CC = C / 128;                        // c chunks per row
-    static constexpr int P_BYTES = kAtTile * kAtHP * 2;       // fp16 P^T (16 KB)
-    static constexpr int TMEM_S = 0;                          // S^T: 128 columns (hi | lo)
-    static constexpr int TMEM_O = 2 * kAtHP;                  // O^T chunk j at TMEM_O + 64 j
-    static constexpr int TMEM_COLS = 512;
-    static constexpr int MISC = 1408;                          // barriers, votes, cross-warp maxima
-    static constexpr int SMEM_BYTES = MISC + 1024 + CC * kAtChunkBytes + kAtQSlots * kAtQChunkBytes + P_BYTES;
+    static constexpr int QT = CC - 1;                         // query chunks held in TMEM
+    static constexpr int TMEM_S = QT * 64;                    // S: 64 columns
+    static constexpr int TMEM_O = TMEM_S + 64;                // O^T chunk j at TMEM_O + 64 j
+    static constexpr int TMEM_COLS = C;
+    static constexpr int Q_STAGE_SLOTS = 2 * QT;              // ring slots that first stage the TMEM query part
+    static constexpr int MISC = 2048;                         // barriers, rescale factors, flags
+    static constexpr int SMEM_BYTES = MISC + 1024 + kAtSlots * kAtChunkBytes + kQChunkBytes + 2 * kAtPBytes;
+    static_assert(TMEM_O + 64 * CC == TMEM_COLS, "tensor memory layout");
+    static_assert(Q_STAGE_SLOTS <= kAtSlots - CC, "the first tile and the staged query share the ring");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
 };
 
 // Where the rows of one query come from, in tiles: tiles [0, tc) hold compressed rows
-// [128 t, 128 t + 128) (masked at n_comp), tiles [tc, tc + tw) hold window rows.
+// [64 t, 64 t + 64) (masked at n_comp), tiles [tc, tc + tw) hold window rows.
 struct TileMap {
     int tc, tw;
     __device__ __forceinline__ int total() const { return tc + tw; }
@@ -112,7 +116,7 @@ __device__ __forceinline__ bool tile_row_valid(const AttendArgs &a, const RowLis
 }
 
 // Register cap: the register file is split across the four SM sub-partitions (16K each) and
-// 11 warps place 3 warps on three of them, so 3 x 32 x 168 <= 16384.
+// 12 warps place 3 on each, so 3 x 32 x 168 <= 16384.
 template <int C>
 __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtensorMap kv_tile_map,
                                                   const __grid_constant__ CUtensorMap kv_row_map,
@@ -124,27 +128,27 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     uint8_t *misc = smem_raw;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw + Cfg::MISC) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *ring = base;                                     // KV slot j = chunk j: 2 boxes [128 rows x 128 B]
-    uint8_t *q_ring = ring + CC * kAtChunkBytes;              // query slots: 2 boxes [128 rows x 128 B]
-    uint8_t *p_buf = q_ring + kAtQSlots * kAtQChunkBytes;     // P^T: [128 rows x 128 B] fp16
-    uint64_t *full = reinterpret_cast<uint64_t *>(misc);
-    uint64_t *empty = full + kAtSlots;
-    uint64_t *conv = empty + kAtSlots;
-    uint64_t *q_full = conv + kAtSlots;
-    uint64_t *q_empty = q_full + kAtQSlots;
-    uint64_t *s_full = q_empty + kAtQSlots;
-    uint64_t *s_empty = s_full + 2;
-    uint64_t *p_full = s_empty + 2;
-    uint64_t *pv_done = p_full + 2;
+    uint8_t *ring = base;                                     // slot s: 2 boxes [64 rows x 128 B]
+    uint8_t *q_tail = ring + kAtSlots * kAtChunkBytes;        // last c chunk of the query image (32 KB)
+    uint8_t *p_buf = q_tail + kQChunkBytes;                   // 2 x P [64 heads x 128 B] fp16
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc);      // chunk landed
+    uint64_t *empty = full + kAtSlots;                        // chunk's PV done: slot free
+    uint64_t *conv = empty + kAtSlots;                        // chunk re-encoded to fp16
+    uint64_t *gather_go = conv + kAtSlots;                    // box 1 may be gathered
+    uint64_t *q_full = gather_go + kAtSlots;                  // query image landed
+    uint64_t *q_ready = q_full + 1;                           // query's TMEM part written
+    uint64_t *q_free = q_ready + 1;                           // staging slots read
+    uint64_t *s_full = q_free + 1;
+    uint64_t *s_empty = s_full + 1;
+    uint64_t *p_full = s_empty + 1;                           // [2]
+    uint64_t *pv_done = p_full + 2;                           // [2]
     uint64_t *vote_bar = pv_done + 2;
-    uint64_t *red_bar = vote_bar + 1;
-    uint64_t *teardown = red_bar + 1;
+    uint64_t *teardown = vote_bar + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(teardown + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    // misc: 27 barriers + TMEM slot + abort flag (224 B), votes, maxima, gather hand-offs
-    int *votes = reinterpret_cast<int *>(misc + 256);                  // [2][8]
-    float *red = reinterpret_cast<float *>(misc + 320);                // [8][32]
-    uint64_t *gather_go = reinterpret_cast<uint64_t *>(misc + 1344);  // [kAtSlots]
+    // misc: 51 barriers + TMEM slot + abort flag (416 B), rescale factors, their flags
+    float *alphas = reinterpret_cast<float *>(misc + 512);    // [2][64]
+    int *flags = reinterpret_cast<int *>(misc + 1024);        // [2][4]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // ---- set-up: barriers, TMEM ----
@@ -152,21 +156,19 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         for (int s = 0; s < kAtSlots; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
-            ptx::mbar_init(&conv[s], kAtSoftmaxWarps);
+            ptx::mbar_init(&conv[s], kAtConvWarps);
             ptx::mbar_init(&gather_go[s], 1);
         }
-        for (int s = 0; s < kAtQSlots; ++s) {
-            ptx::mbar_init(&q_full[s], 1);
-            ptx::mbar_init(&q_empty[s], 1);
-        }
+        ptx::mbar_init(q_full, 1);
+        ptx::mbar_init(q_ready, kAtSoftmaxWarps);
+        ptx::mbar_init(q_free, kAtSoftmaxWarps);
+        ptx::mbar_init(s_full, 1);
+        ptx::mbar_init(s_empty, kAtSoftmaxWarps);
         for (int s = 0; s < 2; ++s) {
-            ptx::mbar_init(&s_full[s], 1);
-            ptx::mbar_init(&s_empty[s], kAtSoftmaxWarps);
-            ptx::mbar_init(&p_full[s], 32 * kAtSoftmaxWarps);
+            ptx::mbar_init(&p_full[s], kAtSoftmaxWarps);
             ptx::mbar_init(&pv_done[s], 1);
         }
         ptx::mbar_init(vote_bar, kAtSoftmaxWarps);
-        ptx::mbar_init(red_bar, kAtSoftmaxWarps);
         ptx::mbar_init(teardown, 1);
         *abort_flag = 0;
         ptx::fence_mbar_init();
@@ -204,12 +206,11 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         return;
     }
 
-    constexpr int kPrefetchTiles = 2;   // contiguous (HCA) tiles are pulled into L2 this far ahead
-
     const int n_tiles = (int)(t1 - t0);
     const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
     const int64_t win_row0 = (int64_t)b * (a.win_bs / C);
-    // Rows 4 lane .. 4 lane + 3 of gathered tile t as 2D-map row coordinates (-1: masked, read as 0).
+    // Rows 4 lane .. 4 lane + 3 (lane < 16) of gathered tile t as 2D-map row coordinates
+    // (-1: masked, read as 0).
     auto gather_rows = [&](int t, int j, int *rc) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -236,341 +237,380 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
 
     if (warp == kAtProducerWarp) {
         // ------------------------------------------------------------ producer ----
-        // Per tile t: KV chunk j of tile t into slot j, once PV(t-1) has released it.
+        // Chunk g = u CC + j (tile u, c chunk j) into slot g % kAtSlots once the PV that read the
+        // slot's previous chunk has completed; the query's staging slots only after the
+        // softmax warps have moved the query to TMEM.
         if (lane == 0) {
             ptx::tma_prefetch(&kv_tile_map);
             ptx::tma_prefetch(&kv_row_map);
             ptx::tma_prefetch(&win_row_map);
         }
         bool ok = true;
+        bool staged_free = Cfg::Q_STAGE_SLOTS == 0;
         const int skip = *(volatile int *)&g_test_skip_tile;   // -1 except in the timeout test
-        int issued[kAtSlots];                                    // last tile loaded into each slot
-        for (int j = 0; j < kAtSlots; ++j) issued[j] = -1;
+        int pf_next = (int)t0 + 1;                               // next tile to prefetch into L2
+        int last_g[kAtSlots];                                    // last chunk loaded into each slot
+#pragma unroll
+        for (int s = 0; s < kAtSlots; ++s) last_g[s] = -1;
         for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
             if (u == skip) break;   // test hook: this tile's chunks are never loaded, so their waits run out
             const int t = (int)t0 + u;
+            const bool gathered = t >= tm.tc || L.idx;
             // the tile's gathered rows, once for its c chunks (the index loads overlap the waits)
             int rc[4] = {-1, -1, -1, -1};
-            if (t >= tm.tc || L.idx) gather_rows(t, 0, rc);
-            for (int j = 0; j < CC && ok; ++j) {
-                // KV chunk j of tile t
-                if (u > 0 && !ptx::mbar_wait(&empty[j], (u - 1) & 1)) {
+            if (gathered && lane < 16) gather_rows(t, 0, rc);
+            for (int j = 0; j < CC; ++j) {
+                const int g = u * CC + j, slot = g % kAtSlots;
+                if (g >= kAtSlots && !ptx::mbar_wait(&empty[slot], ((g / kAtSlots) - 1) & 1)) {
                     ok = false;
                     break;
                 }
-                uint8_t *slot = ring + j * kAtChunkBytes;
-                issued[j] = u;
-                if (lane == 0) ptx::mbar_arrive_expect_tx(&full[j], kAtChunkBytes);
+                if (!staged_free && slot >= kAtSlots - Cfg::Q_STAGE_SLOTS) {
+                    if (!ptx::mbar_wait(q_free, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    staged_free = true;
+                }
+#pragma unroll
+                for (int s = 0; s < kAtSlots; ++s)
+                    if (s == slot) last_g[s] = g;
+                const uint32_t dst = ptx::smem_u32(ring + slot * kAtChunkBytes);
+                if (lane == 0) {
+                    ptx::mbar_arrive_expect_tx(&full[slot], kAtChunkBytes);
+                    if (gathered) ptx::mbar_arrive(&gather_go[slot]);   // box 1 may be gathered now
+                }
                 __syncwarp();
-                const uint32_t dst = ptx::smem_u32(slot);
-                if (t < tm.tc && !L.idx) {
-                    // contiguous compressed rows: two 64-c boxes of 128 rows
+                if (!gathered) {
+                    // contiguous compressed rows: two 64-c boxes of 64 rows
                     if (lane < 2)
-                        ptx::tma_load_2d(dst + lane * (128 * 128), &kv_tile_map, j * 128 + lane * 64,
-                                         (int)(kv_row0 + (int64_t)t * kAtTile), &full[j]);
-                } else {
-                    // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, c box 0; the gather
-                    // warp, released through gather_go[j], issues box 1 (one warp's TMA gathers run
-                    // at about half the rate of two)
-                    if (lane == 0) ptx::mbar_arrive(&gather_go[j]);
+                        ptx::tma_load_2d(dst + lane * kAtBoxBytes, &kv_tile_map, j * 128 + lane * 64,
+                                         (int)(kv_row0 + (int64_t)t * kAtTile), &full[slot]);
+                } else if (lane < 16) {
+                    // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, c box 0
                     const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
-                    ptx::tma_gather4(dst + lane * 512, map, j * 128, rc[0], rc[1], rc[2], rc[3], &full[j]);
+                    ptx::tma_gather4(dst + lane * 512, map, j * 128, rc[0], rc[1], rc[2], rc[3], &full[slot]);
                 }
             }
-            // L2 prefetch of the next contiguous tiles, issued behind this tile's own loads so that
-            // HBM serves those first (at the first tile: the next two)
-            if (!L.idx && lane == 1) {
-                for (int tp = t + (u == 0 ? 1 : kPrefetchTiles); tp <= t + kPrefetchTiles; ++tp)
-                    if (tp < t1 && tp < tm.tc)
+            // L2 prefetch of contiguous tiles ahead, issued behind this tile's own loads; the
+            // distance ramps up over the first tiles, so that at launch, when every CTA loads at
+            // once, the tiles needed first are not queued behind tiles needed later
+            if (ok && !L.idx && lane == 1) {
+                const int target = t + (u < kPrefetchTiles ? u + 1 : kPrefetchTiles);
+                for (; pf_next <= target; ++pf_next)
+                    if (pf_next < t1 && pf_next < tm.tc)
                         for (int x = 0; x < C; x += 64)
-                            ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + (int64_t)tp * kAtTile));
+                            ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + (int64_t)pf_next * kAtTile));
             }
         }
         if (!ok) *abort_flag = 1;
         // No copy may still be landing when the CTA exits: wait (bounded) for the last chunk
-        // issued into each slot.  Normally the softmax warps have already seen these phases
+        // issued into each slot.  Normally the conversion warps have already seen these phases
         // complete, and the waits return at once.  A slot's phase covers the second gather
         // issuer's box as well (its bytes are part of the expected count).
-        for (int j = 0; j < kAtSlots; ++j)
-            if (issued[j] >= 0) ptx::mbar_wait(&full[j], issued[j] & 1);
-    } else if (warp == kAtMmaWarp) {
-        // ------------------------------------------------------------- MMA issue ----
-        // Per tile: S^T = KV . [hi | lo]^T chunk by chunk as the re-encoded chunks become ready;
-        // then, once the softmax has written P,
-        // O^T += V^T P^T chunk by chunk, releasing each KV slot to the producer.  tcgen05 ops
-        // execute in issue order, so S(t+1) never overwrites S^T or P^T still in use.
-        if (lane == 0) {
-            constexpr uint32_t idesc_s = ptx::idesc_f16(128, 2 * kAtHP, false, false);
-            constexpr uint32_t idesc_o = ptx::idesc_f16(128, kAtHP, true, true);
-            const uint32_t p_addr = ptx::smem_u32(p_buf);
-            uint32_t q_used = 0;
-            bool ok = true;
-            for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
-                const uint32_t d = tmem + Cfg::TMEM_S;
-                for (int j = 0; j < CC && ok; ++j) {
-                    const int qs = q_used % kAtQSlots;
-                    if (!ptx::mbar_wait(&conv[j], u & 1) || !ptx::mbar_wait(&q_full[qs], (q_used / kAtQSlots) & 1)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t slot = ptx::smem_u32(ring + j * kAtChunkBytes);
-                    const uint32_t q_addr = ptx::smem_u32(q_ring + qs * kAtQChunkBytes);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = ptx::smem_desc(slot + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024,
-                                                           ptx::kSwizzle128);
-                        const uint64_t bd = ptx::smem_desc(q_addr + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024,
-                                                           ptx::kSwizzle128);
-                        ptx::mma_f16(d, ad, bd, idesc_s, (j > 0 || kk > 0));
-                    }
-                    ptx::mma_commit(&q_empty[qs]);
-                    ++q_used;
-                }
-                if (!ok) break;
-                ptx::mma_commit(&s_full[0]);
-                if (!ptx::mbar_wait(&p_full[0], u & 1)) {
+        for (int s = 0; s < kAtSlots; ++s)
+            if (last_g[s] >= 0) ptx::mbar_wait(&full[s], (last_g[s] / kAtSlots) & 1);
+    } else if (warp == kAtGatherWarp) {
+        // ------------------------------------------------------- second gatherer ----
+        // c box 1 of every gathered chunk, after the producer has claimed the chunk's slot.  The
+        // gathered tiles are all of them (CSA) or the trailing window tiles (HCA), so with gfirst
+        // the first gathered chunk, gathered chunk g is the ((g - gfirst) / kAtSlots)-th to use
+        // its slot's go barrier.
+        bool ok = true;
+        const int u_first = L.idx ? 0 : (int)(tm.tc > t0 ? tm.tc - t0 : 0);
+        const int gfirst = u_first * CC;
+        for (int u = u_first; u < n_tiles && ok && !*abort_flag; ++u) {
+            const int t = (int)t0 + u;
+            int rc[4] = {-1, -1, -1, -1};
+            if (lane < 16) gather_rows(t, 1, rc);
+            for (int j = 0; j < CC; ++j) {
+                const int g = u * CC + j, slot = g % kAtSlots;
+                if (!ptx::mbar_wait(&gather_go[slot], ((g - gfirst) / kAtSlots) & 1)) {
                     ok = false;
                     break;
                 }
-                ptx::tc_fence_after();
-                for (int j = 0; j < CC; ++j) {
-                    const uint32_t slot = ptx::smem_u32(ring + j * kAtChunkBytes);
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint64_t ad = ptx::smem_desc(slot + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
-                        const uint64_t bd = ptx::smem_desc(p_addr + kk * 2048, 128 * 128, 1024, ptx::kSwizzle128);
-                        ptx::mma_f16(tmem + Cfg::TMEM_O + j * kAtHP, ad, bd, idesc_o, (u > 0 || kk > 0));
-                    }
-                    ptx::mma_commit(&empty[j]);
+                if (lane < 16) {
+                    const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
+                    ptx::tma_gather4(ptx::smem_u32(ring + slot * kAtChunkBytes) + kAtBoxBytes + lane * 512, map,
+                                     j * 128 + 64, rc[0], rc[1], rc[2], rc[3], &full[slot]);
                 }
-                ptx::mma_commit(&pv_done[0]);
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (warp == kAtQWarp) {
+        // ---------------------------------------------------------- query image ----
+        // Chunks 0 .. CC-2 into the staging slots (the softmax warps move them to TMEM), the last
+        // chunk into its own area (the smem A operand of the last k steps).
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(q_full, CC * kQChunkBytes);
+            for (int i = 0; i < CC - 1; ++i)
+                ptx::bulk_load(ptx::smem_u32(ring + (kAtSlots - Cfg::Q_STAGE_SLOTS + 2 * i) * kAtChunkBytes),
+                               qimg + i * kQChunkBytes, kQChunkBytes, q_full);
+            ptx::bulk_load(ptx::smem_u32(q_tail), qimg + (CC - 1) * kQChunkBytes, kQChunkBytes, q_full);
+            if (!ptx::mbar_wait(q_full, 0)) *abort_flag = 1;   // landed before the CTA can exit
+        }
+    } else if (warp >= kAtConvWarp0) {
+        // ------------------------------------------------------ fp16 re-encoding ----
+        const int ct = (warp - kAtConvWarp0) * 32 + lane;   // 0 .. 127
+        bool ok = true, range_bad = false;
+        const int total = n_tiles * CC;
+        for (int g = 0; g < total && !*abort_flag; ++g) {
+            const int slot = g % kAtSlots;
+            if (!ptx::mbar_wait(&full[slot], (g / kAtSlots) & 1)) {
+                ok = false;
+                break;
+            }
+            uint4 *chunk = reinterpret_cast<uint4 *>(ring + slot * kAtChunkBytes);
+#pragma unroll
+            for (int k = 0; k < kAtChunkBytes / 16 / (32 * kAtConvWarps); ++k) {
+                uint4 *p = chunk + ct + k * (32 * kAtConvWarps);
+                const uint4 v = *p;
+                range_bad |= bf16x8_exceeds_f16(v);
+                *p = bf16x8_to_f16x8(v);
+            }
+            ptx::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&conv[slot]);
+        }
+        if (!ok) *abort_flag = 1;
+        if (__any_sync(0xffffffffu, range_bad) && lane == 0) raise_error(LCA_DEVERR_FP16_RANGE);
+    } else if (warp == kAtMmaWarp) {
+        // ------------------------------------------------------------- MMA issue ----
+        // S(u) chunk by chunk as the re-encoded chunks become ready, then PV(u-1) once the
+        // softmax has written P(u-1), so that the tensor pipe computes the next tile's logits
+        // while the softmax of the current one runs.  tcgen05 ops execute in issue order.
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = ptx::idesc_f16(128, kAtTile, false, false);
+            constexpr uint32_t idesc_o = ptx::idesc_f16(128, kAtHP, true, false);
+            // Matrix descriptors computed once: a byte offset o inside shared memory moves the
+            // descriptor's start-address field by o / 16, so every operand below is a base
+            // descriptor plus a constant (the issue loop must stay faster than the tensor pipe).
+            const uint64_t kv_k = ptx::smem_desc(ptx::smem_u32(ring), 16, 1024, ptx::kSwizzle128);   // K-major B
+            const uint64_t kv_mn = ptx::smem_desc(ptx::smem_u32(ring), kAtBoxBytes, 1024, ptx::kSwizzle128);  // MN-major A
+            const uint64_t qt_k = ptx::smem_desc(ptx::smem_u32(q_tail), 16, 1024, ptx::kSwizzle128);
+            const uint64_t p_k = ptx::smem_desc(ptx::smem_u32(p_buf), 16, 1024, ptx::kSwizzle128);
+            const uint32_t d_s = tmem + Cfg::TMEM_S;
+            // Issue order is chosen as the operands become ready: PV(v) as soon as P(v) is written
+            // (it releases its chunks' slots to the producer), S(u) once the softmax has drained
+            // S(u-1) and tile u's chunks are re-encoded.  No other order is needed: the softmax
+            // waits for PV(u-1) itself before it rescales O^T, and PV(u-1) can always be issued
+            // by then (its P was written before the softmax of tile u began).
+            bool ok = ptx::mbar_wait(q_ready, 0);
+            ptx::tc_fence_after();
+            int next_s = 0, next_pv = 0, s_chunk = 0;
+            long long idle_since = clock64();
+            const long long limit = *(volatile long long *)&g_wait_limit_cycles;
+            while (ok && next_pv < n_tiles && !*abort_flag) {
+                bool progressed = false;
+                if (next_pv < next_s && ptx::mbar_test(&p_full[next_pv & 1], (next_pv >> 1) & 1)) {
+                    const int v = next_pv++;
+                    ptx::tc_fence_after();
+                    const uint64_t pb = p_k + (uint64_t)((v & 1) * (kAtPBytes >> 4));
+                    const uint32_t first = v > 0 ? 1u : 0u;
+#pragma unroll
+                    for (int j = 0; j < CC; ++j) {
+                        const int g = v * CC + j, slot = g % kAtSlots;
+                        const uint64_t ad0 = kv_mn + (uint64_t)(slot * (kAtChunkBytes >> 4));
+#pragma unroll
+                        for (int kk = 0; kk < kAtTile / 16; ++kk)
+                            ptx::mma_f16(tmem + Cfg::TMEM_O + j * 64, ad0 + kk * (2048 >> 4), pb + kk * 2, idesc_o,
+                                         kk > 0 ? 1u : first);
+                        ptx::mma_commit(&empty[slot]);
+                    }
+                    ptx::mma_commit(&pv_done[v & 1]);
+                    progressed = true;
+                }
+                // S(next_s) chunk by chunk: each chunk's eight k steps as soon as it is re-encoded
+                if (next_s < n_tiles && (s_chunk > 0 || next_s == 0 || ptx::mbar_test(s_empty, (next_s - 1) & 1))) {
+                    const int u = next_s;
+                    while (s_chunk < CC) {
+                        const int g = u * CC + s_chunk, slot = g % kAtSlots;
+                        if (!ptx::mbar_test(&conv[slot], (g / kAtSlots) & 1)) break;
+                        ptx::tc_fence_after();
+                        const uint64_t bd0 = kv_k + (uint64_t)(slot * (kAtChunkBytes >> 4));
+                        if (s_chunk < CC - 1) {
+                            const uint32_t a0 = tmem + s_chunk * 64;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                ptx::mma_f16_ts(d_s, a0 + kk * 8, bd0 + ((kk >> 2) * (kAtBoxBytes >> 4) + (kk & 3) * 2),
+                                                idesc_s, (s_chunk > 0 || kk > 0) ? 1u : 0u);
+                        } else {
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                ptx::mma_f16(d_s, qt_k + ((kk >> 2) * ((128 * 128) >> 4) + (kk & 3) * 2),
+                                             bd0 + ((kk >> 2) * (kAtBoxBytes >> 4) + (kk & 3) * 2), idesc_s,
+                                             (CC > 1 || kk > 0) ? 1u : 0u);
+                        }
+                        ++s_chunk;
+                        progressed = true;
+                    }
+                    if (s_chunk == CC) {
+                        ptx::mma_commit(s_full);
+                        ++next_s;
+                        s_chunk = 0;
+                    }
+                }
+                if (progressed) {
+                    idle_since = clock64();
+                } else if (clock64() - idle_since > limit) {
+                    raise_error(LCA_DEVERR_TIMEOUT);
+                    ok = false;
+                }
             }
             if (!ok) *abort_flag = 1;
             ptx::mma_commit(teardown);
             ptx::mbar_wait(teardown, 0);
         }
-    } else if (warp == kAtGatherWarp) {
-        // ------------------------------------------------------- second gatherer ----
-        // c box 1 of every gathered chunk, after the producer has seen its slot free (gather_go
-        // is arrived on once per gathered chunk of the slot, so its phases count those alone).
-        uint32_t go_count[kAtSlots] = {};
-        bool ok = true;
-        for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
-            const int t = (int)t0 + u;
-            if (t < tm.tc && !L.idx) continue;   // contiguous tile: the producer loads it alone
-            int rc[4];
-            gather_rows(t, 1, rc);
-            for (int j = 0; j < CC; ++j) {
-                if (!ptx::mbar_wait(&gather_go[j], go_count[j] & 1)) {
-                    ok = false;
-                    break;
-                }
-                ++go_count[j];
-                const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
-                ptx::tma_gather4(ptx::smem_u32(ring + j * kAtChunkBytes) + 128 * 128 + lane * 512, map,
-                                 j * 128 + 64, rc[0], rc[1], rc[2], rc[3], &full[j]);
-            }
-        }
-        if (!ok) *abort_flag = 1;
-    } else if (warp == kAtQWarp) {
-        // ---------------------------------------------------------- query chunks ----
-        // Query chunk j (hi | lo, 32 KB) for every S chunk, in consumption order.
-        if (lane == 0) {
-            const int total = CC * n_tiles;
-            int n = 0;
-            for (; n < total && !*abort_flag; ++n) {
-                const int qs = n % kAtQSlots, j = n % CC;
-                if (n >= kAtQSlots && !ptx::mbar_wait(&q_empty[qs], ((n / kAtQSlots) - 1) & 1)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                ptx::mbar_arrive_expect_tx(&q_full[qs], kAtQChunkBytes);
-                ptx::bulk_load(ptx::smem_u32(q_ring + qs * kAtQChunkBytes), qimg + j * kAtQChunkBytes, kAtQChunkBytes,
-                               &q_full[qs]);
-            }
-            // the last chunk issued into each slot has landed before the CTA exits (bounded)
-            for (int m = n - 1; m >= 0 && m >= n - kAtQSlots; --m)
-                ptx::mbar_wait(&q_full[m % kAtQSlots], (m / kAtQSlots) & 1);
-        }
     } else {
         // -------------------------------------------------------------- softmax ----
-        const int sw = warp - kAtSoftmaxWarp0;       // 0..7
-        const int quarter = warp & 3;                // TMEM lane quarter
-        const int half = sw >> 2;                    // heads [32 half, 32 half + 32)
-        const int r = quarter * 32 + lane;           // row of the tile == TMEM lane
-        const uint32_t lane_addr = tmem + ((uint32_t)(quarter * 32) << 16);
-        float m[32], l[32];
+        // Warp q (lane quarter q) owns query rows 32 q .. 32 q + 31: lane l < 16 the hi part of
+        // head 16 q + l, lane l + 16 its lo part.  Per tile the hi lane takes tile rows 0..31 of
+        // its head and the lo lane rows 32..63, each adding the partner's part.
+        const int q = warp & 3;
+        const int part = lane >> 4;
+        const int h = 16 * q + (lane & 15);
+        const uint32_t lane_base = tmem + ((uint32_t)(32 * q) << 16);
+        bool ok = ptx::mbar_wait(q_full, 0);
+        if (ok) {
+            // the query's TMEM part: this lane's row of image chunks 0 .. CC-2
+            const int row = 32 * q + lane;
+            for (int i = 0; i < CC - 1; ++i) {
+                const uint8_t *img = ring + (kAtSlots - Cfg::Q_STAGE_SLOTS + 2 * i) * kAtChunkBytes;
+                uint32_t v[64];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-        }
-        uint32_t votes_done = 0, reds_done = 0;
-        bool ok = true;
-        bool range_bad = false;                      // a row element outside fp16's range
-        const int ctid = sw * 32 + lane;             // 0..255 among the softmax warps
-        for (int u = 0; u < n_tiles && !*abort_flag; ++u) {
-            // ---- re-encode tile u's KV chunks to fp16 as they land (an eighth per warp).  The
-            // slots were refilled after PV(u-1) released them, which needed this tile's P(u-1).
-            for (int j = 0; j < CC && ok; ++j) {
-                if (!ptx::mbar_wait(&full[j], u & 1)) {
-                    ok = false;
-                    break;
-                }
-                uint4 *chunk = reinterpret_cast<uint4 *>(ring + j * kAtChunkBytes);
+                for (int bx = 0; bx < 2; ++bx)
 #pragma unroll
-                for (int k = 0; k < kAtChunkBytes / 16 / (32 * kAtSoftmaxWarps); ++k) {
-                    uint4 *p = chunk + ctid + k * (32 * kAtSoftmaxWarps);
-                    const uint4 v = *p;
-                    range_bad |= bf16x8_exceeds_f16(v);
-                    *p = bf16x8_to_f16x8(v);
-                }
-                ptx::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&conv[j]);
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 w = *reinterpret_cast<const uint4 *>(img + bx * (128 * 128) + sw128(row, k));
+                        v[bx * 32 + 4 * k + 0] = w.x;
+                        v[bx * 32 + 4 * k + 1] = w.y;
+                        v[bx * 32 + 4 * k + 2] = w.z;
+                        v[bx * 32 + 4 * k + 3] = w.w;
+                    }
+                ptx::tmem_st32(lane_base + i * 64, v);
+                ptx::tmem_st32(lane_base + i * 64 + 32, v + 32);
             }
-            if (!ok || !ptx::mbar_wait(&s_full[0], u & 1)) {
+            ptx::tmem_st_wait();
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+            ptx::mbar_arrive(q_ready);
+            ptx::mbar_arrive(q_free);
+        }
+        float m_run = -INFINITY, l_run = 0.f;
+        for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
+            const int t = (int)t0 + u;
+            if (!ptx::mbar_wait(s_full, u & 1)) {
                 ok = false;
                 break;
             }
             ptx::tc_fence_after();
             float x[32];
             {
-                uint32_t vh[32], vl[32];
-                ptx::tmem_ld32(lane_addr + Cfg::TMEM_S + half * 32, vh);
-                ptx::tmem_ld32(lane_addr + Cfg::TMEM_S + kAtHP + half * 32, vl);
+                uint32_t sv[64];
+                ptx::tmem_ld64(lane_base + Cfg::TMEM_S, sv);
                 ptx::tmem_ld_wait();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(s_empty);   // S may be overwritten by the next tile
+                const uint32_t m0 = __ballot_sync(0xffffffffu, tile_row_valid(a, L, tm, t, lane));
+                const uint32_t m1 = __ballot_sync(0xffffffffu, tile_row_valid(a, L, tm, t, lane + 32));
+                const uint32_t mask = part ? m1 : m0;
 #pragma unroll
-                for (int h = 0; h < 32; ++h) x[h] = __uint_as_float(vh[h]) + __uint_as_float(vl[h]);
+                for (int i = 0; i < 32; ++i) {
+                    // hi lane: own hi[i] + partner's lo[i]; lo lane: own lo[32+i] + partner's hi[32+i]
+                    const float send = __uint_as_float(part ? sv[i] : sv[32 + i]);
+                    const float mine = __uint_as_float(part ? sv[32 + i] : sv[i]);
+                    const float other = __shfl_xor_sync(0xffffffffu, send, 16);
+                    x[i] = ((mask >> i) & 1u) ? (mine + other) * a.scale_log2 : -INFINITY;
+                }
             }
-            ptx::tc_fence_before();
-            const bool valid = tile_row_valid(a, L, tm, (int)t0 + u, r);
-            bool need = false;
+            float mx = x[0];
 #pragma unroll
-            for (int h = 0; h < 32; ++h) {
-                x[h] = valid ? x[h] * a.scale_log2 : -INFINITY;
-                need |= x[h] > m[h] + kAtTau;
+            for (int i = 1; i < 32; ++i) mx = fmaxf(mx, x[i]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            float alpha = 1.f;
+            if (mx > m_run + kAtTau) {
+                alpha = m_run == -INFINITY ? 1.f : exp2f(m_run - mx);
+                m_run = mx;
             }
-            // ---- CTA-wide vote among the softmax warps: does any running max move? ----
-            const int vb = votes_done & 1;
-            const bool warp_need = __any_sync(0xffffffffu, need);
-            if (lane == 0) votes[vb * 8 + sw] = warp_need ? 1 : 0;
+            l_run *= alpha;
+            // ---- the rescale factors of all heads, for every warp's quarter of O^T ----
+            const int vb = u & 1;
+            if (part == 0) alphas[vb * 64 + h] = alpha;
+            const bool moved = __any_sync(0xffffffffu, alpha != 1.f);
+            if (lane == 0) flags[vb * 4 + q] = moved ? 1 : 0;
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(vote_bar);
-            if (!ptx::mbar_wait(vote_bar, votes_done & 1)) {
+            if (!ptx::mbar_wait(vote_bar, u & 1)) {
                 ok = false;
                 break;
             }
-            ++votes_done;
-            int any = 0;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) any |= votes[vb * 8 + w];
-            if (any) {
-                // Exact per-head maxima of this tile over the 128 rows (4 warps per head half).
-                // `red` is single-buffered: every warp has read it before any warp passes the
-                // next vote barrier, and only a vote round leads to the next write.
-#pragma unroll
-                for (int h = 0; h < 32; ++h) {
-                    const float mx = warp_max(x[h]);
-                    if (lane == h) red[sw * 32 + h] = mx;
-                }
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(red_bar);
-                if (!ptx::mbar_wait(red_bar, reds_done & 1)) {
+            const bool any = (flags[vb * 4] | flags[vb * 4 + 1] | flags[vb * 4 + 2] | flags[vb * 4 + 3]) != 0;
+            if (any && u > 0) {
+                // O^T holds heads in columns: rescale once PV(u-1) has completed
+                if (!ptx::mbar_wait(&pv_done[(u - 1) & 1], ((u - 1) >> 1) & 1)) {
                     ok = false;
                     break;
                 }
-                ++reds_done;
-                // O^T: PV of the previous tile completed before S^T of this tile (in-order execution)
-#pragma unroll
-                for (int h0 = 0; h0 < 32; h0 += 16) {
-                    float alpha[16];
-                    bool moved = false;
-#pragma unroll
-                    for (int h = 0; h < 16; ++h) {
-                        float mt = m[h0 + h];
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) mt = fmaxf(mt, red[(half * 4 + w) * 32 + h0 + h]);
-                        const float m_old = m[h0 + h] == -INFINITY ? mt : m[h0 + h];
-                        alpha[h] = mt == -INFINITY ? 1.f : exp2f(m_old - mt);
-                        moved |= alpha[h] != 1.f;
-                        m[h0 + h] = mt;
-                        l[h0 + h] *= alpha[h];
-                    }
-                    if (u > 0 && __any_sync(0xffffffffu, moved)) {
+                ptx::tc_fence_after();
 #pragma unroll 1
-                        for (int j = 0; j < CC; ++j) {
-                            uint32_t v[16];
-                            const uint32_t addr = lane_addr + Cfg::TMEM_O + j * kAtHP + half * 32 + h0;
-                            ptx::tmem_ld16(addr, v);
-                            ptx::tmem_ld_wait();
-#pragma unroll
-                            for (int h = 0; h < 16; ++h) v[h] = __float_as_uint(__uint_as_float(v[h]) * alpha[h]);
-                            ptx::tmem_st16(addr, v);
-                        }
-                        ptx::tmem_st_wait();
-                    }
-                }
-                ptx::tc_fence_before();
-            }
-            // probabilities of this row as an fp16 P^T row (32 heads = 4 chunks); the row sum
-            // adds the rounded values, the weights PV applies.  PV of the previous tile, the last
-            // reader of P^T, completed before S^T of this tile.
-            float pr[32];
-#pragma unroll
-            for (int h = 0; h < 32; ++h) {
-                const float ms = m[h] == -INFINITY ? 0.f : m[h];
-                pr[h] = __half2float(__float2half_rn(exp2f(x[h] - ms)));
-                l[h] += pr[h];
-            }
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4)
-                *reinterpret_cast<uint4 *>(p_buf + ptx::sw128_offset(r, half * 4 + c4)) = pack8_f16(pr + 8 * c4);
-            ptx::fence_proxy_async();
-            ptx::mbar_arrive(&p_full[0]);
-        }
-        if (!ok) *abort_flag = 1;
-        // ---- the split's results: row sums, running max, unnormalised O ----
-        if (ok && !*abort_flag && ptx::mbar_wait(&pv_done[0], (n_tiles - 1) & 1)) {
-            ptx::tc_fence_after();
-            // row sums over the 128 rows; the P buffer is free now (every PV is done)
-            float *lsum = reinterpret_cast<float *>(p_buf);
-#pragma unroll
-            for (int h = 0; h < 32; ++h) {
-                const float s = warp_sum(l[h]);
-                if (lane == h) lsum[sw * 32 + h] = s;
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(red_bar);
-            if (ptx::mbar_wait(red_bar, reds_done & 1)) {
-                if (quarter == 0) {   // one warp per head half writes m and l
-                    const int h = half * 32 + lane;
-                    float s = 0.f;
-#pragma unroll
-                    for (int w = 0; w < 4; ++w) s += lsum[(half * 4 + w) * 32 + lane];
-                    float mv = m[0];
-#pragma unroll
-                    for (int k = 1; k < 32; ++k) mv = lane == k ? m[k] : mv;
-                    if (h < a.H) {
-                        a.part_m[pidx0 + h] = mv;
-                        a.part_l[pidx0 + h] = s;
-                    }
-                }
                 for (int j = 0; j < CC; ++j) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(lane_addr + Cfg::TMEM_O + j * kAtHP + half * 32, v);
+                    uint32_t ov[64];
+                    const uint32_t addr = lane_base + Cfg::TMEM_O + j * 64;
+                    ptx::tmem_ld64(addr, ov);
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) {
-                        const int hh = half * 32 + h;
-                        if (hh < a.H) a.part_o[(pidx0 + hh) * C + j * 128 + r] = __uint_as_float(v[h]);
-                    }
+                    for (int hh = 0; hh < 64; ++hh) ov[hh] = __float_as_uint(__uint_as_float(ov[hh]) * alphas[vb * 64 + hh]);
+                    ptx::tmem_st32(addr, ov);
+                    ptx::tmem_st32(addr + 32, ov + 32);
                 }
+                ptx::tmem_st_wait();
+            }
+            // ---- P(u) into buffer u & 1 once PV(u-2), its last reader, has completed ----
+            if (u >= 2 && !ptx::mbar_wait(&pv_done[u & 1], ((u - 2) >> 1) & 1)) {
+                ok = false;
+                break;
+            }
+            const float ms = m_run == -INFINITY ? 0.f : m_run;
+            float pr[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                pr[i] = __half2float(__float2half_rn(exp2f(x[i] - ms)));
+                l_run += pr[i];
+            }
+            uint8_t *pb = p_buf + (u & 1) * kAtPBytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                *reinterpret_cast<uint4 *>(pb + ptx::sw128_offset(h, 4 * part + k)) = pack8_f16(pr + 8 * k);
+            ptx::fence_proxy_async();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&p_full[u & 1]);
+        }
+        if (!ok) *abort_flag = 1;
+        // ---- the split's results: running max, row sum, unnormalised O ----
+        if (ok && !*abort_flag && ptx::mbar_wait(&pv_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1)) {
+            ptx::tc_fence_after();
+            const float l_tot = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+            if (part == 0 && h < a.H) {
+                a.part_m[pidx0 + h] = m_run;
+                a.part_l[pidx0 + h] = l_tot;
+            }
+#pragma unroll 1
+            for (int j = 0; j < CC; ++j) {
+                uint32_t ov[64];
+                ptx::tmem_ld64(lane_base + Cfg::TMEM_O + j * 64, ov);
+                ptx::tmem_ld_wait();
+                float *dst = a.part_o + pidx0 * C + j * 128 + 32 * q + lane;
+#pragma unroll
+                for (int hh = 0; hh < 64; ++hh)
+                    if (hh < a.H) dst[(int64_t)hh * C] = __uint_as_float(ov[hh]);
             }
             ptx::tc_fence_before();
         }
-        if (__any_sync(0xffffffffu, range_bad) && lane == 0) raise_error(LCA_DEVERR_FP16_RANGE);
     }
     __syncthreads();
     if (warp == kAtMmaWarp) {

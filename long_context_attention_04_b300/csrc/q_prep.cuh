@@ -3,13 +3,14 @@
 // position on the trailing R dims ("Partial RoPE"), then the split q = hi + lo into two fp16
 // parts (DeepSeek-V4 hybrid attention, gxgjx.lffhtl.com/lxrt/355279.html, section 混肃穆力机制).
 //
-// Output: per query, an image of [c/128 chunks][2 boxes of 64 c][128 rows][128 bytes], rows
-// 0-63 the hi parts of heads 0-63 and rows 64-127 their lo parts, 128-byte swizzled (16-byte
-// chunk index XOR row % 8): exactly the shared-memory layout of the K-major B operand the
-// attention kernel feeds to tcgen05.mma (N = 128), so the attention kernel bulk-copies one
-// 32 KB chunk next to each KV chunk it multiplies.  Heads past H are zero rows.  hi + lo
-// carries the normalised query to about 22 bits (fp16 keeps 11 each; the query's elements are
-// at most sqrt(c) max|gamma|, far inside fp16's range).
+// Output: per query, an image of [c/128 chunks][2 boxes of 64 c][128 rows][128 bytes],
+// 128-byte swizzled (16-byte chunk index XOR row % 8): the shared-memory layout of a K-major
+// tcgen05.mma operand with 128 rows.  Row 32 g + i holds the hi part of head 16 g + i and row
+// 32 g + 16 + i its lo part (g < 4, i < 16), so that the two parts of a head land in the same
+// 32-lane quarter of tensor memory, 16 lanes apart, when the attention kernel moves the image
+// there as the A operand of its logit product.  Heads past H are zero rows.  hi + lo carries the
+// normalised query to about 22 bits (fp16 keeps 11 each); an element beyond fp16's range is
+// reported (LCA_DEVERR_FP16_RANGE).
 #pragma once
 
 #include "attend_common.cuh"
@@ -28,6 +29,11 @@ __device__ __forceinline__ uint8_t *q_img(const AttendArgs &a, int64_t unit) {
 
 __host__ __device__ __forceinline__ uint32_t sw128(uint32_t row, uint32_t chunk) {
     return row * 128u + (((chunk ^ (row & 7u)) & 7u) << 4);
+}
+
+// Image row of head h's hi (part 0) or lo (part 1) half.
+__host__ __device__ __forceinline__ uint32_t q_img_row(uint32_t h, uint32_t part) {
+    return 32u * (h >> 4) + 16u * part + (h & 15u);
 }
 
 // grid (units, 64 / kQPrepHeads), block 32 * kQPrepHeads: warp w prepares head blockIdx.y*8 + w.
@@ -72,15 +78,15 @@ __global__ void __launch_bounds__(32 * kQPrepHeads) q_prep_kernel(AttendArgs a) 
         for (int u = 0; u < EPL; u += 8) {
             const int e = lane * EPL + u;
             uint8_t *box = img + (e / 128) * kQChunkBytes + ((e % 128) / 64) * (128 * 128);
-            *reinterpret_cast<uint4 *>(box + sw128(h, (e % 64) / 8)) = pack8_f16(v + u);
-            *reinterpret_cast<uint4 *>(box + sw128(kQImgHeads + h, (e % 64) / 8)) = pack8_f16(lo + u);
+            *reinterpret_cast<uint4 *>(box + sw128(q_img_row(h, 0), (e % 64) / 8)) = pack8_f16(v + u);
+            *reinterpret_cast<uint4 *>(box + sw128(q_img_row(h, 1), (e % 64) / 8)) = pack8_f16(lo + u);
         }
     } else {
         const int e = lane * EPL;   // 4 elements: half a 16-byte chunk
         uint8_t *box = img + (e / 128) * kQChunkBytes + ((e % 128) / 64) * (128 * 128) + (e % 8) * 2;
-        *reinterpret_cast<uint2 *>(box + sw128(h, (e % 64) / 8)) =
+        *reinterpret_cast<uint2 *>(box + sw128(q_img_row(h, 0), (e % 64) / 8)) =
             make_uint2(pack_f16x2(v[0], v[1]), pack_f16x2(v[2], v[3]));
-        *reinterpret_cast<uint2 *>(box + sw128(kQImgHeads + h, (e % 64) / 8)) =
+        *reinterpret_cast<uint2 *>(box + sw128(q_img_row(h, 1), (e % 64) / 8)) =
             make_uint2(pack_f16x2(lo[0], lo[1]), pack_f16x2(lo[2], lo[3]));
     }
 }
