@@ -273,7 +273,11 @@ lca_status hca_attend_noalloc(const lca_attn_params *p, int batch, int n_q,
  * before kernels issued earlier on the stream have finished (o and mid are read only after
  * them): the weights must not be written by work still pending on the stream.
  * lca_gemm_bf16 is the plain product it is built from: C[M][N] = A[M][K] . B[N][K]^T
- * (fp32 accumulation, bf16 out), M <= 16 (activations), B the weight rows.
+ * (fp32 accumulation, bf16 out, B the weight rows).  M <= 16 (decode activations) runs on
+ * the CUDA cores, streaming B once; larger M (a prefill chunk's input projections) on the
+ * tensor cores in 128 x 64/128/256 tiles.
+ * lca_gemm_bf16_f32 is the tensor-core product with fp32 C, any M.  A and B rows are
+ * 16-byte aligned with strides (elements) multiples of 8; K a multiple of 8.
  * ------------------------------------------------------------------------------- */
 lca_status lca_grouped_oproj(int batch, int heads, int head_dim, int groups, int d_g, int d_model,
                              const lca_bf16 *o, const lca_bf16 *Wg, const lca_bf16 *Wm,
@@ -281,6 +285,9 @@ lca_status lca_grouped_oproj(int batch, int heads, int head_dim, int groups, int
 lca_status lca_gemm_bf16(int M, int N, int K, const lca_bf16 *A, int64_t lda,
                          const lca_bf16 *B, int64_t ldb, lca_bf16 *C, int64_t ldc,
                          cudaStream_t stream);
+lca_status lca_gemm_bf16_f32(int M, int N, int K, const lca_bf16 *A, int64_t lda,
+                             const lca_bf16 *B, int64_t ldb, float *C, int64_t ldc,
+                             cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
  * Diagnostics.

@@ -312,7 +312,8 @@ def lca_grouped_oproj(o, Wg, Wm, groups: int, mid, y, stream=None):
 
 
 def lca_gemm_bf16(A, B, C, stream=None):
-    """C[M, N] = A[M, K] . B[N, K]^T (bf16 in/out, fp32 accumulation)."""
+    """C[M, N] = A[M, K] . B[N, K]^T (bf16 in, fp32 accumulation; C bf16, or fp32 through
+    lca_gemm_bf16_f32)."""
     M, K = A.shape
     N = B.shape[0]
     if B.dim() != 2 or B.shape[1] != K:
@@ -322,9 +323,15 @@ def lca_gemm_bf16(A, B, C, stream=None):
     for t, n in ((A, "A"), (B, "B"), (C, "C")):
         if t.stride(1) != 1:
             raise ValueError("%s must have unit stride along its rows" % n)
-    st = _lib.load().lca_gemm_bf16(M, N, K, _ptr(A, torch.bfloat16, "A"), A.stride(0),
-                                   _ptr(B, torch.bfloat16, "B"), B.stride(0), _ptr(C, torch.bfloat16, "C"),
+    lib = _lib.load()
+    if C.dtype == torch.float32:
+        st = lib.lca_gemm_bf16_f32(M, N, K, _ptr(A, torch.bfloat16, "A"), A.stride(0),
+                                   _ptr(B, torch.bfloat16, "B"), B.stride(0), _ptr(C, torch.float32, "C"),
                                    C.stride(0), _stream(stream))
+    else:
+        st = lib.lca_gemm_bf16(M, N, K, _ptr(A, torch.bfloat16, "A"), A.stride(0),
+                               _ptr(B, torch.bfloat16, "B"), B.stride(0), _ptr(C, torch.bfloat16, "C"),
+                               C.stride(0), _stream(stream))
     _check(st)
 
 

@@ -18,6 +18,7 @@
 #include "attend_common.cuh"
 #include "attend_tc.cuh"
 #include "gemv.cuh"
+#include "gemm_tc.cuh"
 
 using namespace lca;
 
@@ -821,15 +822,74 @@ lca_status hca_attend_noalloc(const lca_attn_params *p, int batch, int n_q, cons
                        win_batch_stride, win_cap, sink, out, lse, scratch, kNoAllocScratchBytes, stream);
 }
 
-lca_status lca_gemm_bf16(int M, int N, int K, const lca_bf16 *A, int64_t lda, const lca_bf16 *B, int64_t ldb,
-                         lca_bf16 *C, int64_t ldc, cudaStream_t stream) {
-    const char *name = "lca_gemm_bf16";
-    LCA_REQUIRE(M >= 1 && M <= 16 && N >= 1 && K >= 8 && K % 8 == 0, LCA_ERR_UNSUPPORTED,
-                "%s: need 1 <= M <= 16, N >= 1, K a positive multiple of 8 (M=%d N=%d K=%d)", name, M, N, K);
+// The tensor-core product: 128-row tiles of C, BN = 64, 128 or 256 columns by N.
+static lca_status gemm_tc_launch(const char *name, int M, int N, int K, const lca_bf16 *A, int64_t lda,
+                                 const lca_bf16 *B, int64_t ldb, void *C, int64_t ldc, bool f32_out,
+                                 cudaStream_t stream) {
+    const int BN = N <= 64 ? 64 : N <= 128 ? 128 : 256;
+    CUtensorMap a_map, b_map;
+    const uint64_t ad[2] = {(uint64_t)K, (uint64_t)M}, bd[2] = {(uint64_t)K, (uint64_t)N};
+    const uint64_t as[1] = {(uint64_t)lda * 2}, bs[1] = {(uint64_t)ldb * 2};
+    const uint32_t abox[2] = {(uint32_t)kGtBK, (uint32_t)kGtBM}, bbox[2] = {(uint32_t)kGtBK, (uint32_t)BN};
+    if (!make_tensor_map(&a_map, A, 2, ad, as, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&b_map, B, 2, bd, bs, bbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
+    GemmTcArgs g;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.C = C;
+    g.ldc = ldc;
+    const dim3 grid((unsigned)((N + BN - 1) / BN), (unsigned)((M + kGtBM - 1) / kGtBM));
+#define LCA_GEMM_TC(BNV, F32)                                                                                      \
+    do {                                                                                                           \
+        cudaFuncSetAttribute(gemm_tc_kernel<BNV, F32>, cudaFuncAttributeMaxDynamicSharedMemorySize,                \
+                             GemmTcConfig<BNV>::SMEM_BYTES);                                                       \
+        launch_pdl(gemm_tc_kernel<BNV, F32>, grid, dim3(kGtThreads), GemmTcConfig<BNV>::SMEM_BYTES, stream, a_map, \
+                   b_map, g);                                                                                      \
+    } while (0)
+    if (f32_out) {
+        if (BN == 64) LCA_GEMM_TC(64, true);
+        else if (BN == 128) LCA_GEMM_TC(128, true);
+        else LCA_GEMM_TC(256, true);
+    } else {
+        if (BN == 64) LCA_GEMM_TC(64, false);
+        else if (BN == 128) LCA_GEMM_TC(128, false);
+        else LCA_GEMM_TC(256, false);
+    }
+#undef LCA_GEMM_TC
+    return check_launch(name);
+}
+
+static lca_status gemm_validate(const char *name, int M, int N, int K, const void *A, int64_t lda, const void *B,
+                                int64_t ldb, const void *C, int64_t ldc) {
+    LCA_REQUIRE(M >= 1 && N >= 1 && K >= 8 && K % 8 == 0, LCA_ERR_UNSUPPORTED,
+                "%s: need M, N >= 1 and K a positive multiple of 8 (M=%d N=%d K=%d)", name, M, N, K);
     LCA_REQUIRE(A && B && C, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
     LCA_REQUIRE(aligned16(A) && aligned16(B) && lda % 8 == 0 && ldb % 8 == 0 && lda >= K && ldb >= K && ldc >= N,
                 LCA_ERR_INVALID_ARG, "%s: A and B must be 16-byte aligned with strides >= K, multiples of 8", name);
-    lca_status st = gemv_launch(name, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, stream);
+    return LCA_OK;
+}
+
+lca_status lca_gemm_bf16(int M, int N, int K, const lca_bf16 *A, int64_t lda, const lca_bf16 *B, int64_t ldb,
+                         lca_bf16 *C, int64_t ldc, cudaStream_t stream) {
+    const char *name = "lca_gemm_bf16";
+    lca_status st = gemm_validate(name, M, N, K, A, lda, B, ldb, C, ldc);
+    if (st != LCA_OK) return st;
+    if (M <= 16) {
+        st = gemv_launch(name, M, N, K, A, lda, 0, B, ldb, 0, C, ldc, 0, 1, stream);
+    } else {
+        st = gemm_tc_launch(name, M, N, K, A, lda, B, ldb, C, ldc, false, stream);
+    }
+    return st == LCA_OK ? ok() : st;
+}
+
+lca_status lca_gemm_bf16_f32(int M, int N, int K, const lca_bf16 *A, int64_t lda, const lca_bf16 *B, int64_t ldb,
+                             float *C, int64_t ldc, cudaStream_t stream) {
+    const char *name = "lca_gemm_bf16_f32";
+    lca_status st = gemm_validate(name, M, N, K, A, lda, B, ldb, C, ldc);
+    if (st != LCA_OK) return st;
+    st = gemm_tc_launch(name, M, N, K, A, lda, B, ldb, C, ldc, true, stream);
     return st == LCA_OK ? ok() : st;
 }
 

@@ -104,7 +104,9 @@ def test_compress_and_indexer_reject_bad_arguments(lib):
 
 
 def test_projection_rejects_bad_arguments(lib):
-    assert lib.lca_gemm_bf16(17, 8, 64, FAKE, 64, FAKE, 64, FAKE, 8, None) == 2     # M > 16
+    assert lib.lca_gemm_bf16(0, 8, 64, FAKE, 64, FAKE, 64, FAKE, 8, None) == 2      # M = 0
+    assert lib.lca_gemm_bf16(17, 8, 64, FAKE, 60, FAKE, 64, FAKE, 8, None) == 1     # lda % 8
+    assert lib.lca_gemm_bf16_f32(17, 8, 64, FAKE, 64, FAKE, 64, None, 8, None) == 1  # NULL C
     assert lib.lca_gemm_bf16(4, 8, 60, FAKE, 64, FAKE, 64, FAKE, 8, None) == 2      # K % 8
     assert lib.lca_grouped_oproj(4, 64, 512, 7, 1024, 4096, FAKE, FAKE, FAKE, FAKE, FAKE, None) == 1
     assert lib.lca_status_string(3) == b"workspace too small"

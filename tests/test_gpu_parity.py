@@ -504,3 +504,24 @@ def test_attend_reports_values_outside_fp16(where):
     api.hca_attend(p, dev(d["q"]), dev(d["gamma"]), dev(pos), dev(d["kv"]), dev(d["win"]), dev(d["sink"]), out, ws)
     err = api.lca_device_error()
     assert err == (0 if where == "none" else 0x10), hex(err)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 100, 200), (128, 64, 64), (1000, 300, 1024), (257, 513, 4096),
+                                   (17, 24, 16384), (640, 256, 136)])
+def test_tensor_core_gemm_matches_oracle(M, N, K):
+    """The tensor-core product (M > 16 for bf16 out, any M for fp32 out): ragged M, N and K tails,
+    every tile width (N up to 64, 128, 256)."""
+    rng = Rng(30)
+    A = rng.normal_bf16((M, K))
+    Bm = rng.normal_bf16((N, K), 0.05)
+    ref = oracle.gemm_bf16(u16(A), u16(Bm))
+    C32 = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    api.lca_gemm_bf16(dev(A), dev(Bm), C32)
+    assert api.lca_device_error() == 0
+    got = C32.cpu().numpy().astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=2e-6 * rms * math.sqrt(K))
+    if M > 16:
+        C16 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+        api.lca_gemm_bf16(dev(A), dev(Bm), C16)
+        assert_close_bf16_out(C16.cpu().float().numpy(), ref, what="gemm %dx%dx%d" % (M, N, K))
