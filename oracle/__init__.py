@@ -60,6 +60,12 @@ def _load():
         lib.orc_attend.restype = I
         lib.orc_gemm_bf16.argtypes = [L, L, L, P, P, P]
         lib.orc_gemm_bf16.restype = None
+        lib.orc_mhc_coeffs.argtypes = [I, L, I, P, P, P, P, P, P]
+        lib.orc_mhc_coeffs.restype = None
+        lib.orc_mhc_pre.argtypes = [I, L, P, P, P]
+        lib.orc_mhc_pre.restype = None
+        lib.orc_mhc_post.argtypes = [I, L, P, P, P, P, P]
+        lib.orc_mhc_post.restype = None
         lib.orc_grouped_oproj.argtypes = [I, I, I, I, I, P, P, P, P]
         lib.orc_grouped_oproj.restype = I
         _lib = lib
@@ -195,3 +201,46 @@ def grouped_oproj(o, Wg, Wm, groups):
     if rc != 0:
         raise ValueError("orc_grouped_oproj: heads not divisible by groups")
     return y
+
+
+def mhc_coeffs(x, phi, bias, iters=20):
+    """Generated hyper-connection coefficients of one token (manifold-constrained hyper-
+    connections): x uint16 [n, d], phi uint16 [2n + n*n, n*d], bias float32 [2n + n*n] ->
+    (a [n], c [n], B [n, n]) in float64: sigmoid pre and post weights and the Sinkhorn-Knopp
+    projection of exp(z) onto the doubly stochastic matrices (iters row-then-column passes)."""
+    lib = _load()
+    x = _u16(x)
+    phi = _u16(phi)
+    b = _f32(bias)
+    n, d = x.shape
+    assert phi.shape == (2 * n + n * n, n * d) and b.shape == (2 * n + n * n,)
+    a = np.empty(n, np.float64)
+    c = np.empty(n, np.float64)
+    B = np.empty((n, n), np.float64)
+    lib.orc_mhc_coeffs(n, d, iters, _ptr(x), _ptr(phi), _ptr(b), _ptr(a), _ptr(c), _ptr(B))
+    return a, c, B
+
+
+def mhc_pre(x, a):
+    """The layer input h = sum_i a_i x[i] of one token (x uint16 [n, d], a float64 [n])."""
+    lib = _load()
+    x = _u16(x)
+    n, d = x.shape
+    a = np.ascontiguousarray(a, np.float64)
+    h = np.empty(d, np.float64)
+    lib.orc_mhc_pre(n, d, _ptr(x), _ptr(a), _ptr(h))
+    return h
+
+
+def mhc_post(x, B, c, y):
+    """The streams after the layer, x'[i] = sum_j B[i, j] x[j] + c_i y (x uint16 [n, d],
+    B float64 [n, n], c float64 [n], y uint16 [d]) -> float64 [n, d]."""
+    lib = _load()
+    x = _u16(x)
+    y = _u16(y)
+    n, d = x.shape
+    B = np.ascontiguousarray(B, np.float64)
+    c = np.ascontiguousarray(c, np.float64)
+    xo = np.empty((n, d), np.float64)
+    lib.orc_mhc_post(n, d, _ptr(x), _ptr(B), _ptr(c), _ptr(y), _ptr(xo))
+    return xo

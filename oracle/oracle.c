@@ -369,3 +369,82 @@ int orc_grouped_oproj(int H, int c, int G, int d_g, int d_model,
     free(mid);
     return 0;
 }
+
+/*
+ * Manifold-constrained hyper-connections ([P1] section "mHC，给残差集结加层连续"; [P4] section
+ * 3.2 "mHC"): the residual stream is widened to n parallel streams x[i] (i < n, width d) and
+ * each layer mixes them with three maps: A (n weights that form the layer's input), B (an n x n
+ * mixing of the streams) and C (n weights that spread the layer's output back over the
+ * streams).  The maps are generated per token from the input (an input-dependent linear part
+ * plus an input-independent bias); A and C pass through a sigmoid (non-negative, bounded); B is
+ * projected onto the doubly stochastic matrices (rows and columns summing to 1) by the
+ * Sinkhorn-Knopp iteration, row and column normalisations taken in turn, 20 times on the page.
+ * Readings (the pages give no formula): z = flatten(x) . Phi^T + bias with Phi holding one row
+ * of n*d weights per generated value, in the order a (n values), c (n values), B (n*n, row-major);
+ * B starts from exp(z) (a positive matrix, as Sinkhorn-Knopp requires); one iteration is a row
+ * normalisation followed by a column normalisation; the layer input is h = sum_i a_i x[i]; after
+ * the layer, x'[i] = sum_j B[i][j] x[j] + c_i y with y the layer's output.
+ */
+
+/* The generated coefficients of one token: a[n], c[n] (sigmoids) and B[n*n] (Sinkhorn-Knopp). */
+void orc_mhc_coeffs(int n, long d, int iters, const uint16_t *x, const uint16_t *phi, const float *bias,
+                    double *a, double *c, double *B)
+{
+    const long nd = (long)n * d;
+    const int K = 2 * n + n * n;
+    double *z = (double *)malloc(sizeof(double) * (size_t)K);
+    if (!z)
+        return;
+    for (int k = 0; k < K; ++k) {
+        double s = 0.0;
+        for (long f = 0; f < nd; ++f)
+            s += bf16_bits_to_double(x[f]) * bf16_bits_to_double(phi[(size_t)k * (size_t)nd + (size_t)f]);
+        z[k] = s + (double)bias[k];
+    }
+    for (int i = 0; i < n; ++i) {
+        a[i] = 1.0 / (1.0 + exp(-z[i]));
+        c[i] = 1.0 / (1.0 + exp(-z[n + i]));
+    }
+    for (int e = 0; e < n * n; ++e)
+        B[e] = exp(z[2 * n + e]);
+    for (int it = 0; it < iters; ++it) {
+        for (int i = 0; i < n; ++i) {           /* rows */
+            double s = 0.0;
+            for (int j = 0; j < n; ++j)
+                s += B[i * n + j];
+            for (int j = 0; j < n; ++j)
+                B[i * n + j] /= s;
+        }
+        for (int j = 0; j < n; ++j) {           /* columns */
+            double s = 0.0;
+            for (int i = 0; i < n; ++i)
+                s += B[i * n + j];
+            for (int i = 0; i < n; ++i)
+                B[i * n + j] /= s;
+        }
+    }
+    free(z);
+}
+
+/* The layer input of one token: h[e] = sum_i a[i] x[i][e]. */
+void orc_mhc_pre(int n, long d, const uint16_t *x, const double *a, double *h)
+{
+    for (long e = 0; e < d; ++e) {
+        double s = 0.0;
+        for (int i = 0; i < n; ++i)
+            s += a[i] * bf16_bits_to_double(x[(size_t)i * (size_t)d + (size_t)e]);
+        h[e] = s;
+    }
+}
+
+/* The streams after the layer: xo[i][e] = sum_j B[i][j] x[j][e] + c[i] y[e]. */
+void orc_mhc_post(int n, long d, const uint16_t *x, const double *B, const double *c, const uint16_t *y, double *xo)
+{
+    for (int i = 0; i < n; ++i)
+        for (long e = 0; e < d; ++e) {
+            double s = c[i] * bf16_bits_to_double(y[e]);
+            for (int j = 0; j < n; ++j)
+                s += B[i * n + j] * bf16_bits_to_double(x[(size_t)j * (size_t)d + (size_t)e]);
+            xo[(size_t)i * (size_t)d + (size_t)e] = s;
+        }
+}

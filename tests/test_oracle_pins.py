@@ -558,3 +558,102 @@ def test_gemm_matches_numpy():
     A = rand_bits(rng, (7, 33))
     B = rand_bits(rng, (5, 33))
     np.testing.assert_allclose(oracle.gemm_bf16(A, B), from_bits(A) @ from_bits(B).T, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------- manifold-constrained hyper-connections ----
+# The mHC section of the first page (and [P4] 3.2): a, c through a sigmoid, B projected onto the
+# doubly stochastic matrices by Sinkhorn-Knopp (row and column normalisations in turn).
+
+def _mhc_inputs(rng, n, d, z_target=None):
+    """x and phi chosen so that z = flatten(x) . phi^T + bias is known: phi = 0 gives z = bias."""
+    x = rand_bits(rng, (n, d))
+    phi = np.zeros((2 * n + n * n, n * d), np.uint16)
+    bias = np.asarray(z_target, np.float32) if z_target is not None else rng.standard_normal(2 * n + n * n).astype(
+        np.float32)
+    return x, phi, bias
+
+
+def test_mhc_generated_logits_and_sigmoids_match_numpy():
+    rng = np.random.default_rng(60)
+    n, d = 4, 48
+    x = rand_bits(rng, (n, d))
+    phi = rand_bits(rng, (2 * n + n * n, n * d), 0.1)
+    bias = rng.standard_normal(2 * n + n * n).astype(np.float32)
+    a, c, B = oracle.mhc_coeffs(x, phi, bias, iters=0)
+    z = from_bits(phi) @ from_bits(x).reshape(-1) + bias.astype(np.float64)
+    np.testing.assert_allclose(a, 1.0 / (1.0 + np.exp(-z[:n])), rtol=1e-13)
+    np.testing.assert_allclose(c, 1.0 / (1.0 + np.exp(-z[n:2 * n])), rtol=1e-13)
+    # with no iteration B is exp(z) of the last n*n values, row-major
+    np.testing.assert_allclose(B, np.exp(z[2 * n:]).reshape(n, n), rtol=1e-13)
+
+
+def test_sinkhorn_equal_logits_give_uniform_matrix():
+    rng = np.random.default_rng(61)
+    n = 4
+    x, phi, bias = _mhc_inputs(rng, n, 16, np.full(2 * n + n * n, 0.7))
+    _, _, B = oracle.mhc_coeffs(x, phi, bias, iters=1)
+    np.testing.assert_allclose(B, np.full((n, n), 1.0 / n), rtol=1e-15)
+
+
+def test_sinkhorn_columns_exact_rows_converge():
+    rng = np.random.default_rng(62)
+    n = 4
+    x, phi, bias = _mhc_inputs(rng, n, 16)
+    _, _, B = oracle.mhc_coeffs(x, phi, bias, iters=20)
+    np.testing.assert_allclose(B.sum(0), 1.0, atol=1e-14)          # the last pass normalises columns
+    assert np.abs(B.sum(1) - 1.0).max() < 1e-6                     # rows have converged
+    assert (B > 0).all()
+    # one row pass alone leaves rows summing to one; more passes keep B doubly stochastic
+    _, _, B1 = oracle.mhc_coeffs(x, phi, bias, iters=60)
+    np.testing.assert_allclose(B1.sum(1), 1.0, atol=1e-13)
+
+
+def test_sinkhorn_2x2_limit_closed_form():
+    """For a positive 2 x 2 matrix [[p, q], [r, s]] the Sinkhorn-Knopp limit is [[t, 1-t], [1-t, t]]
+    with t / (1 - t) = sqrt(p s / (q r))."""
+    rng = np.random.default_rng(63)
+    n = 2
+    zB = np.array([0.3, -1.1, 0.8, 0.2])
+    x, phi, bias = _mhc_inputs(rng, n, 8, np.concatenate([np.zeros(4), zB]))
+    _, _, B = oracle.mhc_coeffs(x, phi, bias, iters=200)
+    p, q, r, s = np.exp(zB)
+    ratio = math.sqrt(p * s / (q * r))
+    t = ratio / (1.0 + ratio)
+    np.testing.assert_allclose(B, [[t, 1 - t], [1 - t, t]], atol=1e-12)
+
+
+def test_sinkhorn_ignores_a_row_scaling_of_its_input():
+    """Adding a constant to one row of logits multiplies that row of exp(z) by a constant, which
+    the first row normalisation removes: the result is the same for any iteration count."""
+    rng = np.random.default_rng(64)
+    n = 4
+    x, phi, bias = _mhc_inputs(rng, n, 16)
+    shifted = bias.copy()
+    shifted[2 * n + 2 * n: 2 * n + 3 * n] += 1.5                     # row 2 of B
+    for iters in (1, 3, 20):
+        _, _, B0 = oracle.mhc_coeffs(x, phi, bias, iters=iters)
+        _, _, B1 = oracle.mhc_coeffs(x, phi, shifted, iters=iters)
+        np.testing.assert_allclose(B0, B1, rtol=1e-6)
+    # a column shift is not removed after one pass (rows first), so the test can tell them apart
+    col = bias.copy()
+    col[2 * n + 1::n] += 1.5
+    _, _, Bc = oracle.mhc_coeffs(x, phi, col, iters=1)
+    _, _, B0 = oracle.mhc_coeffs(x, phi, bias, iters=1)
+    assert np.abs(Bc - B0).max() > 1e-3
+
+
+def test_mhc_pre_selects_a_stream_and_post_preserves_the_stream_sum():
+    rng = np.random.default_rng(65)
+    n, d = 4, 32
+    x = rand_bits(rng, (n, d))
+    # a: stream 1 fully on, the others off (sigmoid at +-60)
+    a = 1.0 / (1.0 + np.exp(-np.array([-60.0, 60.0, -60.0, -60.0])))
+    np.testing.assert_allclose(oracle.mhc_pre(x, a), from_bits(x[1]), atol=1e-20)
+    # post: with B doubly stochastic (columns summing to one), the sum over streams is the input
+    # streams' sum plus (sum of c) * y
+    _, c, B = oracle.mhc_coeffs(*_mhc_inputs(rng, n, d), iters=20)
+    y = rand_bits(rng, (d,))
+    xo = oracle.mhc_post(x, B, c, y)
+    np.testing.assert_allclose(xo.sum(0), from_bits(x).sum(0) + c.sum() * from_bits(y), atol=1e-12)
+    # and each stream is the textbook mixing
+    np.testing.assert_allclose(xo, B @ from_bits(x) + np.outer(c, from_bits(y)), atol=1e-12)
