@@ -674,8 +674,81 @@ class BlockDecode(Workload):
                            % (t2 - t0, n_csa, n_hca))
 
 
+class MhcLayer(Workload):
+    """Manifold-constrained hyper-connections around one layer: the coefficients and layer input
+    (lca_mhc_pre), then, given the layer's output, the new residual streams (lca_mhc_post)."""
+
+    def __init__(self, cfg: dict, seed: int = 0, stage: bool = True):
+        from long_context_attention_04_b300 import api
+        self.api = api
+        self.cfg = cfg
+        T, n, d = cfg["T"], cfg["n"], cfg["d"]
+        self.T, self.n, self.dim, self.iters = T, n, d, cfg["iters"]
+        rng = wl.Rng(seed, device="cuda")
+        self.d = wl.mhc_inputs(rng, T, n, d)
+        dv = dict(device="cuda")
+        self.h = torch.empty((T, d), dtype=torch.bfloat16, **dv)
+        self.a = torch.empty((T, n), dtype=torch.float32, **dv)
+        self.c = torch.empty((T, n), dtype=torch.float32, **dv)
+        self.B = torch.empty((T, n, n), dtype=torch.float32, **dv)
+        self.x_out = torch.empty((T, n, d), dtype=torch.bfloat16, **dv)
+        self.ws = torch.empty(api.lca_mhc_workspace(T, n), dtype=torch.uint8, **dv)
+        self.tokens = T
+        self.launches = 3          # generated-logit product, pre mixing (with Sinkhorn-Knopp), post mixing
+        self.dominant = "mhc pre + post"
+        self._stage_inputs(("x", "y"), stage)
+        self.host_out = torch.empty(self.x_out.shape, dtype=torch.bfloat16).pin_memory()
+        self.h2d_bytes = sum(t.numel() * t.element_size() for t in self.host_in.values())
+        self.d2h_bytes = self.x_out.numel() * self.x_out.element_size()
+        K = 2 * n + n * n
+        # algorithmic bytes: each of the two calls reads the streams once (the layer runs in
+        # between), the generating weights once, the layer output once; h and the new streams
+        # are written once (the generated logits are a workspace round trip)
+        self.step_bytes = float(T * (2 * n * d * 2 + d * 2 + d * 2 + n * d * 2 + (2 * n + n * n) * 4)
+                                + K * n * d * 2)
+        self.step_flops = 2.0 * T * K * n * d
+        self.dom_bytes, self.dom_flops = self.step_bytes, self.step_flops
+
+    def step(self):
+        d, api = self.d, self.api
+        api.lca_mhc_pre(d["x"], d["phi"], d["bias"], self.h, self.a, self.c, self.B, self.ws, iters=self.iters)
+        api.lca_mhc_post(d["x"], self.B, self.c, d["y"], self.x_out)
+
+    def dominant_call(self):
+        self.step()
+
+    def e2e_step(self):
+        self.stage.upload()
+        self.step()
+        self.host_out.copy_(self.x_out, non_blocking=True)
+
+    def snapshot_host(self):
+        self.host = {k: self.d[k].cpu() for k in ("phi", "bias")}
+
+    def cpu_sample(self, budget_s: float) -> dict:
+        import oracle
+        from workloads import bf16_bits
+        phi = bf16_bits(self.host["phi"])
+        bias = self.host["bias"].numpy()
+        t_total, n_done = 0.0, 0
+        for t in range(self.T):
+            x = bf16_bits(self.host_in["x"][t])
+            y = bf16_bits(self.host_in["y"][t])
+            t0 = time.perf_counter()
+            a, c, B = oracle.mhc_coeffs(x, phi, bias, iters=self.iters)
+            oracle.mhc_pre(x, a)
+            oracle.mhc_post(x, B, c, y)
+            t_total += time.perf_counter() - t0
+            n_done += 1
+            if t_total >= budget_s:
+                break
+        return dict(value=n_done / t_total, unit="tokens/s", cores=1, kind="oracle",
+                    sample="%d of %d tokens (coefficients, layer input, new streams), single-threaded fp64"
+                           % (n_done, self.T))
+
+
 WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill,
-             "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode}
+             "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode, "mhc_prefill_8192": MhcLayer}
 
 
 # ------------------------------------------------------------------- distributed -----
@@ -842,9 +915,10 @@ def measure(name: str, args, flush, world: int, device, rank: int, seed: int, sn
 
 
 # Target configurations timed beside the headline workload (one process, one GPU): HCA decode at
-# 1M context (HBM-bound), the 8192-query CSA prefill chunk at 1M (tensor-bound), and the block of
-# 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound).
-EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "block_decode_1m")
+# 1M context (HBM-bound), the 8192-query CSA prefill chunk at 1M (tensor-bound), the block of
+# 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound), and the hyper-connection
+# mixing around a layer for an 8192-token chunk (HBM-bound).
+EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "block_decode_1m", "mhc_prefill_8192")
 
 
 def run_ours(args):
@@ -1006,10 +1080,21 @@ class _HostOnly:
         import oracle
         from workloads import bf16_bits
         self.oracle = oracle
-        s = cfg["shape"]
+        s = cfg.get("shape")
         self.s = s
         rng = wl.Rng(seed)
         self.kind = name
+        if name.startswith("mhc"):       # hyper-connections of one token: coefficients, pre, post
+            n, d = cfg["n"], cfg["d"]
+            K = 2 * n + n * n
+            self.iters = cfg["iters"]
+            self.x = bf16_bits(rng.normal_bf16((n, d)))
+            self.y = bf16_bits(rng.normal_bf16((d,)))
+            self.phi = bf16_bits(rng.normal_bf16((K, n * d), 1.0 / math.sqrt(n * d)))
+            self.bias = rng.normal_f32((K,)).numpy()
+            self.sample = "coefficients (Sinkhorn-Knopp, %d passes), layer input and new streams of one token" \
+                % self.iters
+            return
         if name.startswith("csa_"):      # a CSA layer: compression, indexer, top-k, attention
             entries = cfg["entries"]
             pos = cfg.get("pos", cfg.get("q_begin", 0) + cfg.get("Tq", 1) - 1)
@@ -1037,6 +1122,12 @@ class _HostOnly:
         self.sink = rng.normal_f32((s.heads,)).numpy()
 
     def one_unit(self):
+        if self.kind.startswith("mhc"):
+            o = self.oracle
+            a, c, B = o.mhc_coeffs(self.x, self.phi, self.bias, iters=self.iters)
+            o.mhc_pre(self.x, a)
+            o.mhc_post(self.x, B, c, self.y)
+            return
         o, s = self.oracle, self.s
         span = 2 * s.ratio if self.kind != "hca_decode_1m" else s.ratio
         bias = np.zeros(span, np.float32)

@@ -290,6 +290,31 @@ lca_status lca_gemm_bf16_f32(int M, int N, int K, const lca_bf16 *A, int64_t lda
                              cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * Manifold-constrained hyper-connections ([P1] section "mHC", [P4] 3.2): the residual stream
+ * is n parallel streams of width d.  Per token, the layer's coefficients are generated from
+ * its input, z = flatten(x) . phi^T + bias (an input-dependent linear part and an input-
+ * independent bias), read in the order a (n values), c (n values), B (n x n, row-major):
+ *   a_i = sigmoid(z_i), c_i = sigmoid(z_{n+i}) (non-negative and bounded),
+ *   B = Sinkhorn-Knopp(exp(z_B)): `iters` passes (20 on the page), each normalising the rows
+ *       to sum 1 and then the columns, so B is doubly stochastic (columns exactly, rows to
+ *       the iteration's convergence).
+ * lca_mhc_pre writes the coefficients and the layer input h = sum_i a_i x[i]; after the layer
+ * (output y), lca_mhc_post writes the new streams x_out[i] = sum_j B[i][j] x[j] + c_i y.
+ *   x, x_out [T][n][d] bf16;  phi [2n + n^2][n d] bf16;  bias [2n + n^2] fp32;
+ *   h, y [T][d] bf16;  a, c [T][n] fp32;  b_mix [T][n][n] fp32.
+ * Supported: n in {1, 2, 4}, d a multiple of 8 up to 65536, iters in [1, 1000].  Arithmetic in
+ * fp32 (z accumulated in fp32 on the tensor cores).  lca_mhc_workspace returns the workspace
+ * lca_mhc_pre needs: 0 bytes in this version (z stays in tensor memory); the workspace
+ * arguments are accepted for a later version that needs one.
+ * ------------------------------------------------------------------------------- */
+size_t lca_mhc_workspace(int T, int n);
+lca_status lca_mhc_pre(int T, int n, int d, int iters, const lca_bf16 *x, const lca_bf16 *phi,
+                       const float *bias, lca_bf16 *h, float *a, float *c, float *b_mix,
+                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
+lca_status lca_mhc_post(int T, int n, int d, const lca_bf16 *x, const float *b_mix, const float *c,
+                        const lca_bf16 *y, lca_bf16 *x_out, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------------- */
 const char *lca_status_string(lca_status s);

@@ -54,6 +54,9 @@ SIGNATURES = {
     "lca_grouped_oproj": ([c_int, c_int, c_int, c_int, c_int, c_int, V, V, V, V, V, V], c_int),
     "lca_gemm_bf16": ([c_int, c_int, c_int, V, c_int64, V, c_int64, V, c_int64, V], c_int),
     "lca_gemm_bf16_f32": ([c_int, c_int, c_int, V, c_int64, V, c_int64, V, c_int64, V], c_int),
+    "lca_mhc_workspace": ([c_int, c_int], c_size_t),
+    "lca_mhc_pre": ([c_int, c_int, c_int, c_int, V, V, V, V, V, V, V, V, c_size_t, V], c_int),
+    "lca_mhc_post": ([c_int, c_int, c_int, V, V, V, V, V, V], c_int),
     "lca_status_string": ([c_int], ctypes.c_char_p),
     "lca_last_error": ([], ctypes.c_char_p),
     "lca_device_error": ([V, ctypes.POINTER(ctypes.c_uint32)], c_int),

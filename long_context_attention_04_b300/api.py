@@ -335,6 +335,46 @@ def lca_gemm_bf16(A, B, C, stream=None):
     _check(st)
 
 
+def lca_mhc_workspace(T: int, n: int) -> int:
+    return int(_lib.load().lca_mhc_workspace(T, n))
+
+
+def lca_mhc_pre(x, phi, bias, h, a, c, b_mix, workspace, iters: int = 20, stream=None):
+    """Hyper-connection coefficients of every token (a, c sigmoids; b_mix by Sinkhorn-Knopp) and
+    the layer input h = sum_i a_i x[i]; x [T, n, d] bf16, phi [2n + n^2, n d] bf16."""
+    if x.dim() != 3 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [T, n, d] tensor")
+    T, n, d = x.shape
+    K = 2 * n + n * n
+    _holds(phi, K * n * d, "phi", exact=True)
+    _holds(bias, K, "bias", exact=True)
+    _holds(h, T * d, "h", exact=True)
+    _holds(a, T * n, "a", exact=True)
+    _holds(c, T * n, "c", exact=True)
+    _holds(b_mix, T * n * n, "b_mix", exact=True)
+    st = _lib.load().lca_mhc_pre(T, n, d, int(iters), _ptr(x, torch.bfloat16, "x"), _ptr(phi, torch.bfloat16, "phi"),
+                                 _ptr(bias, torch.float32, "bias"), _ptr(h, torch.bfloat16, "h"),
+                                 _ptr(a, torch.float32, "a"), _ptr(c, torch.float32, "c"),
+                                 _ptr(b_mix, torch.float32, "b_mix"), _ptr(workspace, None, "workspace"),
+                                 workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+
+
+def lca_mhc_post(x, b_mix, c, y, x_out, stream=None):
+    """The streams after the layer: x_out[:, i] = sum_j b_mix[:, i, j] x[:, j] + c[:, i] y."""
+    if x.dim() != 3 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous [T, n, d] tensor")
+    T, n, d = x.shape
+    _holds(b_mix, T * n * n, "b_mix", exact=True)
+    _holds(c, T * n, "c", exact=True)
+    _holds(y, T * d, "y", exact=True)
+    _holds(x_out, T * n * d, "x_out", exact=True)
+    st = _lib.load().lca_mhc_post(T, n, d, _ptr(x, torch.bfloat16, "x"), _ptr(b_mix, torch.float32, "b_mix"),
+                                  _ptr(c, torch.float32, "c"), _ptr(y, torch.bfloat16, "y"),
+                                  _ptr(x_out, torch.bfloat16, "x_out"), _stream(stream))
+    _check(st)
+
+
 def lca_device_error(stream=None) -> int:
     """Synchronise the stream, read and clear the device error word; returns the word."""
     w = ctypes.c_uint32(0)

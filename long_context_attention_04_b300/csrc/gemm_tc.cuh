@@ -13,10 +13,13 @@
 // epilogue warps (one per TMEM lane quarter) read the accumulator and store fp32 or bf16
 // rows.  Out-of-range rows and K columns of a tile are read as zeros by the TMA unit and
 // out-of-range outputs are not stored, so M, N and K need no padding (K a multiple of 8:
-// 16-byte rows).  Every wait is bounded (LCA_DEVERR_TIMEOUT).
+// 16-byte rows).  Every wait is bounded (LCA_DEVERR_TIMEOUT).  With MHC_N > 0 the product is
+// the hyper-connections' generated values (N = 2n + n^2 <= 32 columns) and the epilogue turns
+// each token row into its coefficients (mhc_coeffs_thread) instead of storing it.
 #pragma once
 
 #include "common.cuh"
+#include "mhc.cuh"
 #include "ptx.cuh"
 
 namespace lca {
@@ -39,9 +42,10 @@ struct GemmTcArgs {
     int M, N, K;
     void *C;                // fp32 or bf16 rows of ldc elements
     int64_t ldc;
+    MhcCoeffArgs mhc;       // MHC_N > 0 only
 };
 
-template <int BN, bool F32_OUT>
+template <int BN, bool F32_OUT, int MHC_N = 0>
 __global__ void __launch_bounds__(kGtThreads) gemm_tc_kernel(const __grid_constant__ CUtensorMap a_map,
                                                            const __grid_constant__ CUtensorMap b_map, GemmTcArgs g) {
     using Cfg = GemmTcConfig<BN>;
@@ -124,6 +128,13 @@ __global__ void __launch_bounds__(kGtThreads) gemm_tc_kernel(const __grid_consta
         if (ptx::mbar_wait(acc_full, 0)) {
             ptx::tc_fence_after();
             const int row = m0 + 32 * q + lane;
+            if constexpr (MHC_N > 0) {
+                // one token per row: its 2n + n^2 generated values are columns 0 .. 31 of the tile
+                uint32_t v[32];
+                ptx::tmem_ld32(tmem + ((uint32_t)(32 * q) << 16), v);
+                ptx::tmem_ld_wait();
+                if (row < g.M) mhc_coeffs_thread<MHC_N>(v, row, g.mhc);
+            } else
 #pragma unroll 1
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 uint32_t v[32];

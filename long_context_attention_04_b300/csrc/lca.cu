@@ -19,6 +19,7 @@
 #include "attend_tc.cuh"
 #include "gemv.cuh"
 #include "gemm_tc.cuh"
+#include "mhc.cuh"
 
 using namespace lca;
 
@@ -890,6 +891,109 @@ lca_status lca_gemm_bf16_f32(int M, int N, int K, const lca_bf16 *A, int64_t lda
     lca_status st = gemm_validate(name, M, N, K, A, lda, B, ldb, C, ldc);
     if (st != LCA_OK) return st;
     st = gemm_tc_launch(name, M, N, K, A, lda, B, ldb, C, ldc, true, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+// ---- manifold-constrained hyper-connections ----
+static lca_status mhc_validate(const char *name, int T, int n, int d) {
+    LCA_REQUIRE(T >= 1, LCA_ERR_INVALID_ARG, "%s: T must be positive", name);
+    LCA_REQUIRE(n == 1 || n == 2 || n == 4, LCA_ERR_UNSUPPORTED, "%s: n = %d streams not in {1, 2, 4}", name, n);
+    LCA_REQUIRE(d >= 8 && d % 8 == 0 && d <= 65536, LCA_ERR_UNSUPPORTED,
+                "%s: d = %d must be a multiple of 8 in [8, 65536]", name, d);
+    return LCA_OK;
+}
+
+size_t lca_mhc_workspace(int T, int n) {
+    (void)T;
+    (void)n;
+    return 0;   // the generated values stay in the product's tensor memory
+}
+
+lca_status lca_mhc_pre(int T, int n, int d, int iters, const lca_bf16 *x, const lca_bf16 *phi, const float *bias,
+                       lca_bf16 *h, float *a, float *c, float *b_mix, void *workspace, size_t workspace_bytes,
+                       cudaStream_t stream) {
+    const char *name = "lca_mhc_pre";
+    (void)workspace;
+    (void)workspace_bytes;
+    lca_status st = mhc_validate(name, T, n, d);
+    if (st != LCA_OK) return st;
+    LCA_REQUIRE(iters >= 1 && iters <= 1000, LCA_ERR_INVALID_ARG, "%s: iters = %d not in [1, 1000]", name, iters);
+    LCA_REQUIRE(x && phi && bias && h && a && c && b_mix, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(x) && aligned16(phi) && aligned16(h), LCA_ERR_INVALID_ARG,
+                "%s: x, phi and h must be 16-byte aligned", name);
+    // the generated values and, in the product's epilogue, the coefficients
+    const int K = 2 * n + n * n, nd = n * d;
+    CUtensorMap a_map, b_map;
+    const uint64_t ad[2] = {(uint64_t)nd, (uint64_t)T}, bd[2] = {(uint64_t)nd, (uint64_t)K};
+    const uint64_t st_row[1] = {(uint64_t)nd * 2};
+    const uint32_t abox[2] = {(uint32_t)kGtBK, (uint32_t)kGtBM}, bbox[2] = {(uint32_t)kGtBK, 64u};
+    if (!make_tensor_map(&a_map, x, 2, ad, st_row, abox, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tensor_map(&b_map, phi, 2, bd, st_row, bbox, CU_TENSOR_MAP_SWIZZLE_128B))
+        return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
+    GemmTcArgs g = {};
+    g.M = T;
+    g.N = K;
+    g.K = nd;
+    g.mhc.bias = bias;
+    g.mhc.a = a;
+    g.mhc.c = c;
+    g.mhc.B = b_mix;
+    g.mhc.iters = iters;
+    const dim3 grid(1, (unsigned)((T + kGtBM - 1) / kGtBM));
+    constexpr int smem = GemmTcConfig<64>::SMEM_BYTES;
+    switch (n) {
+    case 1:
+        cudaFuncSetAttribute(gemm_tc_kernel<64, true, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        launch_pdl(gemm_tc_kernel<64, true, 1>, grid, dim3(kGtThreads), smem, stream, a_map, b_map, g);
+        break;
+    case 2:
+        cudaFuncSetAttribute(gemm_tc_kernel<64, true, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        launch_pdl(gemm_tc_kernel<64, true, 2>, grid, dim3(kGtThreads), smem, stream, a_map, b_map, g);
+        break;
+    default:
+        cudaFuncSetAttribute(gemm_tc_kernel<64, true, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        launch_pdl(gemm_tc_kernel<64, true, 4>, grid, dim3(kGtThreads), smem, stream, a_map, b_map, g);
+        break;
+    }
+    st = check_launch(name);
+    if (st != LCA_OK) return st;
+    MhcMixArgs m = {};
+    m.d = d;
+    m.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    m.a = a;
+    m.h = reinterpret_cast<__nv_bfloat16 *>(h);
+    const dim3 mgrid((unsigned)ceil_div64(d / 8, kMhcThreads), (unsigned)T);
+    switch (n) {
+    case 1: launch_pdl(mhc_pre_mix_kernel<1>, mgrid, dim3(kMhcThreads), 0, stream, m); break;
+    case 2: launch_pdl(mhc_pre_mix_kernel<2>, mgrid, dim3(kMhcThreads), 0, stream, m); break;
+    default: launch_pdl(mhc_pre_mix_kernel<4>, mgrid, dim3(kMhcThreads), 0, stream, m); break;
+    }
+    st = check_launch(name);
+    return st == LCA_OK ? ok() : st;
+}
+
+lca_status lca_mhc_post(int T, int n, int d, const lca_bf16 *x, const float *b_mix, const float *c, const lca_bf16 *y,
+                        lca_bf16 *x_out, cudaStream_t stream) {
+    const char *name = "lca_mhc_post";
+    lca_status st = mhc_validate(name, T, n, d);
+    if (st != LCA_OK) return st;
+    LCA_REQUIRE(x && b_mix && c && y && x_out, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(x) && aligned16(y) && aligned16(x_out), LCA_ERR_INVALID_ARG,
+                "%s: x, y and x_out must be 16-byte aligned", name);
+    MhcMixArgs m = {};
+    m.d = d;
+    m.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    m.B = b_mix;
+    m.c = c;
+    m.y = reinterpret_cast<const __nv_bfloat16 *>(y);
+    m.x_out = reinterpret_cast<__nv_bfloat16 *>(x_out);
+    const dim3 mgrid((unsigned)ceil_div64(d / 8, kMhcThreads), (unsigned)T);
+    switch (n) {
+    case 1: launch_pdl(mhc_post_kernel<1>, mgrid, dim3(kMhcThreads), 0, stream, m); break;
+    case 2: launch_pdl(mhc_post_kernel<2>, mgrid, dim3(kMhcThreads), 0, stream, m); break;
+    default: launch_pdl(mhc_post_kernel<4>, mgrid, dim3(kMhcThreads), 0, stream, m); break;
+    }
+    st = check_launch(name);
     return st == LCA_OK ? ok() : st;
 }
 

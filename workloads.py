@@ -112,6 +112,13 @@ BLOCK_DECODE_1M = dict(
     n_csa=8, n_hca=8, groups=8, d_g=1024, d_model=4096,
     csa=LayerShape(ratio=4, topk=512), hca=LayerShape(ratio=128))
 
+# Manifold-constrained hyper-connections around one layer, for a prefill chunk: 4 residual
+# streams of the V4-Flash hidden size (4096), the generated coefficients (Sinkhorn-Knopp, 20
+# passes), the layer input and, given the layer's output, the new streams.
+MHC_PREFILL_8192 = dict(
+    name="mHC around one layer, 8192 tokens, 4 streams x 4096, Sinkhorn-Knopp 20 passes",
+    kind="mhc", T=8192, n=4, d=4096, iters=20)
+
 WORKLOADS = {
     "tiny_csa_prefill": TINY_CSA_PREFILL,
     "csa_decode_128k": CSA_DECODE_128K,
@@ -119,6 +126,7 @@ WORKLOADS = {
     "csa_prefill_1m": CSA_PREFILL_1M,
     "csa_prefill_128k": CSA_PREFILL_128K,
     "block_decode_1m": BLOCK_DECODE_1M,
+    "mhc_prefill_8192": MHC_PREFILL_8192,
 }
 
 
@@ -226,3 +234,12 @@ def oproj_weights(rng: Rng, heads: int, head_dim: int, groups: int, d_g: int, d_
         Wg=rng.normal_bf16((groups * d_g, (heads // groups) * head_dim), 0.02),
         Wm=rng.normal_bf16((d_model, groups * d_g), 0.02),
     )
+
+
+def mhc_inputs(rng: Rng, T: int, n: int, d: int) -> dict:
+    """Residual streams x [T, n, d] and the layer's output y [T, d] (N(0, 1), bf16); the generating
+    weights phi [2n + n^2, n d] (N(0, 1/(n d)), bf16: unit-scale generated logits) and bias
+    [2n + n^2] (N(0, 1), fp32)."""
+    K = 2 * n + n * n
+    return dict(x=rng.normal_bf16((T, n, d)), y=rng.normal_bf16((T, d)),
+                phi=rng.normal_bf16((K, n * d), 1.0 / math.sqrt(n * d)), bias=rng.normal_f32((K,)))
