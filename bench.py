@@ -674,6 +674,54 @@ class BlockDecode(Workload):
                            % (t2 - t0, n_csa, n_hca))
 
 
+class CsaPrefillProj(CsaPrefill):
+    """The CSA prefill chunk preceded by its input projections: the hidden states of the chunk's
+    staging tokens (m before the chunk, then the chunk) mapped on the tensor cores to the KV and
+    indexer-key token vectors and compressor logits, and those of the chunk's queries to the
+    queries, indexer queries and indexer head weights; then the layer as in CsaPrefill."""
+
+    def __init__(self, cfg: dict, seed: int = 0, stage: bool = True):
+        super().__init__(cfg, seed, stage=False)
+        s, hid, m = self.s, cfg["hidden"], self.s.ratio
+        rng = wl.Rng(seed + 7919, device="cuda")
+        n_tok = self.Tq + m
+        self.hid = hid
+        self.x = rng.normal_bf16((n_tok, hid))
+        self.W = wl.prefill_projection_weights(rng, s, hid)
+        d = self.d
+        # the projections write straight into the layer's per-step input buffers
+        self.proj = [
+            (self.x, self.W["W_kv"], d["tok_v"].view(n_tok, s.head_dim)),
+            (self.x, self.W["W_z"], d["tok_z"].view(n_tok, 1)),
+            (self.x, self.W["W_ki"], d["tok_vi"].view(n_tok, s.idx_dim)),
+            (self.x, self.W["W_zi"], d["tok_zi"].view(n_tok, 1)),
+            (self.x[m:], self.W["W_q"], d["q"].view(self.Tq, s.heads * s.head_dim)),
+            (self.x[m:], self.W["W_qi"], d["q_idx"].view(self.Tq, s.idx_heads * s.idx_dim)),
+            (self.x[m:], self.W["W_w"], d["w_idx"].view(self.Tq, s.idx_heads)),
+        ]
+        self.launches += len(self.proj)
+        self.stage = None
+        self.host_in = {"x": self.x.cpu().pin_memory()}
+        self.h2d_bytes = self.x.numel() * self.x.element_size()
+        proj_flops = 2.0 * hid * (n_tok * (s.head_dim + 1 + s.idx_dim + 1) +
+                                  self.Tq * (s.heads * s.head_dim + s.idx_heads * s.idx_dim + s.idx_heads))
+        self.step_flops += proj_flops
+        self.step_bytes += float(self.x.numel() * 2 + sum(w.numel() * 2 for w in self.W.values()))
+
+    def project(self):
+        for A, Wm, C in self.proj:
+            self.api.lca_gemm_bf16(A, Wm, C)
+
+    def step(self):
+        self.project()
+        super().step()
+
+    def e2e_step(self):
+        self.x.copy_(self.host_in["x"], non_blocking=True)
+        self.step()
+        self.host_out.copy_(self.out, non_blocking=True)
+
+
 class MhcLayer(Workload):
     """Manifold-constrained hyper-connections around one layer: the coefficients and layer input
     (lca_mhc_pre), then, given the layer's output, the new residual streams (lca_mhc_post)."""
@@ -748,7 +796,8 @@ class MhcLayer(Workload):
 
 
 WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill,
-             "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode, "mhc_prefill_8192": MhcLayer}
+             "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode, "mhc_prefill_8192": MhcLayer,
+             "v4flash_decode_1m": BlockDecode, "csa_prefill_1m_proj": CsaPrefillProj}
 
 
 # ------------------------------------------------------------------- distributed -----
@@ -916,9 +965,11 @@ def measure(name: str, args, flush, world: int, device, rank: int, seed: int, sn
 
 # Target configurations timed beside the headline workload (one process, one GPU): HCA decode at
 # 1M context (HBM-bound), the 8192-query CSA prefill chunk at 1M (tensor-bound), the block of
-# 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound), and the hyper-connection
-# mixing around a layer for an 8192-token chunk (HBM-bound).
-EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "block_decode_1m", "mhc_prefill_8192")
+# 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound), the hyper-connection
+# mixing around a layer for an 8192-token chunk (HBM-bound), the 43-layer V4-Flash attention
+# stack at decode (HBM-bound), and the prefill chunk with its input projections (tensor-bound).
+EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "block_decode_1m", "mhc_prefill_8192", "v4flash_decode_1m",
+                   "csa_prefill_1m_proj")
 
 
 def run_ours(args):

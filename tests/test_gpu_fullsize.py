@@ -14,7 +14,7 @@ import torch
 
 import bench
 import oracle
-from helpers import assert_close_rms, assert_rows_close, check_topk, round_bf16_bits
+from helpers import assert_close_bf16_out, assert_close_rms, assert_rows_close, check_topk, round_bf16_bits
 from long_context_attention_04_b300 import api, build as lca_build
 from workloads import WORKLOADS, bf16_bits
 
@@ -184,3 +184,25 @@ def test_csa_prefill_1m_sampled_queries():
             assert_close_rms(_host(wk.out[0, i]).float().numpy(), ro, what="prefill out query %d" % t)
             compared += 1
     assert compared >= len(samples) - 1
+
+
+def test_prefill_input_projections_sampled_rows():
+    """The 1M prefill chunk's input projections (tensor-core products of the 8192 + m staging
+    tokens' hidden states, width 4096) at the benchmark's shapes: sampled rows of every projected
+    tensor against the oracle's product of the same rows."""
+    wk = bench.CsaPrefillProj(WORKLOADS["csa_prefill_1m_proj"], seed=0)
+    wk.project()
+    torch.cuda.synchronize()
+    assert api.lca_device_error() == 0
+    x = bf16_bits(_host(wk.x))
+    m = wk.s.ratio
+    for A, Wm, C in wk.proj:
+        row0 = 0 if A.data_ptr() == wk.x.data_ptr() else m
+        got = _host(C).float().numpy()
+        Wb = bf16_bits(_host(Wm))
+        for r in (0, 1, 4097, C.shape[0] - 1):
+            ref = oracle.gemm_bf16(x[row0 + r:row0 + r + 1], Wb)[0]
+            if C.dtype == torch.float32:
+                np.testing.assert_allclose(got[r], ref, rtol=1e-5, atol=1e-4 * max(1e-30, float(np.abs(ref).max())))
+            else:
+                assert_close_bf16_out(got[r], ref, what="projection row %d" % r)

@@ -112,6 +112,23 @@ BLOCK_DECODE_1M = dict(
     n_csa=8, n_hca=8, groups=8, d_g=1024, d_model=4096,
     csa=LayerShape(ratio=4, topk=512), hca=LayerShape(ratio=128))
 
+# The whole V4-Flash attention stack at decode: 43 layers, CSA and HCA alternating (CSA first:
+# 22 CSA + 21 HCA), each with its grouped output projection, batch 4 at 1M context.
+V4FLASH_DECODE_1M = dict(
+    name="V4-Flash attention stack decode, batch 4, 1M context, 43 layers (22 CSA k=512 + 21 HCA alternating), "
+         "grouped O-proj 64 heads -> 8 x 1024 -> 4096",
+    kind="block_decode", B=4, pos=1048575, csa_entries=262144, hca_entries=8192,
+    n_csa=22, n_hca=21, groups=8, d_g=1024, d_model=4096,
+    csa=LayerShape(ratio=4, topk=512), hca=LayerShape(ratio=128))
+
+# The 1M-context CSA prefill chunk with its input projections: the chunk's hidden states
+# (V4-Flash width 4096) mapped to the queries, indexer queries and weights, and the KV and
+# indexer-key token vectors and compressor logits by plain linear maps (the pages do not give
+# the projections; the tiny configuration's reading) on the tensor cores, then the layer.
+CSA_PREFILL_1M_PROJ = dict(CSA_PREFILL_1M, hidden=4096,
+                           name="CSA chunked prefill with input projections from hidden 4096, 8192 queries at 1M "
+                                "context (262144 entries), k=1024, W=128, H=64")
+
 # Manifold-constrained hyper-connections around one layer, for a prefill chunk: 4 residual
 # streams of the V4-Flash hidden size (4096), the generated coefficients (Sinkhorn-Knopp, 20
 # passes), the layer input and, given the layer's output, the new streams.
@@ -127,6 +144,8 @@ WORKLOADS = {
     "csa_prefill_128k": CSA_PREFILL_128K,
     "block_decode_1m": BLOCK_DECODE_1M,
     "mhc_prefill_8192": MHC_PREFILL_8192,
+    "v4flash_decode_1m": V4FLASH_DECODE_1M,
+    "csa_prefill_1m_proj": CSA_PREFILL_1M_PROJ,
 }
 
 
@@ -243,3 +262,19 @@ def mhc_inputs(rng: Rng, T: int, n: int, d: int) -> dict:
     K = 2 * n + n * n
     return dict(x=rng.normal_bf16((T, n, d)), y=rng.normal_bf16((T, d)),
                 phi=rng.normal_bf16((K, n * d), 1.0 / math.sqrt(n * d)), bias=rng.normal_f32((K,)))
+
+
+def prefill_projection_weights(rng: Rng, s: LayerShape, hidden: int) -> dict:
+    """Plain linear maps from the hidden state (N(0, 0.02), bf16), one weight row per output:
+    queries (H c), KV token vector (c), compressor logit (1), indexer queries (H_I d_I), indexer
+    key vector (d_I), its compressor logit (1), indexer head weights (H_I)."""
+    std = 0.02
+    return dict(
+        W_q=rng.normal_bf16((s.heads * s.head_dim, hidden), std),
+        W_kv=rng.normal_bf16((s.head_dim, hidden), std),
+        W_z=rng.normal_bf16((1, hidden), std),
+        W_qi=rng.normal_bf16((s.idx_heads * s.idx_dim, hidden), std),
+        W_ki=rng.normal_bf16((s.idx_dim, hidden), std),
+        W_zi=rng.normal_bf16((1, hidden), std),
+        W_w=rng.normal_bf16((s.idx_heads, hidden), std),
+    )
