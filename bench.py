@@ -1066,7 +1066,7 @@ def oracle_units(workload: str, seed: int):
     """One token of `workload` for the oracle on synthetic host inputs of the workload's shapes:
     (object with one_unit() and sample, tokens a unit stands for)."""
     cfg = wl.WORKLOADS[workload]
-    if workload == "block_decode_1m":
+    if cfg["kind"] == "block_decode":
         # one token through one CSA and one HCA layer per step, scaled to the block's layer count
         parts = [_HostOnly("csa_decode_128k", dict(entries=cfg["csa_entries"], pos=cfg["pos"], shape=cfg["csa"]),
                            seed),
@@ -1160,6 +1160,11 @@ class _HostOnly:
             self.qi = bf16_bits(rng.normal_bf16((s.idx_heads, s.idx_dim)))
             self.wi = (rng.normal_f32((s.idx_heads,)) / math.sqrt(s.idx_heads)).numpy()
             self.sample = "compression, window row, indexer over %d entries, top-%d, attention" % (entries, s.topk)
+            self.proj = None
+            if "hidden" in cfg:         # the token's input projections come first
+                self.proj = {k: bf16_bits(v) for k, v in wl.prefill_projection_weights(rng, s, cfg["hidden"]).items()}
+                self.x_row = bf16_bits(rng.normal_bf16((1, cfg["hidden"])))
+                self.sample = "input projections from hidden %d, " % cfg["hidden"] + self.sample
         else:
             entries = cfg["entries"]
             self.pos = cfg["pos"]
@@ -1173,6 +1178,9 @@ class _HostOnly:
         self.sink = rng.normal_f32((s.heads,)).numpy()
 
     def one_unit(self):
+        if getattr(self, "proj", None):
+            for W in self.proj.values():
+                self.oracle.gemm_bf16(self.x_row, W)
         if self.kind.startswith("mhc"):
             o = self.oracle
             a, c, B = o.mhc_coeffs(self.x, self.phi, self.bias, iters=self.iters)
