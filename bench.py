@@ -9,6 +9,7 @@ attention with split-K combine.  Workloads (sizes of the pages' V4-Flash configu
   hca_decode_1m              batch 16, 1M context, one query per sequence
   csa_prefill_1m             one 8192-query chunk at 1M context
   csa_prefill_128k           one 2048-query chunk at 128K context (the same kernels, profiler-sized)
+  csa_prefill_1m_scored      the 1M chunk with its scores written out and selected by a separate top-k
 Inputs are seeded synthetic tensors (workloads.py); the caches are larger than L2 and L2 is
 also flushed between timed steps.  Under torchrun each rank runs the workload on its own
 GPU (sequences shard with no exchange: weak scaling); the value is all ranks' tokens over
@@ -471,10 +472,17 @@ class CsaPrefill(Workload):
         self.new_pos = torch.tensor([q_begin], **i32)
         self.q_pos = torch.arange(q_begin, q_begin + Tq, **i32).view(1, Tq)
         self.out = torch.empty((1, Tq, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
-        self.scores = self.layer.ws_idx.view(torch.float32).view(1, Tq, -1)
         self.tokens = Tq
-        self.launches = 8          # 2 compress, window, indexer, top-k, q prep, attention, combine
-        self.dominant = "indexer"
+        # the fused indexer selects the top k as its scores stream; the materialised variant
+        # writes the scores and selects them in a separate pass
+        self.materialise = bool(cfg.get("materialise"))
+        if self.materialise:
+            self.scores = torch.empty((1, Tq, entries), dtype=torch.float32, device="cuda")
+            self.launches = 8      # 2 compress, window, indexer, top-k, q prep, attention, combine
+            self.dominant = "indexer"
+        else:
+            self.launches = 7      # 2 compress, window, indexer with its top-k, q prep, attention, combine
+            self.dominant = "indexer with top-k"
         self.bound = "tensor"
         self._stage_inputs(("tok_v", "tok_z", "tok_vi", "tok_zi", "q", "q_idx", "w_idx"), stage)
         self.host_out = torch.empty(self.out.shape, dtype=torch.bfloat16).pin_memory()
@@ -485,16 +493,27 @@ class CsaPrefill(Workload):
         self.dom_bytes = entries * s.idx_dim * 2 + Tq * s.idx_heads * (s.idx_dim * 2 + 4)
         self.step_bytes, self.step_flops = csa_layer_work(s, 1, n_vis, Tq, entries=entries)
 
+    def _select(self):
+        L, d = self.layer, self.d
+        if self.materialise:
+            self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
+            self.api.lca_topk(self.p, self.scores, self.q_pos, self.entries, L.idx)
+        else:
+            L.select(d["q_idx"], d["w_idx"], self.q_pos)
+
     def dominant_call(self):
-        d = self.d
-        self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], self.layer.idx_cache, self.q_pos, self.scores)
+        # the indexer: with its top-k (fused), or writing the scores (materialised)
+        if self.materialise:
+            d = self.d
+            self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], self.layer.idx_cache, self.q_pos, self.scores)
+        else:
+            self._select()
 
     def step(self):
-        api, L, d = self.api, self.layer, self.d
+        L, d = self.layer, self.d
         L.compress(d["tok_v"], d["tok_z"], d["tok_vi"], d["tok_zi"], self.tok_pos0, self.first, self.Tq // self.s.ratio)
         L.window(d["tok_v"][:, self.s.ratio:], self.new_pos)
-        api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
-        api.lca_topk(self.p, self.scores, self.q_pos, self.entries, L.idx)
+        self._select()
         L.attend(d["q"], self.q_pos, self.out)
 
     def e2e_step(self):
@@ -797,7 +816,8 @@ class MhcLayer(Workload):
 
 WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill,
              "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode, "mhc_prefill_8192": MhcLayer,
-             "v4flash_decode_1m": BlockDecode, "csa_prefill_1m_proj": CsaPrefillProj}
+             "v4flash_decode_1m": BlockDecode, "csa_prefill_1m_proj": CsaPrefillProj,
+             "csa_prefill_1m_scored": CsaPrefill}
 
 
 # ------------------------------------------------------------------- distributed -----
@@ -968,8 +988,8 @@ def measure(name: str, args, flush, world: int, device, rank: int, seed: int, sn
 # 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound), the hyper-connection
 # mixing around a layer for an 8192-token chunk (HBM-bound), the 43-layer V4-Flash attention
 # stack at decode (HBM-bound), and the prefill chunk with its input projections (tensor-bound).
-EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "block_decode_1m", "mhc_prefill_8192", "v4flash_decode_1m",
-                   "csa_prefill_1m_proj")
+EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "csa_prefill_1m_scored", "block_decode_1m", "mhc_prefill_8192",
+                   "v4flash_decode_1m", "csa_prefill_1m_proj")
 
 
 def run_ours(args):

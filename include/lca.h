@@ -65,6 +65,9 @@ typedef enum lca_status {
                                          * the normalised, rotated query, outside fp16's finite
                                          * range (|x| > 65504, inf, nan): the products saturate
                                          * there, so that call's outputs are not accurate */
+#define LCA_DEVERR_SELECT         0x20u /* indexer with top-k: a candidate would not fit its
+                                         * buffer and was dropped (a selection fault; the
+                                         * query's list is then not exact) */
 #define LCA_DEVERR_TIMEOUT        0x100u /* a bounded wait inside a kernel ran out */
 
 /* Layer parameters (names follow the pages' notation). */

@@ -16,11 +16,21 @@
 //   warp 0     TMA producer: query tile per (sequence, query group) (two buffers when the key
 //              ring keeps 6 stages beside them), key tiles into a ring
 //   warp 1     TMEM allocator and MMA issuer (one thread), 2-4 accumulator buffers
-//   warps 2..  epilogue: TMEM -> registers, weighted ReLU sum per query, fp32 score store
+//   warps 2..  epilogue: TMEM -> registers, weighted ReLU sum per query, fp32 score store.
+//              With N = 256 (two accumulator buffers) the 8 epilogue warps form two sets of
+//              4 (a warp group each), set s reading the tiles of buffer s (every other computed
+//              tile): one set's TMEM reads overlap the other set's arithmetic, each set has two
+//              MMA periods per tile, and 10 warps leave 168 registers a thread.  Within a set a
+//              warp group owns COLS_PER_WG columns (whole queries).
+// With FUSE (prefill: 4 queries per tile) the epilogue selects each query's top k as the
+// scores stream (topk_stream.cuh) instead of storing them: every CTA takes whole query
+// groups, so a query's whole row passes through one selection group (the two warp groups,
+// one per set, that score its columns).
 // Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds.
 #pragma once
 
 #include "ptx.cuh"
+#include "topk_stream.cuh"
 
 namespace lca {
 
@@ -35,9 +45,13 @@ struct IndexerTcArgs {
     const int32_t *q_pos;       // [B][n_q]
     float *scores;              // [B][n_q][stride]
     int64_t stride;
+    // fused selection (FUSE): k per query, the ascending lists, the candidate buffers
+    int k;
+    int32_t *out_idx;           // [B][n_q][k]
+    uint2 *cand;                // [grid][2 groups][2 queries][2 buffers][kStCap] (key, index)
 };
 
-template <int DI, int HI, int QPT>
+template <int DI, int HI, int QPT, bool FUSE = false>
 struct IndexerTcConfig {
     static constexpr int N = HI * QPT;                       // MMA N: columns per tile
     static constexpr int BOX = DI < 64 ? DI : 64;            // elements per TMA box row
@@ -48,14 +62,25 @@ struct IndexerTcConfig {
     static constexpr int KSTEPS = DI / 16;
     static constexpr int TILE_BYTES = 128 * DI * 2;          // one key tile
     static constexpr int Q_BYTES = N * DI * 2;               // one query tile
+    // epilogue warps: two sets of 4 at N = 256 (set s reads accumulator buffer s), one set of
+    // 8 at N = 128, of 4 below
     static constexpr int EPI_WARPS = N > 64 ? 8 : 4;
+    static constexpr int SETS = N >= 256 ? 2 : 1;
+    static constexpr int WG_PER_SET = EPI_WARPS / 4 / SETS;  // warp groups per set
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    static constexpr int COLS_PER_WG = N / (EPI_WARPS / 4);  // columns one epilogue warp group owns
+    static constexpr int COLS_PER_WG = N / WG_PER_SET;       // columns one epilogue warp group owns
+    static constexpr int QW = COLS_PER_WG / HI;              // queries one warp group scores
     // accumulator buffers in TMEM: the MMA runs up to ACC_BUFS tiles ahead of the epilogue
     static constexpr int ACC_BUFS = 4 * N <= 512 ? 4 : 2;
     static constexpr int TMEM_COLS = ACC_BUFS * N <= 32 ? 32 : ACC_BUFS * N <= 64 ? 64 : ACC_BUFS * N <= 128 ? 128
                                    : ACC_BUFS * N <= 256 ? 256 : 512;
-    static constexpr int SMEM_LIMIT = 227 * 1024;
+    // fused selection: one selection group per warp group of a set (the same columns in both
+    // sets), two candidate buffers per query
+    static constexpr int ST_BYTES = FUSE ? (int)((WG_PER_SET * sizeof(StreamWg) + 1023) / 1024 * 1024) : 0;
+    static constexpr int64_t CAND_PER_CTA = FUSE ? (int64_t)WG_PER_SET * QW * 2 * kStCap : 0;
+    // head weights of the current query group, one copy per epilogue warp (read as broadcasts)
+    static constexpr int W_BYTES = EPI_WARPS * COLS_PER_WG * 4;
+    static constexpr int SMEM_LIMIT = 227 * 1024 - ST_BYTES - W_BYTES;
     // two query tiles where the key ring still keeps 6 stages (decode: the next sequence's query
     // loads while the MMAs finish the current one, so the ring does not drain at the switch)
     static constexpr int STAGES_2Q = (SMEM_LIMIT - 2 * Q_BYTES - 2048) / TILE_BYTES;
@@ -63,9 +88,12 @@ struct IndexerTcConfig {
     static constexpr int FIXED = QBUF * Q_BYTES + 1024;      // query tiles + barriers
     static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED - 1024) / TILE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr int SMEM_BYTES = 1024 + QBUF * Q_BYTES + STAGES * TILE_BYTES + 1024;
+    static constexpr int SMEM_BYTES = 1024 + QBUF * Q_BYTES + STAGES * TILE_BYTES + 1024 + ST_BYTES + W_BYTES;
     static_assert(N >= 16 && N <= 256 && N % 16 == 0, "MMA N");
+    static_assert(!FUSE || (QW <= kStQueries && 4 * SETS == kStWarps), "fused selection group");
+    static_assert(SETS == 1 || SETS == ACC_BUFS, "a set per accumulator buffer");
     static_assert(COLS_PER_WG % HI == 0, "a warp group owns whole queries");
+    static_assert(HI % 4 == 0, "four partial sums per query");
     static_assert(STAGES >= 2, "ring");
     static_assert(ACC_BUFS * N <= 512, "TMEM");
 };
@@ -94,11 +122,11 @@ struct ItemCursor {
     }
 };
 
-template <int DI, int HI, int QPT>
-__global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
+template <int DI, int HI, int QPT, bool FUSE = false>
+__global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE>::THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                       IndexerTcArgs a) {
-    using Cfg = IndexerTcConfig<DI, HI, QPT>;
+    using Cfg = IndexerTcConfig<DI, HI, QPT, FUSE>;
     constexpr int N = Cfg::N, STAGES = Cfg::STAGES;
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
@@ -115,11 +143,21 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
     uint64_t *teardown = q_empty + Cfg::QBUF;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(teardown + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    StreamWg *st = reinterpret_cast<StreamWg *>(misc + 1024);   // FUSE: one per epilogue warp group
+    float *w_sm = reinterpret_cast<float *>(misc + 1024 + Cfg::ST_BYTES);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t per = a.items / gridDim.x, rem = a.items % gridDim.x;
-    const int64_t it0 = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
-    const int64_t it1 = it0 + per + (blockIdx.x < rem ? 1 : 0);
+    int64_t it0, it1;
+    if constexpr (FUSE) {
+        // whole query groups per CTA: a query's row never spans two CTAs
+        const int64_t G = a.items / a.tiles;
+        it0 = (G * blockIdx.x / gridDim.x) * a.tiles;
+        it1 = (G * (blockIdx.x + 1) / gridDim.x) * a.tiles;
+    } else {
+        const int64_t per = a.items / gridDim.x, rem = a.items % gridDim.x;
+        it0 = blockIdx.x * per + (blockIdx.x < rem ? blockIdx.x : rem);
+        it1 = it0 + per + (blockIdx.x < rem ? 1 : 0);
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -128,7 +166,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
         }
         for (int s = 0; s < Cfg::ACC_BUFS; ++s) {
             ptx::mbar_init(&acc_full[s], 1);
-            ptx::mbar_init(&acc_empty[s], Cfg::EPI_WARPS);
+            ptx::mbar_init(&acc_empty[s], Cfg::EPI_WARPS / Cfg::SETS);
         }
         for (int s = 0; s < Cfg::QBUF; ++s) {
             ptx::mbar_init(&q_full[s], 1);
@@ -136,6 +174,17 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
         }
         ptx::mbar_init(teardown, 1);
         *abort_flag = 0;
+        if constexpr (FUSE) {
+            for (int w = 0; w < Cfg::WG_PER_SET; ++w) {
+                for (int q = 0; q < kStQueries; ++q) {
+                    st[w].kept[q] = 0;
+                    for (int v = 0; v < kStWarps; ++v) st[w].wcnt[q][v] = 0;
+                    st[w].active[q] = 0;
+                    st[w].theta[q] = 0;
+                }
+                ptx::mbar_init(&st[w].bar, kStWarps);
+            }
+        }
         ptx::fence_mbar_init();
     }
     if (warp == 1) {
@@ -215,7 +264,10 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             uint32_t use = 0, groups_seen = 0, acc_use[Cfg::ACC_BUFS] = {};
             int acc = 0;
             bool issued = false;
-            uint32_t q_addr = ptx::smem_u32(q_tile);
+            // descriptors of the ring's and the query tiles' starts; an operand's descriptor is
+            // its base plus (byte offset >> 4) in the start-address field (no carry: < 256 KB)
+            const uint64_t k_desc = ptx::smem_desc(ptx::smem_u32(k_ring), 16, 8 * Cfg::ROWB, Cfg::SWZ);
+            uint64_t q_desc = ptx::smem_desc(ptx::smem_u32(q_tile), 16, 8 * Cfg::ROWB, Cfg::SWZ);
             ItemCursor ic(it0, a.tiles, a.groups);
             for (int64_t it = it0; it < it1 && !*abort_flag; ++it, ic.next()) {
                 const int t = ic.t;
@@ -228,7 +280,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                         *abort_flag = 1;
                         break;
                     }
-                    q_addr = ptx::smem_u32(q_tile + qb * Cfg::Q_BYTES);
+                    q_desc = ptx::smem_desc(ptx::smem_u32(q_tile + qb * Cfg::Q_BYTES), 16, 8 * Cfg::ROWB, Cfg::SWZ);
                     ++groups_seen;
                     cur = bg;
                     vis = group_visible(ic.b, ic.g);
@@ -244,16 +296,13 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t a_addr = ptx::smem_u32(k_ring + s * Cfg::TILE_BYTES);
+                const uint64_t a_desc = k_desc + (uint64_t)((s * Cfg::TILE_BYTES) >> 4);
                 const uint32_t d = tmem + acc * N;
 #pragma unroll
                 for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
                     const int bx = kk / Cfg::KSTEPS_PER_BOX, within = kk % Cfg::KSTEPS_PER_BOX;
-                    const uint64_t ad = ptx::smem_desc(a_addr + bx * 128 * Cfg::ROWB + within * 32, 16,
-                                                       8 * Cfg::ROWB, Cfg::SWZ);
-                    const uint64_t bd = ptx::smem_desc(q_addr + bx * N * Cfg::ROWB + within * 32, 16,
-                                                       8 * Cfg::ROWB, Cfg::SWZ);
-                    ptx::mma_bf16(d, ad, bd, idesc, kk > 0);
+                    ptx::mma_bf16(d, a_desc + (uint64_t)((bx * 128 * Cfg::ROWB + within * 32) >> 4),
+                                  q_desc + (uint64_t)((bx * N * Cfg::ROWB + within * 32) >> 4), idesc, kk > 0);
                 }
                 issued = true;
                 ptx::mma_commit(&empty[s]);
@@ -271,16 +320,41 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
     } else {
         // -------------------------------------------------------------- epilogue ----
         const int ew = warp - 2;                         // 0 .. EPI_WARPS-1
+        const int set = ew / (4 * Cfg::WG_PER_SET);      // the accumulator buffer this warp reads
+        const int wg = (ew >> 2) % Cfg::WG_PER_SET;      // its warp group within the set
         const int quarter = warp & 3;                    // TMEM lane quarter this warp may access
-        const int col0 = (ew / 4) * Cfg::COLS_PER_WG;    // first column of this warp group
-        constexpr int QW = Cfg::COLS_PER_WG / HI;        // queries this warp group scores
+        const int col0 = wg * Cfg::COLS_PER_WG;          // first column of this warp group
+        constexpr int QW = Cfg::QW;                      // queries this warp group scores
         const int row = quarter * 32 + lane;             // tile row == TMEM lane
         int64_t cur = -1;
         int64_t vis = 0;
         int64_t nv[QW];
-        float wr[Cfg::COLS_PER_WG];                      // head weights of this group's queries
+        float *wr = w_sm + ew * Cfg::COLS_PER_WG;        // head weights of this warp group's queries
         uint32_t acc_use[Cfg::ACC_BUFS] = {};
         int acc = 0;
+        // fused selection: the selection group's state (one per warp group of a set), this warp's
+        // segment and thread index in it, the candidate buffers, and this warp's copies of its
+        // segment counts, thresholds and active buffers
+        const int wseg = set * 4 + (ew & 3);
+        const int wtid = wseg * 32 + lane;
+        uint2 *cand = FUSE ? a.cand + ((int64_t)blockIdx.x * Cfg::WG_PER_SET + wg) * (QW * 2 * kStCap) : nullptr;
+        uint32_t st_phase = 0;
+        int my_cnt[QW];
+        uint32_t th[QW];
+        int act[QW];
+#pragma unroll
+        for (int q = 0; q < QW; ++q) {
+            my_cnt[q] = 0;
+            th[q] = 0;
+            act[q] = 0;
+        }
+        constexpr int CH = Cfg::COLS_PER_WG < 32 ? Cfg::COLS_PER_WG : 32;   // TMEM columns per load
+        constexpr int NCH = Cfg::COLS_PER_WG / CH;
+        auto tmem_ld_chunk = [&](uint32_t addr, uint32_t *r) {
+            if constexpr (CH == 32) ptx::tmem_ld32(addr, r);
+            else if constexpr (CH == 16) ptx::tmem_ld16(addr, r);
+            else ptx::tmem_ld8(addr, r);
+        };
         ItemCursor ic(it0, a.tiles, a.groups);
         for (int64_t it = it0; it < it1 && !*abort_flag; ++it, ic.next()) {
             const int t = ic.t;
@@ -289,6 +363,12 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
             if (bg != cur) {
                 cur = bg;
                 vis = group_visible(b, g);
+                __syncwarp();                            // the last group's weights are read
+                for (int c = lane; c < Cfg::COLS_PER_WG; c += 32) {
+                    const int qi = g * QPT + col0 / HI + c / HI;
+                    wr[c] = qi < a.n_q ? __ldg(a.w + ((int64_t)b * a.n_q + qi) * HI + c % HI) : 0.f;
+                }
+                __syncwarp();
 #pragma unroll
                 for (int q = 0; q < QW; ++q) {
                     const int qi = g * QPT + col0 / HI + q;
@@ -302,41 +382,132 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT>::THREADS, 1)
                         }
                     }
                     nv[q] = n;
-                    const float *wq = a.w + ((int64_t)b * a.n_q + qi) * HI;
-#pragma unroll
-                    for (int h = 0; h < HI; ++h) wr[q * HI + h] = qi < a.n_q ? __ldg(wq + h) : 0.f;
                 }
             }
             const int64_t j = (int64_t)t * 128 + row;
             float sc[QW];
 #pragma unroll
             for (int q = 0; q < QW; ++q) sc[q] = 0.f;
-            if ((int64_t)t * 128 < vis) {
+            const bool computed = (int64_t)t * 128 < vis;
+            // this warp's set handles the tile: a computed tile's accumulator buffer, else its parity
+            const bool mine = Cfg::SETS == 1 || (computed ? acc == set : (t & 1) == set);
+            if (computed && !mine) {
+                ++acc_use[acc];
+                acc = acc + 1 == Cfg::ACC_BUFS ? 0 : acc + 1;
+            } else if (computed) {
                 if (!ptx::mbar_wait(&acc_full[acc], acc_use[acc] & 1)) {
                     *abort_flag = 1;
                     break;
                 }
                 ptx::tc_fence_after();
+                // chunks of CH columns, the next chunk's load in flight while this one is summed;
+                // four partial sums per query (head h goes to sum h mod 4), added pairwise at the
+                // end, so the FMA chains are a quarter as long
                 const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + acc * N + col0;
-                // several columns per TMEM round trip (all loads issued before one wait)
-                constexpr int CB = Cfg::COLS_PER_WG <= 64 ? Cfg::COLS_PER_WG : 32;
+                float ps[QW][4];
 #pragma unroll
-                for (int c0 = 0; c0 < Cfg::COLS_PER_WG; c0 += CB) {
-                    uint32_t r[CB];
+                for (int q = 0; q < QW; ++q)
 #pragma unroll
-                    for (int c = 0; c < CB; c += 16) ptx::tmem_ld16(taddr + c0 + c, r + c);
-                    ptx::tmem_ld_wait();
+                    for (int v = 0; v < 4; ++v) ps[q][v] = 0.f;
+                uint32_t rb[2][CH];
+                tmem_ld_chunk(taddr, rb[0]);
+                ptx::tmem_ld_wait();
+                ptx::reg_fence<CH>(rb[0]);
 #pragma unroll
-                    for (int u = 0; u < CB; ++u)
-                        sc[(c0 + u) / HI] = fmaf(wr[c0 + u], fmaxf(__uint_as_float(r[u]), 0.f), sc[(c0 + u) / HI]);
+                for (int c = 0; c < NCH; ++c) {
+                    if (c + 1 < NCH) {
+                        tmem_ld_chunk(taddr + (c + 1) * CH, rb[(c + 1) & 1]);
+                    } else {                             // every TMEM load of this tile has landed
+                        ptx::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < CH; u += 4) {
+                        const float4 w4 = *reinterpret_cast<const float4 *>(wr + c * CH + u);
+                        const float wv[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            ps[(c * CH + u + v) / HI][v] =
+                                fmaf(wv[v], fmaxf(__uint_as_float(rb[c & 1][u + v]), 0.f), ps[(c * CH + u + v) / HI][v]);
+                    }
+                    if (c + 1 < NCH) {
+                        ptx::tmem_ld_wait();
+                        ptx::reg_fence<CH>(rb[(c + 1) & 1]);
+                    }
                 }
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&acc_empty[acc]);
+#pragma unroll
+                for (int q = 0; q < QW; ++q) sc[q] = (ps[q][0] + ps[q][1]) + (ps[q][2] + ps[q][3]);
                 ++acc_use[acc];
                 acc = acc + 1 == Cfg::ACC_BUFS ? 0 : acc + 1;
             }
-            if (j < a.cache_rows) {
+            if constexpr (FUSE) {
+                const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+                for (int q = 0; q < QW; ++q) {
+                    // append the scores at or above the query's threshold to this warp's segment
+                    const uint32_t key = ordered_key(sc[q]);
+                    const bool pass = mine && computed && j < nv[q] && key >= th[q];
+                    const uint32_t m = __ballot_sync(0xffffffffu, pass);
+                    if (m) {
+                        const int pos = my_cnt[q] + __popc(m & lt);
+                        if (pass) {
+                            if (pos < kStSeg)
+                                st_segment(st_buffer(cand, q, act[q]), wseg)[pos] = make_uint2(key, (uint32_t)j);
+                            else
+                                raise_error(LCA_DEVERR_SELECT);
+                        }
+                        my_cnt[q] += __popc(m);
+                    }
+                }
+                const bool last = t == a.tiles - 1;
+                if (last || (t + 1) % kStSyncTiles == 0) {
+                    StreamWg &S = st[wg];
+                    if (lane == 0)
+#pragma unroll
+                        for (int q = 0; q < QW; ++q) S.wcnt[q][wseg] = my_cnt[q];
+                    bool fine = wg_sync(S, st_phase);          // every warp's counts are published
+                    // a query whose segments could overflow before the next check is compacted;
+                    // every warp reads the counts before any warp publishes again (second
+                    // barrier), so all of them take the same branches
+                    bool full[QW];
+#pragma unroll
+                    for (int q = 0; q < QW; ++q) {
+                        int mx = 0;
+#pragma unroll
+                        for (int v = 0; v < kStWarps; ++v) mx = max(mx, S.wcnt[q][v]);
+                        full[q] = mx > kStSegLimit;
+                    }
+                    fine = fine && wg_sync(S, st_phase);
+                    bool changed = false;
+#pragma unroll
+                    for (int q = 0; q < QW; ++q)
+                        if (full[q] && fine) {
+                            fine = wg_compact(S, st_phase, wtid, cand, q, a.k);
+                            changed = true;
+                        }
+                    if (last) {
+#pragma unroll
+                        for (int q = 0; q < QW; ++q) {
+                            const int qi = g * QPT + col0 / HI + q;
+                            int32_t *out = qi < a.n_q ? a.out_idx + ((int64_t)b * a.n_q + qi) * a.k : nullptr;
+                            if (fine) fine = wg_finish(S, st_phase, wtid, cand, q, a.k, out);
+                        }
+                        changed = true;
+                    }
+                    if (!fine) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    if (changed)
+#pragma unroll
+                        for (int q = 0; q < QW; ++q) {
+                            my_cnt[q] = S.wcnt[q][wseg];
+                            th[q] = S.theta[q];
+                            act[q] = S.active[q];
+                        }
+                }
+            } else if (mine && j < a.cache_rows) {
 #pragma unroll
                 for (int q = 0; q < QW; ++q) {
                     const int qi = g * QPT + col0 / HI + q;

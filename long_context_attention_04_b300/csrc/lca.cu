@@ -378,10 +378,10 @@ lca_status indexer_validate(const char *name, const lca_attn_params *p, int batc
     return LCA_OK;
 }
 
-template <int DI, int HI, int QPT>
+template <int DI, int HI, int QPT, bool FUSE = false>
 lca_status indexer_tc_launch(int batch, int n_q, const lca_bf16 *q_idx, const lca_bf16 *k_cache, int64_t k_bs,
                              IndexerTcArgs &a, cudaStream_t stream) {
-    using Cfg = IndexerTcConfig<DI, HI, QPT>;
+    using Cfg = IndexerTcConfig<DI, HI, QPT, FUSE>;
     const CUtensorMapSwizzle sw = Cfg::ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     CUtensorMap kmap, qmap;
     const uint64_t kd[3] = {(uint64_t)DI, (uint64_t)a.cache_rows, (uint64_t)batch};
@@ -397,11 +397,13 @@ lca_status indexer_tc_launch(int batch, int n_q, const lca_bf16 *q_idx, const lc
     a.groups = (n_q + QPT - 1) / QPT;
     a.tiles = (int)ceil_div64(a.cache_rows, 128);
     a.items = (int64_t)batch * a.groups * a.tiles;
-    const int grid = (int)std::min<int64_t>(a.items, device_sm_count());
-    cudaFuncSetAttribute(indexer_tc_kernel<DI, HI, QPT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    // the fused selection hands each CTA whole query groups
+    const int grid = (int)std::min<int64_t>(FUSE ? (int64_t)batch * a.groups : a.items, device_sm_count());
+    cudaFuncSetAttribute(indexer_tc_kernel<DI, HI, QPT, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg::SMEM_BYTES);
-    launch_pdl(indexer_tc_kernel<DI, HI, QPT>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, kmap, qmap, a);
-    return check_launch("csa_indexer_scores");
+    launch_pdl(indexer_tc_kernel<DI, HI, QPT, FUSE>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, kmap, qmap,
+               a);
+    return check_launch(FUSE ? "csa_indexer_topk" : "csa_indexer_scores");
 }
 
 lca_status indexer_launch(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q_idx, const float *w_idx,
@@ -469,6 +471,19 @@ lca_status topk_launch(const lca_attn_params *p, int batch, int n_q, const float
 size_t indexer_ws_bytes(int batch, int n_q, int64_t cache_rows) {
     const int64_t stride = (cache_rows + 3) & ~(int64_t)3;
     return (size_t)batch * n_q * stride * sizeof(float);
+}
+
+// Whether csa_indexer_topk selects inside the indexer (four queries per tile: d_I = 128 with
+// H_I = 64 and n_q >= 3; k within the streaming selection's limit).
+bool indexer_fused(const lca_attn_params *p, int n_q) {
+    return p->idx_dim == 128 && p->idx_heads == 64 && n_q >= 3 && p->topk >= 1 && p->topk <= kStMaxK;
+}
+
+// The fused path's candidate buffers: per CTA, two buffers per warp group and query.
+size_t indexer_cand_bytes(int batch, int n_q) {
+    const int64_t groups = (int64_t)batch * ((n_q + 3) / 4);
+    const int64_t grid = std::min<int64_t>(groups, device_sm_count());
+    return (size_t)grid * IndexerTcConfig<128, 64, 4, true>::CAND_PER_CTA * sizeof(uint2);
 }
 
 }  // namespace
@@ -594,9 +609,8 @@ lca_status lca_topk(const lca_attn_params *p, int batch, int n_q, const float *s
 }
 
 size_t csa_indexer_workspace(const lca_attn_params *p, int batch, int n_q, int64_t cache_rows) {
-    (void)p;
-    if (batch <= 0 || n_q <= 0 || cache_rows <= 0) return 0;
-    return indexer_ws_bytes(batch, n_q, cache_rows);
+    if (!p || batch <= 0 || n_q <= 0 || cache_rows <= 0) return 0;
+    return indexer_fused(p, n_q) ? indexer_cand_bytes(batch, n_q) : indexer_ws_bytes(batch, n_q, cache_rows);
 }
 
 lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q_idx, const float *w_idx,
@@ -608,9 +622,23 @@ lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q, const 
     if (st != LCA_OK) return st;
     LCA_REQUIRE(p->topk >= 1, LCA_ERR_INVALID_ARG, "%s: topk must be positive", name);
     LCA_REQUIRE(out_idx, LCA_ERR_INVALID_ARG, "%s: out_idx is NULL", name);
-    const size_t need = indexer_ws_bytes(batch, n_q, cache_rows);
+    const size_t need = csa_indexer_workspace(p, batch, n_q, cache_rows);
     LCA_REQUIRE(workspace && aligned16(workspace) && workspace_bytes >= need, LCA_ERR_WORKSPACE,
                 "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu", name, need, workspace_bytes);
+    if (indexer_fused(p, n_q)) {
+        // prefill: the selection runs in the indexer's epilogue, no score leaves the chip
+        IndexerTcArgs a = {};
+        a.n_q = n_q;
+        a.ratio = p->ratio;
+        a.cache_rows = cache_rows;
+        a.w = w_idx;
+        a.q_pos = q_pos;
+        a.k = p->topk;
+        a.out_idx = out_idx;
+        a.cand = static_cast<uint2 *>(workspace);
+        st = indexer_tc_launch<128, 64, 4, true>(batch, n_q, q_idx, k_cache, k_batch_stride, a, stream);
+        return st == LCA_OK ? ok() : st;
+    }
     const int64_t stride = (cache_rows + 3) & ~(int64_t)3;
     float *scores = static_cast<float *>(workspace);
     st = indexer_launch(p, batch, n_q, q_idx, w_idx, k_cache, k_batch_stride, cache_rows, q_pos, scores, stride,

@@ -196,6 +196,11 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
 }
 
 // TMEM -> registers: this warp's 32 lanes (lane quarter warpid % 4), 16 / 32 consecutive columns.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *r) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -242,6 +247,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// Marks r[0 .. N) as written at this point, so that the compiler keeps every read of them after
+// the tcgen05.wait::ld that precedes it (the wait names no registers of its own).
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t *r) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Shared-memory matrix descriptor of tcgen05.mma: start address, leading- and stride-

@@ -525,3 +525,59 @@ def test_tensor_core_gemm_matches_oracle(M, N, K):
         C16 = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
         api.lca_gemm_bf16(dev(A), dev(Bm), C16)
         assert_close_bf16_out(C16.cpu().float().numpy(), ref, what="gemm %dx%dx%d" % (M, N, K))
+
+
+
+@pytest.mark.parametrize("B,n_q,rows,k,mode", [(1, 8, 3000, 1024, "plain"), (2, 5, 2000, 512, "dups"),
+                                               (1, 7, 20000, 1024, "dups"), (3, 3, 700, 1024, "plain"),
+                                               (1, 64, 5000, 300, "dups"), (1, 6, 30000, 1024, "few"),
+                                               (2, 4, 12000, 700, "zero")])
+def test_fused_indexer_topk_equals_scores_then_topk(B, n_q, rows, k, mode):
+    """The prefill path (four queries per tile) selects the top k inside the indexer.  It must give
+    the same lists as the scores written out and selected by lca_topk, and the oracle's sets:
+    ragged query groups, queries that see fewer than k entries or none, rows long enough for
+    several compactions of the candidate buffers, and equal scores, which the lower index must
+    win: repeated key rows (dups), five distinct key rows for the whole row, so that thousands of
+    candidates share each score and the compactions must cut by index (few), and zero head
+    weights for one query, whose scores are then all zero (zero)."""
+    rng = Rng(40 + n_q)
+    m, HI, DI = 4, 64, 128
+    p = AttnParams(idx_heads=HI, idx_dim=DI, ratio=m, topk=k)
+    q = rng.normal_bf16((B, n_q, HI, DI))
+    w = rng.normal_f32((B, n_q, HI), 1.0 / math.sqrt(HI))
+    keys = rng.normal_bf16((B, rows, DI))
+    if mode == "dups":
+        keys[:, 1::3] = keys[:, 0::3][:, :keys[:, 1::3].shape[1]]     # row 3i + 1 repeats row 3i
+    elif mode == "few":
+        keys = keys[:, torch.arange(rows) % 5]
+    elif mode == "zero":
+        w[0, 2] = 0.0
+    g = np.random.default_rng(41)
+    pos = torch.from_numpy(g.integers(m * rows // 2, m * rows, size=(B, n_q)).astype(np.int32))
+    pos[0, 0] = m * rows - 1
+    pos[0, 1] = m * (k // 2) + 1          # fewer than k visible
+    pos[-1, -1] = 1                       # none visible
+    ws = torch.empty(api.csa_indexer_workspace(p, B, n_q, rows), dtype=torch.uint8, device=DEV)
+    fused = torch.full((B, n_q, k), -7, dtype=torch.int32, device=DEV)
+    api.csa_indexer_topk(p, dev(q), dev(w), dev(keys), dev(pos), fused, ws)
+    assert api.lca_device_error() == 0
+    stride = (rows + 3) // 4 * 4
+    scores = torch.empty((B, n_q, stride), device=DEV)
+    api.csa_indexer_scores(p, dev(q), dev(w), dev(keys), dev(pos), scores)
+    plain = torch.empty_like(fused)
+    api.lca_topk(p, scores, dev(pos), rows, plain)
+    assert api.lca_device_error() == 0
+    assert torch.equal(fused, plain)
+    # the selection's warp groups synchronise among themselves: repeated calls give the same lists
+    for _ in range(6):
+        again = torch.full_like(fused, -7)
+        api.csa_indexer_topk(p, dev(q), dev(w), dev(keys), dev(pos), again, ws)
+        assert torch.equal(again, fused)
+    assert api.lca_device_error() == 0
+    got = fused.cpu().numpy()
+    qb, wf, kb = u16(q), f32(w), u16(keys)
+    for b in range(B):
+        for i in range(n_q):
+            n_vis = oracle.visible_entries(int(pos[b, i]), m)
+            ref = oracle.indexer_scores(qb[b, i], wf[b, i], kb[b], n_vis)
+            check_topk(got[b, i], ref, k, "b=%d i=%d" % (b, i))

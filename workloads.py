@@ -129,6 +129,12 @@ CSA_PREFILL_1M_PROJ = dict(CSA_PREFILL_1M, hidden=4096,
                            name="CSA chunked prefill with input projections from hidden 4096, 8192 queries at 1M "
                                 "context (262144 entries), k=1024, W=128, H=64")
 
+# The same chunk with the indexer's scores written out (8192 x 262144 fp32) and selected by a
+# separate top-k pass: the path the fused selection replaces, timed beside it.
+CSA_PREFILL_1M_SCORED = dict(CSA_PREFILL_1M, materialise=True,
+                             name="CSA chunked prefill, scores materialised then top-k, 8192 queries at 1M "
+                                  "context (262144 entries), k=1024, W=128, H=64")
+
 # Manifold-constrained hyper-connections around one layer, for a prefill chunk: 4 residual
 # streams of the V4-Flash hidden size (4096), the generated coefficients (Sinkhorn-Knopp, 20
 # passes), the layer input and, given the layer's output, the new streams.
@@ -146,6 +152,7 @@ WORKLOADS = {
     "mhc_prefill_8192": MHC_PREFILL_8192,
     "v4flash_decode_1m": V4FLASH_DECODE_1M,
     "csa_prefill_1m_proj": CSA_PREFILL_1M_PROJ,
+    "csa_prefill_1m_scored": CSA_PREFILL_1M_SCORED,
 }
 
 
