@@ -68,6 +68,18 @@ def _load():
         lib.orc_mhc_post.restype = None
         lib.orc_grouped_oproj.argtypes = [I, I, I, I, I, P, P, P, P]
         lib.orc_grouped_oproj.restype = I
+        lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_decode.restype = D
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_e4m3_encode.restype = ctypes.c_uint8
+        lib.orc_quantize_rows_e4m3.argtypes = [L, I, P, P, P]
+        lib.orc_quantize_rows_e4m3.restype = None
+        lib.orc_dequantize_rows_e4m3.argtypes = [L, I, P, P, P]
+        lib.orc_dequantize_rows_e4m3.restype = None
+        lib.orc_compress_pc.argtypes = [I, I, I, P, P, L, L, P, P, D, I, D, L, L, P]
+        lib.orc_compress_pc.restype = I
+        lib.orc_indexer_scores_e4m3.argtypes = [I, I, P, P, P, P, P, L, P]
+        lib.orc_indexer_scores_e4m3.restype = None
         _lib = lib
     return _lib
 
@@ -244,3 +256,70 @@ def mhc_post(x, B, c, y):
     xo = np.empty((n, d), np.float64)
     lib.orc_mhc_post(n, d, _ptr(x), _ptr(B), _ptr(c), _ptr(y), _ptr(xo))
     return xo
+
+
+def e4m3_decode(code: int) -> float:
+    """Value of one e4m3 code (NaN for S.1111.111)."""
+    return float(_load().orc_e4m3_decode(int(code) & 0xFF))
+
+
+def e4m3_encode(x: float) -> int:
+    """e4m3 code of a float32 value: nearest, ties to even mantissa, saturating at +-448."""
+    return int(_load().orc_e4m3_encode(float(np.float32(x))))
+
+
+def quantize_rows_e4m3(x):
+    """Per-row e4m3 quantisation of bf16 rows x (uint16 [rows, width]): (codes uint8 [rows, width],
+    scales float32 [rows]) with scale = amax/448 and code = e4m3(x/scale)."""
+    lib = _load()
+    x = _u16(x)
+    rows, width = x.shape
+    q = np.empty((rows, width), dtype=np.uint8)
+    sc = np.empty(rows, dtype=np.float32)
+    lib.orc_quantize_rows_e4m3(rows, width, _ptr(x), _ptr(q), _ptr(sc))
+    return q, sc
+
+
+def dequantize_rows_e4m3(q, scale):
+    """scale[r] * e4m3(q[r][i]) as float64 [rows, width]."""
+    lib = _load()
+    q = np.ascontiguousarray(q, dtype=np.uint8)
+    scale = _f32(scale)
+    rows, width = q.shape
+    out = np.empty((rows, width), dtype=np.float64)
+    lib.orc_dequantize_rows_e4m3(rows, width, _ptr(q), _ptr(scale), _ptr(out))
+    return out
+
+
+def compress_pc(tok_v, tok_z, tok_pos0, bias, gamma, eps, rope_dims, rope_base,
+                span, stride, first_entry, n_new):
+    """The compressor with per-channel logits tok_z (float32 [n_tok, width]) and per-channel
+    offset biases bias (float32 [span, width]); otherwise as compress()."""
+    lib = _load()
+    tok_v = _u16(tok_v)
+    tok_z = _f32(tok_z)
+    bias = _f32(bias)
+    g = None if gamma is None else _f32(gamma)
+    n_tok, width = tok_v.shape
+    assert tok_z.shape == (n_tok, width) and bias.shape == (span, width)
+    out = np.empty((n_new, width), dtype=np.float64)
+    rc = lib.orc_compress_pc(span, stride, width, _ptr(tok_v), _ptr(tok_z), tok_pos0, n_tok,
+                             _ptr(bias), _ptr(g), eps, rope_dims, rope_base, first_entry, n_new, _ptr(out))
+    if rc != 0:
+        raise ValueError("orc_compress_pc: tokens needed by the requested entries are missing (rc=%d)" % rc)
+    return out
+
+
+def indexer_scores_e4m3(q8, qscale, w, k8, kscale, n_vis):
+    """Indexer scores over e4m3 rows: q8 uint8 [H_I, d_I] with qscale [H_I], k8 uint8 [rows, d_I]
+    with kscale [rows]; float64 [n_vis]."""
+    lib = _load()
+    q8 = np.ascontiguousarray(q8, dtype=np.uint8)
+    k8 = np.ascontiguousarray(k8, dtype=np.uint8)
+    qscale, kscale, w = _f32(qscale), _f32(kscale), _f32(w)
+    n_heads, dim = q8.shape
+    assert k8.shape[1] == dim and k8.shape[0] >= n_vis and kscale.shape[0] >= n_vis
+    out = np.empty(n_vis, dtype=np.float64)
+    lib.orc_indexer_scores_e4m3(n_heads, dim, _ptr(q8), _ptr(qscale), _ptr(w), _ptr(k8), _ptr(kscale), n_vis,
+                                _ptr(out))
+    return out

@@ -448,3 +448,177 @@ void orc_mhc_post(int n, long d, const uint16_t *x, const double *B, const doubl
             xo[(size_t)i * (size_t)d + (size_t)e] = s;
         }
 }
+
+/*
+ * ----------------------------------------------------------------------------------
+ * FP8 caches and the per-channel compressor (variants of the path, not fixed by the
+ * pages: the news summary ynrysl.com, paragraph on HCA, mentions FP8 storage only in
+ * passing, and [P1] CSA step one calls the compressor's weighting "learned" without
+ * giving its shape).
+ *
+ * e4m3 (the 8-bit float with 1 sign, 4 exponent and 3 mantissa bits, exponent bias 7,
+ * no infinities, S.1111.111 NaN): a code c >= 0x08 (magnitude bits) is normal,
+ * (-1)^s 2^(e-7) (1 + m/8); e = 0 is subnormal, (-1)^s 2^-6 (m/8).  The largest finite
+ * magnitude is 2^8 * 1.75 = 448.
+ */
+double orc_e4m3_decode(uint8_t c)
+{
+    int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m / 8.0, -6);
+    else
+        v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/*
+ * e4m3 code of a float: the nearest finite e4m3 value, a tie going to the code with an
+ * even mantissa (round to nearest even), magnitudes beyond 448 saturating to 448 (the
+ * "satfinite" conversion).  Found by comparing against every finite magnitude code,
+ * so that no step of a bit-level conversion can be wrong.  NaN gives 0x7F.
+ */
+uint8_t orc_e4m3_encode(float x)
+{
+    if (x != x)
+        return 0x7F;
+    uint8_t sign = (signbit(x) ? 0x80 : 0);
+    double a = fabs((double)x);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7E);
+    int best = 0;
+    double best_d = INFINITY;
+    for (int c = 0; c <= 0x7E; ++c) {
+        double d = fabs(orc_e4m3_decode((uint8_t)c) - a);
+        if (d < best_d || (d == best_d && (c & 1) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return (uint8_t)(sign | best);
+}
+
+/*
+ * Per-row e4m3 quantisation of bf16 rows (reading taken for "FP8 caches": one fp32
+ * scale per row, the row's largest magnitude mapped to 448):
+ *     amax = max_i |x_i|,  scale = amax / 448 (fp32),  code_i = e4m3(x_i / scale) (fp32
+ *     division), and x_i is read back as scale * e4m3_value(code_i).
+ * An all-zero row gets scale 0 and zero codes.  The divisions are single-precision
+ * because they decide the codes: both sides round them the same way.
+ */
+void orc_quantize_rows_e4m3(long rows, int width, const uint16_t *x, uint8_t *q, float *scale)
+{
+    for (long r = 0; r < rows; ++r) {
+        const uint16_t *xr = x + (size_t)r * (size_t)width;
+        float amax = 0.0f;
+        for (int i = 0; i < width; ++i) {
+            float v = (float)fabs(bf16_bits_to_double(xr[i]));
+            if (v > amax)
+                amax = v;
+        }
+        volatile float s = amax / 448.0f;
+        scale[r] = s;
+        for (int i = 0; i < width; ++i) {
+            if (amax == 0.0f) {
+                q[(size_t)r * (size_t)width + (size_t)i] = 0;
+                continue;
+            }
+            volatile float y = (float)bf16_bits_to_double(xr[i]) / s;
+            q[(size_t)r * (size_t)width + (size_t)i] = orc_e4m3_encode(y);
+        }
+    }
+}
+
+/* The value of row r, channel i of a per-row-scaled e4m3 array. */
+static double e4m3_value(const uint8_t *q, const float *scale, long r, int width, int i)
+{
+    return (double)scale[r] * orc_e4m3_decode(q[(size_t)r * (size_t)width + (size_t)i]);
+}
+
+/*
+ * The compressor with per-channel weights (reading taken for the open shape of [P1] CSA
+ * step one's "learned" weighting): each channel i has its own logit per token,
+ * z[t][i], and its own learned offset bias, bias[r][i]; the softmax over the window is
+ * taken per channel:
+ *     a_{t,i} = exp(z[t][i] + bias[t - nominal][i]) / sum_{t'} exp(z[t'][i] + bias[...][i]),
+ *     u_i = sum_t a_{t,i} v[t][i];
+ * then RMSNorm and RoPE as in orc_compress.  With every channel's logits and biases
+ * equal it is orc_compress.
+ */
+int orc_compress_pc(int span, int stride, int width,
+                    const uint16_t *tok_v, const float *tok_z, long tok_pos0, long n_tok,
+                    const float *bias, const float *gamma, double eps,
+                    int rope_dims, double rope_base,
+                    long first_entry, long n_new, double *out)
+{
+    double *u = (double *)malloc(sizeof(double) * (size_t)width);
+    if (!u)
+        return -3;
+    for (long e = 0; e < n_new; ++e) {
+        long j = first_entry + e;
+        long end = (long)stride * (j + 1);
+        long nominal_begin = end - span;
+        long begin = nominal_begin < 0 ? 0 : nominal_begin;
+        if (begin < tok_pos0 || end > tok_pos0 + n_tok) {
+            free(u);
+            return -1;
+        }
+        for (int i = 0; i < width; ++i) {
+            double zmax = -INFINITY;
+            for (long t = begin; t < end; ++t) {
+                double s = (double)tok_z[(size_t)(t - tok_pos0) * (size_t)width + (size_t)i] +
+                           (double)bias[(size_t)(t - nominal_begin) * (size_t)width + (size_t)i];
+                if (s > zmax)
+                    zmax = s;
+            }
+            double den = 0.0, num = 0.0;
+            for (long t = begin; t < end; ++t) {
+                double s = (double)tok_z[(size_t)(t - tok_pos0) * (size_t)width + (size_t)i] +
+                           (double)bias[(size_t)(t - nominal_begin) * (size_t)width + (size_t)i];
+                double wgt = exp(s - zmax);
+                den += wgt;
+                num += wgt * bf16_bits_to_double(tok_v[(size_t)(t - tok_pos0) * (size_t)width + (size_t)i]);
+            }
+            u[i] = num / den;
+        }
+        if (gamma)
+            rms_normalize(u, width, gamma, eps);
+        if (rope_dims > 0)
+            rope_rotate(u, width, rope_dims, rope_base, (double)(end - 1));
+        memcpy(out + (size_t)e * (size_t)width, u, sizeof(double) * (size_t)width);
+    }
+    free(u);
+    return 0;
+}
+
+/*
+ * Lightning-indexer scores over e4m3 rows: the same score as orc_indexer_scores,
+ *     s_j = sum_h w_h ReLU(q_h . k_j),
+ * with q_h = qscale[h] * e4m3(q8[h][.]) and k_j = kscale[j] * e4m3(k8[j][.]) read back from
+ * their codes and scales.
+ */
+void orc_indexer_scores_e4m3(int n_heads, int dim, const uint8_t *q8, const float *qscale, const float *w,
+                             const uint8_t *k8, const float *kscale, long n_vis, double *out)
+{
+    for (long j = 0; j < n_vis; ++j) {
+        double s = 0.0;
+        for (int h = 0; h < n_heads; ++h) {
+            double dot = 0.0;
+            for (int d = 0; d < dim; ++d)
+                dot += e4m3_value(q8, qscale, h, dim, d) * e4m3_value(k8, kscale, j, dim, d);
+            double relu = dot > 0.0 ? dot : 0.0;
+            s += (double)w[h] * relu;
+        }
+        out[j] = s;
+    }
+}
+
+/* Rows r of a per-row-scaled e4m3 array read back as doubles (out[r][i]). */
+void orc_dequantize_rows_e4m3(long rows, int width, const uint8_t *q, const float *scale, double *out)
+{
+    for (long r = 0; r < rows; ++r)
+        for (int i = 0; i < width; ++i)
+            out[(size_t)r * (size_t)width + (size_t)i] = e4m3_value(q, scale, r, width, i);
+}

@@ -657,3 +657,114 @@ def test_mhc_pre_selects_a_stream_and_post_preserves_the_stream_sum():
     np.testing.assert_allclose(xo.sum(0), from_bits(x).sum(0) + c.sum() * from_bits(y), atol=1e-12)
     # and each stream is the textbook mixing
     np.testing.assert_allclose(xo, B @ from_bits(x) + np.outer(c, from_bits(y)), atol=1e-12)
+
+
+# ------------------------------------------------------- FP8 (e4m3) caches ----
+# e4m3: 1 sign, 4 exponent (bias 7), 3 mantissa bits, no infinities, S.1111.111 NaN,
+# largest finite 448; the conversion rounds to nearest even and saturates.
+
+def test_e4m3_codes_fixed_by_the_format():
+    assert oracle.e4m3_decode(0x00) == 0.0
+    assert oracle.e4m3_decode(0x01) == 2.0 ** -9            # smallest subnormal
+    assert oracle.e4m3_decode(0x07) == 7 * 2.0 ** -9        # largest subnormal
+    assert oracle.e4m3_decode(0x08) == 2.0 ** -6            # smallest normal
+    assert oracle.e4m3_decode(0x38) == 1.0
+    assert oracle.e4m3_decode(0x30) == 0.5
+    assert oracle.e4m3_decode(0x7E) == 448.0
+    assert oracle.e4m3_decode(0xB8) == -1.0
+    assert math.isnan(oracle.e4m3_decode(0x7F)) and math.isnan(oracle.e4m3_decode(0xFF))
+    # ties go to the even mantissa; beyond 448 saturates
+    assert oracle.e4m3_encode(1.0625) == 0x38               # between 1 (m=0) and 1.125 (m=1)
+    assert oracle.e4m3_encode(1.1875) == 0x3A               # between 1.125 (m=1) and 1.25 (m=2)
+    assert oracle.e4m3_encode(2.0 ** -10) == 0x00           # half the smallest subnormal
+    assert oracle.e4m3_encode(3 * 2.0 ** -10) == 0x02       # between 2^-9 (m=1) and 2^-8 (m=2)
+    assert oracle.e4m3_encode(460.0) == 0x7E and oracle.e4m3_encode(-1e6) == 0xFE
+    assert oracle.e4m3_encode(-0.0) == 0x80
+
+
+def test_e4m3_every_finite_code_round_trips():
+    for c in range(256):
+        if c & 0x7F == 0x7F:
+            continue
+        assert oracle.e4m3_encode(oracle.e4m3_decode(c)) == c
+
+
+def test_e4m3_encode_matches_torch_float8_conversion():
+    """In range, the oracle's code is the one torch's float8_e4m3fn cast gives (a library
+    routine for the same rounding)."""
+    g = np.random.default_rng(5)
+    x = (g.standard_normal(4000) * np.exp(g.uniform(-9, 6, 4000))).astype(np.float32)
+    x = x[np.abs(x) < 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_encode(v) for v in x], dtype=np.uint8)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_quantize_rows_scale_codes_and_round_trip():
+    g = np.random.default_rng(6)
+    x = rand_bits(g, (7, 64), std=3.0)
+    x[3] = to_bits(np.zeros(64))
+    q, sc = oracle.quantize_rows_e4m3(x)
+    xf = from_bits(x)
+    for r in range(7):
+        amax = np.float32(np.abs(xf[r]).max())
+        assert sc[r] == np.float32(amax / np.float32(448.0))
+        if amax == 0:
+            assert (q[r] == 0).all()
+            continue
+        # the largest magnitude maps to +-448; the codes are torch's cast of x / scale in fp32
+        i = int(np.abs(xf[r]).argmax())
+        assert q[r, i] & 0x7F == 0x7E
+        y = (xf[r].astype(np.float32) / sc[r]).astype(np.float32)
+        np.testing.assert_array_equal(q[r], torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    back = oracle.dequantize_rows_e4m3(q, sc)
+    # three mantissa bits: normal values come back within 2^-4 relative
+    big = np.abs(xf) >= 2.0 ** -6 * sc[:, None].astype(np.float64)
+    assert np.all(np.abs(back - xf)[big] <= 2.0 ** -4 * np.abs(xf)[big] + 1e-30)
+
+
+def test_compress_per_channel_equal_channels_is_the_scalar_compressor():
+    g = np.random.default_rng(7)
+    m, width, n_tok = 4, 16, 12
+    v = rand_bits(g, (n_tok, width))
+    z1 = g.standard_normal(n_tok).astype(np.float32)
+    b1 = (0.3 * g.standard_normal(2 * m)).astype(np.float32)
+    gamma = (1 + 0.1 * g.standard_normal(width)).astype(np.float32)
+    ref = oracle.compress(v, z1, 0, b1, gamma, 1e-6, 8, 10000.0, 2 * m, m, 0, n_tok // m)
+    got = oracle.compress_pc(v, np.repeat(z1[:, None], width, 1), 0, np.repeat(b1[:, None], width, 1), gamma, 1e-6,
+                             8, 10000.0, 2 * m, m, 0, n_tok // m)
+    np.testing.assert_allclose(got, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_compress_per_channel_weights_act_per_channel():
+    """A logit far above the others in one channel picks that token's value in that channel
+    only; a channel with equal logits averages the window (closed forms, no norm or RoPE)."""
+    m, width, n_tok = 4, 8, 8
+    g = np.random.default_rng(8)
+    v = rand_bits(g, (n_tok, width))
+    z = np.zeros((n_tok, width), dtype=np.float32)
+    z[5, 2] = 80.0                          # entry 1 covers tokens 0..7; channel 2 picks token 5
+    bias = np.zeros((2 * m, width), dtype=np.float32)
+    out = oracle.compress_pc(v, z, 0, bias, None, 1e-6, 0, 10000.0, 2 * m, m, 1, 1)[0]
+    vf = from_bits(v)
+    assert abs(out[2] - vf[5, 2]) < 1e-12 * max(1.0, abs(vf[5, 2]))
+    np.testing.assert_allclose(out[[0, 1, 3, 4, 5, 6, 7]], vf[:, [0, 1, 3, 4, 5, 6, 7]].mean(0), rtol=1e-13, atol=1e-13)
+
+
+def test_indexer_e4m3_is_the_bf16_indexer_on_the_decoded_values():
+    """With power-of-two scales the decoded rows are exact bf16 values: the e4m3 score equals
+    the bf16 indexer's on those rows."""
+    g = np.random.default_rng(9)
+    H, d, n = 4, 32, 50
+    q8 = g.integers(0, 256, (H, d)).astype(np.uint8)
+    k8 = g.integers(0, 256, (n, d)).astype(np.uint8)
+    q8[(q8 & 0x7F) == 0x7F] = 0x11
+    k8[(k8 & 0x7F) == 0x7F] = 0x22
+    qs = (2.0 ** g.integers(-3, 3, H)).astype(np.float32)
+    ks = (2.0 ** g.integers(-3, 3, n)).astype(np.float32)
+    w = g.standard_normal(H).astype(np.float32)
+    got = oracle.indexer_scores_e4m3(q8, qs, w, k8, ks, n)
+    qv = oracle.dequantize_rows_e4m3(q8, qs)
+    kv = oracle.dequantize_rows_e4m3(k8, ks)
+    ref = oracle.indexer_scores(to_bits(qv), w, to_bits(kv), n)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-9)
