@@ -171,6 +171,80 @@ lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q,
                             void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------
+ * FP8 caches and the per-channel compressor: variants of the path.  The pages name FP8
+ * storage only in passing ([P2] ynrysl.com, the paragraph on HCA) and call the compressor's
+ * weighting "learned" without its shape ([P1] CSA step one); the readings taken are:
+ *
+ * e4m3 rows with one fp32 scale per row: the row's largest magnitude maps to 448 (the
+ * largest finite e4m3 value),
+ *     scale = amax / 448,   code_i = e4m3(x_i / scale),   read back as scale * value(code_i),
+ * with IEEE fp32 divisions and round-to-nearest-even, saturating conversions; an all-zero
+ * row gets scale 0 and zero codes.  e4m3: 1 sign, 4 exponent (bias 7), 3 mantissa bits,
+ * no infinities.
+ *
+ * lca_quantize_rows_e4m3: rows x [rows][width] bf16 (16-byte aligned; width a multiple of
+ * 8, at most 1024) to codes q [rows][width] (8-byte aligned) and scale [rows] fp32.  Caller
+ * owns all buffers; no allocation.  Errors: LCA_ERR_INVALID_ARG for NULL or misaligned
+ * pointers or a bad width.
+ * ------------------------------------------------------------------------------- */
+lca_status lca_quantize_rows_e4m3(const lca_bf16 *x, int64_t rows, int width, uint8_t *q, float *scale,
+                                  cudaStream_t stream);
+
+/* Options of *_compress_kv_ex (the arguments otherwise as *_compress_kv):
+ *   per_channel  0: tok_z [batch][n_tok] and pos_bias [span] as in *_compress_kv.
+ *                1: one logit per token and channel, tok_z [batch][n_tok][width] (16-byte
+ *                   aligned, tok_z_batch_stride in floats, a multiple of 4), and one offset
+ *                   bias per channel, pos_bias [span][width]; the softmax over the window is
+ *                   taken per channel (span = 2m for CSA, m' for HCA).
+ *   e4m3         0: cache is bf16 as in *_compress_kv.
+ *                1: cache holds e4m3 codes (one byte per element, cache_batch_stride and
+ *                   rows in elements; 8-byte aligned); the entry is RMS-normalised and
+ *                   rotated, rounded to bf16, then quantised as by lca_quantize_rows_e4m3,
+ *                   its scale going to cache_scale[b * scale_batch_stride + j]. */
+typedef struct lca_compress_variant {
+    int per_channel;
+    int e4m3;
+    float *cache_scale;
+    int64_t scale_batch_stride;
+} lca_compress_variant;
+
+lca_status csa_compress_kv_ex(const lca_attn_params *p, const lca_compress_variant *variant, int batch, int width,
+                              const lca_bf16 *tok_v, int64_t tok_v_batch_stride, int n_tok,
+                              const float *tok_z, int64_t tok_z_batch_stride,
+                              const int32_t *tok_pos0, const float *pos_bias, const float *gamma,
+                              int apply_rope, const int32_t *first_entry, int n_new,
+                              void *cache, int64_t cache_batch_stride, int64_t cache_rows,
+                              cudaStream_t stream);
+lca_status hca_compress_kv_ex(const lca_attn_params *p, const lca_compress_variant *variant, int batch, int width,
+                              const lca_bf16 *tok_v, int64_t tok_v_batch_stride, int n_tok,
+                              const float *tok_z, int64_t tok_z_batch_stride,
+                              const int32_t *tok_pos0, const float *pos_bias, const float *gamma,
+                              int apply_rope, const int32_t *first_entry, int n_new,
+                              void *cache, int64_t cache_batch_stride, int64_t cache_rows,
+                              cudaStream_t stream);
+
+/* The lightning indexer over e4m3 rows: the score of csa_indexer_scores,
+ *     s_j = sum_h w_h ReLU(q_h . k_j),
+ * with q_h = q_scale[b][i][h] * value(q_idx8[b][i][h][.]) and
+ *      k_j = k_scale[b * k_scale_batch_stride + j] * value(k_cache8[b * k_batch_stride + j * d_I + .]).
+ * The products run on the tensor cores in e4m3 (kind::f8f6f4, K = 32) with fp32 accumulation;
+ * since the scales are non-negative, q_scale is folded into the head weights and k_scale
+ * multiplies the head sum.  Supported: d_I = 128 with 64 heads.  Buffers as in the bf16 calls
+ * (codes 16-byte aligned), the workspace from csa_indexer_workspace. */
+lca_status csa_indexer_scores_e4m3(const lca_attn_params *p, int batch, int n_q,
+                                   const uint8_t *q_idx8, const float *q_scale, const float *w_idx,
+                                   const uint8_t *k_cache8, int64_t k_batch_stride,
+                                   const float *k_scale, int64_t k_scale_batch_stride, int64_t cache_rows,
+                                   const int32_t *q_pos, float *scores, int64_t scores_stride,
+                                   cudaStream_t stream);
+lca_status csa_indexer_topk_e4m3(const lca_attn_params *p, int batch, int n_q,
+                                 const uint8_t *q_idx8, const float *q_scale, const float *w_idx,
+                                 const uint8_t *k_cache8, int64_t k_batch_stride,
+                                 const float *k_scale, int64_t k_scale_batch_stride, int64_t cache_rows,
+                                 const int32_t *q_pos, int32_t *out_idx,
+                                 void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------
  * Core attention ([P1] CSA step three, HCA dense attention and the tricks; [P4] 3.1).
  * For query i of sequence b at position pos = q_pos[b][i], per head h:
  *   q_h  = RoPE(RMSNorm(q[b][i][h]) * gamma_q, pos)

@@ -22,7 +22,12 @@ class lca_attn_params(ctypes.Structure):
     ]
 
 
+class lca_compress_variant(ctypes.Structure):
+    _fields_ = [("per_channel", c_int), ("e4m3", c_int), ("cache_scale", c_void_p), ("scale_batch_stride", c_int64)]
+
+
 P = ctypes.POINTER(lca_attn_params)
+CV = ctypes.POINTER(lca_compress_variant)
 V = c_void_p
 
 # argument types of every entry point, in header order
@@ -57,6 +62,14 @@ SIGNATURES = {
     "lca_mhc_workspace": ([c_int, c_int], c_size_t),
     "lca_mhc_pre": ([c_int, c_int, c_int, c_int, V, V, V, V, V, V, V, V, c_size_t, V], c_int),
     "lca_mhc_post": ([c_int, c_int, c_int, V, V, V, V, V, V], c_int),
+    "lca_quantize_rows_e4m3": ([V, c_int64, c_int, V, V, V], c_int),
+    "csa_compress_kv_ex": ([P, CV, c_int, c_int, V, c_int64, c_int, V, c_int64, V, V, V, c_int, V, c_int, V, c_int64,
+                            c_int64, V], c_int),
+    "hca_compress_kv_ex": ([P, CV, c_int, c_int, V, c_int64, c_int, V, c_int64, V, V, V, c_int, V, c_int, V, c_int64,
+                            c_int64, V], c_int),
+    "csa_indexer_scores_e4m3": ([P, c_int, c_int, V, V, V, V, c_int64, V, c_int64, c_int64, V, V, c_int64, V], c_int),
+    "csa_indexer_topk_e4m3": ([P, c_int, c_int, V, V, V, V, c_int64, V, c_int64, c_int64, V, V, V, c_size_t, V],
+                              c_int),
     "lca_status_string": ([c_int], ctypes.c_char_p),
     "lca_last_error": ([], ctypes.c_char_p),
     "lca_device_error": ([V, ctypes.POINTER(ctypes.c_uint32)], c_int),

@@ -155,6 +155,103 @@ def _idx_q(q_idx, w_idx, p):
     return B, n_q
 
 
+def lca_quantize_rows_e4m3(x, q, scale, stream=None):
+    """Per-row e4m3 codes q (uint8, x's shape) and scales (float32, one per row of the last dim)
+    of the bf16 rows of x."""
+    if not x.is_contiguous() or x.dtype != torch.bfloat16:
+        raise ValueError("x must be a contiguous bf16 tensor")
+    width = x.shape[-1]
+    rows = x.numel() // width
+    if q.dtype != torch.uint8 or q.numel() != x.numel() or not q.is_contiguous():
+        raise ValueError("q must be a contiguous uint8 tensor with x's size")
+    _holds(scale, rows, "scale", exact=True)
+    st = _lib.load().lca_quantize_rows_e4m3(_ptr(x, torch.bfloat16, "x"), rows, width, _ptr(q, torch.uint8, "q"),
+                                            _ptr(scale, torch.float32, "scale"), _stream(stream))
+    _check(st)
+
+
+def compress_kv_ex(csa: bool, p: AttnParams, tok_v, tok_z, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new,
+                   cache, cache_scale=None, per_channel=False, stream=None):
+    """csa_compress_kv_ex / hca_compress_kv_ex.  per_channel: tok_z [B, n_tok, width] and pos_bias
+    [span, width]; a uint8 cache [B, rows, width] is e4m3 with cache_scale [B, rows] (float32)."""
+    B, n_tok, width = tok_v.shape
+    span = 2 * p.ratio if csa else p.ratio
+    if per_channel:
+        if tok_z.dim() != 3 or tuple(tok_z.shape) != (B, n_tok, width) or tok_z.stride(2) != 1 or \
+                tok_z.stride(1) != width:
+            raise ValueError("per-channel tok_z must be [B, n_tok, width] with dense rows")
+        _holds(pos_bias, span * width, "pos_bias", exact=True)
+    else:
+        if tok_z.dim() != 2 or tok_z.stride(1) != 1 or tok_z.shape[0] != B:
+            raise ValueError("tok_z must be [B, n_tok] with unit inner stride")
+        _holds(pos_bias, span, "pos_bias")
+    if cache.shape[0] != B or cache.shape[2] != width:
+        raise ValueError("cache must be [B, rows, width]")
+    e4m3 = cache.dtype == torch.uint8
+    if e4m3:
+        if cache_scale is None or cache_scale.dim() != 2 or tuple(cache_scale.shape) != (B, cache.shape[1]) or \
+                cache_scale.stride(1) != 1:
+            raise ValueError("an e4m3 cache needs cache_scale [B, rows] (float32, unit inner stride)")
+    _holds(tok_pos0, B, "tok_pos0")
+    _holds(first_entry, B, "first_entry")
+    _holds(gamma, width, "gamma")
+    var = _lib.lca_compress_variant(int(per_channel), int(e4m3),
+                                    _ptr(cache_scale, torch.float32, "cache_scale") if e4m3 else None,
+                                    cache_scale.stride(0) if e4m3 else 0)
+    lib = _lib.load()
+    fn = lib.csa_compress_kv_ex if csa else lib.hca_compress_kv_ex
+    st = fn(ctypes.byref(p.c()), ctypes.byref(var), B, width,
+            _ptr(tok_v, torch.bfloat16, "tok_v"), _rows(tok_v, "tok_v"), n_tok,
+            _ptr(tok_z, torch.float32, "tok_z"), tok_z.stride(0), _i32(tok_pos0, "tok_pos0"),
+            _ptr(pos_bias, torch.float32, "pos_bias"), _ptr(gamma, torch.float32, "gamma"), int(apply_rope),
+            _i32(first_entry, "first_entry"), int(n_new),
+            _ptr(cache, torch.uint8 if e4m3 else torch.bfloat16, "cache"), _rows(cache, "cache"), cache.shape[1],
+            _stream(stream))
+    _check(st)
+
+
+def _idx_q8(q8, qs, w, k8, ks, p):
+    if q8.dim() != 4 or not q8.is_contiguous() or tuple(q8.shape[2:]) != (p.idx_heads, p.idx_dim):
+        raise ValueError("q_idx8 must be a contiguous [B, n_q, H_I, d_I] uint8 tensor")
+    B, n_q = q8.shape[0], q8.shape[1]
+    _holds(qs, B * n_q * p.idx_heads, "q_scale", exact=True)
+    _holds(w, B * n_q * p.idx_heads, "w_idx", exact=True)
+    if ks.dim() != 2 or ks.shape[0] != k8.shape[0] or ks.shape[1] < k8.shape[1] or ks.stride(1) != 1:
+        raise ValueError("k_scale must be [B, >= rows] with unit inner stride")
+    return B, n_q
+
+
+def csa_indexer_scores_e4m3(p: AttnParams, q_idx8, q_scale, w_idx, k_cache8, k_scale, q_pos, scores, stream=None):
+    """csa_indexer_scores over e4m3 queries and keys (codes uint8, per-row float32 scales)."""
+    B, n_q = _idx_q8(q_idx8, q_scale, w_idx, k_cache8, k_scale, p)
+    if scores.dim() != 3 or scores.stride(2) != 1 or scores.stride(1) != scores.shape[2] or \
+            scores.stride(0) != n_q * scores.shape[2]:
+        raise ValueError("scores must be a dense [B, n_q, stride] tensor")
+    _holds(q_pos, B * n_q, "q_pos", exact=True)
+    st = _lib.load().csa_indexer_scores_e4m3(
+        ctypes.byref(p.c()), B, n_q, _ptr(q_idx8, torch.uint8, "q_idx8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(w_idx, torch.float32, "w_idx"), _ptr(k_cache8, torch.uint8, "k_cache8"), _rows(k_cache8, "k_cache8"),
+        _ptr(k_scale, torch.float32, "k_scale"), k_scale.stride(0), k_cache8.shape[1], _i32(q_pos, "q_pos"),
+        _ptr(scores, torch.float32, "scores"), scores.shape[2], _stream(stream))
+    _check(st)
+
+
+def csa_indexer_topk_e4m3(p: AttnParams, q_idx8, q_scale, w_idx, k_cache8, k_scale, q_pos, out_idx, workspace,
+                          stream=None):
+    """csa_indexer_topk over e4m3 queries and keys; workspace from csa_indexer_workspace."""
+    B, n_q = _idx_q8(q_idx8, q_scale, w_idx, k_cache8, k_scale, p)
+    if tuple(out_idx.shape) != (B, n_q, p.topk):
+        raise ValueError("out_idx must be [B, n_q, topk]")
+    _holds(q_pos, B * n_q, "q_pos", exact=True)
+    st = _lib.load().csa_indexer_topk_e4m3(
+        ctypes.byref(p.c()), B, n_q, _ptr(q_idx8, torch.uint8, "q_idx8"), _ptr(q_scale, torch.float32, "q_scale"),
+        _ptr(w_idx, torch.float32, "w_idx"), _ptr(k_cache8, torch.uint8, "k_cache8"), _rows(k_cache8, "k_cache8"),
+        _ptr(k_scale, torch.float32, "k_scale"), k_scale.stride(0), k_cache8.shape[1], _i32(q_pos, "q_pos"),
+        _i32(out_idx, "out_idx"), _ptr(workspace, None, "workspace"), workspace.numel() * workspace.element_size(),
+        _stream(stream))
+    _check(st)
+
+
 def csa_indexer_scores(p: AttnParams, q_idx, w_idx, k_cache, q_pos, scores, stream=None):
     """scores[b, i, j] = sum_h w[b,i,h] ReLU(q[b,i,h] . k[b,j]) for j < n_vis(i), -inf beyond."""
     B, n_q = _idx_q(q_idx, w_idx, p)

@@ -141,6 +141,26 @@ __device__ __forceinline__ void rope_cs(const RopeTable &t, int d, int64_t pos, 
     sincospif(two_frac, &sn, &cs);
 }
 
+// e4m3 codes (FP8 caches): round to nearest even, magnitudes past 448 saturate.  hi's code is
+// the upper byte of the result, lo's the lower one.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// The e4m3 codes of f[0..8) / s (IEEE divisions), in memory order; s > 0.
+__device__ __forceinline__ uint2 e4m3x8(const float *f, float s) {
+    uint32_t w[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint32_t lo = cvt_e4m3x2(__fdiv_rn(f[4 * h + 1], s), __fdiv_rn(f[4 * h], s));
+        const uint32_t hi = cvt_e4m3x2(__fdiv_rn(f[4 * h + 3], s), __fdiv_rn(f[4 * h + 2], s));
+        w[h] = lo | (hi << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
 // Order-preserving map of a float to uint32 (larger float -> larger key); -0 maps like +0.
 __device__ __forceinline__ uint32_t ordered_key(float f) {
     if (f == 0.0f) f = 0.0f;

@@ -48,20 +48,26 @@ struct IndexerTcArgs {
     // fused selection (FUSE): k per query, the ascending lists, the candidate buffers
     int k;
     int32_t *out_idx;           // [B][n_q][k]
-    uint2 *cand;                // [grid][2 groups][2 queries][2 buffers][kStCap] (key, index)
+    uint2 *cand;                // fused selection's candidate buffers (key, index)
+    // e4m3 rows (FP8): per (query, head) query scales, per entry key scales
+    const float *q_scale;       // [B][n_q][HI]
+    const float *k_scale;       // [B] rows of ks_bs
+    int64_t ks_bs;
 };
 
-template <int DI, int HI, int QPT, bool FUSE = false>
+template <int DI, int HI, int QPT, bool FUSE = false, bool FP8 = false>
 struct IndexerTcConfig {
     static constexpr int N = HI * QPT;                       // MMA N: columns per tile
-    static constexpr int BOX = DI < 64 ? DI : 64;            // elements per TMA box row
+    static constexpr int ESZ = FP8 ? 1 : 2;                  // bytes per element (e4m3 or bf16)
+    static constexpr int BOX = DI * ESZ < 128 ? DI : 128 / ESZ;   // elements per TMA box row
     static constexpr int NBOX = DI / BOX;                    // boxes per row
-    static constexpr int ROWB = BOX * 2;                     // bytes per box row (128 or 64)
+    static constexpr int ROWB = BOX * ESZ;                   // bytes per box row (128 or 64)
     static constexpr uint32_t SWZ = ROWB == 128 ? ptx::kSwizzle128 : ptx::kSwizzle64;
-    static constexpr int KSTEPS_PER_BOX = BOX / 16;
-    static constexpr int KSTEPS = DI / 16;
-    static constexpr int TILE_BYTES = 128 * DI * 2;          // one key tile
-    static constexpr int Q_BYTES = N * DI * 2;               // one query tile
+    static constexpr int KMMA = 32 / ESZ;                    // K per MMA: 32 bytes of a row
+    static constexpr int KSTEPS_PER_BOX = BOX / KMMA;
+    static constexpr int KSTEPS = DI / KMMA;
+    static constexpr int TILE_BYTES = 128 * DI * ESZ;        // one key tile
+    static constexpr int Q_BYTES = N * DI * ESZ;             // one query tile
     // epilogue warps: two sets of 4 at N = 256 (set s reads accumulator buffer s), one set of
     // 8 at N = 128, of 4 below
     static constexpr int EPI_WARPS = N > 64 ? 8 : 4;
@@ -122,11 +128,11 @@ struct ItemCursor {
     }
 };
 
-template <int DI, int HI, int QPT, bool FUSE = false>
-__global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE>::THREADS, 1)
+template <int DI, int HI, int QPT, bool FUSE = false, bool FP8 = false>
+__global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
                       IndexerTcArgs a) {
-    using Cfg = IndexerTcConfig<DI, HI, QPT, FUSE>;
+    using Cfg = IndexerTcConfig<DI, HI, QPT, FUSE, FP8>;
     constexpr int N = Cfg::N, STAGES = Cfg::STAGES;
     pdl_trigger();
     extern __shared__ uint8_t smem_raw[];
@@ -258,7 +264,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE>::THREADS, 1
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA issue ----
         if (lane == 0) {
-            constexpr uint32_t idesc = ptx::idesc_bf16(128, N, false, false);
+            constexpr uint32_t idesc = FP8 ? ptx::idesc_e4m3(128, N) : ptx::idesc_bf16(128, N, false, false);
             int64_t cur = -1;
             int64_t vis = 0;
             uint32_t use = 0, groups_seen = 0, acc_use[Cfg::ACC_BUFS] = {};
@@ -301,8 +307,10 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE>::THREADS, 1
 #pragma unroll
                 for (int kk = 0; kk < Cfg::KSTEPS; ++kk) {
                     const int bx = kk / Cfg::KSTEPS_PER_BOX, within = kk % Cfg::KSTEPS_PER_BOX;
-                    ptx::mma_bf16(d, a_desc + (uint64_t)((bx * 128 * Cfg::ROWB + within * 32) >> 4),
-                                  q_desc + (uint64_t)((bx * N * Cfg::ROWB + within * 32) >> 4), idesc, kk > 0);
+                    const uint64_t ad = a_desc + (uint64_t)((bx * 128 * Cfg::ROWB + within * 32) >> 4);
+                    const uint64_t bd = q_desc + (uint64_t)((bx * N * Cfg::ROWB + within * 32) >> 4);
+                    if constexpr (FP8) ptx::mma_e4m3(d, ad, bd, idesc, kk > 0);
+                    else ptx::mma_bf16(d, ad, bd, idesc, kk > 0);
                 }
                 issued = true;
                 ptx::mma_commit(&empty[s]);
@@ -366,7 +374,9 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE>::THREADS, 1
                 __syncwarp();                            // the last group's weights are read
                 for (int c = lane; c < Cfg::COLS_PER_WG; c += 32) {
                     const int qi = g * QPT + col0 / HI + c / HI;
-                    wr[c] = qi < a.n_q ? __ldg(a.w + ((int64_t)b * a.n_q + qi) * HI + c % HI) : 0.f;
+                    const int64_t wi = ((int64_t)b * a.n_q + qi) * HI + c % HI;
+                    // e4m3 queries: the (non-negative) query scale moves out of the ReLU into the weight
+                    wr[c] = qi < a.n_q ? (FP8 ? __ldg(a.w + wi) * __ldg(a.q_scale + wi) : __ldg(a.w + wi)) : 0.f;
                 }
                 __syncwarp();
 #pragma unroll
@@ -438,6 +448,12 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE>::THREADS, 1
                 }
 #pragma unroll
                 for (int q = 0; q < QW; ++q) sc[q] = (ps[q][0] + ps[q][1]) + (ps[q][2] + ps[q][3]);
+                if constexpr (FP8) {
+                    // e4m3 keys: the entry's (non-negative) scale multiplies the head sum
+                    const float ks = j < a.cache_rows ? __ldg(a.k_scale + (int64_t)b * a.ks_bs + j) : 0.f;
+#pragma unroll
+                    for (int q = 0; q < QW; ++q) sc[q] *= ks;
+                }
                 ++acc_use[acc];
                 acc = acc + 1 == Cfg::ACC_BUFS ? 0 : acc + 1;
             }

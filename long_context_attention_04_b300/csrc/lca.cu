@@ -13,6 +13,7 @@
 #include "../../include/lca.h"
 #include "common.cuh"
 #include "compress.cuh"
+#include "quant.cuh"
 #include "topk.cuh"
 #include "indexer_tc.cuh"
 #include "attend_common.cuh"
@@ -93,7 +94,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // A bf16 tensor map of rank 2 or 3 (dims innermost first, strides in bytes for dims 1..),
 // tiled boxes with the given swizzle; out-of-range elements read as zero.
 bool make_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_t *dims, const uint64_t *strides,
-                     const uint32_t *box, CUtensorMapSwizzle swizzle) {
+                     const uint32_t *box, CUtensorMapSwizzle swizzle,
+                     CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
     cuuint64_t gd[3], gs[2];
@@ -103,7 +105,7 @@ bool make_tensor_map(CUtensorMap *map, const void *base, int rank, const uint64_
         bd[i] = box[i];
     }
     for (int i = 0; i < rank - 1; ++i) gs[i] = strides[i];
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void *>(base), gd, gs, bd, es,
+    CUresult r = enc(map, dtype, rank, const_cast<void *>(base), gd, gs, bd, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -138,11 +140,13 @@ RowNormRope make_nr(const lca_attn_params *p, const float *gamma, int apply_rope
     return nr;
 }
 
-lca_status compress_impl(const char *name, bool overlap, const lca_attn_params *p, int batch, int width,
+lca_status compress_impl(const char *name, bool overlap, const lca_compress_variant *variant,
+                         const lca_attn_params *p, int batch, int width,
                          const lca_bf16 *tok_v, int64_t tok_v_bs, int n_tok, const float *tok_z,
                          int64_t tok_z_bs, const int32_t *tok_pos0, const float *pos_bias,
                          const float *gamma, int apply_rope, const int32_t *first_entry, int n_new,
-                         lca_bf16 *cache, int64_t cache_bs, int64_t cache_rows, cudaStream_t stream) {
+                         void *cache, int64_t cache_bs, int64_t cache_rows, cudaStream_t stream) {
+    const bool pc = variant && variant->per_channel, fp8 = variant && variant->e4m3;
     LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
     LCA_REQUIRE(batch > 0 && n_tok > 0 && n_new >= 0, LCA_ERR_INVALID_ARG,
                 "%s: batch (%d) and n_tok (%d) must be positive, n_new (%d) >= 0", name, batch, n_tok, n_new);
@@ -153,13 +157,20 @@ lca_status compress_impl(const char *name, bool overlap, const lca_attn_params *
     LCA_REQUIRE(span <= kMaxSpan, LCA_ERR_UNSUPPORTED, "%s: window of %d tokens exceeds %d", name, span, kMaxSpan);
     LCA_REQUIRE(tok_v && tok_z && tok_pos0 && pos_bias && first_entry && cache, LCA_ERR_INVALID_ARG,
                 "%s: a required pointer is NULL", name);
-    LCA_REQUIRE(aligned16(tok_v) && aligned16(cache), LCA_ERR_INVALID_ARG,
-                "%s: tok_v and cache must be 16-byte aligned", name);
+    LCA_REQUIRE(aligned16(tok_v) && (fp8 ? reinterpret_cast<uintptr_t>(cache) % 8 == 0 : aligned16(cache)),
+                LCA_ERR_INVALID_ARG, "%s: tok_v must be 16-byte aligned, cache 16 (bf16) or 8 (e4m3)", name);
     LCA_REQUIRE(tok_v_bs % 8 == 0 && cache_bs % 8 == 0, LCA_ERR_INVALID_ARG,
                 "%s: batch strides must be multiples of 8 elements", name);
-    LCA_REQUIRE(batch == 1 || (tok_v_bs >= (int64_t)n_tok * width && tok_z_bs >= n_tok &&
+    const int64_t z_row = pc ? (int64_t)width : 1;           // logits per token
+    LCA_REQUIRE(batch == 1 || (tok_v_bs >= (int64_t)n_tok * width && tok_z_bs >= n_tok * z_row &&
                                cache_bs >= cache_rows * width),
                 LCA_ERR_INVALID_ARG, "%s: batch strides smaller than one sequence", name);
+    if (pc)
+        LCA_REQUIRE(aligned16(tok_z) && aligned16(pos_bias) && tok_z_bs % 4 == 0, LCA_ERR_INVALID_ARG,
+                    "%s: per-channel tok_z and pos_bias must be 16-byte aligned, tok_z stride %% 4", name);
+    if (fp8)
+        LCA_REQUIRE(variant->cache_scale && (batch == 1 || variant->scale_batch_stride >= cache_rows),
+                    LCA_ERR_INVALID_ARG, "%s: e4m3 cache needs cache_scale with a stride >= cache_rows", name);
     LCA_REQUIRE(cache_rows > 0, LCA_ERR_INVALID_ARG, "%s: cache_rows must be positive", name);
     if (apply_rope)
         LCA_REQUIRE(p->rope_dims > 0 && p->rope_dims % 2 == 0 && p->rope_dims <= width &&
@@ -180,12 +191,21 @@ lca_status compress_impl(const char *name, bool overlap, const lca_attn_params *
     a.bias = pos_bias;
     a.first_entry = first_entry;
     a.n_new = n_new;
-    a.cache = reinterpret_cast<__nv_bfloat16 *>(cache);
+    a.cache = fp8 ? nullptr : reinterpret_cast<__nv_bfloat16 *>(cache);
+    a.cache8 = fp8 ? reinterpret_cast<uint8_t *>(cache) : nullptr;
+    a.cache_scale = fp8 ? variant->cache_scale : nullptr;
+    a.scale_bs = fp8 ? variant->scale_batch_stride : 0;
     a.cache_bs = cache_bs;
     a.cache_rows = cache_rows;
     a.nr = make_nr(p, gamma, apply_rope);
     const int threads = compress_threads(width, a.span);
-    launch_pdl(compress_kernel, dim3(n_new, batch), dim3(threads), threads * 8 * sizeof(float), stream, a);
+    const size_t smem = compress_smem(threads, pc);
+    auto launch = [&](auto kern) {
+        if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        launch_pdl(kern, dim3(n_new, batch), dim3(threads), smem, stream, a);
+    };
+    if (pc) fp8 ? launch(compress_kernel<true, true>) : launch(compress_kernel<true, false>);
+    else fp8 ? launch(compress_kernel<false, true>) : launch(compress_kernel<false, false>);
     lca_status s = check_launch(name);
     return s == LCA_OK ? ok() : s;
 }
@@ -378,31 +398,33 @@ lca_status indexer_validate(const char *name, const lca_attn_params *p, int batc
     return LCA_OK;
 }
 
-template <int DI, int HI, int QPT, bool FUSE = false>
-lca_status indexer_tc_launch(int batch, int n_q, const lca_bf16 *q_idx, const lca_bf16 *k_cache, int64_t k_bs,
+template <int DI, int HI, int QPT, bool FUSE = false, bool FP8 = false>
+lca_status indexer_tc_launch(int batch, int n_q, const void *q_idx, const void *k_cache, int64_t k_bs,
                              IndexerTcArgs &a, cudaStream_t stream) {
-    using Cfg = IndexerTcConfig<DI, HI, QPT, FUSE>;
+    using Cfg = IndexerTcConfig<DI, HI, QPT, FUSE, FP8>;
     const CUtensorMapSwizzle sw = Cfg::ROWB == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    const CUtensorMapDataType dt = FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    constexpr uint64_t E = Cfg::ESZ;
     CUtensorMap kmap, qmap;
     const uint64_t kd[3] = {(uint64_t)DI, (uint64_t)a.cache_rows, (uint64_t)batch};
-    const uint64_t ks[2] = {(uint64_t)DI * 2, (uint64_t)k_bs * 2};
+    const uint64_t ks[2] = {(uint64_t)DI * E, (uint64_t)k_bs * E};
     const uint32_t kb[3] = {(uint32_t)Cfg::BOX, 128u, 1u};
-    if (!make_tensor_map(&kmap, k_cache, 3, kd, ks, kb, sw))
+    if (!make_tensor_map(&kmap, k_cache, 3, kd, ks, kb, sw, dt))
         return fail(LCA_ERR_CUDA, "csa_indexer_scores: key tensor map rejected by the driver");
     const uint64_t qd[2] = {(uint64_t)DI, (uint64_t)batch * n_q * HI};
-    const uint64_t qs[1] = {(uint64_t)DI * 2};
+    const uint64_t qs[1] = {(uint64_t)DI * E};
     const uint32_t qb[2] = {(uint32_t)Cfg::BOX, (uint32_t)Cfg::N};
-    if (!make_tensor_map(&qmap, q_idx, 2, qd, qs, qb, sw))
+    if (!make_tensor_map(&qmap, q_idx, 2, qd, qs, qb, sw, dt))
         return fail(LCA_ERR_CUDA, "csa_indexer_scores: query tensor map rejected by the driver");
     a.groups = (n_q + QPT - 1) / QPT;
     a.tiles = (int)ceil_div64(a.cache_rows, 128);
     a.items = (int64_t)batch * a.groups * a.tiles;
     // the fused selection hands each CTA whole query groups
     const int grid = (int)std::min<int64_t>(FUSE ? (int64_t)batch * a.groups : a.items, device_sm_count());
-    cudaFuncSetAttribute(indexer_tc_kernel<DI, HI, QPT, FUSE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaFuncSetAttribute(indexer_tc_kernel<DI, HI, QPT, FUSE, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg::SMEM_BYTES);
-    launch_pdl(indexer_tc_kernel<DI, HI, QPT, FUSE>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, kmap, qmap,
-               a);
+    launch_pdl(indexer_tc_kernel<DI, HI, QPT, FUSE, FP8>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, kmap,
+               qmap, a);
     return check_launch(FUSE ? "csa_indexer_topk" : "csa_indexer_scores");
 }
 
@@ -466,6 +488,50 @@ lca_status topk_launch(const lca_attn_params *p, int batch, int n_q, const float
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_topk: launch failed: %s", cudaGetErrorString(e));
     return check_launch("lca_topk");
+}
+
+lca_status indexer_e4m3_validate(const char *name, const lca_attn_params *p, int batch, int n_q, const uint8_t *q8,
+                                 const float *q_scale, const float *w_idx, const uint8_t *k8, int64_t k_bs,
+                                 const float *k_scale, int64_t ks_bs, int64_t cache_rows, const int32_t *q_pos) {
+    LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
+    LCA_REQUIRE(batch > 0 && n_q > 0 && cache_rows > 0, LCA_ERR_INVALID_ARG,
+                "%s: batch, n_q and cache_rows must be positive", name);
+    LCA_REQUIRE(p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
+    LCA_REQUIRE(p->idx_dim == 128 && p->idx_heads == 64, LCA_ERR_UNSUPPORTED,
+                "%s: e4m3 indexer supports 64 heads of dim 128 (got %d, %d)", name, p->idx_heads, p->idx_dim);
+    LCA_REQUIRE(q8 && q_scale && w_idx && k8 && k_scale && q_pos, LCA_ERR_INVALID_ARG,
+                "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(aligned16(q8) && aligned16(k8), LCA_ERR_INVALID_ARG, "%s: q_idx8 and k_cache8 must be 16-byte aligned",
+                name);
+    LCA_REQUIRE(k_bs % 16 == 0 && (batch == 1 || (k_bs >= cache_rows * p->idx_dim && ks_bs >= cache_rows)),
+                LCA_ERR_INVALID_ARG, "%s: bad k_batch_stride / k_scale_batch_stride", name);
+    return LCA_OK;
+}
+
+IndexerTcArgs indexer_e4m3_args(const lca_attn_params *p, int n_q, const float *q_scale, const float *w_idx,
+                                const float *k_scale, int64_t ks_bs, int64_t cache_rows, const int32_t *q_pos) {
+    IndexerTcArgs a = {};
+    a.n_q = n_q;
+    a.ratio = p->ratio;
+    a.cache_rows = cache_rows;
+    a.w = w_idx;
+    a.q_pos = q_pos;
+    a.q_scale = q_scale;
+    a.k_scale = k_scale;
+    a.ks_bs = ks_bs;
+    return a;
+}
+
+lca_status indexer_e4m3_scores_launch(const lca_attn_params *p, int batch, int n_q, const uint8_t *q8,
+                                      const float *q_scale, const float *w_idx, const uint8_t *k8, int64_t k_bs,
+                                      const float *k_scale, int64_t ks_bs, int64_t cache_rows, const int32_t *q_pos,
+                                      float *scores, int64_t s_stride, cudaStream_t stream) {
+    IndexerTcArgs a = indexer_e4m3_args(p, n_q, q_scale, w_idx, k_scale, ks_bs, cache_rows, q_pos);
+    a.scores = scores;
+    a.stride = s_stride;
+    if (n_q == 1) return indexer_tc_launch<128, 64, 1, false, true>(batch, n_q, q8, k8, k_bs, a, stream);
+    if (n_q == 2) return indexer_tc_launch<128, 64, 2, false, true>(batch, n_q, q8, k8, k_bs, a, stream);
+    return indexer_tc_launch<128, 64, 4, false, true>(batch, n_q, q8, k8, k_bs, a, stream);
 }
 
 size_t indexer_ws_bytes(int batch, int n_q, int64_t cache_rows) {
@@ -534,7 +600,7 @@ lca_status csa_compress_kv(const lca_attn_params *p, int batch, int width, const
                            const int32_t *tok_pos0, const float *pos_bias, const float *gamma, int apply_rope,
                            const int32_t *first_entry, int n_new, lca_bf16 *cache, int64_t cache_batch_stride,
                            int64_t cache_rows, cudaStream_t stream) {
-    return compress_impl("csa_compress_kv", true, p, batch, width, tok_v, tok_v_batch_stride, n_tok, tok_z,
+    return compress_impl("csa_compress_kv", true, nullptr, p, batch, width, tok_v, tok_v_batch_stride, n_tok, tok_z,
                          tok_z_batch_stride, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache,
                          cache_batch_stride, cache_rows, stream);
 }
@@ -544,9 +610,52 @@ lca_status hca_compress_kv(const lca_attn_params *p, int batch, int width, const
                            const int32_t *tok_pos0, const float *pos_bias, const float *gamma, int apply_rope,
                            const int32_t *first_entry, int n_new, lca_bf16 *cache, int64_t cache_batch_stride,
                            int64_t cache_rows, cudaStream_t stream) {
-    return compress_impl("hca_compress_kv", false, p, batch, width, tok_v, tok_v_batch_stride, n_tok, tok_z,
+    return compress_impl("hca_compress_kv", false, nullptr, p, batch, width, tok_v, tok_v_batch_stride, n_tok, tok_z,
                          tok_z_batch_stride, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache,
                          cache_batch_stride, cache_rows, stream);
+}
+
+lca_status csa_compress_kv_ex(const lca_attn_params *p, const lca_compress_variant *variant, int batch, int width,
+                              const lca_bf16 *tok_v, int64_t tok_v_batch_stride, int n_tok, const float *tok_z,
+                              int64_t tok_z_batch_stride, const int32_t *tok_pos0, const float *pos_bias,
+                              const float *gamma, int apply_rope, const int32_t *first_entry, int n_new, void *cache,
+                              int64_t cache_batch_stride, int64_t cache_rows, cudaStream_t stream) {
+    LCA_REQUIRE(variant, LCA_ERR_INVALID_ARG, "csa_compress_kv_ex: variant is NULL");
+    return compress_impl("csa_compress_kv_ex", true, variant, p, batch, width, tok_v, tok_v_batch_stride, n_tok,
+                         tok_z, tok_z_batch_stride, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache,
+                         cache_batch_stride, cache_rows, stream);
+}
+
+lca_status hca_compress_kv_ex(const lca_attn_params *p, const lca_compress_variant *variant, int batch, int width,
+                              const lca_bf16 *tok_v, int64_t tok_v_batch_stride, int n_tok, const float *tok_z,
+                              int64_t tok_z_batch_stride, const int32_t *tok_pos0, const float *pos_bias,
+                              const float *gamma, int apply_rope, const int32_t *first_entry, int n_new, void *cache,
+                              int64_t cache_batch_stride, int64_t cache_rows, cudaStream_t stream) {
+    LCA_REQUIRE(variant, LCA_ERR_INVALID_ARG, "hca_compress_kv_ex: variant is NULL");
+    return compress_impl("hca_compress_kv_ex", false, variant, p, batch, width, tok_v, tok_v_batch_stride, n_tok,
+                         tok_z, tok_z_batch_stride, tok_pos0, pos_bias, gamma, apply_rope, first_entry, n_new, cache,
+                         cache_batch_stride, cache_rows, stream);
+}
+
+lca_status lca_quantize_rows_e4m3(const lca_bf16 *x, int64_t rows, int width, uint8_t *q, float *scale,
+                                  cudaStream_t stream) {
+    const char *name = "lca_quantize_rows_e4m3";
+    LCA_REQUIRE(x && q && scale, LCA_ERR_INVALID_ARG, "%s: a required pointer is NULL", name);
+    LCA_REQUIRE(rows >= 0 && width >= 8 && width <= 32 * kQuantMaxChunks * 8 && width % 8 == 0, LCA_ERR_INVALID_ARG,
+                "%s: width %d must be a multiple of 8 in [8, %d], rows >= 0", name, width, 32 * kQuantMaxChunks * 8);
+    LCA_REQUIRE(aligned16(x) && reinterpret_cast<uintptr_t>(q) % 8 == 0, LCA_ERR_INVALID_ARG,
+                "%s: x must be 16-byte aligned and q 8-byte aligned", name);
+    if (rows == 0) return ok();
+    LCA_REQUIRE(ceil_div64(rows, kQuantWarps) <= INT32_MAX, LCA_ERR_UNSUPPORTED, "%s: too many rows", name);
+    QuantArgs a;
+    a.x = reinterpret_cast<const __nv_bfloat16 *>(x);
+    a.rows = rows;
+    a.width = width;
+    a.q = q;
+    a.scale = scale;
+    launch_pdl(quantize_rows_kernel, (int)ceil_div64(rows, kQuantWarps), dim3(32 * kQuantWarps), 0, stream, a);
+    lca_status s = check_launch(name);
+    return s == LCA_OK ? ok() : s;
 }
 
 lca_status lca_window_update(const lca_attn_params *p, int batch, const lca_bf16 *tok_v, int64_t tok_v_batch_stride,
@@ -643,6 +752,53 @@ lca_status csa_indexer_topk(const lca_attn_params *p, int batch, int n_q, const 
     float *scores = static_cast<float *>(workspace);
     st = indexer_launch(p, batch, n_q, q_idx, w_idx, k_cache, k_batch_stride, cache_rows, q_pos, scores, stride,
                         stream);
+    if (st != LCA_OK) return st;
+    st = topk_launch(p, batch, n_q, scores, stride, q_pos, cache_rows, out_idx, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+lca_status csa_indexer_scores_e4m3(const lca_attn_params *p, int batch, int n_q, const uint8_t *q_idx8,
+                                   const float *q_scale, const float *w_idx, const uint8_t *k_cache8,
+                                   int64_t k_batch_stride, const float *k_scale, int64_t k_scale_batch_stride,
+                                   int64_t cache_rows, const int32_t *q_pos, float *scores, int64_t scores_stride,
+                                   cudaStream_t stream) {
+    const char *name = "csa_indexer_scores_e4m3";
+    lca_status st = indexer_e4m3_validate(name, p, batch, n_q, q_idx8, q_scale, w_idx, k_cache8, k_batch_stride,
+                                          k_scale, k_scale_batch_stride, cache_rows, q_pos);
+    if (st != LCA_OK) return st;
+    LCA_REQUIRE(scores && aligned16(scores) && scores_stride >= cache_rows && scores_stride % 4 == 0,
+                LCA_ERR_INVALID_ARG, "%s: scores must be 16-byte aligned with a stride >= cache_rows, %% 4", name);
+    st = indexer_e4m3_scores_launch(p, batch, n_q, q_idx8, q_scale, w_idx, k_cache8, k_batch_stride, k_scale,
+                                    k_scale_batch_stride, cache_rows, q_pos, scores, scores_stride, stream);
+    return st == LCA_OK ? ok() : st;
+}
+
+lca_status csa_indexer_topk_e4m3(const lca_attn_params *p, int batch, int n_q, const uint8_t *q_idx8,
+                                 const float *q_scale, const float *w_idx, const uint8_t *k_cache8,
+                                 int64_t k_batch_stride, const float *k_scale, int64_t k_scale_batch_stride,
+                                 int64_t cache_rows, const int32_t *q_pos, int32_t *out_idx, void *workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+    const char *name = "csa_indexer_topk_e4m3";
+    lca_status st = indexer_e4m3_validate(name, p, batch, n_q, q_idx8, q_scale, w_idx, k_cache8, k_batch_stride,
+                                          k_scale, k_scale_batch_stride, cache_rows, q_pos);
+    if (st != LCA_OK) return st;
+    LCA_REQUIRE(p->topk >= 1, LCA_ERR_INVALID_ARG, "%s: topk must be positive", name);
+    LCA_REQUIRE(out_idx, LCA_ERR_INVALID_ARG, "%s: out_idx is NULL", name);
+    const size_t need = csa_indexer_workspace(p, batch, n_q, cache_rows);
+    LCA_REQUIRE(workspace && aligned16(workspace) && workspace_bytes >= need, LCA_ERR_WORKSPACE,
+                "%s: workspace of %zu bytes (16-byte aligned) needed, got %zu", name, need, workspace_bytes);
+    if (indexer_fused(p, n_q)) {
+        IndexerTcArgs a = indexer_e4m3_args(p, n_q, q_scale, w_idx, k_scale, k_scale_batch_stride, cache_rows, q_pos);
+        a.k = p->topk;
+        a.out_idx = out_idx;
+        a.cand = static_cast<uint2 *>(workspace);
+        st = indexer_tc_launch<128, 64, 4, true, true>(batch, n_q, q_idx8, k_cache8, k_batch_stride, a, stream);
+        return st == LCA_OK ? ok() : st;
+    }
+    const int64_t stride = (cache_rows + 3) & ~(int64_t)3;
+    float *scores = static_cast<float *>(workspace);
+    st = indexer_e4m3_scores_launch(p, batch, n_q, q_idx8, q_scale, w_idx, k_cache8, k_batch_stride, k_scale,
+                                    k_scale_batch_stride, cache_rows, q_pos, scores, stride, stream);
     if (st != LCA_OK) return st;
     st = topk_launch(p, batch, n_q, scores, stride, q_pos, cache_rows, out_idx, stream);
     return st == LCA_OK ? ok() : st;
