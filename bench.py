@@ -10,6 +10,7 @@ attention with split-K combine.  Workloads (sizes of the pages' V4-Flash configu
   csa_prefill_1m             one 8192-query chunk at 1M context
   csa_prefill_128k           one 2048-query chunk at 128K context (the same kernels, profiler-sized)
   csa_prefill_1m_scored      the 1M chunk with its scores written out and selected by a separate top-k
+  csa_decode_128k_fp8        csa_decode_128k with the indexer keys and queries in e4m3 (per-row scales)
 Inputs are seeded synthetic tensors (workloads.py); the caches are larger than L2 and L2 is
 also flushed between timed steps.  Under torchrun each rank runs the workload on its own
 GPU (sequences shard with no exchange: weak scaling); the value is all ranks' tokens over
@@ -271,7 +272,16 @@ class CsaDecode(Workload):
         d = wl.decode_inputs(rng, s, B, pos, entries, csa=True)
         self.d = d
         w = LayerWeights(d["gamma_kv"], d["gamma_q"], d["bias_kv"], d["sink"], d["bias_idx"])
-        self.layer = CsaLayer(self.p, w, d["kv_cache"], d["idx_cache"], d["win_kv"], n_q=1)
+        # e4m3 indexer keys: the synthetic bf16 key cache quantised once (per-row scales)
+        self.e4m3 = bool(cfg.get("idx_e4m3"))
+        if self.e4m3:
+            self.idx8 = torch.empty(d["idx_cache"].shape, dtype=torch.uint8, device="cuda")
+            self.idx8_scale = torch.empty(d["idx_cache"].shape[:2], dtype=torch.float32, device="cuda")
+            api.lca_quantize_rows_e4m3(d["idx_cache"], self.idx8, self.idx8_scale)
+            self.layer = CsaLayer(self.p, w, d["kv_cache"], self.idx8, d["win_kv"], n_q=1, idx_scale=self.idx8_scale)
+            api.lca_quantize_rows_e4m3(d["q_idx"], self.layer.q8, self.layer.q8_scale)
+        else:
+            self.layer = CsaLayer(self.p, w, d["kv_cache"], d["idx_cache"], d["win_kv"], n_q=1)
         i32 = dict(dtype=torch.int32, device="cuda")
         self.tok_pos0 = torch.full((B,), d["tok_pos0"], **i32)
         self.first = torch.full((B,), entries - 1, **i32)
@@ -280,7 +290,8 @@ class CsaDecode(Workload):
         self.out = torch.empty((B, 1, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
         self.scores = self.layer.ws_idx.view(torch.float32).view(B, 1, -1)
         self.tokens = B
-        self.launches = 8          # 2 compress, window, q prep, indexer, top-k, attention, combine
+        # 2 compress, window, q prep, (query quantisation,) indexer, top-k, attention, combine
+        self.launches = 9 if self.e4m3 else 8
         self.dominant = "indexer"
         # per-step inputs, pinned on the host for the end-to-end leg
         # (the selection's inputs first; the rest goes up on the side stream during the selection)
@@ -292,13 +303,22 @@ class CsaDecode(Workload):
         # algorithmic bytes of one indexer launch: keys of the visible entries, queries, weights (the
         # scores it writes are a workspace round trip to the top-k, so they are not counted)
         n_vis = (pos + 1) // s.ratio
-        self.dom_bytes = B * (n_vis * s.idx_dim * 2 + s.idx_heads * s.idx_dim * 2 + s.idx_heads * 4)
+        if self.e4m3:   # one byte per key element plus the row's scale; the query's codes and scales
+            self.dom_bytes = B * (n_vis * (s.idx_dim + 4) + s.idx_heads * s.idx_dim + s.idx_heads * 8)
+        else:
+            self.dom_bytes = B * (n_vis * s.idx_dim * 2 + s.idx_heads * s.idx_dim * 2 + s.idx_heads * 4)
         self.dom_flops = 2.0 * B * n_vis * s.idx_heads * s.idx_dim
         self.step_bytes, self.step_flops = csa_layer_work(s, B, n_vis, 1)
+        if self.e4m3:
+            self.step_bytes -= B * n_vis * (s.idx_dim - 4)
 
     def dominant_call(self):
-        d = self.d
-        self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], self.layer.idx_cache, self.q_pos, self.scores)
+        d, L = self.d, self.layer
+        if self.e4m3:
+            self.api.csa_indexer_scores_e4m3(self.p, L.q8, L.q8_scale, d["w_idx"], L.idx_cache, L.idx_scale,
+                                             self.q_pos, self.scores)
+        else:
+            self.api.csa_indexer_scores(self.p, d["q_idx"], d["w_idx"], L.idx_cache, self.q_pos, self.scores)
 
     def step(self, side_prologue=None):
         d = self.d
@@ -339,12 +359,25 @@ class CsaDecode(Workload):
             winb[self.pos % winb.shape[0]] = _round_bits(w_new)
             t2 = time.perf_counter()
             n_vis = oracle.visible_entries(self.pos, s.ratio)
-            sc = oracle.indexer_scores(qi, wi, ixb, n_vis)
+            t_fp8 = 0.0
+            if self.e4m3:
+                # the e4m3 key cache of the sequence (state before the step, not timed), then the
+                # step's own quantisations: the new key row and the queries
+                t4 = time.perf_counter()
+                k8, ks = oracle.quantize_rows_e4m3(ixb[:-1])
+                t5 = time.perf_counter()
+                kn8, kns = oracle.quantize_rows_e4m3(ixb[-1:])
+                q8, qs = oracle.quantize_rows_e4m3(qi)
+                sc = oracle.indexer_scores_e4m3(q8, qs, wi, np.concatenate([k8, kn8]), np.concatenate([ks, kns]),
+                                                n_vis)
+                t_fp8 = t5 - t4
+            else:
+                sc = oracle.indexer_scores(qi, wi, ixb, n_vis)
             idx = oracle.topk(sc, s.topk)
             oracle.attend(q, self.w_host["gamma_q"], self.pos, kvb, self.w_host["sink"], winb, winb.shape[0],
                           s.window, s.rope_dims, s.rope_base, s.rms_eps, self.p.scale, idx=idx)
             t3 = time.perf_counter()
-            t_total += (t1 - t0) + (t3 - t2)
+            t_total += (t1 - t0) + (t3 - t2) - t_fp8
             n_done += 1
             if t_total >= budget_s:
                 break
@@ -817,7 +850,7 @@ class MhcLayer(Workload):
 WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill,
              "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode, "mhc_prefill_8192": MhcLayer,
              "v4flash_decode_1m": BlockDecode, "csa_prefill_1m_proj": CsaPrefillProj,
-             "csa_prefill_1m_scored": CsaPrefill}
+             "csa_prefill_1m_scored": CsaPrefill, "csa_decode_128k_fp8": CsaDecode}
 
 
 # ------------------------------------------------------------------- distributed -----
@@ -988,8 +1021,8 @@ def measure(name: str, args, flush, world: int, device, rank: int, seed: int, sn
 # 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound), the hyper-connection
 # mixing around a layer for an 8192-token chunk (HBM-bound), the 43-layer V4-Flash attention
 # stack at decode (HBM-bound), and the prefill chunk with its input projections (tensor-bound).
-EXTRA_WORKLOADS = ("hca_decode_1m", "csa_prefill_1m", "csa_prefill_1m_scored", "block_decode_1m", "mhc_prefill_8192",
-                   "v4flash_decode_1m", "csa_prefill_1m_proj")
+EXTRA_WORKLOADS = ("csa_decode_128k_fp8", "hca_decode_1m", "csa_prefill_1m", "csa_prefill_1m_scored", "block_decode_1m",
+                   "mhc_prefill_8192", "v4flash_decode_1m", "csa_prefill_1m_proj")
 
 
 def run_ours(args):
@@ -1180,6 +1213,10 @@ class _HostOnly:
             self.qi = bf16_bits(rng.normal_bf16((s.idx_heads, s.idx_dim)))
             self.wi = (rng.normal_f32((s.idx_heads,)) / math.sqrt(s.idx_heads)).numpy()
             self.sample = "compression, window row, indexer over %d entries, top-%d, attention" % (entries, s.topk)
+            self.e4m3 = bool(cfg.get("idx_e4m3"))
+            if self.e4m3:               # the key cache in e4m3 (state before the token, not timed)
+                self.k8, self.ks = oracle.quantize_rows_e4m3(self.keys)
+                self.sample = self.sample.replace("indexer", "e4m3 indexer (keys and queries quantised)")
             self.proj = None
             if "hidden" in cfg:         # the token's input projections come first
                 self.proj = {k: bf16_bits(v) for k, v in wl.prefill_projection_weights(rng, s, cfg["hidden"]).items()}
@@ -1218,7 +1255,13 @@ class _HostOnly:
         scale = 1.0 / math.sqrt(s.head_dim)
         if self.kind != "hca_decode_1m":
             o.compress(self.tok_vi, self.tok_z, p0, bias, None, s.rms_eps, 0, s.rope_base, span, s.ratio, j, 1)
-            sc = o.indexer_scores(self.qi, self.wi, self.keys, o.visible_entries(self.pos, s.ratio))
+            n_vis = o.visible_entries(self.pos, s.ratio)
+            if getattr(self, "e4m3", False):
+                o.quantize_rows_e4m3(self.keys[-1:])             # the new key row
+                q8, qs = o.quantize_rows_e4m3(self.qi)
+                sc = o.indexer_scores_e4m3(q8, qs, self.wi, self.k8, self.ks, n_vis)
+            else:
+                sc = o.indexer_scores(self.qi, self.wi, self.keys, n_vis)
             idx = o.topk(sc, s.topk)
             o.attend(self.q, self.ones, self.pos, self.kv, self.sink, self.win, self.win.shape[0], s.window,
                      s.rope_dims, s.rope_base, s.rms_eps, scale, idx=idx)

@@ -17,11 +17,11 @@
 //              ring keeps 6 stages beside them), key tiles into a ring
 //   warp 1     TMEM allocator and MMA issuer (one thread), 2-4 accumulator buffers
 //   warps 2..  epilogue: TMEM -> registers, weighted ReLU sum per query, fp32 score store.
-//              With N = 256 (two accumulator buffers) the 8 epilogue warps form two sets of
-//              4 (a warp group each), set s reading the tiles of buffer s (every other computed
-//              tile): one set's TMEM reads overlap the other set's arithmetic, each set has two
-//              MMA periods per tile, and 10 warps leave 168 registers a thread.  Within a set a
-//              warp group owns COLS_PER_WG columns (whole queries).
+//              The 8 epilogue warps form two sets of 4 (a warp group each), set s reading the
+//              accumulator buffers b with b mod 2 = s (every other computed tile): one set's
+//              TMEM reads overlap the other set's arithmetic, each set has two MMA periods per
+//              tile, and 10 warps leave 168 registers a thread.  A set's warp group owns all
+//              N columns (whole queries).
 // With FUSE (prefill: 4 queries per tile) the epilogue selects each query's top k as the
 // scores stream (topk_stream.cuh) instead of storing them: every CTA takes whole query
 // groups, so a query's whole row passes through one selection group (the two warp groups,
@@ -67,11 +67,12 @@ struct IndexerTcConfig {
     static constexpr int KSTEPS_PER_BOX = BOX / KMMA;
     static constexpr int KSTEPS = DI / KMMA;
     static constexpr int TILE_BYTES = 128 * DI * ESZ;        // one key tile
+    static constexpr int SC_BYTES = FP8 ? 128 * 4 : 0;       // its 128 key scales (e4m3)
     static constexpr int Q_BYTES = N * DI * ESZ;             // one query tile
-    // epilogue warps: two sets of 4 at N = 256 (set s reads accumulator buffer s), one set of
-    // 8 at N = 128, of 4 below
-    static constexpr int EPI_WARPS = N > 64 ? 8 : 4;
-    static constexpr int SETS = N >= 256 ? 2 : 1;
+    // epilogue warps: two sets of 4 (a warp group each); set s reads the accumulator buffers
+    // b with b mod 2 = s, i.e. every other computed tile
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int SETS = 2;
     static constexpr int WG_PER_SET = EPI_WARPS / 4 / SETS;  // warp groups per set
     static constexpr int THREADS = 64 + 32 * EPI_WARPS;
     static constexpr int COLS_PER_WG = N / WG_PER_SET;       // columns one epilogue warp group owns
@@ -89,15 +90,22 @@ struct IndexerTcConfig {
     static constexpr int SMEM_LIMIT = 227 * 1024 - ST_BYTES - W_BYTES;
     // two query tiles where the key ring still keeps 6 stages (decode: the next sequence's query
     // loads while the MMAs finish the current one, so the ring does not drain at the switch)
-    static constexpr int STAGES_2Q = (SMEM_LIMIT - 2 * Q_BYTES - 2048) / TILE_BYTES;
+    static constexpr int STAGES_2Q = (SMEM_LIMIT - 2 * Q_BYTES - 2048) / (TILE_BYTES + SC_BYTES);
     static constexpr int QBUF = STAGES_2Q >= 6 ? 2 : 1;
     static constexpr int FIXED = QBUF * Q_BYTES + 1024;      // query tiles + barriers
-    static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED - 1024) / TILE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr int SMEM_BYTES = 1024 + QBUF * Q_BYTES + STAGES * TILE_BYTES + 1024 + ST_BYTES + W_BYTES;
+    static constexpr int STAGES_FIT = (SMEM_LIMIT - FIXED - 1024) / (TILE_BYTES + SC_BYTES);
+    // key tiles in flight: the stream is latency-bound per SM, so the (half-size) e4m3 tiles
+    // get more stages
+    static constexpr int STAGES_MAX = FP8 ? 12 : 8;
+    static constexpr int STAGES = STAGES_FIT > STAGES_MAX ? STAGES_MAX : STAGES_FIT;
+    static constexpr int SMEM_BYTES =
+        1024 + QBUF * Q_BYTES + STAGES * (TILE_BYTES + SC_BYTES) + 1024 + ST_BYTES + W_BYTES;
+    // a key stage is free once its MMAs are done and, with e4m3 keys, once the epilogue warps
+    // that score the tile have read its scales
+    static constexpr int EMPTY_COUNT = 1 + (FP8 ? EPI_WARPS / SETS : 0);
     static_assert(N >= 16 && N <= 256 && N % 16 == 0, "MMA N");
     static_assert(!FUSE || (QW <= kStQueries && 4 * SETS == kStWarps), "fused selection group");
-    static_assert(SETS == 1 || SETS == ACC_BUFS, "a set per accumulator buffer");
+    static_assert(ACC_BUFS % SETS == 0, "the sets split the accumulator buffers");
     static_assert(COLS_PER_WG % HI == 0, "a warp group owns whole queries");
     static_assert(HI % 4 == 0, "four partial sums per query");
     static_assert(STAGES >= 2, "ring");
@@ -131,7 +139,7 @@ struct ItemCursor {
 template <int DI, int HI, int QPT, bool FUSE = false, bool FP8 = false>
 __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREADS, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap qmap,
-                      IndexerTcArgs a) {
+                      const __grid_constant__ CUtensorMap smap, IndexerTcArgs a) {
     using Cfg = IndexerTcConfig<DI, HI, QPT, FUSE, FP8>;
     constexpr int N = Cfg::N, STAGES = Cfg::STAGES;
     pdl_trigger();
@@ -139,7 +147,8 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_tile = base;
     uint8_t *k_ring = base + Cfg::QBUF * Cfg::Q_BYTES;
-    uint8_t *misc = k_ring + STAGES * Cfg::TILE_BYTES;
+    float *s_ring = reinterpret_cast<float *>(k_ring + STAGES * Cfg::TILE_BYTES);   // e4m3 key scales
+    uint8_t *misc = k_ring + STAGES * (Cfg::TILE_BYTES + Cfg::SC_BYTES);
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);
     uint64_t *empty = full + STAGES;
     uint64_t *acc_full = empty + STAGES;
@@ -168,7 +177,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&empty[s], Cfg::EMPTY_COUNT);
         }
         for (int s = 0; s < Cfg::ACC_BUFS; ++s) {
             ptx::mbar_init(&acc_full[s], 1);
@@ -252,8 +261,10 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
                     *abort_flag = 1;
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(&full[s], Cfg::TILE_BYTES);
+                ptx::mbar_arrive_expect_tx(&full[s], Cfg::TILE_BYTES + Cfg::SC_BYTES);
                 uint8_t *dst = k_ring + s * Cfg::TILE_BYTES;
+                if constexpr (FP8)   // the tile's key scales (rows past the cache are zero-filled)
+                    ptx::tma_load_2d(ptx::smem_u32(s_ring + s * 128), &smap, t * 128, b, &full[s]);
 #pragma unroll
                 for (int bx = 0; bx < Cfg::NBOX; ++bx)
                     ptx::tma_load_3d(ptx::smem_u32(dst + bx * 128 * Cfg::ROWB), &kmap, bx * Cfg::BOX, t * 128, b,
@@ -363,6 +374,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
             else if constexpr (CH == 16) ptx::tmem_ld16(addr, r);
             else ptx::tmem_ld8(addr, r);
         };
+        uint32_t fidx = 0;                               // computed tiles so far (= key fills)
         ItemCursor ic(it0, a.tiles, a.groups);
         for (int64_t it = it0; it < it1 && !*abort_flag; ++it, ic.next()) {
             const int t = ic.t;
@@ -400,11 +412,27 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
             for (int q = 0; q < QW; ++q) sc[q] = 0.f;
             const bool computed = (int64_t)t * 128 < vis;
             // this warp's set handles the tile: a computed tile's accumulator buffer, else its parity
-            const bool mine = Cfg::SETS == 1 || (computed ? acc == set : (t & 1) == set);
+            const bool mine = Cfg::SETS == 1 || (computed ? acc % Cfg::SETS == set : t % Cfg::SETS == set);
             if (computed && !mine) {
                 ++acc_use[acc];
                 acc = acc + 1 == Cfg::ACC_BUFS ? 0 : acc + 1;
+                ++fidx;
             } else if (computed) {
+                // e4m3 keys: the entry's scale from the tile's key stage (its copy has landed when
+                // the stage's full phase completes; the stage is refilled only after this warp's
+                // arrival on its empty barrier)
+                float ks = 1.f;
+                if constexpr (FP8) {
+                    const int ss = (int)(fidx % STAGES);
+                    if (!ptx::mbar_wait(&full[ss], (fidx / STAGES) & 1)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    ks = s_ring[ss * 128 + row];
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&empty[ss]);
+                }
+                ++fidx;
                 if (!ptx::mbar_wait(&acc_full[acc], acc_use[acc] & 1)) {
                     *abort_flag = 1;
                     break;
@@ -450,7 +478,6 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
                 for (int q = 0; q < QW; ++q) sc[q] = (ps[q][0] + ps[q][1]) + (ps[q][2] + ps[q][3]);
                 if constexpr (FP8) {
                     // e4m3 keys: the entry's (non-negative) scale multiplies the head sum
-                    const float ks = j < a.cache_rows ? __ldg(a.k_scale + (int64_t)b * a.ks_bs + j) : 0.f;
 #pragma unroll
                     for (int q = 0; q < QW; ++q) sc[q] *= ks;
                 }

@@ -416,6 +416,15 @@ lca_status indexer_tc_launch(int batch, int n_q, const void *q_idx, const void *
     const uint32_t qb[2] = {(uint32_t)Cfg::BOX, (uint32_t)Cfg::N};
     if (!make_tensor_map(&qmap, q_idx, 2, qd, qs, qb, sw, dt))
         return fail(LCA_ERR_CUDA, "csa_indexer_scores: query tensor map rejected by the driver");
+    CUtensorMap smap = kmap;                  // e4m3: the key scales, 128 per tile
+    if (FP8) {
+        const uint64_t sd[2] = {(uint64_t)a.cache_rows, (uint64_t)batch};
+        const uint64_t ss[1] = {batch == 1 ? (uint64_t)((a.cache_rows * 4 + 15) / 16 * 16) : (uint64_t)a.ks_bs * 4};
+        const uint32_t sb[2] = {128u, 1u};
+        if (!make_tensor_map(&smap, a.k_scale, 2, sd, ss, sb, CU_TENSOR_MAP_SWIZZLE_NONE,
+                             CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
+            return fail(LCA_ERR_CUDA, "csa_indexer_scores_e4m3: key scale tensor map rejected by the driver");
+    }
     a.groups = (n_q + QPT - 1) / QPT;
     a.tiles = (int)ceil_div64(a.cache_rows, 128);
     a.items = (int64_t)batch * a.groups * a.tiles;
@@ -424,7 +433,7 @@ lca_status indexer_tc_launch(int batch, int n_q, const void *q_idx, const void *
     cudaFuncSetAttribute(indexer_tc_kernel<DI, HI, QPT, FUSE, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          Cfg::SMEM_BYTES);
     launch_pdl(indexer_tc_kernel<DI, HI, QPT, FUSE, FP8>, grid, dim3(Cfg::THREADS), Cfg::SMEM_BYTES, stream, kmap,
-               qmap, a);
+               qmap, smap, a);
     return check_launch(FUSE ? "csa_indexer_topk" : "csa_indexer_scores");
 }
 
@@ -503,8 +512,10 @@ lca_status indexer_e4m3_validate(const char *name, const lca_attn_params *p, int
                 "%s: a required pointer is NULL", name);
     LCA_REQUIRE(aligned16(q8) && aligned16(k8), LCA_ERR_INVALID_ARG, "%s: q_idx8 and k_cache8 must be 16-byte aligned",
                 name);
-    LCA_REQUIRE(k_bs % 16 == 0 && (batch == 1 || (k_bs >= cache_rows * p->idx_dim && ks_bs >= cache_rows)),
-                LCA_ERR_INVALID_ARG, "%s: bad k_batch_stride / k_scale_batch_stride", name);
+    LCA_REQUIRE(k_bs % 16 == 0 && (batch == 1 || (k_bs >= cache_rows * p->idx_dim && ks_bs >= cache_rows &&
+                                                   ks_bs % 4 == 0)),
+                LCA_ERR_INVALID_ARG, "%s: bad k_batch_stride / k_scale_batch_stride (%% 4)", name);
+    LCA_REQUIRE(aligned16(k_scale), LCA_ERR_INVALID_ARG, "%s: k_scale must be 16-byte aligned", name);
     return LCA_OK;
 }
 

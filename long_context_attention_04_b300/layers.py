@@ -36,9 +36,14 @@ class LayerWeights:
 
 class CsaLayer:
     """One CSA layer for B sequences: KV cache [B, rows, c], indexer keys [B, rows, d_I],
-    window ring [B, win_cap, c], plus the index buffer and workspaces of a step of n_q queries."""
+    window ring [B, win_cap, c], plus the index buffer and workspaces of a step of n_q queries.
 
-    def __init__(self, p: AttnParams, weights: LayerWeights, kv_cache, idx_cache, win_kv, n_q: int = 1):
+    Indexer keys in e4m3: pass a uint8 idx_cache with its per-row scales idx_scale [B, rows]
+    (fp32); the keys are then compressed into e4m3 and the step's indexer queries are quantised
+    (one scale per head) before the e4m3 indexer."""
+
+    def __init__(self, p: AttnParams, weights: LayerWeights, kv_cache, idx_cache, win_kv, n_q: int = 1,
+                 idx_scale=None):
         self.p = p
         self.w = weights
         self.kv_cache, self.idx_cache, self.win_kv = kv_cache, idx_cache, win_kv
@@ -47,19 +52,39 @@ class CsaLayer:
         self.idx = torch.empty((B, n_q, p.topk), dtype=torch.int32, device=dev)
         self.ws_idx = torch.empty(api.csa_indexer_workspace(p, B, n_q, rows), dtype=torch.uint8, device=dev)
         self.ws_att = torch.empty(api.csa_attend_workspace(p, B, n_q), dtype=torch.uint8, device=dev)
+        self.e4m3 = idx_cache.dtype == torch.uint8
+        if self.e4m3:
+            if idx_scale is None:
+                raise ValueError("an e4m3 indexer cache needs idx_scale [B, rows]")
+            self.idx_scale = idx_scale
+            self.q8 = torch.empty((B, n_q, p.idx_heads, p.idx_dim), dtype=torch.uint8, device=dev)
+            self.q8_scale = torch.empty((B, n_q, p.idx_heads), dtype=torch.float32, device=dev)
+
+    def compress_keys(self, tok_vi, tok_zi, tok_pos0, first_entry, n_new, stream=None):
+        """The indexer-key entries (no RMSNorm, no RoPE), in bf16 or e4m3."""
+        if self.e4m3:
+            api.compress_kv_ex(True, self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
+                               self.idx_cache, cache_scale=self.idx_scale, stream=stream)
+        else:
+            api.csa_compress_kv(self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
+                                self.idx_cache, stream)
 
     def compress(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, stream=None):
         """Compress n_new entries per sequence into both caches (KV: RMSNorm + RoPE; keys: neither)."""
         api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
                             n_new, self.kv_cache, stream)
-        api.csa_compress_kv(self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
-                            self.idx_cache, stream)
+        self.compress_keys(tok_vi, tok_zi, tok_pos0, first_entry, n_new, stream)
 
     def window(self, new_tok_v, new_pos0, stream=None):
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, stream)
 
     def select(self, q_idx, w_idx, q_pos, stream=None):
-        api.csa_indexer_topk(self.p, q_idx, w_idx, self.idx_cache, q_pos, self.idx, self.ws_idx, stream)
+        if self.e4m3:
+            api.lca_quantize_rows_e4m3(q_idx, self.q8, self.q8_scale, stream)
+            api.csa_indexer_topk_e4m3(self.p, self.q8, self.q8_scale, w_idx, self.idx_cache, self.idx_scale, q_pos,
+                                      self.idx, self.ws_idx, stream)
+        else:
+            api.csa_indexer_topk(self.p, q_idx, w_idx, self.idx_cache, q_pos, self.idx, self.ws_idx, stream)
         return self.idx
 
     def attend(self, q, q_pos, out, lse=None, stream=None, part="csa_attend"):
@@ -95,8 +120,7 @@ class CsaLayer:
         self.attend(q, q_pos, out, stream=side, part="csa_attend_prepare")
         join.record(side)
         if n_new:
-            api.csa_compress_kv(self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
-                                self.idx_cache, main)
+            self.compress_keys(tok_vi, tok_zi, tok_pos0, first_entry, n_new, main)
         self.select(q_idx, w_idx, q_pos, main)
         main.wait_event(join)
         self.attend(q, q_pos, out, stream=main, part="csa_attend_prepared")

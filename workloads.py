@@ -88,6 +88,12 @@ CSA_DECODE_128K = dict(
     kind="csa_decode", B=32, pos=131071, entries=32768,
     shape=LayerShape(ratio=4, topk=512))
 
+# The same decode step with the indexer's keys in e4m3 (one fp32 scale per row): the key
+# entries are compressed into e4m3 and the indexer queries quantised each step.
+CSA_DECODE_128K_FP8 = dict(CSA_DECODE_128K, idx_e4m3=True,
+                           name="CSA decode with e4m3 indexer keys, batch 32, 128K context (32768 entries x 512), "
+                                "k=512, W=128, H=64")
+
 HCA_DECODE_1M = dict(
     name="HCA decode, batch 16, 1M context (8192 entries x 512), W=128, H=64",
     kind="hca_decode", B=16, pos=1048575, entries=8192,
@@ -153,6 +159,7 @@ WORKLOADS = {
     "v4flash_decode_1m": V4FLASH_DECODE_1M,
     "csa_prefill_1m_proj": CSA_PREFILL_1M_PROJ,
     "csa_prefill_1m_scored": CSA_PREFILL_1M_SCORED,
+    "csa_decode_128k_fp8": CSA_DECODE_128K_FP8,
 }
 
 
