@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
         const int row = quarter * 32 + lane;             // tile row == TMEM lane
         int64_t cur = -1;
         int64_t vis = 0;
-        int64_t nv[QW];
+        int nv[QW];                                      // visible entries of each query
         float *wr = w_sm + ew * Cfg::COLS_PER_WG;        // head weights of this warp group's queries
         uint32_t acc_use[Cfg::ACC_BUFS] = {};
         int acc = 0;
@@ -358,15 +358,11 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
         const int wtid = wseg * 32 + lane;
         uint2 *cand = FUSE ? a.cand + ((int64_t)blockIdx.x * Cfg::WG_PER_SET + wg) * (QW * 2 * kStCap) : nullptr;
         uint32_t st_phase = 0;
+        // (the thresholds and active buffers are read from the group's shared state: they change
+        // only at checkpoints, and registers are scarce)
         int my_cnt[QW];
-        uint32_t th[QW];
-        int act[QW];
 #pragma unroll
-        for (int q = 0; q < QW; ++q) {
-            my_cnt[q] = 0;
-            th[q] = 0;
-            act[q] = 0;
-        }
+        for (int q = 0; q < QW; ++q) my_cnt[q] = 0;
         constexpr int CH = Cfg::COLS_PER_WG < 32 ? Cfg::COLS_PER_WG : 32;   // TMEM columns per load
         constexpr int NCH = Cfg::COLS_PER_WG / CH;
         auto tmem_ld_chunk = [&](uint32_t addr, uint32_t *r) {
@@ -403,7 +399,7 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
                             n = a.cache_rows;
                         }
                     }
-                    nv[q] = n;
+                    nv[q] = (int)n;
                 }
             }
             const int64_t j = (int64_t)t * 128 + row;
@@ -490,13 +486,14 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
                 for (int q = 0; q < QW; ++q) {
                     // append the scores at or above the query's threshold to this warp's segment
                     const uint32_t key = ordered_key(sc[q]);
-                    const bool pass = mine && computed && j < nv[q] && key >= th[q];
+                    const bool pass = mine && computed && j < nv[q] && key >= st[wg].theta[q];
                     const uint32_t m = __ballot_sync(0xffffffffu, pass);
                     if (m) {
                         const int pos = my_cnt[q] + __popc(m & lt);
                         if (pass) {
                             if (pos < kStSeg)
-                                st_segment(st_buffer(cand, q, act[q]), wseg)[pos] = make_uint2(key, (uint32_t)j);
+                                st_segment(st_buffer(cand, q, st[wg].active[q]), wseg)[pos] =
+                                    make_uint2(key, (uint32_t)j);
                             else
                                 raise_error(LCA_DEVERR_SELECT);
                         }
@@ -546,8 +543,6 @@ __global__ void __launch_bounds__(IndexerTcConfig<DI, HI, QPT, FUSE, FP8>::THREA
 #pragma unroll
                         for (int q = 0; q < QW; ++q) {
                             my_cnt[q] = S.wcnt[q][wseg];
-                            th[q] = S.theta[q];
-                            act[q] = S.active[q];
                         }
                 }
             } else if (mine && j < a.cache_rows) {

@@ -383,8 +383,8 @@ lca_status indexer_validate(const char *name, const lca_attn_params *p, int batc
                             const float *w_idx, const lca_bf16 *k_cache, int64_t k_bs, int64_t cache_rows,
                             const int32_t *q_pos) {
     LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
-    LCA_REQUIRE(batch > 0 && n_q > 0 && cache_rows > 0, LCA_ERR_INVALID_ARG,
-                "%s: batch, n_q and cache_rows must be positive", name);
+    LCA_REQUIRE(batch > 0 && n_q > 0 && cache_rows > 0 && cache_rows < INT32_MAX, LCA_ERR_INVALID_ARG,
+                "%s: batch, n_q and cache_rows must be positive, cache_rows < 2^31", name);
     LCA_REQUIRE(p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
     LCA_REQUIRE((p->idx_dim == 128 && p->idx_heads == 64) || (p->idx_dim == 64 && p->idx_heads == 32) ||
                     (p->idx_dim == 32 && p->idx_heads == 4),
@@ -503,8 +503,8 @@ lca_status indexer_e4m3_validate(const char *name, const lca_attn_params *p, int
                                  const float *q_scale, const float *w_idx, const uint8_t *k8, int64_t k_bs,
                                  const float *k_scale, int64_t ks_bs, int64_t cache_rows, const int32_t *q_pos) {
     LCA_REQUIRE(p, LCA_ERR_INVALID_ARG, "%s: params is NULL", name);
-    LCA_REQUIRE(batch > 0 && n_q > 0 && cache_rows > 0, LCA_ERR_INVALID_ARG,
-                "%s: batch, n_q and cache_rows must be positive", name);
+    LCA_REQUIRE(batch > 0 && n_q > 0 && cache_rows > 0 && cache_rows < INT32_MAX, LCA_ERR_INVALID_ARG,
+                "%s: batch, n_q and cache_rows must be positive, cache_rows < 2^31", name);
     LCA_REQUIRE(p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
     LCA_REQUIRE(p->idx_dim == 128 && p->idx_heads == 64, LCA_ERR_UNSUPPORTED,
                 "%s: e4m3 indexer supports 64 heads of dim 128 (got %d, %d)", name, p->idx_heads, p->idx_dim);

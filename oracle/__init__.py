@@ -80,6 +80,8 @@ def _load():
         lib.orc_compress_pc.restype = I
         lib.orc_indexer_scores_e4m3.argtypes = [I, I, P, P, P, P, P, L, P]
         lib.orc_indexer_scores_e4m3.restype = None
+        lib.orc_attend_e4m3.argtypes = [I, I, I, D, D, D, P, P, L, P, P, L, P, L, L, P, L, L, P, P, P]
+        lib.orc_attend_e4m3.restype = I
         _lib = lib
     return _lib
 
@@ -323,3 +325,26 @@ def indexer_scores_e4m3(q8, qscale, w, k8, kscale, n_vis):
     lib.orc_indexer_scores_e4m3(n_heads, dim, _ptr(q8), _ptr(qscale), _ptr(w), _ptr(k8), _ptr(kscale), n_vis,
                                 _ptr(out))
     return out
+
+
+def attend_e4m3(q, gamma_q, pos, comp8, comp_scale, sink, win, win_cap, W, rope_dims, rope_base, eps, scale,
+                idx=None, n_dense=0):
+    """attend() over an e4m3 compressed cache: comp8 uint8 [rows, c] with comp_scale float32 [rows]
+    (row j read back as comp_scale[j] * e4m3(comp8[j])); the window ring stays bf16."""
+    lib = _load()
+    q = _u16(q)
+    comp8 = np.ascontiguousarray(comp8, dtype=np.uint8)
+    cs = _f32(comp_scale)
+    win = _u16(win)
+    g = _f32(gamma_q)
+    sk = _f32(sink)
+    H, c = q.shape
+    ix = None if idx is None else np.ascontiguousarray(idx, dtype=np.int32)
+    out = np.empty((H, c), dtype=np.float64)
+    lse = np.empty(H, dtype=np.float64)
+    rc = lib.orc_attend_e4m3(H, c, rope_dims, rope_base, eps, scale, _ptr(q), _ptr(g), pos,
+                             _ptr(comp8), _ptr(cs), comp8.shape[0], _ptr(ix), 0 if ix is None else ix.shape[0],
+                             n_dense, _ptr(win), win_cap, W, _ptr(sk), _ptr(out), _ptr(lse))
+    if rc != 0:
+        raise ValueError("orc_attend_e4m3: index outside the compressed cache (rc=%d)" % rc)
+    return out, lse

@@ -250,41 +250,33 @@ int orc_topk(const double *scores, long n, int k, int32_t *out)
  *   o_h = RoPE(sum_r p_r row_r, -pos);   lse_h = log(exp(sink_h) + sum_r exp(l_r)).
  * Rows already carry RMSNorm and RoPE at their own positions.
  */
-int orc_attend(int H, int c, int rope_dims, double rope_base, double eps, double scale,
-               const uint16_t *q, const float *gamma_q, long pos,
-               const uint16_t *comp, long comp_rows,
-               const int32_t *idx, long n_idx, long n_dense,
-               const uint16_t *win, long win_cap, long W,
-               const float *sink, double *out, double *lse)
+/* One key/value row of the attention: bf16 bit patterns, or (variant) e4m3 codes with the
+ * row's scale, read back as scale * value(code). */
+typedef struct {
+    const uint16_t *bf;
+    const uint8_t *e8;
+    double scale;
+} key_row;
+
+double orc_e4m3_decode(uint8_t c);
+
+static double key_row_value(const key_row *r, int i)
 {
-    long win_begin = pos - W + 1;
-    if (win_begin < 0)
-        win_begin = 0;
-    long n_win = pos - win_begin + 1;
-    long n_comp = idx ? n_idx : n_dense;
-    long max_rows = n_comp + n_win;
-    const uint16_t **rows = (const uint16_t **)malloc(sizeof(*rows) * (size_t)(max_rows > 0 ? max_rows : 1));
+    return r->bf ? bf16_bits_to_double(r->bf[i]) : r->scale * orc_e4m3_decode(r->e8[i]);
+}
+
+/* The per-head part of orc_attend over an assembled row list. */
+static int attend_rows(int H, int c, int rope_dims, double rope_base, double eps, double scale,
+                       const uint16_t *q, const float *gamma_q, long pos, const key_row *rows, long n_rows,
+                       const float *sink, double *out, double *lse)
+{
     double *qh = (double *)malloc(sizeof(double) * (size_t)c);
-    double *logit = (double *)malloc(sizeof(double) * (size_t)(max_rows > 0 ? max_rows : 1));
+    double *logit = (double *)malloc(sizeof(double) * (size_t)(n_rows > 0 ? n_rows : 1));
     double *acc = (double *)malloc(sizeof(double) * (size_t)c);
-    if (!rows || !qh || !logit || !acc) {
-        free(rows); free(qh); free(logit); free(acc);
+    if (!qh || !logit || !acc) {
+        free(qh); free(logit); free(acc);
         return -3;
     }
-    long n_rows = 0;
-    for (long i = 0; i < n_comp; ++i) {
-        long j = idx ? (long)idx[i] : i;
-        if (j < 0)
-            continue;
-        if (j >= comp_rows) {
-            free(rows); free(qh); free(logit); free(acc);
-            return -2;
-        }
-        rows[n_rows++] = comp + (size_t)j * (size_t)c;
-    }
-    for (long t = win_begin; t <= pos; ++t)
-        rows[n_rows++] = win + (size_t)(t % win_cap) * (size_t)c;
-
     for (int h = 0; h < H; ++h) {
         for (int i = 0; i < c; ++i)
             qh[i] = bf16_bits_to_double(q[(size_t)h * (size_t)c + i]);
@@ -296,7 +288,7 @@ int orc_attend(int H, int c, int rope_dims, double rope_base, double eps, double
         for (long r = 0; r < n_rows; ++r) {
             double dot = 0.0;
             for (int i = 0; i < c; ++i)
-                dot += qh[i] * bf16_bits_to_double(rows[r][i]);
+                dot += qh[i] * key_row_value(&rows[r], i);
             logit[r] = scale * dot;
             if (logit[r] > mx)
                 mx = logit[r];
@@ -309,7 +301,7 @@ int orc_attend(int H, int c, int rope_dims, double rope_base, double eps, double
         for (long r = 0; r < n_rows; ++r) {
             double p = exp(logit[r] - mx) / den;
             for (int i = 0; i < c; ++i)
-                acc[i] += p * bf16_bits_to_double(rows[r][i]);
+                acc[i] += p * key_row_value(&rows[r], i);
         }
         if (rope_dims > 0)
             rope_rotate(acc, c, rope_dims, rope_base, -(double)pos);
@@ -317,8 +309,86 @@ int orc_attend(int H, int c, int rope_dims, double rope_base, double eps, double
         if (lse)
             lse[h] = mx + log(den);
     }
-    free(rows); free(qh); free(logit); free(acc);
+    free(qh); free(logit); free(acc);
     return 0;
+}
+
+/* The row list of one query: the compressed rows (comp bf16, or comp8 with comp_scale) then the
+ * window rows.  Returns the count, or -2 for an index outside the cache, -3 for no memory. */
+static long gather_key_rows(int c, long pos, const uint16_t *comp, const uint8_t *comp8, const float *comp_scale,
+                            long comp_rows, const int32_t *idx, long n_idx, long n_dense,
+                            const uint16_t *win, long win_cap, long W, key_row **out_rows)
+{
+    long win_begin = pos - W + 1;
+    if (win_begin < 0)
+        win_begin = 0;
+    long n_win = pos - win_begin + 1;
+    long n_comp = idx ? n_idx : n_dense;
+    long max_rows = n_comp + n_win;
+    key_row *rows = (key_row *)malloc(sizeof(key_row) * (size_t)(max_rows > 0 ? max_rows : 1));
+    if (!rows)
+        return -3;
+    long n_rows = 0;
+    for (long i = 0; i < n_comp; ++i) {
+        long j = idx ? (long)idx[i] : i;
+        if (j < 0)
+            continue;
+        if (j >= comp_rows) {
+            free(rows);
+            return -2;
+        }
+        key_row kr = {0, 0, 0.0};
+        if (comp8) {
+            kr.e8 = comp8 + (size_t)j * (size_t)c;
+            kr.scale = (double)comp_scale[j];
+        } else {
+            kr.bf = comp + (size_t)j * (size_t)c;
+        }
+        rows[n_rows++] = kr;
+    }
+    for (long t = win_begin; t <= pos; ++t) {
+        key_row kr = {win + (size_t)(t % win_cap) * (size_t)c, 0, 0.0};
+        rows[n_rows++] = kr;
+    }
+    *out_rows = rows;
+    return n_rows;
+}
+
+int orc_attend(int H, int c, int rope_dims, double rope_base, double eps, double scale,
+               const uint16_t *q, const float *gamma_q, long pos,
+               const uint16_t *comp, long comp_rows,
+               const int32_t *idx, long n_idx, long n_dense,
+               const uint16_t *win, long win_cap, long W,
+               const float *sink, double *out, double *lse)
+{
+    key_row *rows = 0;
+    long n_rows = gather_key_rows(c, pos, comp, 0, 0, comp_rows, idx, n_idx, n_dense, win, win_cap, W, &rows);
+    if (n_rows < 0)
+        return (int)n_rows;
+    int rc = attend_rows(H, c, rope_dims, rope_base, eps, scale, q, gamma_q, pos, rows, n_rows, sink, out, lse);
+    free(rows);
+    return rc;
+}
+
+/*
+ * The same attention over an e4m3 compressed cache (the FP8 variant): compressed row j is
+ * comp_scale[j] * e4m3(comp8[j][.]); the window rows stay bf16.
+ */
+int orc_attend_e4m3(int H, int c, int rope_dims, double rope_base, double eps, double scale,
+                    const uint16_t *q, const float *gamma_q, long pos,
+                    const uint8_t *comp8, const float *comp_scale, long comp_rows,
+                    const int32_t *idx, long n_idx, long n_dense,
+                    const uint16_t *win, long win_cap, long W,
+                    const float *sink, double *out, double *lse)
+{
+    key_row *rows = 0;
+    long n_rows = gather_key_rows(c, pos, 0, comp8, comp_scale, comp_rows, idx, n_idx, n_dense, win, win_cap, W,
+                                  &rows);
+    if (n_rows < 0)
+        return (int)n_rows;
+    int rc = attend_rows(H, c, rope_dims, rope_base, eps, scale, q, gamma_q, pos, rows, n_rows, sink, out, lse);
+    free(rows);
+    return rc;
 }
 
 /* Plain matrix product out[m*N + n] = sum_k A[m*K + k] * B[n*K + k] (bf16 inputs). */

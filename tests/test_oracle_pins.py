@@ -768,3 +768,24 @@ def test_indexer_e4m3_is_the_bf16_indexer_on_the_decoded_values():
     kv = oracle.dequantize_rows_e4m3(k8, ks)
     ref = oracle.indexer_scores(to_bits(qv), w, to_bits(kv), n)
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-9)
+
+
+def test_attend_e4m3_is_the_attention_over_the_decoded_rows():
+    """With power-of-two row scales the decoded e4m3 rows are exact bf16 values: the e4m3
+    attention equals the bf16 attention over those rows (CSA selection and HCA dense)."""
+    g = np.random.default_rng(11)
+    H, c, rows, W, cap = 4, 64, 40, 8, 16
+    q = rand_bits(g, (H, c))
+    comp8 = g.integers(0, 256, (rows, c)).astype(np.uint8)
+    comp8[(comp8 & 0x7F) >= 0x78] = 0x30               # keep magnitudes moderate, no NaN codes
+    cs = (2.0 ** g.integers(-4, 2, rows)).astype(np.float32)
+    win = rand_bits(g, (cap, c))
+    sink = g.standard_normal(H).astype(np.float32)
+    gam = np.ones(c, np.float32)
+    comp_bf = to_bits(oracle.dequantize_rows_e4m3(comp8, cs))
+    idx = np.array([3, -1, 17, 0, 39, 5], dtype=np.int32)
+    for kw in (dict(idx=idx), dict(n_dense=rows)):
+        o8, l8 = oracle.attend_e4m3(q, gam, 100, comp8, cs, sink, win, cap, W, 16, 10000.0, 1e-6, 0.125, **kw)
+        o16, l16 = oracle.attend(q, gam, 100, comp_bf, sink, win, cap, W, 16, 10000.0, 1e-6, 0.125, **kw)
+        np.testing.assert_allclose(o8, o16, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(l8, l16, rtol=1e-12, atol=1e-12)
