@@ -10,7 +10,8 @@ attention with split-K combine.  Workloads (sizes of the pages' V4-Flash configu
   csa_prefill_1m             one 8192-query chunk at 1M context
   csa_prefill_128k           one 2048-query chunk at 128K context (the same kernels, profiler-sized)
   csa_prefill_1m_scored      the 1M chunk with its scores written out and selected by a separate top-k
-  csa_decode_128k_fp8        csa_decode_128k with the indexer keys and queries in e4m3 (per-row scales)
+  csa_decode_128k_fp8        csa_decode_128k with e4m3 caches: indexer keys (and queries) and KV rows
+  hca_decode_1m_fp8          hca_decode_1m over an e4m3 KV cache (per-row scales)
 Inputs are seeded synthetic tensors (workloads.py); the caches are larger than L2 and L2 is
 also flushed between timed steps.  Under torchrun each rank runs the workload on its own
 GPU (sequences shard with no exchange: weak scaling); the value is all ranks' tokens over
@@ -257,6 +258,14 @@ class Workload:
         raise NotImplementedError
 
 
+def _quantized(api, x):
+    """e4m3 codes and per-row scales of a bf16 cache [B, rows, width] (the library's quantiser)."""
+    q = torch.empty(x.shape, dtype=torch.uint8, device="cuda")
+    sc = torch.empty(x.shape[:2], dtype=torch.float32, device="cuda")
+    api.lca_quantize_rows_e4m3(x, q, sc)
+    return q, sc
+
+
 class CsaDecode(Workload):
     def __init__(self, cfg: dict, seed: int = 0, stage: bool = True):
         from long_context_attention_04_b300 import api
@@ -274,14 +283,15 @@ class CsaDecode(Workload):
         w = LayerWeights(d["gamma_kv"], d["gamma_q"], d["bias_kv"], d["sink"], d["bias_idx"])
         # e4m3 indexer keys: the synthetic bf16 key cache quantised once (per-row scales)
         self.e4m3 = bool(cfg.get("idx_e4m3"))
+        self.kv8 = bool(cfg.get("kv_e4m3"))
+        kv, kv_scale, keys, key_scale = d["kv_cache"], None, d["idx_cache"], None
+        if self.kv8:     # the synthetic bf16 KV cache quantised once (per-row scales)
+            kv, kv_scale = _quantized(api, d["kv_cache"])
         if self.e4m3:
-            self.idx8 = torch.empty(d["idx_cache"].shape, dtype=torch.uint8, device="cuda")
-            self.idx8_scale = torch.empty(d["idx_cache"].shape[:2], dtype=torch.float32, device="cuda")
-            api.lca_quantize_rows_e4m3(d["idx_cache"], self.idx8, self.idx8_scale)
-            self.layer = CsaLayer(self.p, w, d["kv_cache"], self.idx8, d["win_kv"], n_q=1, idx_scale=self.idx8_scale)
+            keys, key_scale = _quantized(api, d["idx_cache"])
+        self.layer = CsaLayer(self.p, w, kv, keys, d["win_kv"], n_q=1, idx_scale=key_scale, kv_scale=kv_scale)
+        if self.e4m3:
             api.lca_quantize_rows_e4m3(d["q_idx"], self.layer.q8, self.layer.q8_scale)
-        else:
-            self.layer = CsaLayer(self.p, w, d["kv_cache"], d["idx_cache"], d["win_kv"], n_q=1)
         i32 = dict(dtype=torch.int32, device="cuda")
         self.tok_pos0 = torch.full((B,), d["tok_pos0"], **i32)
         self.first = torch.full((B,), entries - 1, **i32)
@@ -309,8 +319,10 @@ class CsaDecode(Workload):
             self.dom_bytes = B * (n_vis * s.idx_dim * 2 + s.idx_heads * s.idx_dim * 2 + s.idx_heads * 4)
         self.dom_flops = 2.0 * B * n_vis * s.idx_heads * s.idx_dim
         self.step_bytes, self.step_flops = csa_layer_work(s, B, n_vis, 1)
-        if self.e4m3:
+        if self.e4m3:   # a key row is d_I bytes + its scale instead of 2 d_I
             self.step_bytes -= B * n_vis * (s.idx_dim - 4)
+        if self.kv8:    # a selected KV row is c bytes + its scale instead of 2 c
+            self.step_bytes -= B * s.topk * (s.head_dim - 4)
 
     def dominant_call(self):
         d, L = self.d, self.layer
@@ -374,8 +386,18 @@ class CsaDecode(Workload):
             else:
                 sc = oracle.indexer_scores(qi, wi, ixb, n_vis)
             idx = oracle.topk(sc, s.topk)
-            oracle.attend(q, self.w_host["gamma_q"], self.pos, kvb, self.w_host["sink"], winb, winb.shape[0],
-                          s.window, s.rope_dims, s.rope_base, s.rms_eps, self.p.scale, idx=idx)
+            if self.kv8:
+                t6 = time.perf_counter()
+                kv8, kvs = oracle.quantize_rows_e4m3(kvb[:-1])             # the cache before the step, not timed
+                t7 = time.perf_counter()
+                t_fp8 += t7 - t6
+                kn8, kns = oracle.quantize_rows_e4m3(kvb[-1:])
+                oracle.attend_e4m3(q, self.w_host["gamma_q"], self.pos, np.concatenate([kv8, kn8]),
+                                   np.concatenate([kvs, kns]), self.w_host["sink"], winb, winb.shape[0], s.window,
+                                   s.rope_dims, s.rope_base, s.rms_eps, self.p.scale, idx=idx)
+            else:
+                oracle.attend(q, self.w_host["gamma_q"], self.pos, kvb, self.w_host["sink"], winb, winb.shape[0],
+                              s.window, s.rope_dims, s.rope_base, s.rms_eps, self.p.scale, idx=idx)
             t3 = time.perf_counter()
             t_total += (t1 - t0) + (t3 - t2) - t_fp8
             n_done += 1
@@ -408,7 +430,12 @@ class HcaDecode(Workload):
         d = wl.decode_inputs(rng, s, B, pos, entries, csa=False)
         self.d = d
         w = LayerWeights(d["gamma_kv"], d["gamma_q"], d["bias_kv"], d["sink"])
-        self.layer = HcaLayer(self.p, w, d["kv_cache"], d["win_kv"], n_q=1)
+        self.kv8 = bool(cfg.get("kv_e4m3"))
+        if self.kv8:     # the synthetic bf16 KV cache quantised once (per-row scales)
+            kv8, kv8_scale = _quantized(api, d["kv_cache"])
+            self.layer = HcaLayer(self.p, w, kv8, d["win_kv"], n_q=1, kv_scale=kv8_scale)
+        else:
+            self.layer = HcaLayer(self.p, w, d["kv_cache"], d["win_kv"], n_q=1)
         i32 = dict(dtype=torch.int32, device="cuda")
         self.tok_pos0 = torch.full((B,), d["tok_pos0"], **i32)
         self.first = torch.full((B,), entries - 1, **i32)
@@ -417,7 +444,7 @@ class HcaDecode(Workload):
         self.out = torch.empty((B, 1, s.heads, s.head_dim), dtype=torch.bfloat16, device="cuda")
         self.tokens = B
         self.launches = 5          # compress, window, q prep, attention, combine
-        self.dominant = "attend"
+        self.dominant = "attend e4m3" if self.kv8 else "attend"
         # (the compression's inputs first; the query goes up on the side stream meanwhile)
         self.groups = {"main": ["tok_v", "tok_z"], "side": ["q"]}
         self._stage_inputs(("tok_v", "tok_z", "q"), stage, self.groups)
@@ -426,9 +453,13 @@ class HcaDecode(Workload):
         self.d2h_bytes = self.out.numel() * self.out.element_size()
         n_vis = (pos + 1) // s.ratio
         rows = n_vis + s.window
-        self.dom_bytes = B * (rows * s.head_dim * 2 + 2 * s.heads * s.head_dim * 2)
+        # e4m3 compressed rows: c bytes + the row's scale instead of 2 c
+        comp_row = (s.head_dim + 4) if self.kv8 else 2 * s.head_dim
+        self.dom_bytes = B * (n_vis * comp_row + s.window * s.head_dim * 2 + 2 * s.heads * s.head_dim * 2)
         self.dom_flops = 4.0 * B * rows * s.heads * s.head_dim
         self.step_bytes, self.step_flops = hca_layer_work(s, B, n_vis)
+        if self.kv8:
+            self.step_bytes -= B * n_vis * (2 * s.head_dim - comp_row)
 
     def dominant_call(self):
         # the attention kernel and its split-K combine
@@ -468,10 +499,22 @@ class HcaDecode(Workload):
             t1 = time.perf_counter()
             kvb[-1] = _round_bits(kv_new[0])
             winb[self.pos % winb.shape[0]] = _round_bits(w_new)
+            t_fp8 = 0.0
+            if self.kv8:
+                t4 = time.perf_counter()
+                kv8, kvs = oracle.quantize_rows_e4m3(kvb[:-1])             # the cache before the step, not timed
+                t_fp8 = time.perf_counter() - t4
             t2 = time.perf_counter()
-            oracle.attend(q, self.w_host["gamma_q"], self.pos, kvb, self.w_host["sink"], winb, winb.shape[0],
-                          s.window, s.rope_dims, s.rope_base, s.rms_eps, self.p.scale,
-                          n_dense=oracle.visible_entries(self.pos, s.ratio))
+            if self.kv8:
+                kn8, kns = oracle.quantize_rows_e4m3(kvb[-1:])
+                oracle.attend_e4m3(q, self.w_host["gamma_q"], self.pos, np.concatenate([kv8, kn8]),
+                                   np.concatenate([kvs, kns]), self.w_host["sink"], winb, winb.shape[0], s.window,
+                                   s.rope_dims, s.rope_base, s.rms_eps, self.p.scale,
+                                   n_dense=oracle.visible_entries(self.pos, s.ratio))
+            else:
+                oracle.attend(q, self.w_host["gamma_q"], self.pos, kvb, self.w_host["sink"], winb, winb.shape[0],
+                              s.window, s.rope_dims, s.rope_base, s.rms_eps, self.p.scale,
+                              n_dense=oracle.visible_entries(self.pos, s.ratio))
             t3 = time.perf_counter()
             t_total += (t1 - t0) + (t3 - t2)
             n_done += 1
@@ -850,7 +893,7 @@ class MhcLayer(Workload):
 WORKLOADS = {"csa_decode_128k": CsaDecode, "hca_decode_1m": HcaDecode, "csa_prefill_1m": CsaPrefill,
              "csa_prefill_128k": CsaPrefill, "block_decode_1m": BlockDecode, "mhc_prefill_8192": MhcLayer,
              "v4flash_decode_1m": BlockDecode, "csa_prefill_1m_proj": CsaPrefillProj,
-             "csa_prefill_1m_scored": CsaPrefill, "csa_decode_128k_fp8": CsaDecode}
+             "csa_prefill_1m_scored": CsaPrefill, "csa_decode_128k_fp8": CsaDecode, "hca_decode_1m_fp8": HcaDecode}
 
 
 # ------------------------------------------------------------------- distributed -----
@@ -1021,8 +1064,8 @@ def measure(name: str, args, flush, world: int, device, rank: int, seed: int, sn
 # 8 CSA + 8 HCA layers with output projections at 1M (HBM-bound), the hyper-connection
 # mixing around a layer for an 8192-token chunk (HBM-bound), the 43-layer V4-Flash attention
 # stack at decode (HBM-bound), and the prefill chunk with its input projections (tensor-bound).
-EXTRA_WORKLOADS = ("csa_decode_128k_fp8", "hca_decode_1m", "csa_prefill_1m", "csa_prefill_1m_scored", "block_decode_1m",
-                   "mhc_prefill_8192", "v4flash_decode_1m", "csa_prefill_1m_proj")
+EXTRA_WORKLOADS = ("csa_decode_128k_fp8", "hca_decode_1m", "hca_decode_1m_fp8", "csa_prefill_1m", "csa_prefill_1m_scored",
+                   "block_decode_1m", "mhc_prefill_8192", "v4flash_decode_1m", "csa_prefill_1m_proj")
 
 
 def run_ours(args):
@@ -1233,6 +1276,20 @@ class _HostOnly:
             self.sample = "compression of a %d-token block, window row, attention over %d entries" % (s.ratio, entries)
         self.ones = np.ones(s.head_dim, np.float32)
         self.sink = rng.normal_f32((s.heads,)).numpy()
+        self.kv8 = None
+        if cfg.get("kv_e4m3"):              # the KV cache in e4m3 (state before the token, not timed)
+            self.kv8, self.kvs = oracle.quantize_rows_e4m3(self.kv)
+            self.sample += " (e4m3 KV rows)"
+
+    def _attend(self, **kw):
+        o, s = self.oracle, self.s
+        scale = 1.0 / math.sqrt(s.head_dim)
+        if self.kv8 is not None:
+            o.quantize_rows_e4m3(self.kv[-1:])                # the new entry's row
+            return o.attend_e4m3(self.q, self.ones, self.pos, self.kv8, self.kvs, self.sink, self.win,
+                                 self.win.shape[0], s.window, s.rope_dims, s.rope_base, s.rms_eps, scale, **kw)
+        return o.attend(self.q, self.ones, self.pos, self.kv, self.sink, self.win, self.win.shape[0], s.window,
+                        s.rope_dims, s.rope_base, s.rms_eps, scale, **kw)
 
     def one_unit(self):
         if getattr(self, "proj", None):
@@ -1245,15 +1302,14 @@ class _HostOnly:
             o.mhc_post(self.x, B, c, self.y)
             return
         o, s = self.oracle, self.s
-        span = 2 * s.ratio if self.kind != "hca_decode_1m" else s.ratio
+        span = s.ratio if self.kind.startswith("hca_") else 2 * s.ratio
         bias = np.zeros(span, np.float32)
         p0 = self.pos + 1 - span
         j = (self.pos + 1) // s.ratio - 1
         o.compress(self.tok_v, self.tok_z, p0, bias, self.ones, s.rms_eps, s.rope_dims, s.rope_base, span, s.ratio,
                    j, 1)
         o.window_row(self.tok_v[-1], self.ones, s.rms_eps, s.rope_dims, s.rope_base, self.pos)
-        scale = 1.0 / math.sqrt(s.head_dim)
-        if self.kind != "hca_decode_1m":
+        if not self.kind.startswith("hca_"):
             o.compress(self.tok_vi, self.tok_z, p0, bias, None, s.rms_eps, 0, s.rope_base, span, s.ratio, j, 1)
             n_vis = o.visible_entries(self.pos, s.ratio)
             if getattr(self, "e4m3", False):
@@ -1263,11 +1319,9 @@ class _HostOnly:
             else:
                 sc = o.indexer_scores(self.qi, self.wi, self.keys, n_vis)
             idx = o.topk(sc, s.topk)
-            o.attend(self.q, self.ones, self.pos, self.kv, self.sink, self.win, self.win.shape[0], s.window,
-                     s.rope_dims, s.rope_base, s.rms_eps, scale, idx=idx)
+            self._attend(idx=idx)
         else:
-            o.attend(self.q, self.ones, self.pos, self.kv, self.sink, self.win, self.win.shape[0], s.window,
-                     s.rope_dims, s.rope_base, s.rms_eps, scale, n_dense=o.visible_entries(self.pos, s.ratio))
+            self._attend(n_dense=o.visible_entries(self.pos, s.ratio))
 
 
 def main(argv=None):

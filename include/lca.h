@@ -280,6 +280,32 @@ lca_status hca_attend(const lca_attn_params *p, int batch, int n_q,
                       const float *sink, lca_bf16 *out, float *lse,
                       void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* The attention over an e4m3 compressed cache (the FP8 variant; see the e4m3 reading above):
+ * compressed row j of sequence b is kv_scale[b * kv_scale_batch_stride + j] *
+ * value(kv_cache8[b * kv_batch_stride + j * c + .]) (kv_batch_stride in bytes = elements, a
+ * multiple of 16; kv_cache8 16-byte aligned); the window rows stay bf16.  The rows are
+ * re-encoded in the kernel as fp16(value) x fp16(scale), rounded to fp16 (about 2^-10 relative,
+ * inside the codes' own 2^-4), so the products run as in the bf16 call; against an fp64
+ * evaluation over the same decoded rows the error bound of the bf16 call holds.  A row whose
+ * 448 x scale exceeds fp16's range, or a NaN code in a row that is read, sets
+ * LCA_DEVERR_FP16_RANGE.  Supported: c = 512.  Workspaces from *_attend_workspace; errors as
+ * the bf16 calls.  (No prepare/prepared halves for these calls.) */
+lca_status csa_attend_e4m3(const lca_attn_params *p, int batch, int n_q,
+                           const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                           const uint8_t *kv_cache8, int64_t kv_batch_stride,
+                           const float *kv_scale, int64_t kv_scale_batch_stride, int64_t cache_rows,
+                           const int32_t *idx,
+                           const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                           const float *sink, lca_bf16 *out, float *lse,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
+lca_status hca_attend_e4m3(const lca_attn_params *p, int batch, int n_q,
+                           const lca_bf16 *q, const float *gamma_q, const int32_t *q_pos,
+                           const uint8_t *kv_cache8, int64_t kv_batch_stride,
+                           const float *kv_scale, int64_t kv_scale_batch_stride, int64_t cache_rows,
+                           const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                           const float *sink, lca_bf16 *out, float *lse,
+                           void *workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* The two halves of an attention call, for callers that overlap the query preparation with
  * other work (the selection, the cache updates) on another stream.  *_attend_prepare runs
  * only the query preparation (RMSNorm + RoPE(i) of q, fp16 hi/lo query images) into the workspace;

@@ -70,6 +70,10 @@ SIGNATURES = {
     "csa_indexer_scores_e4m3": ([P, c_int, c_int, V, V, V, V, c_int64, V, c_int64, c_int64, V, V, c_int64, V], c_int),
     "csa_indexer_topk_e4m3": ([P, c_int, c_int, V, V, V, V, c_int64, V, c_int64, c_int64, V, V, V, c_size_t, V],
                               c_int),
+    "csa_attend_e4m3": ([P, c_int, c_int, V, V, V, V, c_int64, V, c_int64, c_int64, V, V, c_int64, c_int, V, V, V, V,
+                         c_size_t, V], c_int),
+    "hca_attend_e4m3": ([P, c_int, c_int, V, V, V, V, c_int64, V, c_int64, c_int64, V, c_int64, c_int, V, V, V, V,
+                         c_size_t, V], c_int),
     "lca_status_string": ([c_int], ctypes.c_char_p),
     "lca_last_error": ([], ctypes.c_char_p),
     "lca_device_error": ([V, ctypes.POINTER(ctypes.c_uint32)], c_int),

@@ -351,6 +351,46 @@ def hca_attend(p: AttnParams, q, gamma_q, q_pos, kv_cache, win_kv, sink, out, wo
     _check(st)
 
 
+def _kv8(kv8, kv_scale):
+    if kv8.dtype != torch.uint8:
+        raise TypeError("kv_cache8 must be uint8 (e4m3 codes)")
+    if kv_scale.dim() != 2 or kv_scale.shape[0] != kv8.shape[0] or kv_scale.shape[1] < kv8.shape[1] or \
+            kv_scale.stride(1) != 1:
+        raise ValueError("kv_scale must be [B, >= rows] with unit inner stride")
+    return (_ptr(kv8, torch.uint8, "kv_cache8"), _rows(kv8, "kv_cache8"), _ptr(kv_scale, torch.float32, "kv_scale"),
+            kv_scale.stride(0), kv8.shape[1])
+
+
+def csa_attend_e4m3(p: AttnParams, q, gamma_q, q_pos, kv_cache8, kv_scale, idx, win_kv, sink, out, workspace, lse=None,
+                    stream=None):
+    """csa_attend over an e4m3 compressed cache (codes uint8 [B, rows, c], scales [B, rows])."""
+    B, n_q = _attend_common(q, p, gamma_q, q_pos, sink, out, lse)
+    if tuple(idx.shape) != (B, n_q, p.topk):
+        raise ValueError("idx must be [B, n_q, topk]")
+    kv, kv_bs, ks, ks_bs, rows = _kv8(kv_cache8, kv_scale)
+    st = _lib.load().csa_attend_e4m3(
+        ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
+        _i32(q_pos, "q_pos"), kv, kv_bs, ks, ks_bs, rows, _i32(idx, "idx"), _ptr(win_kv, torch.bfloat16, "win_kv"),
+        _rows(win_kv, "win_kv"), win_kv.shape[1], _ptr(sink, torch.float32, "sink"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+
+
+def hca_attend_e4m3(p: AttnParams, q, gamma_q, q_pos, kv_cache8, kv_scale, win_kv, sink, out, workspace, lse=None,
+                    stream=None):
+    """hca_attend over an e4m3 compressed cache (codes uint8 [B, rows, c], scales [B, rows])."""
+    B, n_q = _attend_common(q, p, gamma_q, q_pos, sink, out, lse)
+    kv, kv_bs, ks, ks_bs, rows = _kv8(kv_cache8, kv_scale)
+    st = _lib.load().hca_attend_e4m3(
+        ctypes.byref(p.c()), B, n_q, _ptr(q, torch.bfloat16, "q"), _ptr(gamma_q, torch.float32, "gamma_q"),
+        _i32(q_pos, "q_pos"), kv, kv_bs, ks, ks_bs, rows, _ptr(win_kv, torch.bfloat16, "win_kv"),
+        _rows(win_kv, "win_kv"), win_kv.shape[1], _ptr(sink, torch.float32, "sink"), _ptr(out, torch.bfloat16, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(workspace, None, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(st)
+
+
 def csa_attend_prepare(p: AttnParams, q, gamma_q, q_pos, kv_cache, idx, win_kv, sink, out, workspace, lse=None,
                        stream=None):
     """The query preparation of csa_attend alone, into the workspace (see include/lca.h)."""

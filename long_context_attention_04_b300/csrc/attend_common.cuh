@@ -29,6 +29,7 @@ struct AttendArgs {
     const float *gamma_q;         // [C]
     const int32_t *q_pos;         // [B][n_q]
     const __nv_bfloat16 *kv; int64_t kv_bs; int64_t cache_rows;
+    const float *kv_scale; int64_t ks_bs;   // e4m3 compressed rows (KV8): the rows' scales
     const int32_t *idx;           // [B][n_q][n_idx] or nullptr
     const __nv_bfloat16 *win; int64_t win_bs; int win_cap;
     const float *sink;            // [H]

@@ -44,6 +44,12 @@
 //               exceeds it by more than 2^8; the factors go through shared memory so each warp
 //               rescales its quarter of O^T), the P row of the head
 //   warps 8-11  fp16 re-encoding of each landed KV chunk (a quarter each)
+// With KV8 the compressed rows come from an e4m3 cache (one fp32 scale per row; the window
+// rows stay bf16): a compressed chunk lands as 64 rows x 128 codes (8 KB, one 128-byte box per
+// row) in the upper half of its slot, and the re-encoding warps write fp16(scale x value) into
+// the usual fp16 layout over the whole slot (zeros for masked rows): two lanes per row, which
+// read the row's codes before either writes (box 1's row covers exactly the row's codes).  Only
+// the producer gathers such chunks.
 // The split's unnormalised O, running max and row sum go to the workspace; combine_kernel
 // merges the splits with the sink and applies the output RoPE(-pos).
 // Every wait is bounded; a wait that runs out raises LCA_DEVERR_TIMEOUT and the CTA unwinds
@@ -117,7 +123,7 @@ __device__ __forceinline__ bool tile_row_valid(const AttendArgs &a, const RowLis
 
 // Register cap: the register file is split across the four SM sub-partitions (16K each) and
 // 12 warps place 3 on each, so 3 x 32 x 168 <= 16384.
-template <int C>
+template <int C, bool KV8 = false>
 __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtensorMap kv_tile_map,
                                                   const __grid_constant__ CUtensorMap kv_row_map,
                                                   const __grid_constant__ CUtensorMap win_row_map, AttendArgs a) {
@@ -256,6 +262,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             if (u == skip) break;   // test hook: this tile's chunks are never loaded, so their waits run out
             const int t = (int)t0 + u;
             const bool gathered = t >= tm.tc || L.idx;
+            const bool comp8 = KV8 && t < tm.tc;             // e4m3 compressed rows: one 128-code box
             // the tile's gathered rows, once for its c chunks (the index loads overlap the waits)
             int rc[4] = {-1, -1, -1, -1};
             if (gathered && lane < 16) gather_rows(t, 0, rc);
@@ -277,11 +284,21 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                     if (s == slot) last_g[s] = g;
                 const uint32_t dst = ptx::smem_u32(ring + slot * kAtChunkBytes);
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&full[slot], kAtChunkBytes);
-                    if (gathered) ptx::mbar_arrive(&gather_go[slot]);   // box 1 may be gathered now
+                    ptx::mbar_arrive_expect_tx(&full[slot], comp8 ? kAtBoxBytes : kAtChunkBytes);
+                    if (gathered && !comp8) ptx::mbar_arrive(&gather_go[slot]);   // box 1 may be gathered now
                 }
                 __syncwarp();
-                if (!gathered) {
+                if (comp8) {
+                    // e4m3 rows into the slot's upper half: 64 contiguous rows, or lane g's 4 gathered rows
+                    if (!gathered) {
+                        if (lane == 0)
+                            ptx::tma_load_2d(dst + kAtBoxBytes, &kv_tile_map, j * 128,
+                                             (int)(kv_row0 + (int64_t)t * kAtTile), &full[slot]);
+                    } else if (lane < 16) {
+                        ptx::tma_gather4(dst + kAtBoxBytes + lane * 512, &kv_row_map, j * 128, rc[0], rc[1], rc[2],
+                                         rc[3], &full[slot]);
+                    }
+                } else if (!gathered) {
                     // contiguous compressed rows: two 64-c boxes of 64 rows
                     if (lane < 2)
                         ptx::tma_load_2d(dst + lane * kAtBoxBytes, &kv_tile_map, j * 128 + lane * 64,
@@ -299,7 +316,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 const int target = t + (u < kPrefetchTiles ? u + 1 : kPrefetchTiles);
                 for (; pf_next <= target; ++pf_next)
                     if (pf_next < t1 && pf_next < tm.tc)
-                        for (int x = 0; x < C; x += 64)
+                        for (int x = 0; x < C; x += (KV8 ? 128 : 64))
                             ptx::tma_prefetch_2d(&kv_tile_map, x, (int)(kv_row0 + (int64_t)pf_next * kAtTile));
             }
         }
@@ -318,7 +335,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         // the first gathered chunk, gathered chunk g is the ((g - gfirst) / kAtSlots)-th to use
         // its slot's go barrier.
         bool ok = true;
-        const int u_first = L.idx ? 0 : (int)(tm.tc > t0 ? tm.tc - t0 : 0);
+        const int u_first = (L.idx && !KV8) ? 0 : (int)(tm.tc > t0 ? tm.tc - t0 : 0);
         const int gfirst = u_first * CC;
         for (int u = u_first; u < n_tiles && ok && !*abort_flag; ++u) {
             const int t = (int)t0 + u;
@@ -355,19 +372,79 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         const int ct = (warp - kAtConvWarp0) * 32 + lane;   // 0 .. 127
         bool ok = true, range_bad = false;
         const int total = n_tiles * CC;
+        // KV8: lanes 2r and 2r + 1 own row r of a compressed chunk (codes 0..63 and 64..127); the
+        // row's scale (0 for a masked row) is loaded a tile ahead, off the chunk's path
+        const int crow = ct >> 1, chalf = ct & 1;
+        const float *kscale = KV8 ? a.kv_scale + (int64_t)b * a.ks_bs : nullptr;
+        auto load_scale = [&](int u) -> float {
+            const int64_t t = t0 + u;
+            if (!KV8 || u >= n_tiles || t >= tm.tc) return 0.f;
+            const int64_t R = t * kAtTile + crow;
+            if (R >= L.n_comp) return 0.f;
+            int64_t e = R;
+            if (L.idx) {
+                e = __ldg(L.idx + R);
+                if (e < 0 || e >= a.cache_rows) return 0.f;
+            }
+            return __ldg(kscale + e);
+        };
+        float sc_cur = 0.f, sc_next = KV8 ? load_scale(0) : 0.f;
         for (int g = 0; g < total && !*abort_flag; ++g) {
             const int slot = g % kAtSlots;
+            const int u = g / CC;
+            if (KV8 && g % CC == 0) {
+                sc_cur = sc_next;
+                sc_next = load_scale(u + 1);
+            }
             if (!ptx::mbar_wait(&full[slot], (g / kAtSlots) & 1)) {
                 ok = false;
                 break;
             }
-            uint4 *chunk = reinterpret_cast<uint4 *>(ring + slot * kAtChunkBytes);
+            uint8_t *sl = ring + slot * kAtChunkBytes;
+            if (KV8 && t0 + u < tm.tc) {
+                // e4m3 chunk: the row's codes sit in the slot's upper half (swizzled 128-byte rows);
+                // its fp16 values go to box 0 (codes 0..63, this row's lane 2r) and box 1 (codes
+                // 64..127, lane 2r + 1), and box 1's row covers exactly this row's codes: both lanes
+                // read first, then write
+                const int r = crow;
+                uint4 e[4];
 #pragma unroll
-            for (int k = 0; k < kAtChunkBytes / 16 / (32 * kAtConvWarps); ++k) {
-                uint4 *p = chunk + ct + k * (32 * kAtConvWarps);
-                const uint4 v = *p;
-                range_bad |= bf16x8_exceeds_f16(v);
-                *p = bf16x8_to_f16x8(v);
+                for (int i = 0; i < 4; ++i) {
+                    const int u8 = 4 * chalf + i;
+                    e[i] = *reinterpret_cast<const uint4 *>(sl + kAtBoxBytes + r * 128 + ((u8 ^ (r & 7)) << 4));
+                }
+                __syncwarp();
+                // fp16(value) x fp16(scale), rounded to fp16 (about 2^-10 relative, inside the codes'
+                // own 2^-4); the largest e4m3 magnitude, 448, times the scale must fit fp16, and a
+                // NaN code of a row that is read is reported (masked rows, scale 0, become zeros)
+                const float s = sc_cur;
+                const bool live = s > 0.f;
+                const __half2 s2 = __float2half2_rn(s);
+                range_bad |= live && !(s * 448.f <= 65504.f);
+                uint8_t *row = sl + chalf * kAtBoxBytes + r * 128;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t words[4] = {e[i].x, e[i].y, e[i].z, e[i].w};
+                    uint32_t w[8];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        range_bad |= live && __vcmpeq4(words[q] & 0x7f7f7f7fu, 0x7f7f7f7fu) != 0;
+                        w[2 * q] = live ? hmul2_u32(e4m3x2_to_f16x2(words[q] & 0xffffu), s2) : 0u;
+                        w[2 * q + 1] = live ? hmul2_u32(e4m3x2_to_f16x2(words[q] >> 16), s2) : 0u;
+                    }
+                    const int v0 = 2 * i;
+                    *reinterpret_cast<uint4 *>(row + ((v0 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    *reinterpret_cast<uint4 *>(row + (((v0 + 1) ^ (r & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
+            } else {
+                uint4 *chunk = reinterpret_cast<uint4 *>(sl);
+#pragma unroll
+                for (int k = 0; k < kAtChunkBytes / 16 / (32 * kAtConvWarps); ++k) {
+                    uint4 *p = chunk + ct + k * (32 * kAtConvWarps);
+                    const uint4 v = *p;
+                    range_bad |= bf16x8_exceeds_f16(v);
+                    *p = bf16x8_to_f16x8(v);
+                }
             }
             ptx::fence_proxy_async();
             __syncwarp();

@@ -149,6 +149,28 @@ __device__ __forceinline__ uint32_t cvt_e4m3x2(float hi, float lo) {
     return r;
 }
 
+// Two e4m3 codes (the first in the low byte) as their exact values.
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t codes, float &first, float &second) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)codes));
+    first = __half2float(__ushort_as_half((unsigned short)(h & 0xffffu)));
+    second = __half2float(__ushort_as_half((unsigned short)(h >> 16)));
+}
+
+// Two e4m3 codes (the first in the low byte) as an fp16 pair (exact; the first in the low half).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+    uint32_t h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"((uint16_t)codes));
+    return h;
+}
+
+// An fp16 pair times s2 (both halves), rounded to fp16.
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t x, __half2 s2) {
+    __half2 v = *reinterpret_cast<__half2 *>(&x);
+    v = __hmul2(v, s2);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
 // The e4m3 codes of f[0..8) / s (IEEE divisions), in memory order; s > 0.
 __device__ __forceinline__ uint2 e4m3x8(const float *f, float s) {
     uint32_t w[2];

@@ -272,16 +272,25 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
                        const float *gamma_q, const int32_t *q_pos, const lca_bf16 *kv, int64_t kv_bs,
                        int64_t cache_rows, const int32_t *idx, const lca_bf16 *win, int64_t win_bs,
                        int win_cap, const float *sink, lca_bf16 *out, float *lse, void *ws, size_t ws_bytes,
-                       cudaStream_t stream, AttendMode mode = kAttendAll) {
+                       cudaStream_t stream, AttendMode mode = kAttendAll, const uint8_t *kv8 = nullptr,
+                       const float *kv_scale = nullptr, int64_t ks_bs = 0) {
     lca_status st = attend_validate(name, p, batch, n_q);
     if (st != LCA_OK) return st;
     const bool csa = idx != nullptr;
+    const bool e4m3 = kv8 != nullptr;        // the compressed rows come from an e4m3 cache
     if (csa) LCA_REQUIRE(p->topk >= 1, LCA_ERR_INVALID_ARG, "%s: topk must be positive", name);
     else LCA_REQUIRE(p->ratio >= 1, LCA_ERR_INVALID_ARG, "%s: ratio must be positive", name);
-    LCA_REQUIRE(q && gamma_q && q_pos && kv && win && sink && out, LCA_ERR_INVALID_ARG,
+    const void *kvp = e4m3 ? static_cast<const void *>(kv8) : static_cast<const void *>(kv);
+    LCA_REQUIRE(q && gamma_q && q_pos && kvp && win && sink && out, LCA_ERR_INVALID_ARG,
                 "%s: a required pointer is NULL", name);
-    LCA_REQUIRE(aligned16(q) && aligned16(kv) && aligned16(win) && aligned16(out), LCA_ERR_INVALID_ARG,
+    LCA_REQUIRE(aligned16(q) && aligned16(kvp) && aligned16(win) && aligned16(out), LCA_ERR_INVALID_ARG,
                 "%s: q, kv_cache, win_kv and out must be 16-byte aligned", name);
+    if (e4m3) {
+        LCA_REQUIRE(p->head_dim == 512, LCA_ERR_UNSUPPORTED, "%s: e4m3 rows need head_dim 512", name);
+        LCA_REQUIRE(kv_scale && reinterpret_cast<uintptr_t>(kv_scale) % 4 == 0 &&
+                        (batch == 1 || ks_bs >= cache_rows),
+                    LCA_ERR_INVALID_ARG, "%s: kv_scale (4-byte aligned, stride >= cache_rows) is required", name);
+    }
     LCA_REQUIRE(kv_bs % 8 == 0 && win_bs % 8 == 0, LCA_ERR_INVALID_ARG,
                 "%s: batch strides must be multiples of 8 elements", name);
     LCA_REQUIRE(cache_rows > 0, LCA_ERR_INVALID_ARG, "%s: cache_rows must be positive", name);
@@ -312,8 +321,10 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     a.q = reinterpret_cast<const __nv_bfloat16 *>(q);
     a.gamma_q = gamma_q;
     a.q_pos = q_pos;
-    a.kv = reinterpret_cast<const __nv_bfloat16 *>(kv);
+    a.kv = e4m3 ? nullptr : reinterpret_cast<const __nv_bfloat16 *>(kv);
     a.kv_bs = kv_bs;
+    a.kv_scale = kv_scale;
+    a.ks_bs = ks_bs;
     a.cache_rows = cache_rows;
     a.idx = idx;
     a.win = reinterpret_cast<const __nv_bfloat16 *>(win);
@@ -336,11 +347,19 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
     const uint64_t dims_kv[2] = {(uint64_t)C, kv_rows}, dims_win[2] = {(uint64_t)C, win_rows};
     const uint64_t row_bytes[1] = {(uint64_t)C * 2};
     const uint32_t box_tile[2] = {64, (uint32_t)kAtTile}, box_row[2] = {64, 1};
+    // e4m3 rows: 128 codes (128 bytes) per box row
+    const uint64_t row_bytes8[1] = {(uint64_t)C};
+    const uint32_t box_tile8[2] = {128, (uint32_t)kAtTile}, box_row8[2] = {128, 1};
     CUtensorMap kv_tile_map, kv_row_map, win_row_map;
-    if (!make_tensor_map(&kv_tile_map, kv, 2, dims_kv, row_bytes, box_tile, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&kv_row_map, kv, 2, dims_kv, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tensor_map(&win_row_map, win, 2, dims_win, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B))
-        return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
+    const bool maps_ok =
+        (e4m3 ? make_tensor_map(&kv_tile_map, kvp, 2, dims_kv, row_bytes8, box_tile8, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_DATA_TYPE_UINT8) &&
+                    make_tensor_map(&kv_row_map, kvp, 2, dims_kv, row_bytes8, box_row8, CU_TENSOR_MAP_SWIZZLE_128B,
+                                    CU_TENSOR_MAP_DATA_TYPE_UINT8)
+              : make_tensor_map(&kv_tile_map, kvp, 2, dims_kv, row_bytes, box_tile, CU_TENSOR_MAP_SWIZZLE_128B) &&
+                    make_tensor_map(&kv_row_map, kvp, 2, dims_kv, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B)) &&
+        make_tensor_map(&win_row_map, win, 2, dims_win, row_bytes, box_row, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!maps_ok) return fail(LCA_ERR_CUDA, "%s: tensor map rejected by the driver", name);
     if (mode != kAttendPrepared) {
         const dim3 prep_grid((unsigned)pl.units, kQImgHeads / kQPrepHeads);
         switch (C) {
@@ -352,6 +371,12 @@ lca_status attend_impl(const char *name, const lca_attn_params *p, int batch, in
         if (st != LCA_OK) return st;
         if (mode == kAttendPrepareOnly) return ok();
     }
+    if (e4m3) {
+        cudaFuncSetAttribute(attend_tc_kernel<512, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             AttendTcConfig<512>::SMEM_BYTES);
+        launch_pdl(attend_tc_kernel<512, true>, grid, dim3(kAtThreads), AttendTcConfig<512>::SMEM_BYTES, stream,
+                   kv_tile_map, kv_row_map, win_row_map, a);
+    } else
     switch (C) {
     case 128:
         cudaFuncSetAttribute(attend_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -841,6 +866,28 @@ lca_status hca_attend(const lca_attn_params *p, int batch, int n_q, const lca_bf
                       lca_bf16 *out, float *lse, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
     return attend_impl("hca_attend", p, batch, n_q, q, gamma_q, q_pos, kv_cache, kv_batch_stride, cache_rows, nullptr,
                        win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream);
+}
+
+lca_status csa_attend_e4m3(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                           const int32_t *q_pos, const uint8_t *kv_cache8, int64_t kv_batch_stride,
+                           const float *kv_scale, int64_t kv_scale_batch_stride, int64_t cache_rows,
+                           const int32_t *idx, const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap,
+                           const float *sink, lca_bf16 *out, float *lse, void *workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    LCA_REQUIRE(idx, LCA_ERR_INVALID_ARG, "csa_attend_e4m3: idx is NULL");
+    return attend_impl("csa_attend_e4m3", p, batch, n_q, q, gamma_q, q_pos, nullptr, kv_batch_stride, cache_rows,
+                       idx, win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream,
+                       kAttendAll, kv_cache8, kv_scale, kv_scale_batch_stride);
+}
+
+lca_status hca_attend_e4m3(const lca_attn_params *p, int batch, int n_q, const lca_bf16 *q, const float *gamma_q,
+                           const int32_t *q_pos, const uint8_t *kv_cache8, int64_t kv_batch_stride,
+                           const float *kv_scale, int64_t kv_scale_batch_stride, int64_t cache_rows,
+                           const lca_bf16 *win_kv, int64_t win_batch_stride, int win_cap, const float *sink,
+                           lca_bf16 *out, float *lse, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+    return attend_impl("hca_attend_e4m3", p, batch, n_q, q, gamma_q, q_pos, nullptr, kv_batch_stride, cache_rows,
+                       nullptr, win_kv, win_batch_stride, win_cap, sink, out, lse, workspace, workspace_bytes, stream,
+                       kAttendAll, kv_cache8, kv_scale, kv_scale_batch_stride);
 }
 
 // ---- hca_attend_noalloc: the dense attention with its scratch in a static device array ----

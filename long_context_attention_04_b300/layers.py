@@ -40,13 +40,18 @@ class CsaLayer:
 
     Indexer keys in e4m3: pass a uint8 idx_cache with its per-row scales idx_scale [B, rows]
     (fp32); the keys are then compressed into e4m3 and the step's indexer queries are quantised
-    (one scale per head) before the e4m3 indexer."""
+    (one scale per head) before the e4m3 indexer.  KV rows in e4m3: a uint8 kv_cache with
+    kv_scale [B, rows]; the entries are compressed into it and attended over by csa_attend_e4m3."""
 
     def __init__(self, p: AttnParams, weights: LayerWeights, kv_cache, idx_cache, win_kv, n_q: int = 1,
-                 idx_scale=None):
+                 idx_scale=None, kv_scale=None):
         self.p = p
         self.w = weights
         self.kv_cache, self.idx_cache, self.win_kv = kv_cache, idx_cache, win_kv
+        self.kv8 = kv_cache.dtype == torch.uint8
+        if self.kv8 and kv_scale is None:
+            raise ValueError("an e4m3 KV cache needs kv_scale [B, rows]")
+        self.kv_scale = kv_scale
         B, rows = kv_cache.shape[:2]
         dev = kv_cache.device
         self.idx = torch.empty((B, n_q, p.topk), dtype=torch.int32, device=dev)
@@ -69,10 +74,18 @@ class CsaLayer:
             api.csa_compress_kv(self.p, tok_vi, tok_zi, tok_pos0, self.w.bias_idx, None, 0, first_entry, n_new,
                                 self.idx_cache, stream)
 
+    def compress_kv(self, tok_v, tok_z, tok_pos0, first_entry, n_new, stream=None):
+        """The KV entries (RMSNorm + RoPE), in bf16 or e4m3."""
+        if self.kv8:
+            api.compress_kv_ex(True, self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
+                               n_new, self.kv_cache, cache_scale=self.kv_scale, stream=stream)
+        else:
+            api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
+                                n_new, self.kv_cache, stream)
+
     def compress(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, stream=None):
         """Compress n_new entries per sequence into both caches (KV: RMSNorm + RoPE; keys: neither)."""
-        api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
-                            n_new, self.kv_cache, stream)
+        self.compress_kv(tok_v, tok_z, tok_pos0, first_entry, n_new, stream)
         self.compress_keys(tok_vi, tok_zi, tok_pos0, first_entry, n_new, stream)
 
     def window(self, new_tok_v, new_pos0, stream=None):
@@ -88,9 +101,16 @@ class CsaLayer:
         return self.idx
 
     def attend(self, q, q_pos, out, lse=None, stream=None, part="csa_attend"):
-        """The attention; `part` may name csa_attend_prepare or csa_attend_prepared to run one half."""
-        api.csa_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.idx, self.win_kv, self.w.sink, out,
-                       self.ws_att, lse, stream, part)
+        """The attention; `part` may name csa_attend_prepare or csa_attend_prepared to run one half
+        (bf16 KV rows only: over e4m3 rows the call is whole)."""
+        if self.kv8:
+            if part != "csa_attend":
+                raise ValueError("the e4m3 attention has no separate halves")
+            api.csa_attend_e4m3(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.kv_scale, self.idx,
+                                self.win_kv, self.w.sink, out, self.ws_att, lse, stream)
+        else:
+            api.csa_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.idx, self.win_kv, self.w.sink, out,
+                           self.ws_att, lse, stream, part)
 
     def step(self, tok_v, tok_z, tok_vi, tok_zi, tok_pos0, first_entry, n_new, new_tok_v, new_pos0,
              q, q_idx, w_idx, q_pos, out, stream=None):
@@ -114,40 +134,56 @@ class CsaLayer:
         if side_prologue is not None:
             side_prologue(side)
         if n_new:
-            api.csa_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
-                                n_new, self.kv_cache, side)
+            self.compress_kv(tok_v, tok_z, tok_pos0, first_entry, n_new, side)
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, side)
-        self.attend(q, q_pos, out, stream=side, part="csa_attend_prepare")
+        if not self.kv8:
+            self.attend(q, q_pos, out, stream=side, part="csa_attend_prepare")
         join.record(side)
         if n_new:
             self.compress_keys(tok_vi, tok_zi, tok_pos0, first_entry, n_new, main)
         self.select(q_idx, w_idx, q_pos, main)
         main.wait_event(join)
-        self.attend(q, q_pos, out, stream=main, part="csa_attend_prepared")
+        self.attend(q, q_pos, out, stream=main, part="csa_attend" if self.kv8 else "csa_attend_prepared")
 
 
 class HcaLayer:
-    """One HCA layer for B sequences: KV cache [B, rows, c] and window ring [B, win_cap, c]."""
+    """One HCA layer for B sequences: KV cache [B, rows, c] and window ring [B, win_cap, c].
+    KV rows in e4m3: a uint8 kv_cache with kv_scale [B, rows] (fp32)."""
 
-    def __init__(self, p: AttnParams, weights: LayerWeights, kv_cache, win_kv, n_q: int = 1):
+    def __init__(self, p: AttnParams, weights: LayerWeights, kv_cache, win_kv, n_q: int = 1, kv_scale=None):
         self.p = p
         self.w = weights
         self.kv_cache, self.win_kv = kv_cache, win_kv
+        self.kv8 = kv_cache.dtype == torch.uint8
+        if self.kv8 and kv_scale is None:
+            raise ValueError("an e4m3 KV cache needs kv_scale [B, rows]")
+        self.kv_scale = kv_scale
         B, rows = kv_cache.shape[:2]
         self.ws_att = torch.empty(api.hca_attend_workspace(p, B, n_q, rows), dtype=torch.uint8,
                                   device=kv_cache.device)
 
     def compress(self, tok_v, tok_z, tok_pos0, first_entry, n_new, stream=None):
-        api.hca_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
-                            n_new, self.kv_cache, stream)
+        if self.kv8:
+            api.compress_kv_ex(False, self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
+                               n_new, self.kv_cache, cache_scale=self.kv_scale, stream=stream)
+        else:
+            api.hca_compress_kv(self.p, tok_v, tok_z, tok_pos0, self.w.bias_kv, self.w.gamma_kv, 1, first_entry,
+                                n_new, self.kv_cache, stream)
 
     def window(self, new_tok_v, new_pos0, stream=None):
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, stream)
 
     def attend(self, q, q_pos, out, lse=None, stream=None, part="hca_attend"):
-        """The attention; `part` may name hca_attend_prepare or hca_attend_prepared to run one half."""
-        api.hca_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.win_kv, self.w.sink, out,
-                       self.ws_att, lse, stream, part)
+        """The attention; `part` may name hca_attend_prepare or hca_attend_prepared to run one half
+        (bf16 KV rows only: over e4m3 rows the call is whole)."""
+        if self.kv8:
+            if part != "hca_attend":
+                raise ValueError("the e4m3 attention has no separate halves")
+            api.hca_attend_e4m3(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.kv_scale, self.win_kv,
+                                self.w.sink, out, self.ws_att, lse, stream)
+        else:
+            api.hca_attend(self.p, q, self.w.gamma_q, q_pos, self.kv_cache, self.win_kv, self.w.sink, out,
+                           self.ws_att, lse, stream, part)
 
     def step(self, tok_v, tok_z, tok_pos0, first_entry, n_new, new_tok_v, new_pos0, q, q_pos, out, stream=None):
         if n_new:
@@ -168,12 +204,13 @@ class HcaLayer:
         if side_prologue is not None:
             side_prologue(side)
         api.lca_window_update(self.p, new_tok_v, new_pos0, self.w.gamma_kv, self.win_kv, side)
-        self.attend(q, q_pos, out, stream=side, part="hca_attend_prepare")
+        if not self.kv8:
+            self.attend(q, q_pos, out, stream=side, part="hca_attend_prepare")
         join.record(side)
         if n_new:
             self.compress(tok_v, tok_z, tok_pos0, first_entry, n_new, main)
         main.wait_event(join)
-        self.attend(q, q_pos, out, stream=main, part="hca_attend_prepared")
+        self.attend(q, q_pos, out, stream=main, part="hca_attend" if self.kv8 else "hca_attend_prepared")
 
 
 class StepGraph:

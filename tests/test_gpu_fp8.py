@@ -1,7 +1,8 @@
 """GPU parity of the FP8 (e4m3) cache variants and the per-channel compressor, through the C ABI.
 
 The e4m3 codes are integers: the GPU quantiser must give the oracle's codes and scales bit for
-bit.  The indexer over e4m3 rows is compared with the oracle evaluating the same bytes (codes
+bit.  The attention over e4m3 rows is held to the bf16 attention's bound against the oracle over
+the same decoded rows.  The indexer over e4m3 rows is compared with the oracle evaluating the same bytes (codes
 and scales the oracle produced from seeded bf16 inputs), at the bf16 indexer's tolerance, and
 its top-k sets must match except at near-ties.  The compressor variants are compared with the
 oracle at the bf16 compressor's tolerance (plus e4m3 rounding for the e4m3 cache).
@@ -13,7 +14,7 @@ import pytest
 import torch
 
 import oracle
-from helpers import assert_rows_close, bf16_to_f64, check_topk, f32, u16
+from helpers import assert_close_rms, assert_rows_close, bf16_to_f64, check_topk, f32, u16
 from long_context_attention_04_b300 import api, build as lca_build
 from long_context_attention_04_b300.api import AttnParams
 from workloads import Rng, bits_to_bf16
@@ -192,3 +193,77 @@ def test_indexer_e4m3_close_to_bf16_indexer():
     a, b = s8.cpu().numpy().ravel(), s16.cpu().numpy().ravel()
     rel = np.sqrt(np.mean((a - b) ** 2)) / np.sqrt(np.mean(b * b))
     assert rel < 0.05, rel
+
+
+# ------------------------------------------------------------ e4m3 attention ----
+
+def _attend8_inputs(seed, B, n_q, H, c, rows, W, cap):
+    rng = Rng(seed)
+    kv = rng.normal_bf16((B, rows, c))
+    k8, ks = oracle.quantize_rows_e4m3(u16(kv).reshape(-1, c))
+    return dict(q=rng.normal_bf16((B, n_q, H, c)), k8=k8.reshape(B, rows, c), ks=ks.reshape(B, rows),
+                win=rng.normal_bf16((B, cap, c)), gamma=(0.5 + torch.rand(c, generator=rng.g)).float(),
+                sink=rng.normal_f32((H,)))
+
+
+def _check_attend8(p, d, pos, out, lse, idx=None):
+    o, l = out.cpu().float().numpy(), lse.cpu().numpy()
+    B, n_q = pos.shape
+    for b in range(B):
+        for i in range(n_q):
+            kw = dict(idx=idx[b, i]) if idx is not None else dict(n_dense=oracle.visible_entries(int(pos[b, i]),
+                                                                                                   p.ratio))
+            ro, rl = oracle.attend_e4m3(u16(d["q"][b, i]), f32(d["gamma"]), int(pos[b, i]), d["k8"][b], d["ks"][b],
+                                        f32(d["sink"]), u16(d["win"][b]), d["win"].shape[1], p.window, p.rope_dims,
+                                        p.rope_base, p.rms_eps, p.scale, **kw)
+            assert_close_rms(o[b, i], ro, what="e4m3 b=%d i=%d" % (b, i))
+            np.testing.assert_allclose(l[b, i], rl, rtol=0, atol=2e-3 * max(1.0, np.abs(rl).max()))
+
+
+def test_hca_attend_e4m3_matches_oracle():
+    """Dense attention over e4m3 rows against the oracle reading the same codes and scales: ragged,
+    full, one-entry and zero-entry row lists; the rows a query cannot see hold NaN codes and NaN
+    scales, which must not reach the output."""
+    B, n_q, m, rows, H, c, W = 3, 2, 4, 700, 64, 512, 128
+    cap = W + 8
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=m)
+    d = _attend8_inputs(95, B, n_q, H, c, rows, W, cap)
+    d["k8"][1, 1:] = 0x7F              # sequence 1 sees at most entry 0
+    d["ks"][1, 1:] = np.nan
+    pos = np.array([[m * 650 - 1, m * 700 - 1], [4, 0], [m * 333 + 1, m * 129 - 2]], dtype=np.int32)
+    out = torch.empty((B, n_q, H, c), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, n_q, H), dtype=torch.float32, device=DEV)
+    ws = torch.empty(api.hca_attend_workspace(p, B, n_q, rows), dtype=torch.uint8, device=DEV)
+    api.hca_attend_e4m3(p, dev(d["q"]), dev(d["gamma"]), _t(pos), _t(d["k8"]), _t(d["ks"]), dev(d["win"]),
+                        dev(d["sink"]), out, ws, lse)
+    assert api.lca_device_error() == 0
+    _check_attend8(p, d, pos, out, lse)
+
+
+@pytest.mark.parametrize("k,W", [(512, 128), (300, 1)])
+def test_csa_attend_e4m3_matches_oracle(k, W):
+    """Attention over gathered e4m3 rows (selections with -1 padding, an empty selection) plus bf16
+    window rows, against the oracle on the same bytes; unselected rows hold NaN codes."""
+    B, n_q, rows, H, c = 2, 2, 3000, 64, 512
+    cap = W + 5
+    p = AttnParams(heads=H, head_dim=c, rope_dims=64, window=W, ratio=4, topk=k)
+    d = _attend8_inputs(96, B, n_q, H, c, rows, W, cap)
+    g = np.random.default_rng(97)
+    idx = np.full((B, n_q, k), -1, np.int32)
+    counts = [[k, k - 37], [k // 3, 0]]
+    used = np.zeros((B, rows), bool)
+    for b in range(B):
+        for i in range(n_q):
+            sel = np.sort(g.choice(rows, counts[b][i], replace=False))
+            idx[b, i, :len(sel)] = sel
+            used[b, sel] = True
+    d["k8"][~used] = 0x7F
+    d["ks"][~used] = np.nan
+    pos = np.array([[4 * rows - 1, 9000], [3, 700]], dtype=np.int32)
+    out = torch.empty((B, n_q, H, c), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, n_q, H), dtype=torch.float32, device=DEV)
+    ws = torch.empty(api.csa_attend_workspace(p, B, n_q), dtype=torch.uint8, device=DEV)
+    api.csa_attend_e4m3(p, dev(d["q"]), dev(d["gamma"]), _t(pos), _t(d["k8"]), _t(d["ks"]), _t(idx), dev(d["win"]),
+                        dev(d["sink"]), out, ws, lse)
+    assert api.lca_device_error() == 0
+    _check_attend8(p, d, pos, out, lse, idx=idx)

@@ -88,11 +88,12 @@ CSA_DECODE_128K = dict(
     kind="csa_decode", B=32, pos=131071, entries=32768,
     shape=LayerShape(ratio=4, topk=512))
 
-# The same decode step with the indexer's keys in e4m3 (one fp32 scale per row): the key
-# entries are compressed into e4m3 and the indexer queries quantised each step.
-CSA_DECODE_128K_FP8 = dict(CSA_DECODE_128K, idx_e4m3=True,
-                           name="CSA decode with e4m3 indexer keys, batch 32, 128K context (32768 entries x 512), "
-                                "k=512, W=128, H=64")
+# The same decode step with FP8 caches: the indexer keys and the KV entries in e4m3 (one fp32
+# scale per row); the step compresses into e4m3, quantises its indexer queries, and attends over
+# the e4m3 rows (the window rows stay bf16).
+CSA_DECODE_128K_FP8 = dict(CSA_DECODE_128K, idx_e4m3=True, kv_e4m3=True,
+                           name="CSA decode with e4m3 caches (keys and KV), batch 32, 128K context "
+                                "(32768 entries x 512), k=512, W=128, H=64")
 
 HCA_DECODE_1M = dict(
     name="HCA decode, batch 16, 1M context (8192 entries x 512), W=128, H=64",
@@ -110,6 +111,11 @@ CSA_PREFILL_128K = dict(
     name="CSA chunked prefill, 2048 queries at 128K context (32768 entries), k=1024, W=128, H=64",
     kind="csa_prefill_chunk", B=1, q_begin=129024, Tq=2048, entries=32768,
     shape=LayerShape(ratio=4, topk=1024))
+
+# The HCA decode step over an e4m3 KV cache (one fp32 scale per row).
+HCA_DECODE_1M_FP8 = dict(HCA_DECODE_1M, kv_e4m3=True,
+                         name="HCA decode with an e4m3 KV cache, batch 16, 1M context (8192 entries x 512), W=128, "
+                              "H=64")
 
 BLOCK_DECODE_1M = dict(
     name="V4-Flash-style block decode, batch 4, 1M context, 8 CSA (k=512) + 8 HCA layers, "
@@ -160,6 +166,7 @@ WORKLOADS = {
     "csa_prefill_1m_proj": CSA_PREFILL_1M_PROJ,
     "csa_prefill_1m_scored": CSA_PREFILL_1M_SCORED,
     "csa_decode_128k_fp8": CSA_DECODE_128K_FP8,
+    "hca_decode_1m_fp8": HCA_DECODE_1M_FP8,
 }
 
 
