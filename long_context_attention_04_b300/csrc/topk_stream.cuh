@@ -66,11 +66,13 @@ struct StreamWg {                        // shared state of one selection group
 };
 
 // The candidates of one query: the kept region of its active buffer (range 0) and the warps'
-// segments (ranges 1 .. kStWarps), with their counts as published in shared memory.
+// segments (ranges 1 .. kStWarps), with their counts as published in shared memory.  (Every
+// routine below takes any source with nranges(), range(r) and count(r).)
 struct StSrc {
     const uint2 *buf;
     const int *wcnt;
     int kept;
+    __device__ __forceinline__ int nranges() const { return 1 + kStWarps; }
     __device__ __forceinline__ int count(int r) const {
         const int c = r == 0 ? kept : wcnt[r - 1];
         const int cap = r == 0 ? kStKeep : kStSeg;   // appends past the end were dropped
@@ -110,10 +112,11 @@ __device__ __forceinline__ bool wg_sync(StreamWg &s, uint32_t &phase) {
 
 // f(e, valid) for every slot of every range, kStBatch loads issued before any is used; the
 // trip counts are the same in every lane (f may use warp collectives).
-template <typename F>
-__device__ __forceinline__ void st_for_each(const StSrc &src, int tid, F f) {
+template <typename Src, typename F>
+__device__ __forceinline__ void st_for_each(const Src &src, int tid, F f) {
+    const int nr = src.nranges();
 #pragma unroll 1
-    for (int r = 0; r <= kStWarps; ++r) {
+    for (int r = 0; r < nr; ++r) {
         const uint2 *c = src.range(r);
         const int n = src.count(r);
         for (int i0 = 0; i0 < n; i0 += kStBatch * kStThreads) {
@@ -133,8 +136,8 @@ __device__ __forceinline__ void st_for_each(const StSrc &src, int tid, F f) {
 // take(e) holds, then the bin that holds the want-th element (1-based) counted from the top
 // bin (desc) or the bottom bin (asc), the number of elements before that bin in that order,
 // and the bin's own count: s.sel_bin, s.sel_above, s.sel_cnt.
-template <typename Take, typename Digit>
-__device__ bool wg_radix_step(StreamWg &s, uint32_t &phase, int tid, const StSrc &src, int nb, int want, bool desc,
+template <typename Src, typename Take, typename Digit>
+__device__ bool wg_radix_step(StreamWg &s, uint32_t &phase, int tid, const Src &src, int nb, int want, bool desc,
                               Take take, Digit digit) {
     for (int b = tid; b < kStBins; b += kStThreads) s.hist[b] = 0;
     if (!wg_sync(s, phase)) return false;
@@ -200,7 +203,8 @@ struct StSel {
 // Narrows the selection of the top `want` (key desc, index asc) of the candidates until the
 // candidates taken number at most `limit` (want <= limit; limit == want selects exactly want).
 // want <= the number of candidates.  On return *kept is the number of candidates taken.
-__device__ bool wg_select(StreamWg &s, uint32_t &phase, int tid, const StSrc &src, int want, int limit, StSel &sel,
+template <typename Src>
+__device__ bool wg_select(StreamWg &s, uint32_t &phase, int tid, const Src &src, int want, int limit, StSel &sel,
                           int &kept) {
     sel = StSel();
     int need = want;                                  // still to take inside the current bin
@@ -278,10 +282,10 @@ __device__ __forceinline__ int bitonic_keep(int e, int a, int b, int size, int s
     return (lo == up) ? min(a, b) : max(a, b);
 }
 
-// The final top k of query q, ascending by index and -1 padded, to out[0 .. k) (out may be null:
-// the state is reset all the same).
-__device__ bool wg_finish(StreamWg &s, uint32_t &phase, int tid, uint2 *cand, int q, int k, int32_t *out) {
-    const StSrc src = st_source(s, cand, q);
+// The top k of a source (score descending, index ascending), ascending by index and -1 padded,
+// to out[0 .. k) (out may be null).  Called by all threads of the group.
+template <typename Src>
+__device__ bool wg_select_sorted(StreamWg &s, uint32_t &phase, int tid, const Src &src, int k, int32_t *out) {
     const int n = src.total();
     const int take_n = n < k ? n : k;
     StSel sel;                                        // km = im = 0: everything taken
@@ -346,7 +350,11 @@ __device__ bool wg_finish(StreamWg &s, uint32_t &phase, int tid, uint2 *cand, in
             if (i < k) out[i] = i < take_n ? v[r] : -1;
         }
     }
-    if (!wg_sync(s, phase)) return false;
+    return wg_sync(s, phase);
+}
+
+// Query q's state back to empty, after its row (or its segment of a row) is done.
+__device__ bool wg_reset(StreamWg &s, uint32_t &phase, int tid, int q) {
     if (tid == 0) {
         s.kept[q] = 0;
 #pragma unroll
@@ -355,6 +363,13 @@ __device__ bool wg_finish(StreamWg &s, uint32_t &phase, int tid, uint2 *cand, in
         s.theta[q] = 0;
     }
     return wg_sync(s, phase);
+}
+
+// The final top k of query q, ascending by index and -1 padded, to out[0 .. k) (out may be null:
+// the state is reset all the same).
+__device__ bool wg_finish(StreamWg &s, uint32_t &phase, int tid, uint2 *cand, int q, int k, int32_t *out) {
+    const StSrc src = st_source(s, cand, q);
+    return wg_select_sorted(s, phase, tid, src, k, out) && wg_reset(s, phase, tid, q);
 }
 
 }  // namespace lca

@@ -206,3 +206,83 @@ def test_prefill_input_projections_sampled_rows():
                 np.testing.assert_allclose(got[r], ref, rtol=1e-5, atol=1e-4 * max(1e-30, float(np.abs(ref).max())))
             else:
                 assert_close_bf16_out(got[r], ref, what="projection row %d" % r)
+
+
+# ------------------------------------------------------------- FP8 (e4m3) caches ----
+# The oracle quantises the same seeded bf16 caches with its own quantiser (bit-exact with the
+# library's, tests/test_gpu_fp8.py), so every oracle input comes from the generator.
+
+def _e4m3_row_close(codes, scale, ref, what):
+    """A stored e4m3 row against the oracle's fp64 row: 2^-4 relative (three mantissa bits), half
+    the smallest step of the row's scale, and the bf16 rounding before the quantisation."""
+    back = oracle.dequantize_rows_e4m3(np.asarray(codes)[None], np.asarray([scale], np.float32))[0]
+    ref = np.asarray(ref, np.float64)
+    bound = 2.0 ** -4 * np.abs(ref) + 2.0 ** -9 * float(scale) + 2e-3 * np.sqrt(np.mean(ref * ref))
+    assert (np.abs(back - ref) <= bound).all(), what
+
+
+def test_csa_decode_128k_fp8_sampled_sequence():
+    """The CSA decode step with e4m3 keys and KV rows: the new entries (e4m3), the top-k of the e4m3
+    indexer and the attention over e4m3 rows, against the oracle on its own quantised caches."""
+    wk = bench.CsaDecode(WORKLOADS["csa_decode_128k_fp8"], seed=0)
+    s, d, pos, E = wk.s, wk.d, wk.pos, wk.entries
+    b = 5
+    kvb, ixb, winb = (bf16_bits(_host(d[k][b])) for k in ("kv_cache", "idx_cache", "win_kv"))
+    wk.step()
+    torch.cuda.synchronize()
+    assert api.lca_device_error() == 0
+    cap = d["win_kv"].shape[1]
+    g = d["gamma_kv"].cpu().numpy()
+    tv, tz = bf16_bits(_host(d["tok_v"][b])), _host(d["tok_z"][b]).numpy()
+    tvi, tzi = bf16_bits(_host(d["tok_vi"][b])), _host(d["tok_zi"][b]).numpy()
+    kv_new = oracle.compress(tv, tz, d["tok_pos0"], d["bias_kv"].cpu().numpy(), g, s.rms_eps, s.rope_dims,
+                             s.rope_base, 2 * s.ratio, s.ratio, E - 1, 1)[0]
+    k_new = oracle.compress(tvi, tzi, d["tok_pos0"], d["bias_idx"].cpu().numpy(), None, s.rms_eps, 0, s.rope_base,
+                            2 * s.ratio, s.ratio, E - 1, 1)[0]
+    w_new = oracle.window_row(tv[-1], g, s.rms_eps, s.rope_dims, s.rope_base, pos)
+    L = wk.layer
+    _e4m3_row_close(_host(L.kv_cache[b, E - 1]).numpy(), float(L.kv_scale[b, E - 1]), kv_new, "kv entry")
+    _e4m3_row_close(_host(L.idx_cache[b, E - 1]).numpy(), float(L.idx_scale[b, E - 1]), k_new, "key entry")
+    assert_rows_close(L.win_kv[b, pos % cap], w_new, "window row")
+    kvb[E - 1] = round_bf16_bits(kv_new)
+    ixb[E - 1] = round_bf16_bits(k_new)
+    winb[pos % cap] = round_bf16_bits(w_new)
+    kv8, kvs = oracle.quantize_rows_e4m3(kvb)
+    ix8, ixs = oracle.quantize_rows_e4m3(ixb)
+    q8, qs = oracle.quantize_rows_e4m3(bf16_bits(_host(d["q_idx"][b, 0])))
+    n_vis = oracle.visible_entries(pos, s.ratio)
+    sc = oracle.indexer_scores_e4m3(q8, qs, _host(d["w_idx"][b, 0]).numpy(), ix8, ixs, n_vis)
+    gpu_idx = _host(L.idx[b, 0]).numpy()
+    if check_topk(gpu_idx, sc, s.topk, what="fp8 topk") == 0:
+        ro, _ = oracle.attend_e4m3(bf16_bits(_host(d["q"][b, 0])), d["gamma_q"].cpu().numpy(), pos, kv8, kvs,
+                                   d["sink"].cpu().numpy(), winb, cap, s.window, s.rope_dims, s.rope_base, s.rms_eps,
+                                   wk.p.scale, idx=oracle.topk(sc, s.topk))
+        assert_close_rms(_host(wk.out[b, 0]).float().numpy(), ro, what="fp8 csa out")
+
+
+def test_hca_decode_1m_fp8_sampled_sequence():
+    """The HCA decode step over an e4m3 KV cache: the new entry and the attention against the oracle
+    on its own quantised cache."""
+    wk = bench.HcaDecode(WORKLOADS["hca_decode_1m_fp8"], seed=0)
+    s, d, pos, E = wk.s, wk.d, wk.pos, wk.entries
+    b = 11
+    kvb, winb = bf16_bits(_host(d["kv_cache"][b])), bf16_bits(_host(d["win_kv"][b]))
+    wk.step()
+    torch.cuda.synchronize()
+    assert api.lca_device_error() == 0
+    cap = d["win_kv"].shape[1]
+    g = d["gamma_kv"].cpu().numpy()
+    tv, tz = bf16_bits(_host(d["tok_v"][b])), _host(d["tok_z"][b]).numpy()
+    kv_new = oracle.compress(tv, tz, d["tok_pos0"], d["bias_kv"].cpu().numpy(), g, s.rms_eps, s.rope_dims,
+                             s.rope_base, s.ratio, s.ratio, E - 1, 1)[0]
+    w_new = oracle.window_row(tv[-1], g, s.rms_eps, s.rope_dims, s.rope_base, pos)
+    L = wk.layer
+    _e4m3_row_close(_host(L.kv_cache[b, E - 1]).numpy(), float(L.kv_scale[b, E - 1]), kv_new, "kv entry")
+    assert_rows_close(L.win_kv[b, pos % cap], w_new, "window row")
+    kvb[E - 1] = round_bf16_bits(kv_new)
+    winb[pos % cap] = round_bf16_bits(w_new)
+    kv8, kvs = oracle.quantize_rows_e4m3(kvb)
+    ro, _ = oracle.attend_e4m3(bf16_bits(_host(d["q"][b, 0])), d["gamma_q"].cpu().numpy(), pos, kv8, kvs,
+                               d["sink"].cpu().numpy(), winb, cap, s.window, s.rope_dims, s.rope_base, s.rms_eps,
+                               wk.p.scale, n_dense=oracle.visible_entries(pos, s.ratio))
+    assert_close_rms(_host(wk.out[b, 0]).float().numpy(), ro, what="fp8 hca out")
