@@ -429,8 +429,8 @@ const char *lca_last_error(void);
 lca_status lca_device_error(cudaStream_t stream, uint32_t *word);
 /* For tests of the failure path only.  Sets, on the current device, the bound of every wait
  * inside the kernels (SM clock cycles; <= 0 restores the default of 2e9, about a second) and
- * a tile index (per CTA, counted from 0) whose rows the attention kernel leaves unloaded
- * (< 0: none), so that the waits on that tile run out: the kernel then stops, frees its
+ * a tile index (per CTA, counted from 0; 1 or later, 0 is rejected) whose rows the attention
+ * kernel leaves unloaded (< 0: none), so that the waits on that tile run out: the kernel then stops, frees its
  * tensor memory, and lca_device_error reports LCA_ERR_TIMEOUT.  Affects every later launch
  * on the device until reset with lca_test_hooks(0, -1). */
 lca_status lca_test_hooks(long long wait_limit_cycles, int attend_skip_tile);

@@ -160,14 +160,17 @@ __device__ __forceinline__ void q_hat_warp(const AttendArgs &a, const QLane<C> &
         const bool in_rope = lane >= lane0;
         const bool lower = lane < lane0 + hl;
         const int partner = lower ? lane + hl : lane - hl;
+        // all partner values first, then one branch: the shuffles and the table reads pipeline
+        // instead of forming one dependent chain per element
+        float other[EPL];
 #pragma unroll
-        for (int u = 0; u < EPL; ++u) {
-            const float other = __shfl_sync(0xffffffffu, v[u], in_rope ? partner : lane);
-            if (in_rope) {
-                const int e = lane * EPL + u;
-                const int d = lower ? e - first : e - first - half;
-                const float cs = rcs[d], sn = rsn[d];
-                v[u] = lower ? v[u] * cs - other * sn : other * sn + v[u] * cs;
+        for (int u = 0; u < EPL; ++u) other[u] = __shfl_sync(0xffffffffu, v[u], in_rope ? partner : lane);
+        if (in_rope) {
+            const int d0 = lane * EPL - first - (lower ? 0 : half);
+#pragma unroll
+            for (int u = 0; u < EPL; ++u) {
+                const float cs = rcs[d0 + u], sn = rsn[d0 + u];
+                v[u] = lower ? v[u] * cs - other[u] * sn : other[u] * sn + v[u] * cs;
             }
         }
     }

@@ -34,10 +34,11 @@
 //
 // Roles (one CTA per (query, split), one CTA per SM, 12 warps):
 //   warp 0      TMA producer of KV chunks (box 0 of gathered chunks, both boxes of contiguous)
-//   warp 1      TMEM allocator and MMA issuer (one thread)
+//   warp 1      TMEM allocator and issuer of the logit products S (one thread)
 //   warp 2      second issuer of row gathers (box 1 of gathered chunks): TMA gathers from one
 //               warp reach about half the rate of two
-//   warp 3      bulk copy of the prepared query image (q_prep_kernel) into shared memory
+//   warp 3      bulk copy of the prepared query image (q_prep_kernel) into shared memory, then
+//               issuer of the PV products (one thread)
 //   warps 4-7   softmax, one per TMEM lane quarter: the query's TMEM part at the start, then per
 //               tile one head per thread pair (hi lane + lo lane), 32 rows each, online base-2
 //               softmax with a conditional rescale (the running max moves only when a logit
@@ -175,7 +176,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             ptx::mbar_init(&pv_done[s], 1);
         }
         ptx::mbar_init(vote_bar, kAtSoftmaxWarps);
-        ptx::mbar_init(teardown, 1);
+        ptx::mbar_init(teardown, 2);   // both MMA issuers
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
@@ -259,7 +260,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
 #pragma unroll
         for (int s = 0; s < kAtSlots; ++s) last_g[s] = -1;
         for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
-            if (u == skip) break;   // test hook: this tile's chunks are never loaded, so their waits run out
+            if (u > 0 && u == skip) break;   // test hook (tile 1 or later): its chunks are never loaded, so
+                                             // their waits run out; tile 0's loads never wait for the read
             const int t = (int)t0 + u;
             const bool gathered = t >= tm.tc || L.idx;
             const bool comp8 = KV8 && t < tm.tc;             // e4m3 compressed rows: one 128-code box
@@ -356,16 +358,45 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         }
         if (!ok) *abort_flag = 1;
     } else if (warp == kAtQWarp) {
-        // ---------------------------------------------------------- query image ----
+        // ---------------------------------------------------- query image, then PV ----
         // Chunks 0 .. CC-2 into the staging slots (the softmax warps move them to TMEM), the last
-        // chunk into its own area (the smem A operand of the last k steps).
+        // chunk into its own area (the smem A operand of the last k steps).  Then this warp's
+        // lane 0 issues every PV product: PV(v) as soon as P(v) is written, independently of the
+        // logit products, which warp 1 issues on another SM sub-partition (one issuing thread
+        // for both lost about half its issue rate to the other warps of its sub-partition).
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(q_full, CC * kQChunkBytes);
             for (int i = 0; i < CC - 1; ++i)
                 ptx::bulk_load(ptx::smem_u32(ring + (kAtSlots - Cfg::Q_STAGE_SLOTS + 2 * i) * kAtChunkBytes),
                                qimg + i * kQChunkBytes, kQChunkBytes, q_full);
             ptx::bulk_load(ptx::smem_u32(q_tail), qimg + (CC - 1) * kQChunkBytes, kQChunkBytes, q_full);
-            if (!ptx::mbar_wait(q_full, 0)) *abort_flag = 1;   // landed before the CTA can exit
+            bool ok = ptx::mbar_wait(q_full, 0);   // landed before the CTA can exit
+            constexpr uint32_t idesc_o = ptx::idesc_f16(128, kAtHP, true, false);
+            const uint64_t kv_mn = ptx::smem_desc(ptx::smem_u32(ring), kAtBoxBytes, 1024, ptx::kSwizzle128);  // MN-major A
+            const uint64_t p_k = ptx::smem_desc(ptx::smem_u32(p_buf), 16, 1024, ptx::kSwizzle128);
+            for (int v = 0; v < n_tiles && ok && !*abort_flag; ++v) {
+                if (!ptx::mbar_wait(&p_full[v & 1], (v >> 1) & 1)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint64_t pb = p_k + (uint64_t)((v & 1) * (kAtPBytes >> 4));
+                const uint32_t first = v > 0 ? 1u : 0u;
+#pragma unroll
+                for (int j = 0; j < CC; ++j) {
+                    const int g = v * CC + j, slot = g % kAtSlots;
+                    const uint64_t ad0 = kv_mn + (uint64_t)(slot * (kAtChunkBytes >> 4));
+#pragma unroll
+                    for (int kk = 0; kk < kAtTile / 16; ++kk)
+                        ptx::mma_f16(tmem + Cfg::TMEM_O + j * 64, ad0 + kk * (2048 >> 4), pb + kk * 2, idesc_o,
+                                     kk > 0 ? 1u : first);
+                    ptx::mma_commit(&empty[slot]);   // the slot's S product completed before P(v) existed
+                }
+                ptx::mma_commit(&pv_done[v & 1]);
+            }
+            if (!ok) *abort_flag = 1;
+            ptx::mma_commit(teardown);
+            ptx::mbar_wait(teardown, 0);
         }
     } else if (warp >= kAtConvWarp0) {
         // ------------------------------------------------------ fp16 re-encoding ----
@@ -453,87 +484,49 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         if (!ok) *abort_flag = 1;
         if (__any_sync(0xffffffffu, range_bad) && lane == 0) raise_error(LCA_DEVERR_FP16_RANGE);
     } else if (warp == kAtMmaWarp) {
-        // ------------------------------------------------------------- MMA issue ----
-        // S(u) chunk by chunk as the re-encoded chunks become ready, then PV(u-1) once the
-        // softmax has written P(u-1), so that the tensor pipe computes the next tile's logits
-        // while the softmax of the current one runs.  tcgen05 ops execute in issue order.
+        // ------------------------------------------------------------- S issue ----
+        // S(u) chunk by chunk as the re-encoded chunks become ready, once the softmax has read
+        // S(u-1) out of tensor memory; PV is issued by warp 3.  Each issuer commits its own
+        // products (tcgen05.commit tracks the issuing thread's operations).
         if (lane == 0) {
             constexpr uint32_t idesc_s = ptx::idesc_f16(128, kAtTile, false, false);
-            constexpr uint32_t idesc_o = ptx::idesc_f16(128, kAtHP, true, false);
             // Matrix descriptors computed once: a byte offset o inside shared memory moves the
             // descriptor's start-address field by o / 16, so every operand below is a base
             // descriptor plus a constant (the issue loop must stay faster than the tensor pipe).
             const uint64_t kv_k = ptx::smem_desc(ptx::smem_u32(ring), 16, 1024, ptx::kSwizzle128);   // K-major B
-            const uint64_t kv_mn = ptx::smem_desc(ptx::smem_u32(ring), kAtBoxBytes, 1024, ptx::kSwizzle128);  // MN-major A
             const uint64_t qt_k = ptx::smem_desc(ptx::smem_u32(q_tail), 16, 1024, ptx::kSwizzle128);
-            const uint64_t p_k = ptx::smem_desc(ptx::smem_u32(p_buf), 16, 1024, ptx::kSwizzle128);
             const uint32_t d_s = tmem + Cfg::TMEM_S;
-            // Issue order is chosen as the operands become ready: PV(v) as soon as P(v) is written
-            // (it releases its chunks' slots to the producer), S(u) once the softmax has drained
-            // S(u-1) and tile u's chunks are re-encoded.  No other order is needed: the softmax
-            // waits for PV(u-1) itself before it rescales O^T, and PV(u-1) can always be issued
-            // by then (its P was written before the softmax of tile u began).
             bool ok = ptx::mbar_wait(q_ready, 0);
             ptx::tc_fence_after();
-            int next_s = 0, next_pv = 0, s_chunk = 0;
-            long long idle_since = clock64();
-            const long long limit = *(volatile long long *)&g_wait_limit_cycles;
-            while (ok && next_pv < n_tiles && !*abort_flag) {
-                bool progressed = false;
-                if (next_pv < next_s && ptx::mbar_test(&p_full[next_pv & 1], (next_pv >> 1) & 1)) {
-                    const int v = next_pv++;
-                    ptx::tc_fence_after();
-                    const uint64_t pb = p_k + (uint64_t)((v & 1) * (kAtPBytes >> 4));
-                    const uint32_t first = v > 0 ? 1u : 0u;
-#pragma unroll
-                    for (int j = 0; j < CC; ++j) {
-                        const int g = v * CC + j, slot = g % kAtSlots;
-                        const uint64_t ad0 = kv_mn + (uint64_t)(slot * (kAtChunkBytes >> 4));
-#pragma unroll
-                        for (int kk = 0; kk < kAtTile / 16; ++kk)
-                            ptx::mma_f16(tmem + Cfg::TMEM_O + j * 64, ad0 + kk * (2048 >> 4), pb + kk * 2, idesc_o,
-                                         kk > 0 ? 1u : first);
-                        ptx::mma_commit(&empty[slot]);
-                    }
-                    ptx::mma_commit(&pv_done[v & 1]);
-                    progressed = true;
-                }
-                // S(next_s) chunk by chunk: each chunk's eight k steps as soon as it is re-encoded
-                if (next_s < n_tiles && (s_chunk > 0 || next_s == 0 || ptx::mbar_test(s_empty, (next_s - 1) & 1))) {
-                    const int u = next_s;
-                    while (s_chunk < CC) {
-                        const int g = u * CC + s_chunk, slot = g % kAtSlots;
-                        if (!ptx::mbar_test(&conv[slot], (g / kAtSlots) & 1)) break;
-                        ptx::tc_fence_after();
-                        const uint64_t bd0 = kv_k + (uint64_t)(slot * (kAtChunkBytes >> 4));
-                        if (s_chunk < CC - 1) {
-                            const uint32_t a0 = tmem + s_chunk * 64;
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                ptx::mma_f16_ts(d_s, a0 + kk * 8, bd0 + ((kk >> 2) * (kAtBoxBytes >> 4) + (kk & 3) * 2),
-                                                idesc_s, (s_chunk > 0 || kk > 0) ? 1u : 0u);
-                        } else {
-#pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                ptx::mma_f16(d_s, qt_k + ((kk >> 2) * ((128 * 128) >> 4) + (kk & 3) * 2),
-                                             bd0 + ((kk >> 2) * (kAtBoxBytes >> 4) + (kk & 3) * 2), idesc_s,
-                                             (CC > 1 || kk > 0) ? 1u : 0u);
-                        }
-                        ++s_chunk;
-                        progressed = true;
-                    }
-                    if (s_chunk == CC) {
-                        ptx::mma_commit(s_full);
-                        ++next_s;
-                        s_chunk = 0;
-                    }
-                }
-                if (progressed) {
-                    idle_since = clock64();
-                } else if (clock64() - idle_since > limit) {
-                    raise_error(LCA_DEVERR_TIMEOUT);
+            for (int u = 0; u < n_tiles && ok && !*abort_flag; ++u) {
+                if (u > 0 && !ptx::mbar_wait(s_empty, (u - 1) & 1)) {
                     ok = false;
+                    break;
                 }
+                for (int jc = 0; jc < CC; ++jc) {
+                    const int g = u * CC + jc, slot = g % kAtSlots;
+                    if (!ptx::mbar_wait(&conv[slot], (g / kAtSlots) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint64_t bd0 = kv_k + (uint64_t)(slot * (kAtChunkBytes >> 4));
+                    if (jc < CC - 1) {
+                        const uint32_t a0 = tmem + jc * 64;
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            ptx::mma_f16_ts(d_s, a0 + kk * 8, bd0 + ((kk >> 2) * (kAtBoxBytes >> 4) + (kk & 3) * 2),
+                                            idesc_s, (jc > 0 || kk > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            ptx::mma_f16(d_s, qt_k + ((kk >> 2) * ((128 * 128) >> 4) + (kk & 3) * 2),
+                                         bd0 + ((kk >> 2) * (kAtBoxBytes >> 4) + (kk & 3) * 2), idesc_s,
+                                         (CC > 1 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                if (!ok) break;
+                ptx::mma_commit(s_full);
             }
             if (!ok) *abort_flag = 1;
             ptx::mma_commit(teardown);

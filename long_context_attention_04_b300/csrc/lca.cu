@@ -611,7 +611,8 @@ const char *lca_last_error(void) { return t_last_error.c_str(); }
 
 lca_status lca_test_hooks(long long wait_limit_cycles, int attend_skip_tile) {
     const long long limit = wait_limit_cycles > 0 ? wait_limit_cycles : 2000000000LL;
-    const int skip = attend_skip_tile >= 0 ? attend_skip_tile : -1;
+    LCA_REQUIRE(attend_skip_tile != 0, LCA_ERR_INVALID_ARG, "lca_test_hooks: the skipped tile must be 1 or later");
+    const int skip = attend_skip_tile >= 1 ? attend_skip_tile : -1;
     cudaError_t e = cudaMemcpyToSymbol(g_wait_limit_cycles, &limit, sizeof limit);
     if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_test_skip_tile, &skip, sizeof skip);
     if (e != cudaSuccess) return fail(LCA_ERR_CUDA, "lca_test_hooks: %s", cudaGetErrorString(e));
