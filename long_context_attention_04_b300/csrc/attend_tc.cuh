@@ -594,13 +594,18 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                     const float send = __uint_as_float(part ? sv[i] : sv[32 + i]);
                     const float mine = __uint_as_float(part ? sv[32 + i] : sv[i]);
                     const float other = __shfl_xor_sync(0xffffffffu, send, 16);
-                    x[i] = ((mask >> i) & 1u) ? (mine + other) * a.scale_log2 : -INFINITY;
+                    x[i] = ((mask >> i) & 1u) ? mine + other : -INFINITY;   // unscaled logit
                 }
             }
-            float mx = x[0];
+            // the row maximum by a tree (depth 5, not a chain of 31), then in base-2 units (scale > 0)
+            float mt[16];
 #pragma unroll
-            for (int i = 1; i < 32; ++i) mx = fmaxf(mx, x[i]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            for (int i = 0; i < 16; ++i) mt[i] = fmaxf(x[i], x[i + 16]);
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
+            float mx = fmaxf(mt[0], __shfl_xor_sync(0xffffffffu, mt[0], 16)) * a.scale_log2;
             float alpha = 1.f;
             if (mx > m_run + kAtTau) {
                 alpha = m_run == -INFINITY ? 1.f : exp2f(m_run - mx);
@@ -645,16 +650,20 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 break;
             }
             const float ms = m_run == -INFINITY ? 0.f : m_run;
-            float pr[32];
+            // P in fp16, two values per conversion; the row sum adds the same rounded values
+            uint32_t pw[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                pr[i] = __half2float(__float2half_rn(exp2f(x[i] - ms)));
-                l_run += pr[i];
+            for (int i = 0; i < 32; i += 2) {
+                pw[i / 2] = pack_f16x2(ex2_approx(fmaf(x[i], a.scale_log2, -ms)),
+                                       ex2_approx(fmaf(x[i + 1], a.scale_log2, -ms)));
+                const float2 pf = __half22float2(*reinterpret_cast<const __half2 *>(&pw[i / 2]));
+                l_run += pf.x + pf.y;
             }
             uint8_t *pb = p_buf + (u & 1) * kAtPBytes;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(pb + ptx::sw128_offset(h, 4 * part + k)) = pack8_f16(pr + 8 * k);
+                *reinterpret_cast<uint4 *>(pb + ptx::sw128_offset(h, 4 * part + k)) =
+                    make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
             ptx::fence_proxy_async();
             ptx::tc_fence_before();
             __syncwarp();

@@ -90,6 +90,14 @@ __device__ __forceinline__ bool bf16x8_exceeds_f16(const uint4 &v) {
     return __vcmpgeu2(a, 0x47804780u) != 0;
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22; -inf gives 0, results below
+// 2^-126 flush to 0): the attention's probabilities, which are then rounded to fp16.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
