@@ -40,7 +40,7 @@
 //   warp 3      bulk copy of the prepared query image (q_prep_kernel) into shared memory, then
 //               issuer of the PV products (one thread)
 //   warps 4-7   softmax, one per TMEM lane quarter: the query's TMEM part at the start, then per
-//               tile one head per thread pair (hi lane + lo lane), 32 rows each, online base-2
+//               tile one head per thread pair (hi lane + lo lane), half the rows each, online base-2
 //               softmax with a conditional rescale (the running max moves only when a logit
 //               exceeds it by more than 2^8; the factors go through shared memory so each warp
 //               rescales its quarter of O^T), the P row of the head
@@ -65,10 +65,13 @@ namespace lca {
 
 constexpr int kAtHP = 64;                                // padded heads (MMA N of PV)
 constexpr int kAtTile = 64;                              // rows per tile (MMA N of the logit product)
-constexpr int kAtSlots = 10;                             // KV chunk slots in the ring
-constexpr int kAtChunkBytes = kAtTile * 128 * 2;         // KV chunk: 64 rows x 128 c (16 KB)
-constexpr int kAtBoxBytes = kAtTile * 128;               // one 64-c box of a chunk (8 KB)
-constexpr int kAtPBytes = kAtHP * kAtTile * 2;           // P: 64 heads x 64 rows, fp16 (8 KB)
+constexpr int kAtChunkBytes = kAtTile * 128 * 2;         // KV chunk: kAtTile rows x 128 c
+constexpr int kAtBoxBytes = kAtTile * 128;               // one 64-c box of a chunk
+constexpr int kAtSlots = (160 * 1024) / kAtChunkBytes;   // KV chunk slots in the ring (160 KB)
+constexpr int kAtPBytes = kAtHP * 128;                   // P: 64 heads x kAtTile rows fp16, 128-byte rows (8 KB)
+constexpr int kAtRpl = kAtTile / 2;                      // tile rows per softmax lane (hi lane: the first half)
+static_assert(kAtTile % 16 == 0 && kAtTile >= 32 && kAtTile <= 64 && kAtRpl % 8 == 0, "tile rows");
+static_assert(kAtChunkBytes % 1024 == 0 && kAtBoxBytes % 1024 == 0, "128-byte swizzled boxes start on 1 KB");
 constexpr int kAtProducerWarp = 0;
 constexpr int kAtMmaWarp = 1;
 constexpr int kAtGatherWarp = 2;                         // second issuer of row gathers
@@ -88,7 +91,8 @@ struct AttendTcConfig {
     static constexpr int TMEM_S = QT * 64;                    // S: 64 columns
     static constexpr int TMEM_O = TMEM_S + 64;                // O^T chunk j at TMEM_O + 64 j
     static constexpr int TMEM_COLS = C;
-    static constexpr int Q_STAGE_SLOTS = 2 * QT;              // ring slots that first stage the TMEM query part
+    // ring slots (at its end) that first stage the TMEM query part, image chunk i at offset i x 32 KB
+    static constexpr int Q_STAGE_SLOTS = (QT * kQChunkBytes + kAtChunkBytes - 1) / kAtChunkBytes;
     static constexpr int MISC = 2048;                         // barriers, rescale factors, flags
     static constexpr int SMEM_BYTES = MISC + 1024 + kAtSlots * kAtChunkBytes + kQChunkBytes + 2 * kAtPBytes;
     static_assert(TMEM_O + 64 * CC == TMEM_COLS, "tensor memory layout");
@@ -135,7 +139,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     uint8_t *misc = smem_raw;
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw + Cfg::MISC) + 1023) &
                                                 ~uintptr_t(1023));
-    uint8_t *ring = base;                                     // slot s: 2 boxes [64 rows x 128 B]
+    uint8_t *ring = base;                                     // slot s: 2 boxes [kAtTile rows x 128 B]
     uint8_t *q_tail = ring + kAtSlots * kAtChunkBytes;        // last c chunk of the query image (32 KB)
     uint8_t *p_buf = q_tail + kQChunkBytes;                   // 2 x P [64 heads x 128 B] fp16
     uint64_t *full = reinterpret_cast<uint64_t *>(misc);      // chunk landed
@@ -153,9 +157,10 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     uint64_t *teardown = vote_bar + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(teardown + 1);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    // misc: 51 barriers + TMEM slot + abort flag (416 B), rescale factors, their flags
-    float *alphas = reinterpret_cast<float *>(misc + 512);    // [2][64]
-    int *flags = reinterpret_cast<int *>(misc + 1024);        // [2][4]
+    // misc: 4 kAtSlots + 11 barriers, TMEM slot, abort flag; rescale factors; their flags
+    float *alphas = reinterpret_cast<float *>(misc + 640);    // [2][64]
+    int *flags = reinterpret_cast<int *>(misc + 1280);        // [2][4]
+    static_assert((4 * kAtSlots + 11) * 8 + 8 <= 640, "barriers fit below the rescale factors");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // ---- set-up: barriers, TMEM ----
@@ -216,7 +221,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     const int n_tiles = (int)(t1 - t0);
     const int64_t kv_row0 = (int64_t)b * (a.kv_bs / C);
     const int64_t win_row0 = (int64_t)b * (a.win_bs / C);
-    // Rows 4 lane .. 4 lane + 3 (lane < 16) of gathered tile t as 2D-map row coordinates
+    // Rows 4 lane .. 4 lane + 3 (lane < kAtTile / 4) of gathered tile t as 2D-map row coordinates
     // (-1: masked, read as 0).
     auto gather_rows = [&](int t, int j, int *rc) {
 #pragma unroll
@@ -267,7 +272,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             const bool comp8 = KV8 && t < tm.tc;             // e4m3 compressed rows: one 128-code box
             // the tile's gathered rows, once for its c chunks (the index loads overlap the waits)
             int rc[4] = {-1, -1, -1, -1};
-            if (gathered && lane < 16) gather_rows(t, 0, rc);
+            if (gathered && lane < kAtTile / 4) gather_rows(t, 0, rc);
             for (int j = 0; j < CC; ++j) {
                 const int g = u * CC + j, slot = g % kAtSlots;
                 if (g >= kAtSlots && !ptx::mbar_wait(&empty[slot], ((g / kAtSlots) - 1) & 1)) {
@@ -296,7 +301,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                         if (lane == 0)
                             ptx::tma_load_2d(dst + kAtBoxBytes, &kv_tile_map, j * 128,
                                              (int)(kv_row0 + (int64_t)t * kAtTile), &full[slot]);
-                    } else if (lane < 16) {
+                    } else if (lane < kAtTile / 4) {
                         ptx::tma_gather4(dst + kAtBoxBytes + lane * 512, &kv_row_map, j * 128, rc[0], rc[1], rc[2],
                                          rc[3], &full[slot]);
                     }
@@ -305,7 +310,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                     if (lane < 2)
                         ptx::tma_load_2d(dst + lane * kAtBoxBytes, &kv_tile_map, j * 128 + lane * 64,
                                          (int)(kv_row0 + (int64_t)t * kAtTile), &full[slot]);
-                } else if (lane < 16) {
+                } else if (lane < kAtTile / 4) {
                     // indexed rows: lane g gathers rows 4g .. 4g+3 of the tile, c box 0
                     const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
                     ptx::tma_gather4(dst + lane * 512, map, j * 128, rc[0], rc[1], rc[2], rc[3], &full[slot]);
@@ -342,14 +347,14 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         for (int u = u_first; u < n_tiles && ok && !*abort_flag; ++u) {
             const int t = (int)t0 + u;
             int rc[4] = {-1, -1, -1, -1};
-            if (lane < 16) gather_rows(t, 1, rc);
+            if (lane < kAtTile / 4) gather_rows(t, 1, rc);
             for (int j = 0; j < CC; ++j) {
                 const int g = u * CC + j, slot = g % kAtSlots;
                 if (!ptx::mbar_wait(&gather_go[slot], ((g - gfirst) / kAtSlots) & 1)) {
                     ok = false;
                     break;
                 }
-                if (lane < 16) {
+                if (lane < kAtTile / 4) {
                     const CUtensorMap *map = t < tm.tc ? &kv_row_map : &win_row_map;
                     ptx::tma_gather4(ptx::smem_u32(ring + slot * kAtChunkBytes) + kAtBoxBytes + lane * 512, map,
                                      j * 128 + 64, rc[0], rc[1], rc[2], rc[3], &full[slot]);
@@ -367,7 +372,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(q_full, CC * kQChunkBytes);
             for (int i = 0; i < CC - 1; ++i)
-                ptx::bulk_load(ptx::smem_u32(ring + (kAtSlots - Cfg::Q_STAGE_SLOTS + 2 * i) * kAtChunkBytes),
+                ptx::bulk_load(ptx::smem_u32(ring + (kAtSlots - Cfg::Q_STAGE_SLOTS) * kAtChunkBytes + i * kQChunkBytes),
                                qimg + i * kQChunkBytes, kQChunkBytes, q_full);
             ptx::bulk_load(ptx::smem_u32(q_tail), qimg + (CC - 1) * kQChunkBytes, kQChunkBytes, q_full);
             bool ok = ptx::mbar_wait(q_full, 0);   // landed before the CTA can exit
@@ -409,7 +414,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
         const float *kscale = KV8 ? a.kv_scale + (int64_t)b * a.ks_bs : nullptr;
         auto load_scale = [&](int u) -> float {
             const int64_t t = t0 + u;
-            if (!KV8 || u >= n_tiles || t >= tm.tc) return 0.f;
+            if (!KV8 || u >= n_tiles || t >= tm.tc || crow >= kAtTile) return 0.f;
             const int64_t R = t * kAtTile + crow;
             if (R >= L.n_comp) return 0.f;
             int64_t e = R;
@@ -438,12 +443,14 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 // 64..127, lane 2r + 1), and box 1's row covers exactly this row's codes: both lanes
                 // read first, then write
                 const int r = crow;
-                uint4 e[4];
+                const bool has_row = r < kAtTile;     // lanes past the tile's rows idle
+                uint4 e[4] = {};
+                if (has_row)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int u8 = 4 * chalf + i;
-                    e[i] = *reinterpret_cast<const uint4 *>(sl + kAtBoxBytes + r * 128 + ((u8 ^ (r & 7)) << 4));
-                }
+                    for (int i = 0; i < 4; ++i) {
+                        const int u8 = 4 * chalf + i;
+                        e[i] = *reinterpret_cast<const uint4 *>(sl + kAtBoxBytes + r * 128 + ((u8 ^ (r & 7)) << 4));
+                    }
                 __syncwarp();
                 // fp16(value) x fp16(scale), rounded to fp16 (about 2^-10 relative, inside the codes'
                 // own 2^-4); the largest e4m3 magnitude, 448, times the scale must fit fp16, and a
@@ -454,7 +461,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 range_bad |= live && !(s * 448.f <= 65504.f);
                 uint8_t *row = sl + chalf * kAtBoxBytes + r * 128;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 4 && has_row; ++i) {
                     const uint32_t words[4] = {e[i].x, e[i].y, e[i].z, e[i].w};
                     uint32_t w[8];
 #pragma unroll
@@ -535,8 +542,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     } else {
         // -------------------------------------------------------------- softmax ----
         // Warp q (lane quarter q) owns query rows 32 q .. 32 q + 31: lane l < 16 the hi part of
-        // head 16 q + l, lane l + 16 its lo part.  Per tile the hi lane takes tile rows 0..31 of
-        // its head and the lo lane rows 32..63, each adding the partner's part.
+        // head 16 q + l, lane l + 16 its lo part.  Per tile the hi lane takes the first kAtRpl tile
+        // rows of its head and the lo lane the other kAtRpl, each adding the partner's part.
         const int q = warp & 3;
         const int part = lane >> 4;
         const int h = 16 * q + (lane & 15);
@@ -546,7 +553,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             // the query's TMEM part: this lane's row of image chunks 0 .. CC-2
             const int row = 32 * q + lane;
             for (int i = 0; i < CC - 1; ++i) {
-                const uint8_t *img = ring + (kAtSlots - Cfg::Q_STAGE_SLOTS + 2 * i) * kAtChunkBytes;
+                const uint8_t *img = ring + (kAtSlots - Cfg::Q_STAGE_SLOTS) * kAtChunkBytes + i * kQChunkBytes;
                 uint32_t v[64];
 #pragma unroll
                 for (int bx = 0; bx < 2; ++bx)
@@ -577,34 +584,37 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 break;
             }
             ptx::tc_fence_after();
-            float x[32];
+            float x[kAtRpl];
             {
-                uint32_t sv[64];
-                ptx::tmem_ld64(lane_base + Cfg::TMEM_S, sv);
+                uint32_t sv[kAtTile];
+                ptx::tmem_ld32(lane_base + Cfg::TMEM_S, sv);
+                if constexpr (kAtTile == 64) ptx::tmem_ld32(lane_base + Cfg::TMEM_S + 32, sv + 32);
+                else if constexpr (kAtTile == 48) ptx::tmem_ld16(lane_base + Cfg::TMEM_S + 32, sv + 32);
                 ptx::tmem_ld_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(s_empty);   // S may be overwritten by the next tile
+                // row validity of the tile's rows (64-bit: bit r for row r), this lane's half
                 const uint32_t m0 = __ballot_sync(0xffffffffu, tile_row_valid(a, L, tm, t, lane));
-                const uint32_t m1 = __ballot_sync(0xffffffffu, tile_row_valid(a, L, tm, t, lane + 32));
-                const uint32_t mask = part ? m1 : m0;
+                const uint32_t m1 = kAtTile > 32 ? __ballot_sync(0xffffffffu, tile_row_valid(a, L, tm, t, lane + 32)) : 0u;
+                const uint32_t mask = (uint32_t)((((uint64_t)m1 << 32) | m0) >> (part * kAtRpl));
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    // hi lane: own hi[i] + partner's lo[i]; lo lane: own lo[32+i] + partner's hi[32+i]
-                    const float send = __uint_as_float(part ? sv[i] : sv[32 + i]);
-                    const float mine = __uint_as_float(part ? sv[32 + i] : sv[i]);
+                for (int i = 0; i < kAtRpl; ++i) {
+                    // hi lane: own hi[i] + partner's lo[i]; lo lane: own lo[R+i] + partner's hi[R+i]
+                    const float send = __uint_as_float(part ? sv[i] : sv[kAtRpl + i]);
+                    const float mine = __uint_as_float(part ? sv[kAtRpl + i] : sv[i]);
                     const float other = __shfl_xor_sync(0xffffffffu, send, 16);
                     x[i] = ((mask >> i) & 1u) ? mine + other : -INFINITY;   // unscaled logit
                 }
             }
-            // the row maximum by a tree (depth 5, not a chain of 31), then in base-2 units (scale > 0)
-            float mt[16];
+            // the row maximum by a tree (not a chain), then in base-2 units (scale > 0)
+            float mt[kAtRpl];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) mt[i] = fmaxf(x[i], x[i + 16]);
+            for (int i = 0; i < kAtRpl; ++i) mt[i] = x[i];
 #pragma unroll
-            for (int w = 8; w >= 1; w >>= 1)
+            for (int n = kAtRpl; n > 1; n = (n + 1) / 2)
 #pragma unroll
-                for (int i = 0; i < w; ++i) mt[i] = fmaxf(mt[i], mt[i + w]);
+                for (int i = 0; i < n / 2; ++i) mt[i] = fmaxf(mt[i], mt[(n + 1) / 2 + i]);
             float mx = fmaxf(mt[0], __shfl_xor_sync(0xffffffffu, mt[0], 16)) * a.scale_log2;
             float alpha = 1.f;
             if (mx > m_run + kAtTau) {
@@ -651,9 +661,9 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             }
             const float ms = m_run == -INFINITY ? 0.f : m_run;
             // P in fp16, two values per conversion; the row sum adds the same rounded values
-            uint32_t pw[16];
+            uint32_t pw[kAtRpl / 2];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
+            for (int i = 0; i < kAtRpl; i += 2) {
                 pw[i / 2] = pack_f16x2(ex2_approx(fmaf(x[i], a.scale_log2, -ms)),
                                        ex2_approx(fmaf(x[i + 1], a.scale_log2, -ms)));
                 const float2 pf = __half22float2(*reinterpret_cast<const __half2 *>(&pw[i / 2]));
@@ -661,8 +671,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
             }
             uint8_t *pb = p_buf + (u & 1) * kAtPBytes;
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-                *reinterpret_cast<uint4 *>(pb + ptx::sw128_offset(h, 4 * part + k)) =
+            for (int k = 0; k < kAtRpl / 8; ++k)
+                *reinterpret_cast<uint4 *>(pb + ptx::sw128_offset(h, (kAtRpl / 8) * part + k)) =
                     make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
             ptx::fence_proxy_async();
             ptx::tc_fence_before();
