@@ -101,13 +101,6 @@ __device__ __forceinline__ const __nv_bfloat16 *row_source(const AttendArgs &a, 
     return nullptr;
 }
 
-// Tiles [t0, t1) of `tile_rows` rows handled by split s of S.
-__device__ __forceinline__ void split_range(int64_t n_rows, int tile_rows, int s, int S, int64_t &t0, int64_t &t1) {
-    const int64_t T = (n_rows + tile_rows - 1) / tile_rows;
-    t0 = T * s / S;
-    t1 = T * (s + 1) / S;
-}
-
 // Query prologue for head h (one warp): RMSNorm over C with gamma_q, then RoPE(pos) on the
 // trailing R dims.  Lane l holds elements [l*EPL, l*EPL+EPL) in v[] on return.
 // cos/sin of the R/2 RoPE angles at position pos, one pair per thread (threads [0, R/2)).

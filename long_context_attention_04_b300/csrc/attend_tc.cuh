@@ -114,6 +114,20 @@ __device__ __forceinline__ TileMap tile_map(const RowList &L) {
     return m;
 }
 
+// Tiles [t0, t1) of split `split` of `splits`: contiguous ranges of equal cost, where a tile of
+// window rows (row gathers) costs kAtWinCost tiles of contiguous compressed rows (2D boxes) in a
+// dense (HCA) list (the gathers stream at about half the rate of the boxes, and the window
+// tiles all fall to the last split); every tile of a gathered (CSA) list costs one.
+constexpr int kAtWinCost = 2;
+__device__ __forceinline__ void split_tiles(const TileMap &m, bool gathered, int split, int splits, int64_t &t0,
+                                            int64_t &t1) {
+    const int64_t w = gathered ? 1 : kAtWinCost;
+    const int64_t total = m.tc + w * m.tw;
+    auto tile_at = [&](int64_t c) { return c <= m.tc ? c : m.tc + (c - m.tc + w - 1) / w; };
+    t0 = tile_at(total * split / splits);
+    t1 = tile_at(total * (split + 1) / splits);
+}
+
 // Whether row r of tile t is a real key/value row.
 __device__ __forceinline__ bool tile_row_valid(const AttendArgs &a, const RowList &L, const TileMap &m, int t, int r) {
     if (t < m.tc) {
@@ -199,8 +213,8 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
     const int b = unit / a.n_q, qi = unit % a.n_q;
     const RowList L = make_row_list(a, b, qi);
     const TileMap tm = tile_map(L);
-    const int64_t t0 = (int64_t)tm.total() * split / a.splits;
-    const int64_t t1 = (int64_t)tm.total() * (split + 1) / a.splits;
+    int64_t t0, t1;
+    split_tiles(tm, L.idx != nullptr, split, a.splits, t0, t1);
     const int64_t pidx0 = ((int64_t)unit * a.splits + split) * a.H;
     const uint8_t *qimg = q_img<C>(a, unit);
 
@@ -443,7 +457,7 @@ __global__ void __maxnreg__(168) attend_tc_kernel(const __grid_constant__ CUtens
                 // 64..127, lane 2r + 1), and box 1's row covers exactly this row's codes: both lanes
                 // read first, then write
                 const int r = crow;
-                const bool has_row = r < kAtTile;     // lanes past the tile's rows idle
+                const bool has_row = kAtTile == 64 || r < kAtTile;   // lanes past the tile's rows idle
                 uint4 e[4] = {};
                 if (has_row)
 #pragma unroll
