@@ -30,9 +30,12 @@
 // Rows of a query: compressed rows (CSA: the selected entries; HCA: entries 0..n_vis), then
 // the window rows; tiles never mix the two.  All loads are TMA: contiguous compressed tiles
 // (HCA) as 2D boxes of 64 rows, indexed rows (CSA selections, window ring rows) with 4-row
-// gathers; masked rows are fetched at coordinate -1 and arrive as zeros.
+// gathers; masked rows are fetched at coordinate -1 and arrive as zeros.  A query's tiles are
+// cut into contiguous split ranges of equal cost (split_tiles).  The tile height is kAtTile
+// (64; the kernel is written for 32 to 64).
 //
-// Roles (one CTA per (query, split), one CTA per SM, 12 warps):
+// Roles (one CTA per (query, split), one CTA per SM, 12 warps; the two MMA issuers sit on
+// different SM sub-partitions, warp id mod 4):
 //   warp 0      TMA producer of KV chunks (box 0 of gathered chunks, both boxes of contiguous)
 //   warp 1      TMEM allocator and issuer of the logit products S (one thread)
 //   warp 2      second issuer of row gathers (box 1 of gathered chunks): TMA gathers from one
@@ -40,8 +43,8 @@
 //   warp 3      bulk copy of the prepared query image (q_prep_kernel) into shared memory, then
 //               issuer of the PV products (one thread)
 //   warps 4-7   softmax, one per TMEM lane quarter: the query's TMEM part at the start, then per
-//               tile one head per thread pair (hi lane + lo lane), half the rows each, online base-2
-//               softmax with a conditional rescale (the running max moves only when a logit
+//               tile one head per thread pair (hi lane + lo lane), half the rows each, online
+//               base-2 softmax with a conditional rescale (the running max moves only when a logit
 //               exceeds it by more than 2^8; the factors go through shared memory so each warp
 //               rescales its quarter of O^T), the P row of the head
 //   warps 8-11  fp16 re-encoding of each landed KV chunk (a quarter each)
